@@ -1,0 +1,154 @@
+/*
+ * ssd.h -- C ABI of libssd: the Mamba-2 SSD (state-space duality) chunked-scan
+ * forward on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (the same one, whatever path computes it):
+ *
+ *   delta[b,t,h] = softplus(dt[b,t,h] + dt_bias[h])            (no clamp)
+ *   s_{-1}       = init_state[b,h]        (zeros when init_state == NULL)
+ *   s_t          = exp(delta[b,t,h] A[h]) s_{t-1} + delta[b,t,h] x[b,t,h,:] (outer) B[b,t,g(h),:]
+ *   y[b,t,h,:]   = s_t C[b,t,g(h),:] + D[h] x[b,t,h,:]           (D == NULL: no skip)
+ *   final_state[b,h] = s_{L-1}
+ *   g(h) = h / (nheads / ngroups)
+ *
+ * Sources: flash-linear-attention "fla/layers/mamba2.py" (Mamba2.torch_forward,
+ * the naive chunked SSD; the mamba_chunk_scan_combined call with
+ * dt_softplus=True, dt_bias, D, return_final_states=True); burn-mamba
+ * "mamba2/ssd/serial.rs" (ssd_serial and kernels k1..k5: chunk cumsum of
+ * dt*A, C.B^T per chunk, chunk states, serial state passing, chunk scan with
+ * the exp-segsum mask and D skip); burn-mamba "Mamba2SsdInput" rustdoc
+ * (ssd_minimal, Steps 1-4, paper Section 4.1 Eq. 20/22/23); lrnnx
+ * "ops/selective_scan.html" (selective_scan_ref: the token recurrence).
+ *
+ * Layouts: every tensor is a dense, row-major (C-contiguous) array.
+ *   x, y         [batch, seqlen, nheads, headdim]   io dtype (fp32 or bf16)
+ *   B, C         [batch, seqlen, ngroups, dstate]   io dtype
+ *   dt           [batch, seqlen, nheads]            fp32, raw (before bias and softplus)
+ *   dt_bias, A, D [nheads]                          fp32; A must be < 0 for a decaying state
+ *   init_state, final_state [batch, nheads, headdim, dstate]  fp32
+ *
+ * Ownership: the caller owns every buffer it passes. Device pointers must be
+ * device-resident on the current CUDA device and 16-byte aligned. Calls are
+ * asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ * stream) unless stated otherwise; the library keeps no pointer to caller
+ * memory after a call returns.
+ *
+ * Errors: no entry point aborts, traps or throws. Arguments are checked on
+ * the host before anything is launched. A device-side wait that runs past
+ * its time limit records SSD_ERR_DEVICE_TIMEOUT in a per-device status word
+ * (see ssd_device_status) instead of hanging.
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,     /* bad dims, NULL required pointer, ngroups mismatch, ... */
+    SSD_ERR_UNSUPPORTED = 2,     /* valid but outside what the chosen path implements */
+    SSD_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed */
+    SSD_ERR_DEVICE_TIMEOUT = 4,  /* a bounded device-side wait gave up */
+    SSD_ERR_WORKSPACE = 5        /* caller workspace too small or misaligned */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/* Which kernels compute the forward.
+ *   SSD_PATH_AUTO: tensor-core path when supported, else the SIMT path.
+ *   SSD_PATH_SIMT: fp32 CUDA-core kernels, any supported shape, the five
+ *                  stages at exactly chunk_len (chunk states in workspace).
+ *   SSD_PATH_TC:   fused tcgen05/TMA kernel (bf16 io, headdim 64,
+ *                  dstate 128 or 256, chunk_len 128 or 256). */
+typedef enum { SSD_PATH_AUTO = 0, SSD_PATH_SIMT = 1, SSD_PATH_TC = 2 } ssd_path;
+
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, ngroups, dstate;
+} ssd_dims;
+
+/*
+ * ssd_fwd -- the SSD chunked-scan forward (the five stages of burn-mamba
+ * "serial.rs" ssd_serial / fla "mamba2.py" naive chunked SSD).
+ *
+ * dims            shapes; every field >= 1; nheads % ngroups == 0.
+ * io_dtype        dtype of x, B, C and y.
+ * x, dt, dt_bias, A, B, C   device inputs (required).
+ * D               device [nheads] fp32 or NULL (no skip term).
+ * init_state      device [b,h,p,n] fp32 or NULL (zero initial state).
+ * chunk_len       chunk length Q, 1..256 (SIMT); 128 or 256 (tensor-core path).
+ * ngroups         must equal dims->ngroups.
+ * y               device output [b,L,h,p], io dtype (required).
+ * final_state     device output [b,h,p,n] fp32, or NULL (not written).
+ * stream          cudaStream_t.
+ *
+ * Scratch comes from a library-owned per-device workspace that grows on
+ * demand (cudaMalloc on first use or growth; freed by ssd_release). Calls
+ * that share that workspace must not overlap on the device: issue them on
+ * one stream, or use ssd_fwd_ws with a workspace per stream.
+ * Returns SSD_OK once the work is enqueued.
+ */
+SSD_API ssd_status ssd_fwd(const ssd_dims* dims, ssd_dtype io_dtype,
+                   const void* x, const float* dt, const float* dt_bias, const float* A,
+                   const void* B, const void* C, const float* D, const float* init_state,
+                   int chunk_len, int ngroups, void* y, float* final_state, void* stream);
+
+/*
+ * ssd_fwd_ws -- ssd_fwd with an explicit path and caller-owned device
+ * workspace of at least ssd_fwd_workspace_bytes(...) bytes, 256-byte aligned.
+ * The workspace must not be used by another call that overlaps on the device.
+ */
+SSD_API ssd_status ssd_fwd_ws(const ssd_dims* dims, ssd_dtype io_dtype,
+                      const void* x, const float* dt, const float* dt_bias, const float* A,
+                      const void* B, const void* C, const float* D, const float* init_state,
+                      int chunk_len, int ngroups, void* y, float* final_state,
+                      ssd_path path, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes ssd_fwd_ws needs for these arguments (0 if they are invalid). */
+SSD_API size_t ssd_fwd_workspace_bytes(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len, ssd_path path);
+
+/* The path SSD_PATH_AUTO picks for these arguments: SSD_PATH_TC or SSD_PATH_SIMT. */
+SSD_API ssd_path ssd_select_path(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len);
+
+/*
+ * ssd_fwd_host -- end-to-end call on HOST buffers (same layouts and meaning
+ * as ssd_fwd; pinned host memory makes the copies asynchronous). Copies the
+ * inputs to library-owned device buffers, runs the forward, copies y (and
+ * final_state when non-NULL) back, and synchronizes `stream` before
+ * returning, so the outputs are ready on return. Device-side timeouts are
+ * reported in the return value.
+ */
+SSD_API ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype,
+                        const void* x, const float* dt, const float* dt_bias, const float* A,
+                        const void* B, const void* C, const float* D, const float* init_state,
+                        int chunk_len, int ngroups, void* y, float* final_state, void* stream);
+
+/* Synchronizes `stream`, then returns and clears the current device's status
+ * word: SSD_OK, SSD_ERR_DEVICE_TIMEOUT, or SSD_ERR_CUDA if the sync failed. */
+SSD_API ssd_status ssd_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+SSD_API const char* ssd_status_string(ssd_status status);
+
+/* Kernels this library has launched in this process (all devices, all calls). */
+SSD_API uint64_t ssd_kernel_launches(void);
+
+/* Frees the library-owned device and pinned buffers of every device. Not safe
+ * while calls that use them are in flight. */
+SSD_API void ssd_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_H_ */

@@ -1,0 +1,236 @@
+"""Mamba-2 SSD chunked-scan forward on GB300: Python binding of libssd.so.
+
+A thin ctypes layer over the C ABI declared in include/ssd.h. It only checks
+and marshals arguments (shapes, dtypes, contiguity, device, stream handle);
+every step of the forward runs in the library's CUDA kernels. There is no
+fallback: if libssd.so is missing or fails to load, every call raises.
+
+    from mamba_ssd_chunked_gb300 import ssd_fwd
+    y, final_state = ssd_fwd(x, dt, dt_bias, A, B, C, D, init_state, chunk_len=256)
+
+Tensors (torch, CUDA, contiguous):
+    x [b, L, h, p] and B, C [b, L, g, n] in bf16 or fp32 (all three alike);
+    dt [b, L, h], dt_bias [h], A [h], D [h] fp32; init_state [b, h, p, n] fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+__all__ = [
+    "SsdError", "library", "ssd_fwd", "ssd_fwd_host", "ssd_device_status", "ssd_fwd_workspace_bytes",
+    "ssd_select_path", "ssd_kernel_launches", "ssd_release", "Dims", "PATHS", "STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "libssd.so")
+
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_CUDA",
+          4: "SSD_ERR_DEVICE_TIMEOUT", 5: "SSD_ERR_WORKSPACE"}
+PATHS = {"auto": 0, "simt": 1, "tc": 2}
+DTYPES = {"f32": 0, "bf16": 1}
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_int64) for k in ("batch", "seqlen", "nheads", "headdim", "ngroups", "dstate")]
+
+
+class SsdError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library() -> ctypes.CDLL:
+    """Load libssd.so (built by __graft_entry__.build() or mamba_ssd_chunked_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIBRARY):
+        raise RuntimeError(f"{LIBRARY} is missing: build it with `python -m mamba_ssd_chunked_gb300.build`")
+    lib = ctypes.CDLL(LIBRARY)
+    vp, fp, i, i64 = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    pdims = ctypes.POINTER(Dims)
+    lib.ssd_fwd.restype = i
+    lib.ssd_fwd.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, i, vp, fp, vp]
+    lib.ssd_fwd_ws.restype = i
+    lib.ssd_fwd_ws.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, i, vp, fp, i, vp, ctypes.c_size_t, vp]
+    lib.ssd_fwd_host.restype = i
+    lib.ssd_fwd_host.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, i, vp, fp, vp]
+    lib.ssd_fwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssd_fwd_workspace_bytes.argtypes = [pdims, i, i, i]
+    lib.ssd_select_path.restype = i
+    lib.ssd_select_path.argtypes = [pdims, i, i]
+    lib.ssd_device_status.restype = i
+    lib.ssd_device_status.argtypes = [vp]
+    lib.ssd_status_string.restype = ctypes.c_char_p
+    lib.ssd_status_string.argtypes = [i]
+    lib.ssd_kernel_launches.restype = ctypes.c_uint64
+    lib.ssd_kernel_launches.argtypes = []
+    lib.ssd_release.restype = None
+    lib.ssd_release.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _io_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return DTYPES["bf16"]
+    if t.dtype == torch.float32:
+        return DTYPES["f32"]
+    raise TypeError(f"x/B/C must be bf16 or fp32, got {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, shape, dtype, device_type, optional=False):
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device.type != device_type:
+        raise ValueError(f"{name} must be on {device_type}, got {t.device}")
+
+
+def _dims(x, B) -> Dims:
+    b, L, h, p = x.shape
+    g, n = B.shape[2], B.shape[3]
+    return Dims(b, L, h, p, g, n)
+
+
+def _check_all(x, dt, dt_bias, A, B, C, D, init_state, device_type):
+    torch = _torch()
+    if x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be [b, L, h, p] and B [b, L, g, n]")
+    b, L, h, p = x.shape
+    g, n = B.shape[2], B.shape[3]
+    io = x.dtype
+    _check(x, "x", (b, L, h, p), io, device_type)
+    _check(B, "B", (b, L, g, n), io, device_type)
+    _check(C, "C", (b, L, g, n), io, device_type)
+    f32 = torch.float32
+    _check(dt, "dt", (b, L, h), f32, device_type)
+    _check(dt_bias, "dt_bias", (h,), f32, device_type)
+    _check(A, "A", (h,), f32, device_type)
+    _check(D, "D", (h,), f32, device_type, optional=True)
+    _check(init_state, "init_state", (b, h, p, n), f32, device_type, optional=True)
+
+
+def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: int = 256,
+            ngroups: Optional[int] = None, y=None, final_state=None, return_final_state: bool = True,
+            path: str = "auto", workspace=None, stream=None) -> Tuple[object, Optional[object]]:
+    """Run the SSD forward on the GPU through ssd_fwd / ssd_fwd_ws.
+
+    Returns (y, final_state); final_state is None when return_final_state is
+    False. With path != "auto" or an explicit workspace (a uint8 CUDA tensor)
+    the call goes through ssd_fwd_ws; otherwise through ssd_fwd with the
+    library-owned workspace. Asynchronous on `stream` (default: torch's
+    current stream).
+    """
+    torch = _torch()
+    _check_all(x, dt, dt_bias, A, B, C, D, init_state, "cuda")
+    lib = library()
+    dims = _dims(x, B)
+    if ngroups is None:
+        ngroups = dims.ngroups
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _check(y, "y", tuple(x.shape), x.dtype, "cuda")
+    if final_state is None and return_final_state:
+        final_state = torch.empty((dims.batch, dims.nheads, dims.headdim, dims.dstate), dtype=torch.float32,
+                                  device=x.device)
+    elif final_state is not None:
+        _check(final_state, "final_state", (dims.batch, dims.nheads, dims.headdim, dims.dstate), torch.float32,
+               "cuda")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    io = _io_code(x)
+    if path == "auto" and workspace is None:
+        rc = lib.ssd_fwd(ctypes.byref(dims), io, _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
+                         _ptr(D), _ptr(init_state), int(chunk_len), int(ngroups), _ptr(y), _ptr(final_state),
+                         stream)
+    else:
+        code = PATHS[path]
+        need = lib.ssd_fwd_workspace_bytes(ctypes.byref(dims), io, int(chunk_len), code)
+        if workspace is None:
+            workspace = torch.empty(max(int(need), 1), dtype=torch.uint8, device=x.device)
+        rc = lib.ssd_fwd_ws(ctypes.byref(dims), io, _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
+                            _ptr(D), _ptr(init_state), int(chunk_len), int(ngroups), _ptr(y), _ptr(final_state),
+                            code, workspace.data_ptr(), workspace.numel(), stream)
+    if rc != 0:
+        raise SsdError(rc, "ssd_fwd")
+    return y, final_state
+
+
+def ssd_fwd_host(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: int = 256,
+                 ngroups: Optional[int] = None, y=None, final_state=None, return_final_state: bool = True,
+                 stream=None):
+    """End-to-end call on host (CPU, ideally pinned) torch tensors through ssd_fwd_host.
+
+    Copies in, computes, copies out and synchronizes; returns CPU (y, final_state).
+    """
+    torch = _torch()
+    _check_all(x, dt, dt_bias, A, B, C, D, init_state, "cpu")
+    lib = library()
+    dims = _dims(x, B)
+    if ngroups is None:
+        ngroups = dims.ngroups
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((dims.batch, dims.nheads, dims.headdim, dims.dstate), dtype=torch.float32)
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    rc = lib.ssd_fwd_host(ctypes.byref(dims), _io_code(x), _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B),
+                          _ptr(C), _ptr(D), _ptr(init_state), int(chunk_len), int(ngroups), _ptr(y),
+                          _ptr(final_state), stream)
+    if rc != 0:
+        raise SsdError(rc, "ssd_fwd_host")
+    return y, final_state
+
+
+def ssd_device_status(stream=None) -> int:
+    """Synchronize the stream and return (and clear) the device status code."""
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    return int(library().ssd_device_status(stream))
+
+
+def ssd_fwd_workspace_bytes(batch, seqlen, nheads, headdim, ngroups, dstate, io="bf16", chunk_len=256,
+                            path="auto") -> int:
+    d = Dims(batch, seqlen, nheads, headdim, ngroups, dstate)
+    return int(library().ssd_fwd_workspace_bytes(ctypes.byref(d), DTYPES[io], int(chunk_len), PATHS[path]))
+
+
+def ssd_select_path(batch, seqlen, nheads, headdim, ngroups, dstate, io="bf16", chunk_len=256) -> str:
+    d = Dims(batch, seqlen, nheads, headdim, ngroups, dstate)
+    code = int(library().ssd_select_path(ctypes.byref(d), DTYPES[io], int(chunk_len)))
+    return {v: k for k, v in PATHS.items()}[code]
+
+
+def ssd_kernel_launches() -> int:
+    return int(library().ssd_kernel_launches())
+
+
+def ssd_release() -> None:
+    library().ssd_release()

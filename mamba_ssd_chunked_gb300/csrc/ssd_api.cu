@@ -1,0 +1,316 @@
+// The C ABI of libssd (include/ssd.h): argument checks, path selection,
+// library-owned workspaces and staging buffers, the device status word.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+// Bit 0: a bounded device-side wait gave up (see the kernels).
+__device__ unsigned g_status_word;
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s per device-side wait
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    unsigned* status = nullptr;     // device address of g_status_word
+    void* ws = nullptr;             // library-owned workspace
+    size_t ws_bytes = 0;
+    // staging for ssd_fwd_host
+    void* dev_io = nullptr;
+    size_t dev_io_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Limit on a kernel's wait for state published by another CTA. The
+// environment variable SSD_DEVICE_WAIT_NS (read at every call) overrides it;
+// tests shrink it to exercise the timeout path.
+unsigned long long wait_limit_ns() {
+    const char* e = std::getenv("SSD_DEVICE_WAIT_NS");
+    if (e && *e) {
+        const unsigned long long x = std::strtoull(e, nullptr, 10);
+        if (x > 0) return x;
+    }
+    return kDefaultWaitNs;
+}
+
+ssd_status current_device(int* dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return SSD_ERR_CUDA;
+    if (*dev < 0 || *dev >= kMaxDevices) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+// Device address of the status word for the current device (cached).
+ssd_status status_word(int dev, unsigned** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& s = g_dev[dev];
+    if (!s.status) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return SSD_ERR_CUDA;
+        s.status = static_cast<unsigned*>(p);
+    }
+    *out = s.status;
+    return SSD_OK;
+}
+
+ssd_status check_dims(const ssd_dims* d, ssd_dtype io, int chunk_len, int ngroups) {
+    if (!d) return SSD_ERR_INVALID_ARG;
+    if (d->batch < 1 || d->seqlen < 1 || d->nheads < 1 || d->headdim < 1 || d->ngroups < 1 || d->dstate < 1)
+        return SSD_ERR_INVALID_ARG;
+    if (d->nheads % d->ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (ngroups != d->ngroups) return SSD_ERR_INVALID_ARG;
+    if (io != SSD_F32 && io != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (chunk_len < 1) return SSD_ERR_INVALID_ARG;
+    return SSD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ssd_status check_pointers(const void* x, const float* dt, const float* dt_bias, const float* A, const void* B,
+                          const void* C, const float* D, const float* init, const void* y, const float* fs) {
+    if (!x || !dt || !dt_bias || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    for (const void* p : {x, static_cast<const void*>(dt), static_cast<const void*>(dt_bias),
+                          static_cast<const void*>(A), B, C, y})
+        if (!aligned16(p)) return SSD_ERR_UNSUPPORTED;
+    for (const void* p : {static_cast<const void*>(D), static_cast<const void*>(init), static_cast<const void*>(fs)})
+        if (p && !aligned16(p)) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+ssd_path resolve_path(const ssd_dims& d, ssd_dtype io, int chunk_len, ssd_path want) {
+    if (want == SSD_PATH_AUTO) return tc_supported(d, io, chunk_len) ? SSD_PATH_TC : SSD_PATH_SIMT;
+    return want;
+}
+
+bool path_supported(const ssd_dims& d, ssd_dtype io, int chunk_len, ssd_path path) {
+    if (path == SSD_PATH_TC) return tc_supported(d, io, chunk_len);
+    if (path == SSD_PATH_SIMT) return simt_supported(d, chunk_len);
+    return false;
+}
+
+size_t workspace_for(const ssd_dims& d, int chunk_len, ssd_path path) {
+    return path == SSD_PATH_TC ? tc_workspace_bytes(d, chunk_len) : simt_workspace_bytes(d, chunk_len);
+}
+
+ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* dt, const float* dt_bias,
+               const float* A, const void* B, const void* C, const float* D, const float* init, int chunk_len,
+               int ngroups, void* y, float* fs, ssd_path path, void* ws, size_t ws_bytes, bool own_ws,
+               void* stream) {
+    ssd_status st = check_dims(dims, io, chunk_len, ngroups);
+    if (st != SSD_OK) return st;
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_SIMT && path != SSD_PATH_TC) return SSD_ERR_INVALID_ARG;
+    st = check_pointers(x, dt, dt_bias, A, B, C, D, init, y, fs);
+    if (st != SSD_OK) return st;
+    const ssd_path p = resolve_path(*dims, io, chunk_len, path);
+    if (!path_supported(*dims, io, chunk_len, p)) return SSD_ERR_UNSUPPORTED;
+    const size_t need = workspace_for(*dims, chunk_len, p);
+    if (!own_ws &&
+        (ws_bytes < need || (need > 0 && !ws) || (reinterpret_cast<uintptr_t>(ws) % kWorkspaceAlign) != 0))
+        return SSD_ERR_WORKSPACE;
+
+    int dev = 0;
+    st = current_device(&dev);
+    if (st != SSD_OK) return st;
+    unsigned* status = nullptr;
+    st = status_word(dev, &status);
+    if (st != SSD_OK) return st;
+
+    if (own_ws) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState& s = g_dev[dev];
+        if (s.ws_bytes < need) {
+            if (s.ws) {
+                // a smaller workspace may still be in use by work queued earlier
+                if (cudaDeviceSynchronize() != cudaSuccess) return SSD_ERR_CUDA;
+                cudaFree(s.ws);
+                s.ws = nullptr;
+                s.ws_bytes = 0;
+            }
+            if (cudaMalloc(&s.ws, need) != cudaSuccess) return SSD_ERR_CUDA;
+            s.ws_bytes = need;
+        }
+        ws = s.ws;
+        ws_bytes = s.ws_bytes;
+    }
+
+    FwdArgs a;
+    a.d = *dims;
+    a.io = io;
+    a.x = x;
+    a.dt = dt;
+    a.dt_bias = dt_bias;
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.D = D;
+    a.init = init;
+    a.chunk_len = chunk_len;
+    a.y = y;
+    a.final_state = fs;
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.status_word = status;
+    a.wait_limit_ns = wait_limit_ns();
+    return p == SSD_PATH_TC ? tc_forward(a, ws, ws_bytes) : simt_forward(a, ws, ws_bytes);
+}
+
+size_t elem_bytes(ssd_dtype io) { return io == SSD_F32 ? 4 : 2; }
+
+}  // namespace
+
+void note_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+ssd_status ssd_fwd(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, const float* dt, const float* dt_bias,
+                   const float* A, const void* B, const void* C, const float* D, const float* init_state,
+                   int chunk_len, int ngroups, void* y, float* final_state, void* stream) {
+    return run(dims, io_dtype, x, dt, dt_bias, A, B, C, D, init_state, chunk_len, ngroups, y, final_state,
+               SSD_PATH_AUTO, nullptr, 0, true, stream);
+}
+
+ssd_status ssd_fwd_ws(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, const float* dt,
+                      const float* dt_bias, const float* A, const void* B, const void* C, const float* D,
+                      const float* init_state, int chunk_len, int ngroups, void* y, float* final_state,
+                      ssd_path path, void* workspace, size_t workspace_bytes, void* stream) {
+    return run(dims, io_dtype, x, dt, dt_bias, A, B, C, D, init_state, chunk_len, ngroups, y, final_state, path,
+               workspace, workspace_bytes, false, stream);
+}
+
+size_t ssd_fwd_workspace_bytes(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len, ssd_path path) {
+    if (check_dims(dims, io_dtype, chunk_len, dims ? static_cast<int>(dims->ngroups) : 0) != SSD_OK) return 0;
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_SIMT && path != SSD_PATH_TC) return 0;
+    const ssd_path p = resolve_path(*dims, io_dtype, chunk_len, path);
+    if (!path_supported(*dims, io_dtype, chunk_len, p)) return 0;
+    return workspace_for(*dims, chunk_len, p);
+}
+
+ssd_path ssd_select_path(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len) {
+    if (!dims) return SSD_PATH_SIMT;
+    return resolve_path(*dims, io_dtype, chunk_len, SSD_PATH_AUTO);
+}
+
+ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, const float* dt,
+                        const float* dt_bias, const float* A, const void* B, const void* C, const float* D,
+                        const float* init_state, int chunk_len, int ngroups, void* y, float* final_state,
+                        void* stream) {
+    ssd_status st = check_dims(dims, io_dtype, chunk_len, ngroups);
+    if (st != SSD_OK) return st;
+    if (!x || !dt || !dt_bias || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    const ssd_dims& d = *dims;
+    const size_t eb = elem_bytes(io_dtype);
+    const size_t sz_x = eb * d.batch * d.seqlen * d.nheads * d.headdim;
+    const size_t sz_dt = 4 * d.batch * d.seqlen * d.nheads;
+    const size_t sz_h = 4 * d.nheads;
+    const size_t sz_bc = eb * d.batch * d.seqlen * d.ngroups * d.dstate;
+    const size_t sz_state = 4 * d.batch * d.nheads * d.headdim * d.dstate;
+    // device layout: x, y, dt, B, C, dt_bias, A, D, init, final
+    const size_t sizes[10] = {sz_x, sz_x, sz_dt, sz_bc, sz_bc, sz_h, sz_h, sz_h, sz_state, sz_state};
+    size_t offs[10], total = 0;
+    for (int i = 0; i < 10; ++i) {
+        offs[i] = total;
+        total += align_up(sizes[i], kWorkspaceAlign);
+    }
+    int dev = 0;
+    st = current_device(&dev);
+    if (st != SSD_OK) return st;
+    char* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState& s = g_dev[dev];
+        if (s.dev_io_bytes < total) {
+            if (s.dev_io) {
+                if (cudaDeviceSynchronize() != cudaSuccess) return SSD_ERR_CUDA;
+                cudaFree(s.dev_io);
+                s.dev_io = nullptr;
+                s.dev_io_bytes = 0;
+            }
+            if (cudaMalloc(&s.dev_io, total) != cudaSuccess) return SSD_ERR_CUDA;
+            s.dev_io_bytes = total;
+        }
+        base = static_cast<char*>(s.dev_io);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const void* src[10] = {x, nullptr, dt, B, C, dt_bias, A, D, init_state, nullptr};
+    for (int i = 0; i < 10; ++i) {
+        if (!src[i]) continue;
+        if (cudaMemcpyAsync(base + offs[i], src[i], sizes[i], cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return SSD_ERR_CUDA;
+    }
+    st = ssd_fwd(dims, io_dtype, base + offs[0], reinterpret_cast<const float*>(base + offs[2]),
+                 reinterpret_cast<const float*>(base + offs[5]), reinterpret_cast<const float*>(base + offs[6]),
+                 base + offs[3], base + offs[4], D ? reinterpret_cast<const float*>(base + offs[7]) : nullptr,
+                 init_state ? reinterpret_cast<const float*>(base + offs[8]) : nullptr, chunk_len, ngroups,
+                 base + offs[1], final_state ? reinterpret_cast<float*>(base + offs[9]) : nullptr, stream);
+    if (st != SSD_OK) return st;
+    if (cudaMemcpyAsync(y, base + offs[1], sizes[1], cudaMemcpyDeviceToHost, s) != cudaSuccess) return SSD_ERR_CUDA;
+    if (final_state &&
+        cudaMemcpyAsync(final_state, base + offs[9], sizes[9], cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    return ssd_device_status(stream);
+}
+
+ssd_status ssd_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSD_ERR_CUDA;
+    int dev = 0;
+    ssd_status st = current_device(&dev);
+    if (st != SSD_OK) return st;
+    unsigned* word = nullptr;
+    st = status_word(dev, &word);
+    if (st != SSD_OK) return st;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SSD_ERR_CUDA;
+    if (v != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SSD_ERR_CUDA;
+        return SSD_ERR_DEVICE_TIMEOUT;
+    }
+    return SSD_OK;
+}
+
+const char* ssd_status_string(ssd_status status) {
+    switch (status) {
+        case SSD_OK: return "ok";
+        case SSD_ERR_INVALID_ARG: return "invalid argument";
+        case SSD_ERR_UNSUPPORTED: return "unsupported shape, dtype, chunk length or alignment";
+        case SSD_ERR_CUDA: return "CUDA error";
+        case SSD_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case SSD_ERR_WORKSPACE: return "workspace too small or misaligned";
+    }
+    return "unknown status";
+}
+
+uint64_t ssd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void ssd_release(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int prev = 0;
+    const bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
+    for (int d = 0; d < kMaxDevices; ++d) {
+        DeviceState& s = g_dev[d];
+        if (!s.ws && !s.dev_io) continue;
+        if (cudaSetDevice(d) != cudaSuccess) continue;
+        cudaDeviceSynchronize();
+        if (s.ws) cudaFree(s.ws);
+        if (s.dev_io) cudaFree(s.dev_io);
+        s.ws = nullptr;
+        s.ws_bytes = 0;
+        s.dev_io = nullptr;
+        s.dev_io_bytes = 0;
+    }
+    if (have_prev) cudaSetDevice(prev);
+}
+
+}  // extern "C"

@@ -1,0 +1,49 @@
+// Host-side declarations shared by the translation units of libssd.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// One forward call, arguments already validated.
+struct FwdArgs {
+    ssd_dims d;
+    ssd_dtype io;
+    const void* x;
+    const float* dt;
+    const float* dt_bias;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const float* init;
+    int chunk_len;
+    void* y;
+    float* final_state;
+    cudaStream_t stream;
+    unsigned* status_word;             // device word: bit 0 = a bounded wait timed out
+    unsigned long long wait_limit_ns;  // per-wait wall-clock limit on the device
+};
+
+// CUDA-core path: the five stages at exactly chunk_len, chunk states in workspace.
+bool simt_supported(const ssd_dims& d, int chunk_len);
+size_t simt_workspace_bytes(const ssd_dims& d, int chunk_len);
+ssd_status simt_forward(const FwdArgs& a, void* ws, size_t ws_bytes);
+
+// Fused tcgen05/TMA path.
+bool tc_supported(const ssd_dims& d, ssd_dtype io, int chunk_len);
+size_t tc_workspace_bytes(const ssd_dims& d, int chunk_len);
+ssd_status tc_forward(const FwdArgs& a, void* ws, size_t ws_bytes);
+
+// Launch bookkeeping (every kernel launch of the library goes through it).
+void note_launches(uint64_t n);
+
+constexpr size_t kWorkspaceAlign = 256;
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace ssd

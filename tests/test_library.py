@@ -1,0 +1,138 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every
+entry point include/ssd.h declares, and rejects bad arguments on the host
+before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mamba_ssd_chunked_gb300 as pkg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mamba_ssd_chunked_gb300 import build
+    build.build()
+    return pkg.library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ssd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"SSD_API\s+[\w\s\*]+?\b(ssd_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = declared_functions()
+    for n in ("ssd_fwd", "ssd_fwd_ws", "ssd_fwd_host", "ssd_fwd_workspace_bytes", "ssd_device_status",
+              "ssd_status_string", "ssd_kernel_launches", "ssd_release", "ssd_select_path"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libssd.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.ssd_status_string(code)
+    assert lib.ssd_status_string(99) == b"unknown status"
+
+
+def _dims(**kw):
+    base = dict(batch=2, seqlen=300, nheads=4, headdim=64, ngroups=2, dstate=128)
+    base.update(kw)
+    return pkg.Dims(*[base[k] for k in ("batch", "seqlen", "nheads", "headdim", "ngroups", "dstate")])
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("bad", [
+    dict(batch=0), dict(seqlen=0), dict(nheads=0), dict(headdim=0), dict(dstate=0), dict(ngroups=0),
+    dict(nheads=6, ngroups=4),
+])
+def test_bad_dims_rejected_on_host(lib, bad):
+    d = _dims(**bad)
+    rc = lib.ssd_fwd(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, d.ngroups, FAKE,
+                     None, None)
+    assert rc == 1
+
+
+def test_null_required_pointer_rejected(lib):
+    d = _dims()
+    rc = lib.ssd_fwd(ctypes.byref(d), 1, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 2, FAKE, None, None)
+    assert rc == 1
+    rc = lib.ssd_fwd(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 2, None, None, None)
+    assert rc == 1
+
+
+def test_ngroups_argument_must_match_dims(lib):
+    d = _dims()
+    rc = lib.ssd_fwd(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 1, FAKE, None, None)
+    assert rc == 1
+
+
+def test_bad_dtype_and_chunk_rejected(lib):
+    d = _dims()
+    assert lib.ssd_fwd(ctypes.byref(d), 7, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 2, FAKE, None,
+                       None) == 1
+    assert lib.ssd_fwd(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 0, 2, FAKE, None,
+                       None) == 1
+
+
+def test_misaligned_pointer_is_unsupported(lib):
+    d = _dims()
+    rc = lib.ssd_fwd(ctypes.byref(d), 1, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 2, FAKE, None,
+                     None)
+    assert rc == 2
+
+
+def test_unsupported_chunk_len(lib):
+    d = _dims()
+    rc = lib.ssd_fwd(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 512, 2, FAKE, None, None)
+    assert rc == 2
+    rc = lib.ssd_fwd_ws(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 64, 2, FAKE, None, 2,
+                        FAKE, 1 << 30, None)
+    assert rc == 2  # the tensor-core path takes chunk_len 128 or 256 only
+
+
+def test_workspace_too_small(lib):
+    d = _dims()
+    need = lib.ssd_fwd_workspace_bytes(ctypes.byref(d), 1, 256, 2)
+    assert need > 0
+    rc = lib.ssd_fwd_ws(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 2, FAKE, None, 2,
+                        FAKE, need - 1, None)
+    assert rc == 5
+    rc = lib.ssd_fwd_ws(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 2, FAKE, None, 2,
+                        FAKE + 16, need + 64, None)
+    assert rc == 5  # not 256-byte aligned
+
+
+def test_path_selection(lib):
+    assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 256) == "tc"
+    assert pkg.ssd_select_path(1, 131072, 64, 64, 1, 256, "bf16", 256) == "tc"
+    assert pkg.ssd_select_path(1, 256, 4, 16, 1, 16, "f32", 64) == "simt"
+    assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "f32", 256) == "simt"
+    assert pkg.ssd_select_path(4, 4096, 80, 32, 1, 128, "bf16", 256) == "simt"
+    assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 64) == "simt"
+
+
+def test_workspace_sizes(lib):
+    # tensor-core path: counters + two fp32 state slots per (batch, head)
+    b, h, p, n = 4, 80, 64, 128
+    need = pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, n, "bf16", 256, "tc")
+    slots = 4 * b * h * 2 * p * n
+    assert slots <= need <= slots + 4096
+    # SIMT path: one fp32 state per chunk
+    need = pkg.ssd_fwd_workspace_bytes(1, 256, 4, 16, 1, 16, "f32", 64, "simt")
+    assert need >= 4 * 1 * 4 * 4 * 16 * 16
+    assert pkg.ssd_fwd_workspace_bytes(1, 256, 4, 16, 1, 16, "f32", 64, "tc") == 0
+
+
+def test_kernel_counter_starts_without_launches(lib):
+    assert lib.ssd_kernel_launches() >= 0
