@@ -189,6 +189,12 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
     return row * 128u + (((chunk ^ (row & 7u)) & 7u) << 4);
 }
 
+// ---------------------------------------------------------------- named barriers
+// bar.sync on barrier `id` (1..15) for `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---------------------------------------------------------------- global flags
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;

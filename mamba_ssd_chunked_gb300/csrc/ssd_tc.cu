@@ -1,32 +1,42 @@
 // Fused tcgen05/TMA path of the SSD forward (bf16 io, fp32 accumulation).
 //
-// One CTA computes one 128-token block of one (batch, head) chain; blocks are
-// handed out by an atomic ticket in block-major order (all heads and batches
-// of block k before any of block k+1). Inside the CTA, the five stages of the
-// chunked SSD (burn-mamba "mamba2/ssd/serial.rs" k1..k5; fla "mamba2.py"
-// naive chunked SSD) run as:
+// Work unit: one 128-token block of one batch row for a group of up to 8
+// heads that read the same B/C group. Units are handed out by an atomic
+// ticket in block-major order (every batch row and head group of block k
+// before any unit of block k+1), so a unit only ever waits on units that
+// took their tickets earlier.
 //
-//   k1  dt = softplus(dt_raw + dt_bias), cs = inclusive cumsum of dt*A      warp-shuffle scan
-//   k2  CB = C . B^T                       [128 x 128, K = dstate]           tcgen05.mma -> TMEM
-//   k3  S^T = B^T . diag(dt e^{cs_end - cs}) . X   [dstate x 64, K = 128]   tcgen05.mma -> TMEM
-//   k5a Yd = (L o CB o dt + D I) . X       [128 x 64, K = 128]              mask in registers, tcgen05.mma
-//   k4  s_out = e^{cs_end} s_in + S        fp32, chained through global slots (bounded waits)
-//   k5b Yo = C . s_in^T                    [128 x 64, K = dstate]           tcgen05.mma
-//       y  = e^{cs} o Yo + Yd              epilogue, TMA store
+// Per unit the CTA loads B and C once and computes C.B^T once; its heads are
+// then processed by SLOTS warpgroup pairs ("slots", 256 threads each) that
+// take alternate heads, so one slot's waits overlap the other's work. Per
+// head the five stages of the chunked SSD (burn-mamba "mamba2/ssd/serial.rs"
+// k1..k5; fla "mamba2.py" naive chunked SSD) run as:
 //
-// The D skip rides on the diagonal of the masked matrix (D x_t = D I x).
+//   k1  dt = softplus(dt_raw + dt_bias), cs = inclusive cumsum of dt*A   (per unit, all heads)
+//   k2  CB = C . B^T                 [128 x 128, K = dstate]   once per unit, tcgen05 -> TMEM
+//   k3  S^T = B^T . diag(dt e^{cs_end-cs}) . X   [dstate x 64, K = 128]   tcgen05 -> TMEM
+//   k5a Yd = (L o CB o dt + D I) . X [128 x 64, K = 128]       mask in registers, tcgen05
+//   k4  s_out = e^{cs_end} s_in + S  fp32, chained through global slots (bounded waits)
+//   k5b Yo = C . s_in^T              [128 x 64, K = dstate]    tcgen05
+//       y  = e^{cs} o Yo + Yd        epilogue, TMA store
+//
+// The D skip rides on the diagonal of the masked matrix (D x_t = (D I) x).
+// Below the 32x32 diagonal tiles the decay e^{cs_t - cs_s} is factored as
+// e^{cs_t - cs_r} e^{cs_r - cs_s} with r the first row of the tile row, both
+// factors <= 1 (cs is non-increasing), so those entries need no exponential.
 // A chunk_len of 256 is computed as two consecutive 128-token blocks: the
 // decomposition is exact for any chunk boundary, and the state between the
 // two halves is passed through the same chained slots.
 //
 // Operand staging (128-byte swizzle throughout; see ptx.cuh):
-//   sX [t][p]  (TMA)      B operand of k5a (MN-major, K = t)
-//   sB [t][n]  (TMA)      B operand of k2 (K-major), A operand of k3 (MN-major)
-//   sC [t][n]  (TMA)      A operand of k2 and k5b (K-major)
-//   sW [t][p]  (threads)  dt e^{cs_end-cs} X, B operand of k3 (MN-major)
-//   sM [t][s]  (threads)  masked CB, A operand of k5a (K-major), aliases sB
-//   sH [n][p]  (threads)  s_in in bf16, B operand of k5b (MN-major)
-//   sY [t][p]  (threads)  y tile for the TMA store, aliases sX
+//   sB [t][n]  (TMA, per unit)   B operand of k2 (K-major), A operand of k3 (MN-major)
+//   sC [t][n]  (TMA, per unit)   A operand of k2 and k5b (K-major)
+//   per slot:
+//   sX [t][p]  (TMA, per head)   B operand of k5a (MN-major, K = t)
+//   sW [t][p]  (threads)         dt e^{cs_end-cs} X, B operand of k3 (MN-major)
+//   sM [t][s]  (threads)         masked CB, A operand of k5a (K-major)
+//   sH [n][p]  (threads)         s_in in bf16, B operand of k5b (MN-major): in sW (dstate 128) or sM (256)
+//   sY [t][p]  (threads)         y tile for the TMA store: in sM (dstate 128) or sW (256)
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -38,33 +48,40 @@
 namespace ssd {
 namespace {
 
-constexpr int kT = 128;        // tokens per block (MMA M for k2, k5a, k5b)
-constexpr int kP = 64;         // headdim handled by this kernel
-constexpr int kThreads = 256;  // 8 warps: warp w owns TMEM lanes 32*(w%4).., column half w/4
+constexpr int kT = 128;               // tokens per block (MMA M for k2, k5a, k5b)
+constexpr int kP = 64;                // headdim handled by this kernel
+constexpr int kMaxHeads = 8;          // heads per unit at most
 constexpr uint32_t kTile = kT * 128;  // one 128-row x 128-byte swizzled tile (16 KB)
 constexpr uint32_t kPoison = 0xFFFFFFFFu;
+// Limit on waits for this CTA's own TMA copies and MMAs (they complete in
+// microseconds; the limit only guards against a wedged pipeline).
+constexpr unsigned long long kLocalWaitNs = 2000000000ull;
 
 template <int NST>
 struct Cfg {
-    static constexpr int NKB = NST / 64;                       // 64-wide dstate blocks
-    static constexpr uint32_t OFF_X = 0;
-    static constexpr uint32_t OFF_B = OFF_X + kTile;
+    static constexpr int NKB = NST / 64;                    // 64-wide dstate blocks
+    static constexpr int SLOTS = (NST == 128) ? 2 : 1;
+    static constexpr int THREADS = 256 * SLOTS;
+    static constexpr uint32_t OFF_B = 0;
     static constexpr uint32_t OFF_C = OFF_B + NKB * kTile;
-    static constexpr uint32_t OFF_W = OFF_C + NKB * kTile;
-    static constexpr uint32_t OFF_MISC = OFF_W + kTile;
-    static constexpr uint32_t OFF_M = OFF_B;                   // 2 tiles
-    static constexpr uint32_t OFF_H = (NST == 128) ? OFF_W : OFF_B + 2 * kTile;
-    static constexpr uint32_t OFF_Y = OFF_X;
-    static constexpr uint32_t MISC_BYTES = 2048;
+    static constexpr uint32_t OFF_SLOT = OFF_C + NKB * kTile;
+    static constexpr uint32_t SLOT_BYTES = 4 * kTile;       // X, W, M (2 tiles)
+    static constexpr uint32_t SX = 0, SW = kTile, SM = 2 * kTile;  // offsets inside a slot
+    static constexpr uint32_t SH = (NST == 128) ? SW : SM;
+    static constexpr uint32_t SY = (NST == 128) ? SM : SW;
+    static constexpr uint32_t OFF_MISC = OFF_SLOT + SLOTS * SLOT_BYTES;
+    // misc: 4 per-head tables [kMaxHeads][128] floats, per-slot v tables [4][128], scan totals
+    static constexpr uint32_t TAB_BYTES = 4 * kMaxHeads * kT * 4;
+    static constexpr uint32_t V_BYTES = SLOTS * 4 * kT * 4;
+    static constexpr uint32_t MISC_BYTES = TAB_BYTES + V_BYTES + 512 + 256;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
-    static constexpr uint32_t TMEM_COLS = (NST == 128) ? 256 : 512;
+    static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_CB = 0;
-    static constexpr uint32_t COL_O = 0;                       // reuses CB columns after the mask
-    static constexpr uint32_t COL_S = 128;                     // NST/128 tiles of 64 columns
-    static constexpr uint32_t COL_D = 128 + (NST / 128) * 64;
-    static constexpr uint32_t TX_BYTES = kTile + 2 * NKB * kTile;
-    static constexpr int MIN_BLOCKS = (NST == 128) ? 2 : 1;
-    static_assert(OFF_H + NST * 128 <= (NST == 128 ? OFF_W + kTile : OFF_B + NKB * kTile), "sH overflow");
+    __host__ __device__ static constexpr uint32_t col_s(int slot) { return 128 + 128 * slot; }
+    __host__ __device__ static constexpr uint32_t col_d(int slot) { return NST == 128 ? 192 + 128 * slot : 256; }
+    __host__ __device__ static constexpr uint32_t col_o(int slot) { return col_s(slot); }
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(NST == 128 || SLOTS == 1, "one slot for dstate 256");
 };
 
 struct TcParams {
@@ -78,14 +95,10 @@ struct TcParams {
     uint32_t* flags;       // [batch*H][2]: block index + 1 of the state in the slot
     uint32_t* ticket;      // block-major work counter
     uint32_t* status;      // device status word
-    int batch, H, G, nblk;
+    int batch, H, G, nblk, hpu, ngrp;  // hpu heads per unit, ngrp = H / hpu head groups
     long long L;
     unsigned long long chain_wait_ns;  // limit on waiting for the previous block's state
 };
-
-// Limit on waits for this CTA's own TMA copies and MMAs (they complete in
-// microseconds; the limit only guards against a wedged pipeline).
-constexpr unsigned long long kLocalWaitNs = 2000000000ull;
 
 __device__ __forceinline__ float softplus_f(float v) {
     return v > 0.f ? v + log1pf(expf(-v)) : log1pf(expf(v));
@@ -101,32 +114,43 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
     return __bfloat1622float2(b);
 }
 
+// Bounded wait; a timeout is recorded in the status word (bit 1) and the
+// caller proceeds (its results are then invalid, and the host is told).
+__device__ __forceinline__ void wait_local(uint64_t* bar, uint32_t parity, uint32_t* status) {
+    if (!ptx::mbar_wait(bar, parity, kLocalWaitNs)) atomicOr(status, 2u);
+}
+
 template <int NST>
-__global__ void __launch_bounds__(kThreads, Cfg<NST>::MIN_BLOCKS)
+__global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
     ssd_tc_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
                  const TcParams prm) {
     using K = Cfg<NST>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* sCs = reinterpret_cast<float*>(smem + K::OFF_MISC);  // [128] inclusive cumsum of dt*A
-    float* sDt = sCs + kT;                                      // [128] dt
-    float* sWarp = sDt + kT;                                    // [8]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sWarp + 8);    // [5]: tma, cb, s, d, o
-    uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 5);
-    int* sInfo = reinterpret_cast<int*>(sTmem + 1);             // [0] unit, [1] abort
+    float* tCs = reinterpret_cast<float*>(smem + K::OFF_MISC);  // [head][t] inclusive cumsum of dt*A
+    float* tDt = tCs + kMaxHeads * kT;                          // [head][t] dt
+    float* tWt = tDt + kMaxHeads * kT;                          // [head][t] dt e^{cs_end - cs}
+    float* tEt = tWt + kMaxHeads * kT;                          // [head][t] e^{cs}
+    float* tV = tEt + kMaxHeads * kT;                           // [slot][q][s] e^{cs_{32q} - cs_s} dt_s
+    float* tTot = tV + K::SLOTS * 4 * kT;                       // [head][4] scan totals
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tTot + kMaxHeads * 4 + 32);
+    // bars: [0] B/C, [1] CB, then per slot s: [2+4s] X, [3+4s] S, [4+4s] D, [5+4s] O
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 + 4 * K::SLOTS);
+    int* sInfo = reinterpret_cast<int*>(sTmem + 1);             // [0] unit, [1+s] chain abort of slot s
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
+    const int slot = tid >> 8, stid = tid & 255, swarp = stid >> 5;
+    const int quarter = warp & 3, half = swarp >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
 
     if (tid == 0) {
         sInfo[0] = static_cast<int>(atomicAdd(prm.ticket, 1u));
-        sInfo[1] = 0;
 #pragma unroll
-        for (int i = 0; i < 5; ++i) ptx::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 2 + 4 * K::SLOTS; ++i) ptx::mbar_init(&bars[i], 1);
         ptx::fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == 0) {
         ptx::tmem_alloc(sTmem, K::TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -135,61 +159,78 @@ __global__ void __launch_bounds__(kThreads, Cfg<NST>::MIN_BLOCKS)
     ptx::tc_fence_after();
     const uint32_t tmem = *sTmem;
     const int unit = sInfo[0];
-    const int h = unit % prm.H;
-    const int b = (unit / prm.H) % prm.batch;
-    const int blk = unit / (prm.H * prm.batch);
-    const int g = h / (prm.H / prm.G);
+    const int grp = unit % prm.ngrp;
+    const int b = (unit / prm.ngrp) % prm.batch;
+    const int blk = unit / (prm.ngrp * prm.batch);
+    const int h0 = grp * prm.hpu;
+    const int g = h0 / (prm.H / prm.G);
     const int t0 = blk * kT;
     const long long L = prm.L;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int hpu = prm.hpu;
+    const uint32_t sbase = ptx::smem_u32(smem);
+    uint8_t* slot_base = smem + K::OFF_SLOT + slot * K::SLOT_BYTES;
+    const uint32_t slot_addr = sbase + K::OFF_SLOT + slot * K::SLOT_BYTES;
+    uint64_t* bar_x = &bars[2 + 4 * slot];
+    uint64_t* bar_s = &bars[3 + 4 * slot];
+    uint64_t* bar_d = &bars[4 + 4 * slot];
+    uint64_t* bar_o = &bars[5 + 4 * slot];
+    const bool leader = (stid == 0);
 
-    // ---- TMA: x, B, C tiles of this block
+    // ---- TMA: B and C for the unit; X for each slot's first head
     if (tid == 0) {
-        ptx::mbar_arrive_expect_tx(&bars[0], K::TX_BYTES);
-        ptx::tma_load_4d(smem + K::OFF_X, &tm_x, &bars[0], 0, h, t0, b);
+        ptx::mbar_arrive_expect_tx(&bars[0], 2 * K::NKB * kTile);
 #pragma unroll
         for (int kb = 0; kb < K::NKB; ++kb) {
             ptx::tma_load_4d(smem + K::OFF_B + kb * kTile, &tm_b, &bars[0], 64 * kb, g, t0, b);
             ptx::tma_load_4d(smem + K::OFF_C + kb * kTile, &tm_c, &bars[0], 64 * kb, g, t0, b);
         }
     }
+    if (leader && slot < hpu) {
+        ptx::mbar_arrive_expect_tx(bar_x, kTile);
+        ptx::tma_load_4d(slot_base + K::SX, &tm_x, bar_x, 0, h0 + slot, t0, b);
+    }
 
-    // ---- k1: dt and the inclusive cumsum of dt*A (padding past L has dt = 0)
-    const float A_h = prm.A[h];
-    if (tid < kT) {
-        const long long t = static_cast<long long>(t0) + tid;
+    // ---- k1 for every head of the unit: dt, inclusive cumsum of dt*A (32-token warp scans)
+    for (int task = warp; task < hpu * 4; task += K::THREADS / 32) {
+        const int j = task >> 2, c4 = task & 3;
+        const int h = h0 + j;
+        const long long t = static_cast<long long>(t0) + 32 * c4 + lane;
         float dtv = 0.f;
         if (t < L) dtv = softplus_f(prm.dt[(static_cast<long long>(b) * L + t) * prm.H + h] + prm.dt_bias[h]);
-        float v = dtv * A_h;
+        float v = dtv * prm.A[h];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const float o = __shfl_up_sync(0xffffffffu, v, off);
             if (lane >= off) v += o;
         }
-        if (lane == 31) sWarp[warp] = v;
-        sDt[tid] = dtv;
-        sCs[tid] = v;
+        tDt[j * kT + 32 * c4 + lane] = dtv;
+        tCs[j * kT + 32 * c4 + lane] = v;
+        if (lane == 31) tTot[j * 4 + c4] = v;
     }
     __syncthreads();
-    if (tid < kT) {
+    for (int e = tid; e < hpu * kT; e += K::THREADS) {
+        const int j = e / kT, t = e % kT, c4 = t >> 5;
         float pre = 0.f;
-        for (int w = 0; w < warp; ++w) pre += sWarp[w];
-        sCs[tid] += pre;
+        for (int c = 0; c < c4; ++c) pre += tTot[j * 4 + c];
+        tCs[e] += pre;
     }
     __syncthreads();
-    const float cs_end = sCs[kT - 1];
+    for (int e = tid; e < hpu * kT; e += K::THREADS) {
+        const int j = e / kT;
+        const float cs = tCs[e];
+        const float cs_end = tCs[j * kT + kT - 1];
+        tWt[e] = tDt[e] * __expf(cs_end - cs);
+        tEt[e] = __expf(cs);
+    }
+    __syncthreads();
 
-    bool ok = ptx::mbar_wait(&bars[0], 0, kLocalWaitNs);
-    ok = __syncthreads_and(ok);
-    const bool tma_ok = ok;
-
-    // ---- k2: CB = C . B^T  (M = t, N = s, K = n; both operands K-major)
+    // ---- k2: CB = C . B^T once per unit (M = t, N = s, K = n; both K-major)
     constexpr uint32_t IDESC_CB = ptx::idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 64, true, true);
     constexpr uint32_t IDESC_D = ptx::idesc_bf16_f32(128, 64, false, true);
     constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(128, 64, false, true);
-    const uint32_t sbase = ptx::smem_u32(smem);
-    if (tid == 0 && ok) {
+    if (tid == 0) {
+        wait_local(&bars[0], 0, prm.status);
         ptx::tc_fence_after();
 #pragma unroll
         for (int k = 0; k < NST / 16; ++k) {
@@ -201,264 +242,296 @@ __global__ void __launch_bounds__(kThreads, Cfg<NST>::MIN_BLOCKS)
         ptx::mma_commit(&bars[1]);
     }
 
-    // ---- sW = X scaled by dt_t e^{cs_end - cs_t} (row t of sX is row t of sW)
-    if (ok) {
+    // ---- per-slot head loop
+    bool b_ready = false;  // this thread has seen B/C land
+    int it = 0;
+    for (int j = slot; j < hpu; j += K::SLOTS, ++it) {
+        const int h = h0 + j;
+        const uint32_t ph = it & 1;
+        const float* cs = tCs + j * kT;
+        const float* dts = tDt + j * kT;
+        const float* wts = tWt + j * kT;
+        float* vt = tV + slot * 4 * kT;
+
+        // (a) the previous head's y store must have read its staging tile
+        if (it > 0) {
+            if (leader) ptx::bulk_wait_group_read0();
+            ptx::named_sync(1 + slot, 256);
+        }
+        if (!b_ready) {
+            wait_local(&bars[0], 0, prm.status);
+            b_ready = true;
+        }
+        wait_local(bar_x, ph, prm.status);
+
+        // (b) sW = X scaled by dt_t e^{cs_end - cs_t}; v table for the factored mask
 #pragma unroll
-        for (int i = 0; i < (kT * 8) / kThreads; ++i) {
-            const int chunk = tid + i * kThreads;   // 16-byte chunk index, 8 per row
+        for (int i = 0; i < (kT * 8) / 256; ++i) {
+            const int chunk = stid + i * 256;  // 16-byte chunk, 8 per 128-byte row
             const int row = chunk >> 3;
-            const float w = sDt[row] * __expf(cs_end - sCs[row]);
-            const uint4 v = *reinterpret_cast<const uint4*>(smem + K::OFF_X + chunk * 16);
-            float2 f0 = unpack_bf16x2(v.x), f1 = unpack_bf16x2(v.y), f2 = unpack_bf16x2(v.z),
-                   f3 = unpack_bf16x2(v.w);
+            const float w = wts[row];
+            const uint4 v = *reinterpret_cast<const uint4*>(slot_base + K::SX + chunk * 16);
+            const float2 f0 = unpack_bf16x2(v.x), f1 = unpack_bf16x2(v.y), f2 = unpack_bf16x2(v.z),
+                         f3 = unpack_bf16x2(v.w);
             uint4 o;
             o.x = pack_bf16x2(f0.x * w, f0.y * w);
             o.y = pack_bf16x2(f1.x * w, f1.y * w);
             o.z = pack_bf16x2(f2.x * w, f2.y * w);
             o.w = pack_bf16x2(f3.x * w, f3.y * w);
-            *reinterpret_cast<uint4*>(smem + K::OFF_W + chunk * 16) = o;
+            *reinterpret_cast<uint4*>(slot_base + K::SW + chunk * 16) = o;
         }
-    }
-    ptx::fence_proxy_async_smem();
-    __syncthreads();
+        if (stid < 192) {
+            // q = 1: s < 32 (stid 0..31); q = 2: s < 64 (32..95); q = 3: s < 96 (96..191)
+            const int q = stid < 32 ? 1 : (stid < 96 ? 2 : 3);
+            const int s = stid - (q == 1 ? 0 : (q == 2 ? 32 : 96));
+            vt[q * kT + s] = __expf(cs[32 * q] - cs[s]) * dts[s];
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::named_sync(1 + slot, 256);
 
-    // ---- k3: S^T = B^T . W  (M = n, N = p, K = t; both operands MN-major)
-    if (tid == 0 && ok) {
+        // (c) k3: S^T = B^T . W  (M = n, N = p, K = t; both MN-major)
+        if (leader) {
+            ptx::tc_fence_after();
 #pragma unroll
-        for (int mt = 0; mt < NST / 128; ++mt) {
+            for (int mt = 0; mt < NST / 128; ++mt) {
 #pragma unroll
-            for (int k = 0; k < kT / 16; ++k) {
-                const uint64_t da = ptx::desc_sw128(sbase + K::OFF_B + 2 * mt * kTile + k * 2048, kTile, 1024);
-                const uint64_t db = ptx::desc_sw128(sbase + K::OFF_W + k * 2048, kTile, 1024);
-                ptx::mma_bf16(tmem + K::COL_S + 64 * mt, da, db, IDESC_S, k > 0);
+                for (int k = 0; k < kT / 16; ++k) {
+                    const uint64_t da = ptx::desc_sw128(sbase + K::OFF_B + 2 * mt * kTile + k * 2048, kTile, 1024);
+                    const uint64_t db = ptx::desc_sw128(slot_addr + K::SW + k * 2048, kTile, 1024);
+                    ptx::mma_bf16(tmem + K::col_s(slot) + 64 * mt, da, db, IDESC_S, k > 0);
+                }
             }
+            ptx::mma_commit(bar_s);
         }
-        ptx::mma_commit(&bars[2]);
-    }
 
-    // ---- k5a mask: M[t][s] = CB[t][s] e^{cs_t - cs_s} dt_s (s < t), CB[t][t] dt_t + D (s = t), 0 (s > t)
-    if (ok) ok = ptx::mbar_wait(&bars[1], 0, kLocalWaitNs) && ptx::mbar_wait(&bars[2], 0, kLocalWaitNs);
-    ok = __syncthreads_and(ok);  // warp-collective TMEM loads below need a uniform decision
-    const bool cb_s_pending = tma_ok && !ok;  // issued but not seen to complete
-    ptx::tc_fence_after();
-    const float D_h = prm.D ? prm.D[h] : 0.f;
-    {
-        const int t = quarter * 32 + lane;
-        const float cs_t = sCs[t];
-        uint8_t* mrow = smem + K::OFF_M + half * kTile;
-        if (half == 1 && quarter < 2) {
-            // rows 0..63, columns 64..127: strictly above the diagonal
-            const uint4 z = make_uint4(0, 0, 0, 0);
+        // (d) k5a mask from CB: rows t = 32*quarter + lane, columns 64*half .. +63
+        if (it == 0) wait_local(&bars[1], 0, prm.status);
+        ptx::tc_fence_after();
+        {
+            const int t = quarter * 32 + lane;
+            const float cs_t = cs[t];
+            const float D_h = prm.D ? prm.D[h] : 0.f;
+            const float u_t = __expf(cs_t - cs[32 * quarter]);
+            const float* vq = vt + quarter * kT;
+            uint8_t* mblk = slot_base + K::SM + half * kTile;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(mrow + ptx::swz128(t, j)) = z;
-        } else if (ok) {
+            for (int kk = 0; kk < 2; ++kk) {
+                const int k = 2 * half + kk;  // 32-column tile index along s
+                if (k > quarter) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
+                    for (int jj = 0; jj < 4; ++jj) *reinterpret_cast<uint4*>(mblk + ptx::swz128(t, kk * 4 + jj)) = z;
+                    continue;
+                }
                 uint32_t r[32];
-                ptx::tmem_ld32(tmem + lane_base + K::COL_CB + half * 64 + part * 32, r);
+                ptx::tmem_ld32(tmem + lane_base + K::COL_CB + 32 * k, r);
                 ptx::tmem_wait_ld(r);
+                uint32_t pk[16];
+                if (k < quarter) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t packed[4];
+                    for (int e = 0; e < 16; ++e) {
+                        const int s = 32 * k + 2 * e;
+                        pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * u_t * vq[s],
+                                            __uint_as_float(r[2 * e + 1]) * u_t * vq[s + 1]);
+                    }
+                } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < 16; ++e) {
                         float m2[2];
 #pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const int cl = j * 8 + e * 2 + q;            // column within the 32-wide part
-                            const int s = half * 64 + part * 32 + cl;
-                            const float cb = __uint_as_float(r[cl]);
+                        for (int q2 = 0; q2 < 2; ++q2) {
+                            const int s = 32 * k + 2 * e + q2;
+                            const float cb = __uint_as_float(r[2 * e + q2]);
                             float m = 0.f;
-                            if (s < t) m = cb * __expf(cs_t - sCs[s]) * sDt[s];
-                            else if (s == t) m = cb * sDt[s] + D_h;
-                            m2[q] = m;
+                            if (s < t) m = cb * __expf(cs_t - cs[s]) * dts[s];
+                            else if (s == t) m = cb * dts[s] + D_h;
+                            m2[q2] = m;
                         }
-                        packed[e] = pack_bf16x2(m2[0], m2[1]);
+                        pk[e] = pack_bf16x2(m2[0], m2[1]);
                     }
-                    *reinterpret_cast<uint4*>(mrow + ptx::swz128(t, part * 4 + j)) =
-                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
                 }
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    *reinterpret_cast<uint4*>(mblk + ptx::swz128(t, kk * 4 + jj)) =
+                        make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
             }
         }
-    }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::named_sync(1 + slot, 256);
 
-    // ---- k5a: Yd = M . X  (M = t, N = p, K = s; A K-major, B MN-major)
-    if (tid == 0 && ok) {
-        ptx::tc_fence_after();
+        // (e) k5a: Yd = M . X  (M = t, N = p, K = s; A K-major, B MN-major)
+        if (leader) {
+            ptx::tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < kT / 16; ++k) {
-            const uint64_t da = ptx::desc_sw128(sbase + K::OFF_M + (k >> 2) * kTile + (k & 3) * 32, 16, 1024);
-            const uint64_t db = ptx::desc_sw128(sbase + K::OFF_X + k * 2048, kTile, 1024);
-            ptx::mma_bf16(tmem + K::COL_D, da, db, IDESC_D, k > 0);
-        }
-        ptx::mma_commit(&bars[3]);
-    }
-
-    // ---- k4: chained state passing. Thread (quarter, half) owns state rows
-    // n = 32*quarter + lane (+128 per tile) and columns p = 32*half .. +31.
-    const int chain = b * prm.H + h;
-    uint32_t* my_flag = prm.flags + chain * 2 + (blk & 1);
-    if (blk > 0 && tid == 0) {
-        const uint32_t* pf = prm.flags + chain * 2 + ((blk - 1) & 1);
-        const uint32_t want = static_cast<uint32_t>(blk);
-        uint32_t v = ptx::ld_acquire_gpu(pf);
-        if (v != want) {
-            const uint64_t t_start = ptx::globaltimer_ns();
-            while (v != want && v != kPoison) {
-                if (ptx::globaltimer_ns() - t_start > prm.chain_wait_ns) break;
-                __nanosleep(64);
-                v = ptx::ld_acquire_gpu(pf);
+            for (int k = 0; k < kT / 16; ++k) {
+                const uint64_t da =
+                    ptx::desc_sw128(slot_addr + K::SM + (k >> 2) * kTile + (k & 3) * 32, 16, 1024);
+                const uint64_t db = ptx::desc_sw128(slot_addr + K::SX + k * 2048, kTile, 1024);
+                ptx::mma_bf16(tmem + K::col_d(slot), da, db, IDESC_D, k > 0);
             }
+            ptx::mma_commit(bar_d);
         }
-        if (v != want) sInfo[1] = 1;
-    }
-    if (!ok && tid == 0) sInfo[1] = 1;
-    __syncthreads();
-    const bool chain_ok = (sInfo[1] == 0);
-    {
-        const int n0 = quarter * 32 + lane;
-        const float* prev = prm.slots + (static_cast<size_t>(chain) * 2 + ((blk - 1) & 1)) * kP * NST;
-        float* mine = prm.slots + (static_cast<size_t>(chain) * 2 + (blk & 1)) * kP * NST;
-        const float a_blk = __expf(cs_end);
-        const bool last = (blk == prm.nblk - 1);
-        const size_t fs_base = static_cast<size_t>(chain) * kP * NST;
+
+        // (f) k4: chained state passing for chain (b, h). Thread (quarter, half)
+        // owns state rows n = 32*quarter + lane (+128 per tile), columns p = 32*half .. +31.
+        const int chain = b * prm.H + h;
+        if (leader) {
+            int abort = 0;
+            if (blk > 0) {
+                const uint32_t* pf = prm.flags + chain * 2 + ((blk - 1) & 1);
+                const uint32_t want = static_cast<uint32_t>(blk);
+                uint32_t v = ptx::ld_acquire_gpu(pf);
+                if (v != want) {
+                    const uint64_t t_start = ptx::globaltimer_ns();
+                    while (v != want && v != kPoison) {
+                        if (ptx::globaltimer_ns() - t_start > prm.chain_wait_ns) break;
+                        __nanosleep(64);
+                        v = ptx::ld_acquire_gpu(pf);
+                    }
+                }
+                abort = (v != want);
+            }
+            sInfo[1 + slot] = abort;
+        }
+        ptx::named_sync(1 + slot, 256);
+        const bool chain_ok = (sInfo[1 + slot] == 0);
+        {
+            const int n0 = quarter * 32 + lane;
+            const float* prev = prm.slots + (static_cast<size_t>(chain) * 2 + ((blk - 1) & 1)) * kP * NST;
+            float* mine = prm.slots + (static_cast<size_t>(chain) * 2 + (blk & 1)) * kP * NST;
+            const float a_blk = tEt[j * kT + kT - 1];  // e^{cs_end}
+            const bool last = (blk == prm.nblk - 1);
+            const size_t fs_base = static_cast<size_t>(chain) * kP * NST;
+            wait_local(bar_s, ph, prm.status);
+            if (NST != 128) wait_local(bar_d, ph, prm.status);  // sH shares sM with k5a's operand
+            ptx::tc_fence_after();
 #pragma unroll
-        for (int mt = 0; mt < NST / 128; ++mt) {
-            const int n = n0 + 128 * mt;
-            uint32_t r[32];
-            if (chain_ok) {
-                ptx::tmem_ld32(tmem + lane_base + K::COL_S + 64 * mt + half * 32, r);
+            for (int mt = 0; mt < NST / 128; ++mt) {
+                const int n = n0 + 128 * mt;
+                float hin[32];
+                if (blk == 0) {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int p = half * 32 + jj;
+                        hin[jj] = prm.init ? prm.init[fs_base + static_cast<size_t>(p) * NST + n] : 0.f;
+                    }
+                } else if (chain_ok) {
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const int p4 = half * 8 + j4;
+                        const float4 v =
+                            __ldcg(reinterpret_cast<const float4*>(prev + (static_cast<size_t>(p4) * NST + n) * 4));
+                        hin[4 * j4 + 0] = v.x;
+                        hin[4 * j4 + 1] = v.y;
+                        hin[4 * j4 + 2] = v.z;
+                        hin[4 * j4 + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) hin[jj] = 0.f;
+                }
+                uint32_t r[32];
+                ptx::tmem_ld32(tmem + lane_base + K::col_s(slot) + 64 * mt + half * 32, r);
                 ptx::tmem_wait_ld(r);
-            }
-            float hin[32];
-            if (blk == 0) {
+                if (chain_ok) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int p = half * 32 + j;
-                    hin[j] = prm.init ? prm.init[fs_base + static_cast<size_t>(p) * NST + n] : 0.f;
-                }
-            } else if (chain_ok) {
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const int p4 = half * 8 + j4;
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(prev + (static_cast<size_t>(p4) * NST + n) * 4));
-                    hin[4 * j4 + 0] = v.x;
-                    hin[4 * j4 + 1] = v.y;
-                    hin[4 * j4 + 2] = v.z;
-                    hin[4 * j4 + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) hin[j] = 0.f;
-            }
-            if (chain_ok) {
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    float4 o;
-                    o.x = fmaf(a_blk, hin[4 * j4 + 0], __uint_as_float(r[4 * j4 + 0]));
-                    o.y = fmaf(a_blk, hin[4 * j4 + 1], __uint_as_float(r[4 * j4 + 1]));
-                    o.z = fmaf(a_blk, hin[4 * j4 + 2], __uint_as_float(r[4 * j4 + 2]));
-                    o.w = fmaf(a_blk, hin[4 * j4 + 3], __uint_as_float(r[4 * j4 + 3]));
-                    const int p4 = half * 8 + j4;
-                    __stcg(reinterpret_cast<float4*>(mine + (static_cast<size_t>(p4) * NST + n) * 4), o);
-                    if (last && prm.final_state) {
-                        const int p = 4 * p4;
-                        prm.final_state[fs_base + static_cast<size_t>(p + 0) * NST + n] = o.x;
-                        prm.final_state[fs_base + static_cast<size_t>(p + 1) * NST + n] = o.y;
-                        prm.final_state[fs_base + static_cast<size_t>(p + 2) * NST + n] = o.z;
-                        prm.final_state[fs_base + static_cast<size_t>(p + 3) * NST + n] = o.w;
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        float4 o;
+                        o.x = fmaf(a_blk, hin[4 * j4 + 0], __uint_as_float(r[4 * j4 + 0]));
+                        o.y = fmaf(a_blk, hin[4 * j4 + 1], __uint_as_float(r[4 * j4 + 1]));
+                        o.z = fmaf(a_blk, hin[4 * j4 + 2], __uint_as_float(r[4 * j4 + 2]));
+                        o.w = fmaf(a_blk, hin[4 * j4 + 3], __uint_as_float(r[4 * j4 + 3]));
+                        const int p4 = half * 8 + j4;
+                        __stcg(reinterpret_cast<float4*>(mine + (static_cast<size_t>(p4) * NST + n) * 4), o);
+                        if (last && prm.final_state) {
+                            const int p = 4 * p4;
+                            prm.final_state[fs_base + static_cast<size_t>(p + 0) * NST + n] = o.x;
+                            prm.final_state[fs_base + static_cast<size_t>(p + 1) * NST + n] = o.y;
+                            prm.final_state[fs_base + static_cast<size_t>(p + 2) * NST + n] = o.z;
+                            prm.final_state[fs_base + static_cast<size_t>(p + 3) * NST + n] = o.w;
+                        }
                     }
                 }
-            }
-            // s_in^T in bf16 for k5b: row n of sH, columns p = 32*half .. +31 (4 chunks)
-            uint8_t* hrow = smem + K::OFF_H;
+                // s_in^T in bf16 for k5b: row n of sH, columns p = 32*half .. +31 (4 chunks)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint4 o;
-                o.x = pack_bf16x2(hin[8 * j + 0], hin[8 * j + 1]);
-                o.y = pack_bf16x2(hin[8 * j + 2], hin[8 * j + 3]);
-                o.z = pack_bf16x2(hin[8 * j + 4], hin[8 * j + 5]);
-                o.w = pack_bf16x2(hin[8 * j + 6], hin[8 * j + 7]);
-                *reinterpret_cast<uint4*>(hrow + ptx::swz128(n, half * 4 + j)) = o;
+                for (int jj = 0; jj < 4; ++jj) {
+                    uint4 o;
+                    o.x = pack_bf16x2(hin[8 * jj + 0], hin[8 * jj + 1]);
+                    o.y = pack_bf16x2(hin[8 * jj + 2], hin[8 * jj + 3]);
+                    o.z = pack_bf16x2(hin[8 * jj + 4], hin[8 * jj + 5]);
+                    o.w = pack_bf16x2(hin[8 * jj + 6], hin[8 * jj + 7]);
+                    *reinterpret_cast<uint4*>(slot_base + K::SH + ptx::swz128(n, half * 4 + jj)) = o;
+                }
             }
         }
-    }
-    __threadfence();
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        ptx::st_release_gpu(my_flag, chain_ok ? static_cast<uint32_t>(blk + 1) : kPoison);
-        if (!chain_ok) atomicOr(prm.status, 1u);
-    }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::named_sync(1 + slot, 256);
 
-    // ---- k5b: Yo = C . s_in^T  (M = t, N = p, K = n; A K-major, B MN-major)
-    if (tid == 0 && chain_ok) {
-        ptx::tc_fence_after();
+        // (g) k5b: Yo = C . s_in^T  (M = t, N = p, K = n; A K-major, B MN-major), into S's columns
+        if (leader && chain_ok) {
+            ptx::tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < NST / 16; ++k) {
-            const uint64_t da = ptx::desc_sw128(sbase + K::OFF_C + (k >> 2) * kTile + (k & 3) * 32, 16, 1024);
-            const uint64_t db = ptx::desc_sw128(sbase + K::OFF_H + k * 2048, kTile, 1024);
-            ptx::mma_bf16(tmem + K::COL_O, da, db, IDESC_O, k > 0);
-        }
-        ptx::mma_commit(&bars[4]);
-    }
-
-    // ---- epilogue: y = e^{cs_t} Yo + Yd, staged in sY (= sX) and stored by TMA
-    const bool d_issued = ok;         // k5a was issued iff the mask phase completed
-    const bool o_issued = chain_ok;   // k5b was issued iff the chain delivered a state
-    bool ep_ok = chain_ok && ptx::mbar_wait(&bars[3], 0, kLocalWaitNs) && ptx::mbar_wait(&bars[4], 0, kLocalWaitNs);
-    ep_ok = __syncthreads_and(ep_ok);
-    ptx::tc_fence_after();
-    if (ep_ok) {
-        const int t = quarter * 32 + lane;
-        const float e_t = __expf(sCs[t]);
-        uint32_t ro[32], rd[32];
-        ptx::tmem_ld32(tmem + lane_base + K::COL_O + half * 32, ro);
-        ptx::tmem_ld32(tmem + lane_base + K::COL_D + half * 32, rd);
-        ptx::tmem_wait_ld(ro);
-        ptx::tmem_wait_ld(rd);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c0 = 8 * j + 2 * e;
-                pk[e] = pack_bf16x2(fmaf(e_t, __uint_as_float(ro[c0]), __uint_as_float(rd[c0])),
-                                    fmaf(e_t, __uint_as_float(ro[c0 + 1]), __uint_as_float(rd[c0 + 1])));
+            for (int k = 0; k < NST / 16; ++k) {
+                const uint64_t da = ptx::desc_sw128(sbase + K::OFF_C + (k >> 2) * kTile + (k & 3) * 32, 16, 1024);
+                const uint64_t db = ptx::desc_sw128(slot_addr + K::SH + k * 2048, kTile, 1024);
+                ptx::mma_bf16(tmem + K::col_o(slot), da, db, IDESC_O, k > 0);
             }
-            *reinterpret_cast<uint4*>(smem + K::OFF_Y + ptx::swz128(t, half * 4 + j)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            ptx::mma_commit(bar_o);
         }
-    }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        if (ep_ok) {
-            ptx::tma_store_4d(&tm_y, smem + K::OFF_Y, 0, h, t0, b);
+        // publish this block's state (the successor block of the chain waits on it)
+        __threadfence();
+        ptx::named_sync(1 + slot, 256);
+        if (leader) {
+            ptx::st_release_gpu(prm.flags + chain * 2 + (blk & 1),
+                                chain_ok ? static_cast<uint32_t>(blk + 1) : kPoison);
+            if (!chain_ok) atomicOr(prm.status, 1u);
+        }
+
+        // (h) epilogue: y = e^{cs_t} Yo + Yd, staged in sY and stored by TMA
+        wait_local(bar_d, ph, prm.status);
+        if (leader && j + K::SLOTS < hpu) {
+            // sX is free once k5a has read it: prefetch the slot's next head
+            ptx::mbar_arrive_expect_tx(bar_x, kTile);
+            ptx::tma_load_4d(slot_base + K::SX, &tm_x, bar_x, 0, h + K::SLOTS, t0, b);
+        }
+        if (chain_ok) {
+            wait_local(bar_o, ph, prm.status);
+            ptx::tc_fence_after();
+            const int t = quarter * 32 + lane;
+            const float e_t = tEt[j * kT + t];
+            uint32_t ro[32], rd[32];
+            ptx::tmem_ld32(tmem + lane_base + K::col_o(slot) + half * 32, ro);
+            ptx::tmem_ld32(tmem + lane_base + K::col_d(slot) + half * 32, rd);
+            ptx::tmem_wait_ld(ro);
+            ptx::tmem_wait_ld(rd);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c0 = 8 * jj + 2 * e;
+                    pk[e] = pack_bf16x2(fmaf(e_t, __uint_as_float(ro[c0]), __uint_as_float(rd[c0])),
+                                        fmaf(e_t, __uint_as_float(ro[c0 + 1]), __uint_as_float(rd[c0 + 1])));
+                }
+                *reinterpret_cast<uint4*>(slot_base + K::SY + ptx::swz128(t, half * 4 + jj)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::named_sync(1 + slot, 256);
+        if (leader && chain_ok) {
+            ptx::tma_store_4d(&tm_y, slot_base + K::SY, 0, h, t0, b);
             ptx::bulk_commit_group();
-            ptx::bulk_wait_group_read0();
-        } else {
-            atomicOr(prm.status, 1u);
-            // Drain before releasing TMEM and shared memory: every copy and MMA
-            // this CTA started must have landed (each wait is bounded).
-            if (!tma_ok) ptx::mbar_wait(&bars[0], 0, kLocalWaitNs);
-            if (cb_s_pending) {
-                ptx::mbar_wait(&bars[1], 0, kLocalWaitNs);
-                ptx::mbar_wait(&bars[2], 0, kLocalWaitNs);
-            }
-            if (d_issued) ptx::mbar_wait(&bars[3], 0, kLocalWaitNs);
-            if (o_issued) ptx::mbar_wait(&bars[4], 0, kLocalWaitNs);
         }
     }
+    if (leader) ptx::bulk_wait_group_read0();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == 1) ptx::tmem_dealloc(tmem, K::TMEM_COLS);
+    if (warp == 0) ptx::tmem_dealloc(tmem, K::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- host side
@@ -497,6 +570,14 @@ size_t tc_counters_bytes(const ssd_dims& d) {
     return align_up(sizeof(uint32_t) * static_cast<size_t>(1 + 2 * d.batch * d.nheads), kWorkspaceAlign);
 }
 
+// Heads per unit: the largest of 8, 4, 2, 1 that divides the heads of one group.
+int heads_per_unit(const ssd_dims& d) {
+    const int64_t r = d.nheads / d.ngroups;
+    for (int c = kMaxHeads; c > 1; c >>= 1)
+        if (r % c == 0) return c;
+    return 1;
+}
+
 template <int NST>
 ssd_status launch(const FwdArgs& a, void* ws) {
     using K = Cfg<NST>;
@@ -524,13 +605,15 @@ ssd_status launch(const FwdArgs& a, void* ws) {
     p.H = static_cast<int>(d.nheads);
     p.G = static_cast<int>(d.ngroups);
     p.nblk = static_cast<int>((d.seqlen + kT - 1) / kT);
+    p.hpu = heads_per_unit(d);
+    p.ngrp = p.H / p.hpu;
     p.L = d.seqlen;
     p.chain_wait_ns = a.wait_limit_ns;
     if (cudaFuncSetAttribute(ssd_tc_fused<NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(K::SMEM_BYTES)) != cudaSuccess)
         return SSD_ERR_CUDA;
-    const long long units = static_cast<long long>(p.nblk) * d.batch * d.nheads;
-    ssd_tc_fused<NST><<<static_cast<unsigned>(units), kThreads, K::SMEM_BYTES, a.stream>>>(tx, tb, tc, ty, p);
+    const long long units = static_cast<long long>(p.nblk) * d.batch * p.ngrp;
+    ssd_tc_fused<NST><<<static_cast<unsigned>(units), K::THREADS, K::SMEM_BYTES, a.stream>>>(tx, tb, tc, ty, p);
     note_launches(1);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
