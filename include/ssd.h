@@ -106,7 +106,11 @@ SSD_API ssd_status ssd_fwd(const ssd_dims* dims, ssd_dtype io_dtype,
 /*
  * ssd_fwd_ws -- ssd_fwd with an explicit path and caller-owned device
  * workspace of at least ssd_fwd_workspace_bytes(...) bytes, 256-byte aligned.
- * The workspace must not be used by another call that overlaps on the device.
+ * Zero-fill the workspace once before its first use and keep it for this
+ * library afterwards: the tensor-core path passes chunk states between CTAs
+ * through it as tagged words, and a tag is only trusted because stale
+ * contents can only be zeros or this library's own earlier tags. The
+ * workspace must not be used by another call that overlaps on the device.
  */
 SSD_API ssd_status ssd_fwd_ws(const ssd_dims* dims, ssd_dtype io_dtype,
                       const void* x, const float* dt, const float* dt_bias, const float* A,

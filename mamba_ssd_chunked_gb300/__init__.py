@@ -141,8 +141,9 @@ def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: int = 2
 
     Returns (y, final_state); final_state is None when return_final_state is
     False. With path != "auto" or an explicit workspace (a uint8 CUDA tensor)
-    the call goes through ssd_fwd_ws; otherwise through ssd_fwd with the
-    library-owned workspace. Asynchronous on `stream` (default: torch's
+    the call goes through ssd_fwd_ws (a caller workspace must be zero-filled
+    before its first use); otherwise through ssd_fwd with the library-owned
+    workspace. Asynchronous on `stream` (default: torch's
     current stream).
     """
     torch = _torch()
@@ -172,7 +173,7 @@ def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: int = 2
         code = PATHS[path]
         need = lib.ssd_fwd_workspace_bytes(ctypes.byref(dims), io, int(chunk_len), code)
         if workspace is None:
-            workspace = torch.empty(max(int(need), 1), dtype=torch.uint8, device=x.device)
+            workspace = torch.zeros(max(int(need), 1), dtype=torch.uint8, device=x.device)
         rc = lib.ssd_fwd_ws(ctypes.byref(dims), io, _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
                             _ptr(D), _ptr(init_state), int(chunk_len), int(ngroups), _ptr(y), _ptr(final_state),
                             code, workspace.data_ptr(), workspace.numel(), stream)

@@ -136,6 +136,8 @@ ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* d
                 s.ws_bytes = 0;
             }
             if (cudaMalloc(&s.ws, need) != cudaSuccess) return SSD_ERR_CUDA;
+            // the tensor-core path's state slots must start zero-filled (see ssd_fwd_ws)
+            if (cudaMemset(s.ws, 0, need) != cudaSuccess) return SSD_ERR_CUDA;
             s.ws_bytes = need;
         }
         ws = s.ws;

@@ -21,9 +21,11 @@
 //       y  = e^{cs} o Yo + Yd        epilogue, TMA store
 //
 // The D skip rides on the diagonal of the masked matrix (D x_t = (D I) x).
-// Below the 32x32 diagonal tiles the decay e^{cs_t - cs_s} is factored as
-// e^{cs_t - cs_r} e^{cs_r - cs_s} with r the first row of the tile row, both
-// factors <= 1 (cs is non-increasing), so those entries need no exponential.
+// The decay e^{cs_t - cs_s} of row t is factored as u_t v_q(s) with
+// u_t = e^{cs_t - cs_r}, v_q(s) = e^{cs_r - cs_s} dt_s and r the first row of
+// t's 32-row quarter q, so the mask needs no per-entry exponential: the row
+// factor u_t moves to the epilogue (and D to D/u_t on the diagonal). Quarters
+// whose decay exceeds kMaxFactorLog keep exact entries instead.
 // A chunk_len of 256 is computed as two consecutive 128-token blocks: the
 // decomposition is exact for any chunk boundary, and the state between the
 // two halves is passed through the same chained slots.
@@ -36,10 +38,11 @@
 //   sW [t][p]  (threads)         dt e^{cs_end-cs} X, B operand of k3 (MN-major)
 //   sM [t][s]  (threads)         masked CB, A operand of k5a (K-major)
 //   sH [n][p]  (threads)         s_in in bf16, B operand of k5b (MN-major): in sW (dstate 128) or sM (256)
-//   sY [t][p]  (threads)         y tile for the TMA store: in sM (dstate 128) or sW (256)
+//   sY [t][p]  (threads)         y tile for the TMA store, in sW (after k5b has read sH)
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -56,6 +59,9 @@ constexpr uint32_t kPoison = 0xFFFFFFFFu;
 // Limit on waits for this CTA's own TMA copies and MMAs (they complete in
 // microseconds; the limit only guards against a wedged pipeline).
 constexpr unsigned long long kLocalWaitNs = 2000000000ull;
+// Largest decay (in nats) across a 32-row quarter for which the mask is stored
+// in factored form; e^{60} * |D| stays far inside the bf16/fp32 range.
+constexpr float kMaxFactorLog = 60.f;
 
 template <int NST>
 struct Cfg {
@@ -68,7 +74,7 @@ struct Cfg {
     static constexpr uint32_t SLOT_BYTES = 4 * kTile;       // X, W, M (2 tiles)
     static constexpr uint32_t SX = 0, SW = kTile, SM = 2 * kTile;  // offsets inside a slot
     static constexpr uint32_t SH = (NST == 128) ? SW : SM;
-    static constexpr uint32_t SY = (NST == 128) ? SM : SW;
+    static constexpr uint32_t SY = SW;
     static constexpr uint32_t OFF_MISC = OFF_SLOT + SLOTS * SLOT_BYTES;
     // misc: 4 per-head tables [kMaxHeads][128] floats, per-slot v tables [4][128], scan totals
     static constexpr uint32_t TAB_BYTES = 4 * kMaxHeads * kT * 4;
@@ -91,14 +97,20 @@ struct TcParams {
     const float* D;
     const float* init;
     float* final_state;
-    float* slots;          // [batch*H][2][P/4][NST][4] fp32 chained states
-    uint32_t* flags;       // [batch*H][2]: block index + 1 of the state in the slot
+    uint64_t* slots;       // [batch*H][2][P/2][NST][2] chained states: fp32 value | tag << 32
     uint32_t* ticket;      // block-major work counter
+    uint32_t epoch;        // per-call tag component
     uint32_t* status;      // device status word
     int batch, H, G, nblk, hpu, ngrp;  // hpu heads per unit, ngrp = H / hpu head groups
     long long L;
     unsigned long long chain_wait_ns;  // limit on waiting for the previous block's state
 };
+
+// Tag of the state block `blk` publishes in call `epoch`: never 0 (so zeroed
+// memory never matches) and never kPoison, for blk < 65535.
+__device__ __forceinline__ uint32_t state_tag(uint32_t epoch, int blk) {
+    return ((epoch % 65535u + 1u) << 16) | static_cast<uint32_t>((blk + 1) & 0xFFFF);
+}
 
 __device__ __forceinline__ float softplus_f(float v) {
     return v > 0.f ? v + log1pf(expf(-v)) : log1pf(expf(v));
@@ -134,7 +146,9 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
     float* tEt = tWt + kMaxHeads * kT;                          // [head][t] e^{cs}
     float* tV = tEt + kMaxHeads * kT;                           // [slot][q][s] e^{cs_{32q} - cs_s} dt_s
     float* tTot = tV + K::SLOTS * 4 * kT;                       // [head][4] scan totals
+    float* tD = tTot + kMaxHeads * 4;                           // [head] D
     uint64_t* bars = reinterpret_cast<uint64_t*>(tTot + kMaxHeads * 4 + 32);
+    static_assert(kMaxHeads * 4 + kMaxHeads <= kMaxHeads * 4 + 32, "tD fits before the barriers");
     // bars: [0] B/C, [1] CB, then per slot s: [2+4s] X, [3+4s] S, [4+4s] D, [5+4s] O
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 + 4 * K::SLOTS);
     int* sInfo = reinterpret_cast<int*>(sTmem + 1);             // [0] unit, [1+s] chain abort of slot s
@@ -206,6 +220,7 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
         tDt[j * kT + 32 * c4 + lane] = dtv;
         tCs[j * kT + 32 * c4 + lane] = v;
         if (lane == 31) tTot[j * 4 + c4] = v;
+        if (c4 == 0 && lane == 0) tD[j] = prm.D ? prm.D[h] : 0.f;
     }
     __syncthreads();
     for (int e = tid; e < hpu * kT; e += K::THREADS) {
@@ -242,6 +257,12 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
         ptx::mma_commit(&bars[1]);
     }
 
+    // Matrix descriptors are built once per issue from the operand base; a K
+    // step adds its byte offset to the start-address field (offsets stay far
+    // below the field's range).
+    auto kmaj = [](int k) { return static_cast<uint64_t>(((k >> 2) * kTile + (k & 3) * 32) >> 4); };
+    auto mnmaj = [](int k) { return static_cast<uint64_t>((k * 2048) >> 4); };
+
     // ---- per-slot head loop
     bool b_ready = false;  // this thread has seen B/C land
     int it = 0;
@@ -252,6 +273,24 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
         const float* dts = tDt + j * kT;
         const float* wts = tWt + j * kT;
         float* vt = tV + slot * 4 * kT;
+        // k4 bookkeeping for chain (b, h). Thread (quarter, half) owns state rows
+        // n = 32*quarter + lane (+128 per tile) and columns p = 32*half .. +31.
+        const int chain = b * prm.H + h;
+        const uint64_t* prev = prm.slots + (static_cast<size_t>(chain) * 2 + ((blk - 1) & 1)) * kP * NST;
+        uint64_t* mine = prm.slots + (static_cast<size_t>(chain) * 2 + (blk & 1)) * kP * NST;
+        const uint32_t want = state_tag(prm.epoch, blk - 1);
+        const uint32_t mine_tag = state_tag(prm.epoch, blk);
+        const size_t fs_base = static_cast<size_t>(chain) * kP * NST;
+        const int n0 = quarter * 32 + lane;
+        // Slot layout [p/2][n][2] of 64-bit words: this thread's 32 words (rows
+        // p = 32*half .. +31 of column n) come as 16 pairs of adjacent words.
+        uint64_t w[32];
+        auto load_words = [&](int mt) {
+            const int n = n0 + 128 * mt;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                ptx::ld_relaxed_2xb64(prev + (static_cast<size_t>(16 * half + i) * NST + n) * 2, w[2 * i], w[2 * i + 1]);
+        };
 
         // (a) the previous head's y store must have read its staging tile
         if (it > 0) {
@@ -280,11 +319,11 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
             o.w = pack_bf16x2(f3.x * w, f3.y * w);
             *reinterpret_cast<uint4*>(slot_base + K::SW + chunk * 16) = o;
         }
-        if (stid < 192) {
-            // q = 1: s < 32 (stid 0..31); q = 2: s < 64 (32..95); q = 3: s < 96 (96..191)
-            const int q = stid < 32 ? 1 : (stid < 96 ? 2 : 3);
-            const int s = stid - (q == 1 ? 0 : (q == 2 ? 32 : 96));
-            vt[q * kT + s] = __expf(cs[32 * q] - cs[s]) * dts[s];
+        // v_q(s) = e^{cs_{32q} - cs_s} dt_s for s < 32q + 32: 32 + 64 + 96 + 128 = 320 entries
+        for (int idx = stid; idx < 320; idx += 256) {
+            const int q = idx < 32 ? 0 : (idx < 96 ? 1 : (idx < 192 ? 2 : 3));
+            const int s = idx - (q == 0 ? 0 : (q == 1 ? 32 : (q == 2 ? 96 : 192)));
+            vt[q * kT + s] = __expf(fminf(cs[32 * q] - cs[s], kMaxFactorLog)) * dts[s];
         }
         ptx::fence_proxy_async_smem();
         ptx::named_sync(1 + slot, 256);
@@ -292,35 +331,47 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
         // (c) k3: S^T = B^T . W  (M = n, N = p, K = t; both MN-major)
         if (leader) {
             ptx::tc_fence_after();
+            const uint64_t dsc_b_mn = ptx::desc_sw128(sbase + K::OFF_B, kTile, 1024);  // B^T, MN-major
+            const uint64_t dsc_w = ptx::desc_sw128(slot_addr + K::SW, kTile, 1024);   // W, MN-major
 #pragma unroll
             for (int mt = 0; mt < NST / 128; ++mt) {
 #pragma unroll
-                for (int k = 0; k < kT / 16; ++k) {
-                    const uint64_t da = ptx::desc_sw128(sbase + K::OFF_B + 2 * mt * kTile + k * 2048, kTile, 1024);
-                    const uint64_t db = ptx::desc_sw128(slot_addr + K::SW + k * 2048, kTile, 1024);
-                    ptx::mma_bf16(tmem + K::col_s(slot) + 64 * mt, da, db, IDESC_S, k > 0);
-                }
+                for (int k = 0; k < kT / 16; ++k)
+                    ptx::mma_bf16(tmem + K::col_s(slot) + 64 * mt, dsc_b_mn + ((2 * mt * kTile) >> 4) + mnmaj(k),
+                                  dsc_w + mnmaj(k), IDESC_S, k > 0);
             }
             ptx::mma_commit(bar_s);
         }
 
-        // (d) k5a mask from CB: rows t = 32*quarter + lane, columns 64*half .. +63
+        // (d) k5a mask from CB: rows t = 32*quarter + lane, columns 64*half .. +63.
+        // Row quarter q = `quarter` uses the reference row r = 32q:
+        //   e^{cs_t - cs_s} dt_s = u_t v_q(s),  u_t = e^{cs_t - cs_r} <= 1,  v_q(s) = e^{cs_r - cs_s} dt_s.
+        // "Factored" quarters (decay across the quarter <= kMaxFactorLog) store
+        // M'[t][s] = CB v_q(s) (+ D/u_t on the diagonal) and the epilogue scales the
+        // row by u_t; other quarters store the exact M (u_t applied here, per entry).
         if (it == 0) wait_local(&bars[1], 0, prm.status);
         ptx::tc_fence_after();
         {
             const int t = quarter * 32 + lane;
             const float cs_t = cs[t];
-            const float D_h = prm.D ? prm.D[h] : 0.f;
-            const float u_t = __expf(cs_t - cs[32 * quarter]);
+            const float cs_r = cs[32 * quarter];
+            const bool factored = (cs_r - cs[32 * quarter + 31]) <= kMaxFactorLog;  // warp-uniform
+            const float D_h = tD[j];
+            const float u_t = __expf(cs_t - cs_r);
             const float* vq = vt + quarter * kT;
             uint8_t* mblk = slot_base + K::SM + half * kTile;
+            // strictly-upper tiles stay zero once written, unless sM is reused for sH
+            const bool write_zeros = (K::SH == K::SM) || it == 0;
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const int k = 2 * half + kk;  // 32-column tile index along s
                 if (k > quarter) {
-                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    if (write_zeros) {
+                        const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) *reinterpret_cast<uint4*>(mblk + ptx::swz128(t, kk * 4 + jj)) = z;
+                        for (int jj = 0; jj < 4; ++jj)
+                            *reinterpret_cast<uint4*>(mblk + ptx::swz128(t, kk * 4 + jj)) = z;
+                    }
                     continue;
                 }
                 uint32_t r[32];
@@ -328,24 +379,46 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
                 ptx::tmem_wait_ld(r);
                 uint32_t pk[16];
                 if (k < quarter) {
+                    const float sc = factored ? 1.f : u_t;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int s = 32 * k + 2 * e;
-                        pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * u_t * vq[s],
-                                            __uint_as_float(r[2 * e + 1]) * u_t * vq[s + 1]);
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 v4 = *reinterpret_cast<const float4*>(vq + 32 * k + 4 * e4);
+                        pk[2 * e4] = pack_bf16x2(__uint_as_float(r[4 * e4]) * (sc * v4.x),
+                                                 __uint_as_float(r[4 * e4 + 1]) * (sc * v4.y));
+                        pk[2 * e4 + 1] = pack_bf16x2(__uint_as_float(r[4 * e4 + 2]) * (sc * v4.z),
+                                                     __uint_as_float(r[4 * e4 + 3]) * (sc * v4.w));
+                    }
+                } else if (factored) {
+                    // diagonal tile, factored: causal select, D/u_t on the diagonal
+                    const float d_over_u = D_h / u_t;
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 v4 = *reinterpret_cast<const float4*>(vq + 32 * k + 4 * e4);
+                        const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+                        float m4[4];
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            const int c = 4 * e4 + q2;  // column inside the tile; the row is `lane`
+                            const float m = __uint_as_float(r[c]) * vv[q2];
+                            m4[q2] = c < lane ? m : (c == lane ? m + d_over_u : 0.f);
+                        }
+                        pk[2 * e4] = pack_bf16x2(m4[0], m4[1]);
+                        pk[2 * e4 + 1] = pack_bf16x2(m4[2], m4[3]);
                     }
                 } else {
+                    // diagonal tile, exact: decay below the diagonal, D on it, zeros above
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         float m2[2];
 #pragma unroll
                         for (int q2 = 0; q2 < 2; ++q2) {
-                            const int s = 32 * k + 2 * e + q2;
-                            const float cb = __uint_as_float(r[2 * e + q2]);
-                            float m = 0.f;
-                            if (s < t) m = cb * __expf(cs_t - cs[s]) * dts[s];
-                            else if (s == t) m = cb * dts[s] + D_h;
-                            m2[q2] = m;
+                            const int c = 2 * e + q2;
+                            const int s = 32 * k + c;
+                            const float cb = __uint_as_float(r[c]);
+                            const float decay = __expf(fminf(cs_t - cs[s], 0.f));
+                            const float below = cb * decay * dts[s];
+                            const float diag = fmaf(cb, dts[s], D_h);
+                            m2[q2] = c < lane ? below : (c == lane ? diag : 0.f);
                         }
                         pk[e] = pack_bf16x2(m2[0], m2[1]);
                     }
@@ -363,50 +436,23 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
         // (e) k5a: Yd = M . X  (M = t, N = p, K = s; A K-major, B MN-major)
         if (leader) {
             ptx::tc_fence_after();
+            const uint64_t dsc_m = ptx::desc_sw128(slot_addr + K::SM, 16, 1024);     // M, K-major
+            const uint64_t dsc_x = ptx::desc_sw128(slot_addr + K::SX, kTile, 1024);  // X, MN-major
 #pragma unroll
-            for (int k = 0; k < kT / 16; ++k) {
-                const uint64_t da =
-                    ptx::desc_sw128(slot_addr + K::SM + (k >> 2) * kTile + (k & 3) * 32, 16, 1024);
-                const uint64_t db = ptx::desc_sw128(slot_addr + K::SX + k * 2048, kTile, 1024);
-                ptx::mma_bf16(tmem + K::col_d(slot), da, db, IDESC_D, k > 0);
-            }
+            for (int k = 0; k < kT / 16; ++k)
+                ptx::mma_bf16(tmem + K::col_d(slot), dsc_m + kmaj(k), dsc_x + mnmaj(k), IDESC_D, k > 0);
             ptx::mma_commit(bar_d);
         }
 
-        // (f) k4: chained state passing for chain (b, h). Thread (quarter, half)
-        // owns state rows n = 32*quarter + lane (+128 per tile), columns p = 32*half .. +31.
-        const int chain = b * prm.H + h;
-        if (leader) {
-            int abort = 0;
-            if (blk > 0) {
-                const uint32_t* pf = prm.flags + chain * 2 + ((blk - 1) & 1);
-                const uint32_t want = static_cast<uint32_t>(blk);
-                uint32_t v = ptx::ld_acquire_gpu(pf);
-                if (v != want) {
-                    const uint64_t t_start = ptx::globaltimer_ns();
-                    while (v != want && v != kPoison) {
-                        if (ptx::globaltimer_ns() - t_start > prm.chain_wait_ns) break;
-                        __nanosleep(64);
-                        v = ptx::ld_acquire_gpu(pf);
-                    }
-                }
-                abort = (v != want);
-            }
-            sInfo[1 + slot] = abort;
-        }
-        ptx::named_sync(1 + slot, 256);
-        const bool chain_ok = (sInfo[1 + slot] == 0);
+        // (f) k4: s_in from the previous block (tagged words: each 64-bit word
+        // holds a value and the tag of the block that wrote it, so a word with
+        // the expected tag is valid by itself; no flag or fence is needed),
+        // s_out = e^{cs_end} s_in + S published the same way, s_in^T to sH in bf16.
+        bool my_ok = true;
         {
-            const int n0 = quarter * 32 + lane;
-            const float* prev = prm.slots + (static_cast<size_t>(chain) * 2 + ((blk - 1) & 1)) * kP * NST;
-            float* mine = prm.slots + (static_cast<size_t>(chain) * 2 + (blk & 1)) * kP * NST;
             const float a_blk = tEt[j * kT + kT - 1];  // e^{cs_end}
             const bool last = (blk == prm.nblk - 1);
-            const size_t fs_base = static_cast<size_t>(chain) * kP * NST;
-            wait_local(bar_s, ph, prm.status);
-            if (NST != 128) wait_local(bar_d, ph, prm.status);  // sH shares sM with k5a's operand
-            ptx::tc_fence_after();
-#pragma unroll
+#pragma unroll 1
             for (int mt = 0; mt < NST / 128; ++mt) {
                 const int n = n0 + 128 * mt;
                 float hin[32];
@@ -416,44 +462,59 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
                         const int p = half * 32 + jj;
                         hin[jj] = prm.init ? prm.init[fs_base + static_cast<size_t>(p) * NST + n] : 0.f;
                     }
-                } else if (chain_ok) {
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const int p4 = half * 8 + j4;
-                        const float4 v =
-                            __ldcg(reinterpret_cast<const float4*>(prev + (static_cast<size_t>(p4) * NST + n) * 4));
-                        hin[4 * j4 + 0] = v.x;
-                        hin[4 * j4 + 1] = v.y;
-                        hin[4 * j4 + 2] = v.z;
-                        hin[4 * j4 + 3] = v.w;
-                    }
                 } else {
+                    load_words(mt);
+                    uint32_t missing = 0;
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) hin[jj] = 0.f;
+                    for (int jj = 0; jj < 32; ++jj)
+                        if (static_cast<uint32_t>(w[jj] >> 32) != want) missing |= 1u << jj;
+                    if (missing) {
+                        // the previous block is still writing (or failed): poll the missing
+                        // words until they carry the expected tag, a poison tag, or time runs out
+                        const uint64_t t_start = ptx::globaltimer_ns();
+                        bool poisoned = false;
+                        while (missing && !poisoned) {
+                            if (ptx::globaltimer_ns() - t_start > prm.chain_wait_ns) break;
+                            __nanosleep(32);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                if (missing & (3u << (2 * i))) {
+                                    ptx::ld_relaxed_2xb64(prev + (static_cast<size_t>(16 * half + i) * NST + n) * 2,
+                                                          w[2 * i], w[2 * i + 1]);
+#pragma unroll
+                                    for (int e = 0; e < 2; ++e) {
+                                        const uint32_t tg = static_cast<uint32_t>(w[2 * i + e] >> 32);
+                                        if (tg == want) missing &= ~(1u << (2 * i + e));
+                                        poisoned |= (tg == kPoison);
+                                    }
+                                }
+                            }
+                        }
+                        if (missing) my_ok = false;
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) hin[jj] = __uint_as_float(static_cast<uint32_t>(w[jj]));
+                }
+                if (mt == 0) {
+                    wait_local(bar_s, ph, prm.status);
+                    if (K::SH == K::SM) wait_local(bar_d, ph, prm.status);  // sH shares sM with k5a's operand
+                    ptx::tc_fence_after();
                 }
                 uint32_t r[32];
                 ptx::tmem_ld32(tmem + lane_base + K::col_s(slot) + 64 * mt + half * 32, r);
                 ptx::tmem_wait_ld(r);
-                if (chain_ok) {
+                const uint64_t tag_hi = static_cast<uint64_t>(my_ok ? mine_tag : kPoison) << 32;
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        float4 o;
-                        o.x = fmaf(a_blk, hin[4 * j4 + 0], __uint_as_float(r[4 * j4 + 0]));
-                        o.y = fmaf(a_blk, hin[4 * j4 + 1], __uint_as_float(r[4 * j4 + 1]));
-                        o.z = fmaf(a_blk, hin[4 * j4 + 2], __uint_as_float(r[4 * j4 + 2]));
-                        o.w = fmaf(a_blk, hin[4 * j4 + 3], __uint_as_float(r[4 * j4 + 3]));
-                        const int p4 = half * 8 + j4;
-                        __stcg(reinterpret_cast<float4*>(mine + (static_cast<size_t>(p4) * NST + n) * 4), o);
-                        if (last && prm.final_state) {
-                            const int p = 4 * p4;
-                            prm.final_state[fs_base + static_cast<size_t>(p + 0) * NST + n] = o.x;
-                            prm.final_state[fs_base + static_cast<size_t>(p + 1) * NST + n] = o.y;
-                            prm.final_state[fs_base + static_cast<size_t>(p + 2) * NST + n] = o.z;
-                            prm.final_state[fs_base + static_cast<size_t>(p + 3) * NST + n] = o.w;
-                        }
+                for (int i = 0; i < 16; ++i) {
+                    const float o0 = fmaf(a_blk, hin[2 * i], __uint_as_float(r[2 * i]));
+                    const float o1 = fmaf(a_blk, hin[2 * i + 1], __uint_as_float(r[2 * i + 1]));
+                    ptx::st_relaxed_2xb64(mine + (static_cast<size_t>(16 * half + i) * NST + n) * 2,
+                                          tag_hi | __float_as_uint(o0), tag_hi | __float_as_uint(o1));
+                    if (last && prm.final_state) {
+                        prm.final_state[fs_base + static_cast<size_t>(32 * half + 2 * i) * NST + n] = o0;
+                        prm.final_state[fs_base + static_cast<size_t>(32 * half + 2 * i + 1) * NST + n] = o1;
                     }
                 }
-                // s_in^T in bf16 for k5b: row n of sH, columns p = 32*half .. +31 (4 chunks)
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     uint4 o;
@@ -467,40 +528,37 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
-        ptx::named_sync(1 + slot, 256);
+        const bool chain_ok = ptx::named_sync_and(1 + slot, 256, my_ok);
+        if (leader && !chain_ok) atomicOr(prm.status, 1u);
 
-        // (g) k5b: Yo = C . s_in^T  (M = t, N = p, K = n; A K-major, B MN-major), into S's columns
-        if (leader && chain_ok) {
-            ptx::tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < NST / 16; ++k) {
-                const uint64_t da = ptx::desc_sw128(sbase + K::OFF_C + (k >> 2) * kTile + (k & 3) * 32, 16, 1024);
-                const uint64_t db = ptx::desc_sw128(slot_addr + K::SH + k * 2048, kTile, 1024);
-                ptx::mma_bf16(tmem + K::col_o(slot), da, db, IDESC_O, k > 0);
-            }
-            ptx::mma_commit(bar_o);
-        }
-        // publish this block's state (the successor block of the chain waits on it)
-        __threadfence();
-        ptx::named_sync(1 + slot, 256);
+        // (g) leader: k5b Yo = C . s_in^T (M = t, N = p, K = n; A K-major, B MN-major)
+        // into S's columns; refill sX for the slot's next head once k5a has read it.
         if (leader) {
-            ptx::st_release_gpu(prm.flags + chain * 2 + (blk & 1),
-                                chain_ok ? static_cast<uint32_t>(blk + 1) : kPoison);
-            if (!chain_ok) atomicOr(prm.status, 1u);
+            if (chain_ok) {
+                ptx::tc_fence_after();
+                const uint64_t dsc_c_k = ptx::desc_sw128(sbase + K::OFF_C, 16, 1024);     // C, K-major
+                const uint64_t dsc_h = ptx::desc_sw128(slot_addr + K::SH, kTile, 1024);  // s_in^T, MN-major
+#pragma unroll
+                for (int k = 0; k < NST / 16; ++k)
+                    ptx::mma_bf16(tmem + K::col_o(slot), dsc_c_k + kmaj(k), dsc_h + mnmaj(k), IDESC_O, k > 0);
+                ptx::mma_commit(bar_o);
+            }
+            wait_local(bar_d, ph, prm.status);
+            if (j + K::SLOTS < hpu) {
+                ptx::mbar_arrive_expect_tx(bar_x, kTile);
+                ptx::tma_load_4d(slot_base + K::SX, &tm_x, bar_x, 0, h + K::SLOTS, t0, b);
+            }
         }
 
-        // (h) epilogue: y = e^{cs_t} Yo + Yd, staged in sY and stored by TMA
+        // (h) epilogue: y = e^{cs_t} Yo + u_t Yd' (u_t = 1 for exact quarters), staged in sY, TMA store
         wait_local(bar_d, ph, prm.status);
-        if (leader && j + K::SLOTS < hpu) {
-            // sX is free once k5a has read it: prefetch the slot's next head
-            ptx::mbar_arrive_expect_tx(bar_x, kTile);
-            ptx::tma_load_4d(slot_base + K::SX, &tm_x, bar_x, 0, h + K::SLOTS, t0, b);
-        }
         if (chain_ok) {
             wait_local(bar_o, ph, prm.status);
             ptx::tc_fence_after();
             const int t = quarter * 32 + lane;
             const float e_t = tEt[j * kT + t];
+            const float cs_r = cs[32 * quarter];
+            const float u_eff = (cs_r - cs[32 * quarter + 31]) <= kMaxFactorLog ? __expf(cs[t] - cs_r) : 1.f;
             uint32_t ro[32], rd[32];
             ptx::tmem_ld32(tmem + lane_base + K::col_o(slot) + half * 32, ro);
             ptx::tmem_ld32(tmem + lane_base + K::col_d(slot) + half * 32, rd);
@@ -512,8 +570,8 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c0 = 8 * jj + 2 * e;
-                    pk[e] = pack_bf16x2(fmaf(e_t, __uint_as_float(ro[c0]), __uint_as_float(rd[c0])),
-                                        fmaf(e_t, __uint_as_float(ro[c0 + 1]), __uint_as_float(rd[c0 + 1])));
+                    pk[e] = pack_bf16x2(fmaf(e_t, __uint_as_float(ro[c0]), u_eff * __uint_as_float(rd[c0])),
+                                        fmaf(e_t, __uint_as_float(ro[c0 + 1]), u_eff * __uint_as_float(rd[c0 + 1])));
                 }
                 *reinterpret_cast<uint4*>(slot_base + K::SY + ptx::swz128(t, half * 4 + jj)) =
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -566,9 +624,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t tc_counters_bytes(const ssd_dims& d) {
-    return align_up(sizeof(uint32_t) * static_cast<size_t>(1 + 2 * d.batch * d.nheads), kWorkspaceAlign);
-}
+size_t tc_counters_bytes(const ssd_dims&) { return kWorkspaceAlign; }
+
+std::atomic<uint32_t> g_epoch{0};
 
 // Heads per unit: the largest of 8, 4, 2, 1 that divides the heads of one group.
 int heads_per_unit(const ssd_dims& d) {
@@ -598,8 +656,8 @@ ssd_status launch(const FwdArgs& a, void* ws) {
     p.init = a.init;
     p.final_state = a.final_state;
     p.ticket = static_cast<uint32_t*>(ws);
-    p.flags = p.ticket + 1;
-    p.slots = reinterpret_cast<float*>(static_cast<char*>(ws) + counters);
+    p.slots = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + counters);
+    p.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
     p.status = a.status_word;
     p.batch = static_cast<int>(d.batch);
     p.H = static_cast<int>(d.nheads);
@@ -626,13 +684,14 @@ bool tc_supported(const ssd_dims& d, ssd_dtype io, int chunk_len) {
     if (d.dstate != 128 && d.dstate != 256) return false;
     if (chunk_len != 128 && chunk_len != 256) return false;
     const long long nblk = (d.seqlen + kT - 1) / kT;
+    if (nblk >= 65535) return false;  // state tags carry the block index in 16 bits
     if (nblk * d.batch * d.nheads >= (1ll << 31)) return false;
     if (d.seqlen >= (1ll << 31) || d.batch >= (1ll << 31) || d.nheads >= (1 << 20)) return false;
     return true;
 }
 
 size_t tc_workspace_bytes(const ssd_dims& d, int /*chunk_len*/) {
-    const size_t slots = sizeof(float) * static_cast<size_t>(d.batch * d.nheads) * 2 * kP * d.dstate;
+    const size_t slots = sizeof(uint64_t) * static_cast<size_t>(d.batch * d.nheads) * 2 * kP * d.dstate;
     return tc_counters_bytes(d) + align_up(slots, kWorkspaceAlign);
 }
 

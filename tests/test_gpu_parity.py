@@ -46,6 +46,20 @@ def test_tensor_core_path_matches_oracle(shape, chunk_len):
     check_against_oracle(shape, "bf16", chunk_len, "tc", seed=sum(shape) + chunk_len)
 
 
+@pytest.mark.parametrize("dt_shift,A_scale", [(3.0, 4.0), (-2.0, 0.25), (0.0, 1.0)])
+def test_tensor_core_path_strong_and_weak_decay(dt_shift, A_scale):
+    """Heads whose decay across 32 tokens is far above (strong) or below (weak)
+    the range where the kernel stores the causal mask in factored form."""
+    inp = make_inputs(2, 520, 8, 64, 2, 128, io_dtype="bf16", init="normal", seed=41)
+    inp["dt"] = (inp["dt"] + dt_shift).astype(np.float32)
+    inp["A"] = (inp["A"] * A_scale).astype(np.float32)
+    t = to_device(inp, "bf16")
+    y, fs = run_gpu(t, 256, "tc")
+    y_ref, f_ref = oracle_full(inp)
+    assert rel_err(y.float().cpu().numpy(), y_ref) < 2e-2
+    assert rel_err(fs.cpu().numpy(), f_ref) < 2e-2
+
+
 @pytest.mark.parametrize("init,with_D", [("zero", True), ("normal", False), ("zero", False)])
 def test_tensor_core_path_optional_inputs(init, with_D):
     check_against_oracle((2, 400, 4, 64, 2, 128), "bf16", 256, "tc", init=init, with_D=with_D, seed=7)
@@ -134,7 +148,7 @@ def test_caller_workspace_and_explicit_stream():
     inp = make_inputs(2, 500, 4, 64, 1, 128, io_dtype="bf16", init="normal", seed=23)
     t = to_device(inp, "bf16")
     need = pkg.ssd_fwd_workspace_bytes(2, 500, 4, 64, 1, 128, "bf16", 256, "tc")
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         y, fs = pkg.ssd_fwd(t["x"], t["dt"], t["dt_bias"], t["A"], t["B"], t["C"], t["D"], t["init_state"],
