@@ -151,6 +151,33 @@ SSD_API uint64_t ssd_kernel_launches(void);
  * while calls that use them are in flight. */
 SSD_API void ssd_release(void);
 
+/*
+ * ssd_fwd_noalloc -- the fused tensor-core forward on a fixed scratch array
+ * compiled into the library, for callers that must not allocate device
+ * memory: code running under a memory manager that owns all of the device's
+ * memory and forbids allocations behind its back, and latency-critical loops
+ * where cudaMalloc (which may synchronise the device) is not acceptable. (The
+ * pages have no counterpart: their kernels allocate their intermediates.)
+ *
+ * Arguments, layouts and results are those of ssd_fwd; the inputs and outputs
+ * are still the caller's buffers. Only the tensor-core path runs here
+ * (SSD_ERR_UNSUPPORTED otherwise). The scratch is a 16 MiB (16777216-byte)
+ * file-scope device array; a call whose scratch need (ssd_fwd_workspace_bytes
+ * with SSD_PATH_TC) exceeds it returns SSD_ERR_WORKSPACE before launching
+ * anything: at most 127 (batch, head) chains at dstate 128, 63 at dstate 256.
+ *
+ * No cudaMalloc, cudaFree or allocating library routine is called. The first
+ * call on a device looks up the array's device address and zero-fills it,
+ * synchronously, so make that first call before any stream capture. Every call
+ * on a device shares the one array and it keeps the last call's contents (the
+ * per-call work counter is cleared by each call): calls that overlap on the
+ * GPU, on any streams, race and must not be issued.
+ */
+SSD_API ssd_status ssd_fwd_noalloc(const ssd_dims* dims, ssd_dtype io_dtype,
+                                   const void* x, const float* dt, const float* dt_bias, const float* A,
+                                   const void* B, const void* C, const float* D, const float* init_state,
+                                   int chunk_len, int ngroups, void* y, float* final_state, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

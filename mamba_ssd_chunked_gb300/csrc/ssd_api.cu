@@ -166,6 +166,34 @@ ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* d
 
 size_t elem_bytes(ssd_dtype io) { return io == SSD_F32 ? 4 : 2; }
 
+// ---- fixed scratch for ssd_fwd_noalloc
+// Some callers must not allocate device memory (see ssd_fwd_noalloc in
+// ssd.h), so that entry point runs the fused kernel on this file-scope array
+// instead of the library-owned workspace. It is part of the loaded module:
+// every device that loads the library holds these bytes until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the fixed scratch on device `dev` (which must be current).
+// The first call per device looks the address up and zero-fills the array
+// once; both are synchronous, which is why the first ssd_fwd_noalloc call on a
+// device belongs before any stream capture.
+ssd_status noalloc_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SSD_ERR_CUDA;
+        if (cudaMemset(p, 0, kNoAllocScratchBytes) != cudaSuccess) return SSD_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return SSD_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SSD_OK;
+}
+
 }  // namespace
 
 void note_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -313,6 +341,46 @@ void ssd_release(void) {
         s.dev_io_bytes = 0;
     }
     if (have_prev) cudaSetDevice(prev);
+}
+
+
+ssd_status ssd_fwd_noalloc(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, const float* dt,
+                           const float* dt_bias, const float* A, const void* B, const void* C, const float* D,
+                           const float* init_state, int chunk_len, int ngroups, void* y, float* final_state,
+                           void* stream) {
+    ssd_status st = check_dims(dims, io_dtype, chunk_len, ngroups);
+    if (st != SSD_OK) return st;
+    st = check_pointers(x, dt, dt_bias, A, B, C, D, init_state, y, final_state);
+    if (st != SSD_OK) return st;
+    if (!tc_supported(*dims, io_dtype, chunk_len)) return SSD_ERR_UNSUPPORTED;
+    if (tc_workspace_bytes(*dims, chunk_len) > kNoAllocScratchBytes) return SSD_ERR_WORKSPACE;
+    int dev = 0;
+    st = current_device(&dev);
+    if (st != SSD_OK) return st;
+    unsigned* status = nullptr;
+    st = status_word(dev, &status);
+    if (st != SSD_OK) return st;
+    void* scratch = nullptr;
+    st = noalloc_scratch(dev, &scratch);
+    if (st != SSD_OK) return st;
+    FwdArgs a;
+    a.d = *dims;
+    a.io = io_dtype;
+    a.x = x;
+    a.dt = dt;
+    a.dt_bias = dt_bias;
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.D = D;
+    a.init = init_state;
+    a.chunk_len = chunk_len;
+    a.y = y;
+    a.final_state = final_state;
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.status_word = status;
+    a.wait_limit_ns = wait_limit_ns();
+    return tc_forward(a, scratch, kNoAllocScratchBytes);
 }
 
 }  // extern "C"
