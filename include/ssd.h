@@ -164,7 +164,7 @@ SSD_API void ssd_release(void);
  * (SSD_ERR_UNSUPPORTED otherwise). The scratch is a 16 MiB (16777216-byte)
  * file-scope device array; a call whose scratch need (ssd_fwd_workspace_bytes
  * with SSD_PATH_TC) exceeds it returns SSD_ERR_WORKSPACE before launching
- * anything: at most 127 (batch, head) chains at dstate 128, 63 at dstate 256.
+ * anything: at most 255 (batch, head) chains at dstate 128, 127 at dstate 256.
  *
  * No cudaMalloc, cudaFree or allocating library routine is called. The first
  * call on a device looks up the array's device address and zero-fills it,

@@ -7,16 +7,19 @@
 // took their tickets earlier.
 //
 // Per unit the CTA loads B and C once and computes C.B^T once; its heads are
-// then processed by SLOTS warpgroup pairs ("slots", 256 threads each) that
-// take alternate heads, so one slot's waits overlap the other's work. Per
-// head the five stages of the chunked SSD (burn-mamba "mamba2/ssd/serial.rs"
-// k1..k5; fla "mamba2.py" naive chunked SSD) run as:
+// then processed by SLOTS "slots" (256 threads each) that take alternate
+// heads, so one slot's waits overlap the other's work. Helper warps keep
+// latency off the slots: one MMA warp issues every tcgen05.mma on the slots'
+// requests, and one state agent per slot moves chunk states between global
+// memory and the slot's staging buffer with bulk copies.
+// Per head the five stages of the chunked SSD (burn-mamba
+// "mamba2/ssd/serial.rs" k1..k5; fla "mamba2.py" naive chunked SSD) run as:
 //
 //   k1  dt = softplus(dt_raw + dt_bias), cs = inclusive cumsum of dt*A   (per unit, all heads)
 //   k2  CB = C . B^T                 [128 x 128, K = dstate]   once per unit, tcgen05 -> TMEM
 //   k3  S^T = B^T . diag(dt e^{cs_end-cs}) . X   [dstate x 64, K = 128]   tcgen05 -> TMEM
-//   k5a Yd = (L o CB o dt + D I) . X [128 x 64, K = 128]       mask in registers, tcgen05
-//   k4  s_out = e^{cs_end} s_in + S  fp32, chained through global slots (bounded waits)
+//   k5a Yd = (L o CB o dt + D I) . X [128 x 64, K = 128]       mask in registers -> TMEM, tcgen05
+//   k4  s_out = e^{cs_end} s_in + S  fp32, chained through global memory (flag per block)
 //   k5b Yo = C . s_in^T              [128 x 64, K = dstate]    tcgen05
 //       y  = e^{cs} o Yo + Yd        epilogue, TMA store
 //
@@ -28,7 +31,14 @@
 // whose decay exceeds kMaxFactorLog keep exact entries instead.
 // A chunk_len of 256 is computed as two consecutive 128-token blocks: the
 // decomposition is exact for any chunk boundary, and the state between the
-// two halves is passed through the same chained slots.
+// two halves is passed like any other block boundary.
+//
+// Chunk-state passing: block blk of chain (b, h) reads s_in from global slot
+// (chain, (blk-1) & 1) once flag (chain, (blk-1) & 1) reads blk, and publishes
+// s_out to slot (chain, blk & 1), then (after its bulk store completes and a
+// fence) sets that flag to blk + 1. A block only waits on an earlier ticket.
+// The state agent of each slot does the polling, the bulk copies and the
+// fence, so the slot's threads only touch shared memory.
 //
 // Operand staging (128-byte swizzle throughout; see ptx.cuh):
 //   sB [t][n]  (TMA, per unit)   B operand of k2 (K-major), A operand of k3 (MN-major)
@@ -36,9 +46,11 @@
 //   per slot:
 //   sX [t][p]  (TMA, per head)   B operand of k5a (MN-major, K = t)
 //   sW [t][p]  (threads)         dt e^{cs_end-cs} X, B operand of k3 (MN-major)
-//   sM [t][s]  (threads)         masked CB, A operand of k5a (K-major)
-//   sH [n][p]  (threads)         s_in in bf16, B operand of k5b (MN-major): in sW (dstate 128) or sM (256)
+//   sH [n][p]  (threads)         s_in in bf16, B operand of k5b (MN-major): in sW (dstate 128)
+//                                or across sX and sW (dstate 256)
 //   sY [t][p]  (threads)         y tile for the TMA store, in sW (after k5b has read sH)
+//   sT [p][n]  (bulk copies)     fp32 state staging, one 128-column tile of the state at a time
+//   TMEM: C.B^T (fp32), per slot the masked matrix M (bf16, A operand of k5a), S^T / Yo, Yd.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -55,6 +67,7 @@ constexpr int kT = 128;               // tokens per block (MMA M for k2, k5a, k5
 constexpr int kP = 64;                // headdim handled by this kernel
 constexpr int kMaxHeads = 8;          // heads per unit at most
 constexpr uint32_t kTile = kT * 128;  // one 128-row x 128-byte swizzled tile (16 KB)
+constexpr uint32_t kStateTile = kP * 128 * 4;  // fp32 state tile: 64 rows p x 128 columns n (32 KB)
 constexpr uint32_t kPoison = 0xFFFFFFFFu;
 // Limit on waits for this CTA's own TMA copies and MMAs (they complete in
 // microseconds; the limit only guards against a wedged pipeline).
@@ -66,26 +79,33 @@ constexpr float kMaxFactorLog = 60.f;
 template <int NST>
 struct Cfg {
     static constexpr int NKB = NST / 64;                    // 64-wide dstate blocks
+    static constexpr int MT = NST / 128;                    // 128-row state tiles
     static constexpr int SLOTS = (NST == 128) ? 2 : 1;
-    static constexpr int THREADS = 256 * SLOTS;
+    static constexpr int MATH_THREADS = 256 * SLOTS;        // the slots
+    static constexpr int MMA_WARP = MATH_THREADS / 32;      // then the MMA warp, then one agent per slot
+    static constexpr int THREADS = MATH_THREADS + 32 + 32 * SLOTS;
+    static constexpr int NBARS = 2 + 9 * SLOTS;
     static constexpr uint32_t OFF_B = 0;
     static constexpr uint32_t OFF_C = OFF_B + NKB * kTile;
     static constexpr uint32_t OFF_SLOT = OFF_C + NKB * kTile;
-    static constexpr uint32_t SLOT_BYTES = 4 * kTile;       // X, W, M (2 tiles)
-    static constexpr uint32_t SX = 0, SW = kTile, SM = 2 * kTile;  // offsets inside a slot
-    static constexpr uint32_t SH = (NST == 128) ? SW : SM;
+    static constexpr uint32_t SLOT_BYTES = 2 * kTile + kStateTile;  // X, W, state tile
+    static constexpr uint32_t SX = 0, SW = kTile, ST = 2 * kTile;   // offsets inside a slot
+    static constexpr uint32_t SH = (NST == 128) ? SW : SX;          // dstate 256: sH spans sX and sW
     static constexpr uint32_t SY = SW;
     static constexpr uint32_t OFF_MISC = OFF_SLOT + SLOTS * SLOT_BYTES;
     // misc: 4 per-head tables [kMaxHeads][128] floats, per-slot v tables [4][128], scan totals
     static constexpr uint32_t TAB_BYTES = 4 * kMaxHeads * kT * 4;
     static constexpr uint32_t V_BYTES = SLOTS * 4 * kT * 4;
-    static constexpr uint32_t MISC_BYTES = TAB_BYTES + V_BYTES + 512 + 256;
+    static constexpr uint32_t MISC_BYTES = TAB_BYTES + V_BYTES + 512 + 512;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_CB = 0;
-    __host__ __device__ static constexpr uint32_t col_s(int slot) { return 128 + 128 * slot; }
-    __host__ __device__ static constexpr uint32_t col_d(int slot) { return NST == 128 ? 192 + 128 * slot : 256; }
+    // per slot: M (64 packed bf16 columns), S^T (64 per state tile; Yo reuses it), Yd (64)
+    __host__ __device__ static constexpr uint32_t col_m(int slot) { return 128 + (128 + 64 * MT) * slot; }
+    __host__ __device__ static constexpr uint32_t col_s(int slot) { return col_m(slot) + 64; }
+    __host__ __device__ static constexpr uint32_t col_d(int slot) { return col_s(slot) + 64 * MT; }
     __host__ __device__ static constexpr uint32_t col_o(int slot) { return col_s(slot); }
+    static_assert(col_d(SLOTS - 1) + 64 <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(NST == 128 || SLOTS == 1, "one slot for dstate 256");
 };
@@ -97,20 +117,14 @@ struct TcParams {
     const float* D;
     const float* init;
     float* final_state;
-    uint64_t* slots;       // [batch*H][2][P/2][NST][2] chained states: fp32 value | tag << 32
+    float* slots;          // [batch*H][2][MT][P][128] fp32 chained states
+    uint32_t* flags;       // [batch*H][2]: block index + 1 of the state in the slot (kPoison: failed)
     uint32_t* ticket;      // block-major work counter
-    uint32_t epoch;        // per-call tag component
     uint32_t* status;      // device status word
     int batch, H, G, nblk, hpu, ngrp;  // hpu heads per unit, ngrp = H / hpu head groups
     long long L;
     unsigned long long chain_wait_ns;  // limit on waiting for the previous block's state
 };
-
-// Tag of the state block `blk` publishes in call `epoch`: never 0 (so zeroed
-// memory never matches) and never kPoison, for blk < 65535.
-__device__ __forceinline__ uint32_t state_tag(uint32_t epoch, int blk) {
-    return ((epoch % 65535u + 1u) << 16) | static_cast<uint32_t>((blk + 1) & 0xFFFF);
-}
 
 __device__ __forceinline__ float softplus_f(float v) {
     return v > 0.f ? v + log1pf(expf(-v)) : log1pf(expf(v));
@@ -148,20 +162,22 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
     float* tTot = tV + K::SLOTS * 4 * kT;                       // [head][4] scan totals
     float* tD = tTot + kMaxHeads * 4;                           // [head] D
     uint64_t* bars = reinterpret_cast<uint64_t*>(tTot + kMaxHeads * 4 + 32);
-    static_assert(kMaxHeads * 4 + kMaxHeads <= kMaxHeads * 4 + 32, "tD fits before the barriers");
-    // bars: [0] B/C, [1] CB, then per slot s: [2+4s] X, [3+4s] S, [4+4s] D, [5+4s] O
-    uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 + 4 * K::SLOTS);
-    int* sInfo = reinterpret_cast<int*>(sTmem + 1);             // [0] unit, [1+s] chain abort of slot s
+    // bars: [0] B/C landed, [1] CB done; per slot s at 2 + 9s: X landed, S done, Yd done, Yo done,
+    // requests to the MMA warp (W ready: k3, M ready: k5a, s_in ready: k5b), state tile landed
+    // (agent -> slot), state tile staged (slot -> agent)
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + K::NBARS);
+    int* sInfo = reinterpret_cast<int*>(sTmem + 1);  // [0] unit, [1+s] skip k5b, [3+s] chain failed
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slot = tid >> 8, stid = tid & 255, swarp = stid >> 5;
+    const bool is_math = tid < K::MATH_THREADS;
+    const int slot = is_math ? (tid >> 8) : 0, stid = tid & 255, swarp = stid >> 5;
     const int quarter = warp & 3, half = swarp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
 
     if (tid == 0) {
         sInfo[0] = static_cast<int>(atomicAdd(prm.ticket, 1u));
 #pragma unroll
-        for (int i = 0; i < 2 + 4 * K::SLOTS; ++i) ptx::mbar_init(&bars[i], 1);
+        for (int i = 0; i < K::NBARS; ++i) ptx::mbar_init(&bars[i], 1);
         ptx::fence_mbar_init();
     }
     if (warp == 0) {
@@ -181,14 +197,20 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
     const int t0 = blk * kT;
     const long long L = prm.L;
     const int hpu = prm.hpu;
+    const bool last_blk = (blk == prm.nblk - 1);
     const uint32_t sbase = ptx::smem_u32(smem);
     uint8_t* slot_base = smem + K::OFF_SLOT + slot * K::SLOT_BYTES;
-    const uint32_t slot_addr = sbase + K::OFF_SLOT + slot * K::SLOT_BYTES;
-    uint64_t* bar_x = &bars[2 + 4 * slot];
-    uint64_t* bar_s = &bars[3 + 4 * slot];
-    uint64_t* bar_d = &bars[4 + 4 * slot];
-    uint64_t* bar_o = &bars[5 + 4 * slot];
-    const bool leader = (stid == 0);
+    auto bar_of = [&](int sl, int k) { return &bars[2 + 9 * sl + k]; };
+    uint64_t* bar_x = bar_of(slot, 0);
+    uint64_t* bar_s = bar_of(slot, 1);
+    uint64_t* bar_d = bar_of(slot, 2);
+    uint64_t* bar_o = bar_of(slot, 3);
+    uint64_t* req_s = bar_of(slot, 4);
+    uint64_t* req_d = bar_of(slot, 5);
+    uint64_t* req_o = bar_of(slot, 6);
+    uint64_t* bar_st = bar_of(slot, 7);
+    uint64_t* bar_pub = bar_of(slot, 8);
+    const bool leader = is_math && stid == 0;
 
     // ---- TMA: B and C for the unit; X for each slot's first head
     if (tid == 0) {
@@ -239,58 +261,193 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
     }
     __syncthreads();
 
-    // ---- k2: CB = C . B^T once per unit (M = t, N = s, K = n; both K-major)
     constexpr uint32_t IDESC_CB = ptx::idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 64, true, true);
     constexpr uint32_t IDESC_D = ptx::idesc_bf16_f32(128, 64, false, true);
     constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(128, 64, false, true);
-    if (tid == 0) {
-        wait_local(&bars[0], 0, prm.status);
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < NST / 16; ++k) {
-            const uint32_t koff = (k >> 2) * kTile + (k & 3) * 32;
-            const uint64_t da = ptx::desc_sw128(sbase + K::OFF_C + koff, 16, 1024);
-            const uint64_t db = ptx::desc_sw128(sbase + K::OFF_B + koff, 16, 1024);
-            ptx::mma_bf16(tmem + K::COL_CB, da, db, IDESC_CB, k > 0);
-        }
-        ptx::mma_commit(&bars[1]);
-    }
-
     // Matrix descriptors are built once per issue from the operand base; a K
     // step adds its byte offset to the start-address field (offsets stay far
     // below the field's range).
     auto kmaj = [](int k) { return static_cast<uint64_t>(((k >> 2) * kTile + (k & 3) * 32) >> 4); };
     auto mnmaj = [](int k) { return static_cast<uint64_t>((k * 2048) >> 4); };
+    auto heads_of = [&](int sl) { return sl < hpu ? (hpu - sl + K::SLOTS - 1) / K::SLOTS : 0; };
+
+    if (warp == K::MMA_WARP) {
+        // ---- the MMA warp: k2 once, then k3 / k5a / k5b for each head on the slots' requests
+        if (lane == 0) {
+            wait_local(&bars[0], 0, prm.status);
+            ptx::tc_fence_after();
+            const uint64_t dsc_c_k = ptx::desc_sw128(sbase + K::OFF_C, 16, 1024);     // C, K-major
+            const uint64_t dsc_b_k = ptx::desc_sw128(sbase + K::OFF_B, 16, 1024);     // B, K-major
+            const uint64_t dsc_b_mn = ptx::desc_sw128(sbase + K::OFF_B, kTile, 1024);  // B^T, MN-major
+#pragma unroll
+            for (int k = 0; k < NST / 16; ++k)
+                ptx::mma_bf16(tmem + K::COL_CB, dsc_c_k + kmaj(k), dsc_b_k + kmaj(k), IDESC_CB, k > 0);
+            ptx::mma_commit(&bars[1]);
+            // Requests arrive per slot in the order k3, k5a, k5b for each of the slot's heads.
+            int nh[K::SLOTS], done[K::SLOTS], stage[K::SLOTS];
+            int pending = 0;
+#pragma unroll
+            for (int sl = 0; sl < K::SLOTS; ++sl) {
+                nh[sl] = heads_of(sl);
+                done[sl] = 0;
+                stage[sl] = 0;
+                pending += 3 * nh[sl];
+            }
+            uint64_t idle_since = ptx::globaltimer_ns();
+            while (pending > 0) {
+                bool progressed = false;
+#pragma unroll
+                for (int sl = 0; sl < K::SLOTS; ++sl) {
+                    if (done[sl] >= nh[sl]) continue;
+                    if (!ptx::mbar_test_wait(bar_of(sl, 4 + stage[sl]), done[sl] & 1)) continue;
+                    ptx::tc_fence_after();
+                    const uint32_t saddr = sbase + K::OFF_SLOT + sl * K::SLOT_BYTES;
+                    if (stage[sl] == 0) {
+                        // k3: S^T = B^T . W  (M = n, N = p, K = t; both MN-major)
+                        const uint64_t dsc_w = ptx::desc_sw128(saddr + K::SW, kTile, 1024);
+#pragma unroll
+                        for (int mt = 0; mt < K::MT; ++mt)
+#pragma unroll
+                            for (int k = 0; k < kT / 16; ++k)
+                                ptx::mma_bf16(tmem + K::col_s(sl) + 64 * mt,
+                                              dsc_b_mn + ((2 * mt * kTile) >> 4) + mnmaj(k), dsc_w + mnmaj(k),
+                                              IDESC_S, k > 0);
+                        ptx::mma_commit(bar_of(sl, 1));
+                    } else if (stage[sl] == 1) {
+                        // k5a: Yd = M . X  (M = t, N = p, K = s; A from TMEM, B MN-major)
+                        const uint64_t dsc_x = ptx::desc_sw128(saddr + K::SX, kTile, 1024);
+#pragma unroll
+                        for (int k = 0; k < kT / 16; ++k)
+                            ptx::mma_bf16_ta(tmem + K::col_d(sl), tmem + K::col_m(sl) + 8 * k, dsc_x + mnmaj(k),
+                                             IDESC_D, k > 0);
+                        ptx::mma_commit(bar_of(sl, 2));
+                    } else {
+                        // k5b: Yo = C . s_in^T  (M = t, N = p, K = n; A K-major, B MN-major), into S's columns
+                        if (!sInfo[1 + sl]) {
+                            const uint64_t dsc_h = ptx::desc_sw128(saddr + K::SH, kTile, 1024);
+#pragma unroll
+                            for (int k = 0; k < NST / 16; ++k)
+                                ptx::mma_bf16(tmem + K::col_o(sl), dsc_c_k + kmaj(k), dsc_h + mnmaj(k), IDESC_O,
+                                              k > 0);
+                        }
+                        ptx::mma_commit(bar_of(sl, 3));
+                    }
+                    if (++stage[sl] == 3) {
+                        stage[sl] = 0;
+                        ++done[sl];
+                    }
+                    --pending;
+                    progressed = true;
+                }
+                const uint64_t now = ptx::globaltimer_ns();
+                if (progressed) {
+                    idle_since = now;
+                } else if (now - idle_since > 2 * kLocalWaitNs) {
+                    atomicOr(prm.status, 2u);  // a slot stopped requesting: give up
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (!is_math) {
+        // ---- state agent of slot `sl`: fetch s_in tiles, publish s_out tiles and the block's flag
+        const int sl = warp - K::MMA_WARP - 1;
+        if (lane == 0) {
+            uint8_t* st_buf = smem + K::OFF_SLOT + sl * K::SLOT_BYTES + K::ST;
+            uint64_t* a_st = bar_of(sl, 7);
+            uint64_t* a_pub = bar_of(sl, 8);
+            uint32_t ph_pub = 0;
+            const int nh = heads_of(sl);
+            for (int q = 0; q < nh; ++q) {
+                const int h = h0 + sl + q * K::SLOTS;
+                const int chain = b * prm.H + h;
+                bool fail = false;
+                if (blk > 0) {
+                    const uint32_t* pf = prm.flags + chain * 2 + ((blk - 1) & 1);
+                    const uint32_t want = static_cast<uint32_t>(blk);
+                    uint32_t v = ptx::ld_relaxed_gpu(pf);
+                    if (v != want) {
+                        const uint64_t t_start = ptx::globaltimer_ns();
+                        while (v != want && v != kPoison) {
+                            if (ptx::globaltimer_ns() - t_start > prm.chain_wait_ns) break;
+                            __nanosleep(64);
+                            v = ptx::ld_relaxed_gpu(pf);
+                        }
+                    }
+                    fail = (v != want);
+                    if (!fail) {
+                        ptx::fence_acquire_gpu();
+                        ptx::fence_proxy_async_global();  // the bulk loads below read what the flag guards
+                    }
+                }
+                sInfo[3 + sl] = fail ? 1 : 0;
+                const float* prev =
+                    prm.slots + (static_cast<size_t>(chain) * 2 + ((blk - 1) & 1)) * K::MT * (kStateTile / 4);
+                float* mine = prm.slots + (static_cast<size_t>(chain) * 2 + (blk & 1)) * K::MT * (kStateTile / 4);
+                const size_t fs_base = static_cast<size_t>(chain) * kP * NST;
+#pragma unroll 1
+                for (int mt = 0; mt < K::MT; ++mt) {
+                    // fetch s_in tile mt into the staging buffer
+                    if (fail || (blk == 0 && !prm.init)) {
+                        ptx::mbar_arrive(a_st);  // nothing to load: the slot uses zeros (or gives up)
+                    } else if (blk == 0) {
+                        ptx::mbar_arrive_expect_tx(a_st, kStateTile);
+                        if (K::MT == 1) {
+                            ptx::bulk_load(st_buf, prm.init + fs_base, kStateTile, a_st);
+                        } else {
+                            for (int p = 0; p < kP; ++p)
+                                ptx::bulk_load(st_buf + p * 512,
+                                               prm.init + fs_base + static_cast<size_t>(p) * NST + 128 * mt, 512, a_st);
+                        }
+                    } else {
+                        ptx::mbar_arrive_expect_tx(a_st, kStateTile);
+                        ptx::bulk_load(st_buf, prev + static_cast<size_t>(mt) * (kStateTile / 4), kStateTile, a_st);
+                    }
+                    // the slot stages s_out tile mt in place; write it out
+                    wait_local(a_pub, ph_pub, prm.status);
+                    ph_pub ^= 1;
+                    if (!fail) {
+                        if (!last_blk) {
+                            ptx::bulk_store(mine + static_cast<size_t>(mt) * (kStateTile / 4), st_buf, kStateTile);
+                        } else if (prm.final_state) {
+                            if (K::MT == 1) {
+                                ptx::bulk_store(prm.final_state + fs_base, st_buf, kStateTile);
+                            } else {
+                                for (int p = 0; p < kP; ++p)
+                                    ptx::bulk_store(prm.final_state + fs_base + static_cast<size_t>(p) * NST + 128 * mt,
+                                                    st_buf + p * 512, 512);
+                            }
+                        }
+                        ptx::bulk_commit_group();
+                        ptx::bulk_wait_group_read0();  // the staging buffer may be refilled
+                    }
+                }
+                // the state is in global memory before the flag says so
+                ptx::bulk_wait_group0();
+                if (!last_blk) {
+                    ptx::fence_proxy_async_global();
+                    __threadfence();
+                    ptx::st_relaxed_gpu(prm.flags + chain * 2 + (blk & 1),
+                                        fail ? kPoison : static_cast<uint32_t>(blk + 1));
+                }
+                if (fail) atomicOr(prm.status, 1u);
+            }
+        }
+        __syncwarp();
+    }
 
     // ---- per-slot head loop
     bool b_ready = false;  // this thread has seen B/C land
     int it = 0;
-    for (int j = slot; j < hpu; j += K::SLOTS, ++it) {
+    for (int j = slot; is_math && j < hpu; j += K::SLOTS, ++it) {
         const int h = h0 + j;
         const uint32_t ph = it & 1;
         const float* cs = tCs + j * kT;
         const float* dts = tDt + j * kT;
         const float* wts = tWt + j * kT;
         float* vt = tV + slot * 4 * kT;
-        // k4 bookkeeping for chain (b, h). Thread (quarter, half) owns state rows
-        // n = 32*quarter + lane (+128 per tile) and columns p = 32*half .. +31.
-        const int chain = b * prm.H + h;
-        const uint64_t* prev = prm.slots + (static_cast<size_t>(chain) * 2 + ((blk - 1) & 1)) * kP * NST;
-        uint64_t* mine = prm.slots + (static_cast<size_t>(chain) * 2 + (blk & 1)) * kP * NST;
-        const uint32_t want = state_tag(prm.epoch, blk - 1);
-        const uint32_t mine_tag = state_tag(prm.epoch, blk);
-        const size_t fs_base = static_cast<size_t>(chain) * kP * NST;
-        const int n0 = quarter * 32 + lane;
-        // Slot layout [p/2][n][2] of 64-bit words: this thread's 32 words (rows
-        // p = 32*half .. +31 of column n) come as 16 pairs of adjacent words.
-        uint64_t w[32];
-        auto load_words = [&](int mt) {
-            const int n = n0 + 128 * mt;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                ptx::ld_relaxed_2xb64(prev + (static_cast<size_t>(16 * half + i) * NST + n) * 2, w[2 * i], w[2 * i + 1]);
-        };
+        float* st_buf = reinterpret_cast<float*>(slot_base + K::ST);
 
         // (a) the previous head's y store must have read its staging tile
         if (it > 0) {
@@ -328,22 +485,10 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
         ptx::fence_proxy_async_smem();
         ptx::named_sync(1 + slot, 256);
 
-        // (c) k3: S^T = B^T . W  (M = n, N = p, K = t; both MN-major)
-        if (leader) {
-            ptx::tc_fence_after();
-            const uint64_t dsc_b_mn = ptx::desc_sw128(sbase + K::OFF_B, kTile, 1024);  // B^T, MN-major
-            const uint64_t dsc_w = ptx::desc_sw128(slot_addr + K::SW, kTile, 1024);   // W, MN-major
-#pragma unroll
-            for (int mt = 0; mt < NST / 128; ++mt) {
-#pragma unroll
-                for (int k = 0; k < kT / 16; ++k)
-                    ptx::mma_bf16(tmem + K::col_s(slot) + 64 * mt, dsc_b_mn + ((2 * mt * kTile) >> 4) + mnmaj(k),
-                                  dsc_w + mnmaj(k), IDESC_S, k > 0);
-            }
-            ptx::mma_commit(bar_s);
-        }
+        // (c) k3 is issued by the MMA warp
+        if (leader) ptx::mbar_arrive(req_s);
 
-        // (d) k5a mask from CB: rows t = 32*quarter + lane, columns 64*half .. +63.
+        // (d) k5a mask from CB: rows t = 32*quarter + lane, columns 64*half .. +63, into TMEM.
         // Row quarter q = `quarter` uses the reference row r = 32q:
         //   e^{cs_t - cs_s} dt_s = u_t v_q(s),  u_t = e^{cs_t - cs_r} <= 1,  v_q(s) = e^{cs_r - cs_s} dt_s.
         // "Factored" quarters (decay across the quarter <= kMaxFactorLog) store
@@ -359,34 +504,27 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
             const float D_h = tD[j];
             const float u_t = __expf(cs_t - cs_r);
             const float* vq = vt + quarter * kT;
-            uint8_t* mblk = slot_base + K::SM + half * kTile;
-            // strictly-upper tiles stay zero once written, unless sM is reused for sH
-            const bool write_zeros = (K::SH == K::SM) || it == 0;
+            uint32_t pk[32];  // this thread's 64 columns of M as packed bf16 pairs
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const int k = 2 * half + kk;  // 32-column tile index along s
                 if (k > quarter) {
-                    if (write_zeros) {
-                        const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                            *reinterpret_cast<uint4*>(mblk + ptx::swz128(t, kk * 4 + jj)) = z;
-                    }
+                    for (int e = 0; e < 16; ++e) pk[16 * kk + e] = 0u;
                     continue;
                 }
                 uint32_t r[32];
                 ptx::tmem_ld32(tmem + lane_base + K::COL_CB + 32 * k, r);
                 ptx::tmem_wait_ld(r);
-                uint32_t pk[16];
                 if (k < quarter) {
                     const float sc = factored ? 1.f : u_t;
 #pragma unroll
                     for (int e4 = 0; e4 < 8; ++e4) {
                         const float4 v4 = *reinterpret_cast<const float4*>(vq + 32 * k + 4 * e4);
-                        pk[2 * e4] = pack_bf16x2(__uint_as_float(r[4 * e4]) * (sc * v4.x),
-                                                 __uint_as_float(r[4 * e4 + 1]) * (sc * v4.y));
-                        pk[2 * e4 + 1] = pack_bf16x2(__uint_as_float(r[4 * e4 + 2]) * (sc * v4.z),
-                                                     __uint_as_float(r[4 * e4 + 3]) * (sc * v4.w));
+                        pk[16 * kk + 2 * e4] = pack_bf16x2(__uint_as_float(r[4 * e4]) * (sc * v4.x),
+                                                           __uint_as_float(r[4 * e4 + 1]) * (sc * v4.y));
+                        pk[16 * kk + 2 * e4 + 1] = pack_bf16x2(__uint_as_float(r[4 * e4 + 2]) * (sc * v4.z),
+                                                               __uint_as_float(r[4 * e4 + 3]) * (sc * v4.w));
                     }
                 } else if (factored) {
                     // diagonal tile, factored: causal select, D/u_t on the diagonal
@@ -402,8 +540,8 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
                             const float m = __uint_as_float(r[c]) * vv[q2];
                             m4[q2] = c < lane ? m : (c == lane ? m + d_over_u : 0.f);
                         }
-                        pk[2 * e4] = pack_bf16x2(m4[0], m4[1]);
-                        pk[2 * e4 + 1] = pack_bf16x2(m4[2], m4[3]);
+                        pk[16 * kk + 2 * e4] = pack_bf16x2(m4[0], m4[1]);
+                        pk[16 * kk + 2 * e4 + 1] = pack_bf16x2(m4[2], m4[3]);
                     }
                 } else {
                     // diagonal tile, exact: decay below the diagonal, D on it, zeros above
@@ -420,101 +558,48 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
                             const float diag = fmaf(cb, dts[s], D_h);
                             m2[q2] = c < lane ? below : (c == lane ? diag : 0.f);
                         }
-                        pk[e] = pack_bf16x2(m2[0], m2[1]);
+                        pk[16 * kk + e] = pack_bf16x2(m2[0], m2[1]);
                     }
                 }
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    *reinterpret_cast<uint4*>(mblk + ptx::swz128(t, kk * 4 + jj)) =
-                        make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
             }
+            ptx::tmem_st32(tmem + lane_base + K::col_m(slot) + 32 * half, pk);
+            ptx::tmem_wait_st();
         }
-        ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         ptx::named_sync(1 + slot, 256);
 
-        // (e) k5a: Yd = M . X  (M = t, N = p, K = s; A K-major, B MN-major)
-        if (leader) {
-            ptx::tc_fence_after();
-            const uint64_t dsc_m = ptx::desc_sw128(slot_addr + K::SM, 16, 1024);     // M, K-major
-            const uint64_t dsc_x = ptx::desc_sw128(slot_addr + K::SX, kTile, 1024);  // X, MN-major
-#pragma unroll
-            for (int k = 0; k < kT / 16; ++k)
-                ptx::mma_bf16(tmem + K::col_d(slot), dsc_m + kmaj(k), dsc_x + mnmaj(k), IDESC_D, k > 0);
-            ptx::mma_commit(bar_d);
-        }
+        // (e) k5a is issued by the MMA warp
+        if (leader) ptx::mbar_arrive(req_d);
 
-        // (f) k4: s_in from the previous block (tagged words: each 64-bit word
-        // holds a value and the tag of the block that wrote it, so a word with
-        // the expected tag is valid by itself; no flag or fence is needed),
-        // s_out = e^{cs_end} s_in + S published the same way, s_in^T to sH in bf16.
-        bool my_ok = true;
+        // (f) k4: s_out = e^{cs_end} s_in + S per 128-column state tile, staged in place
+        // for the agent; s_in^T to sH in bf16 for k5b. Thread (quarter, half) owns
+        // state column n = 32*quarter + lane of the tile and rows p = 32*half .. +31.
+        bool chain_ok = true;
         {
             const float a_blk = tEt[j * kT + kT - 1];  // e^{cs_end}
-            const bool last = (blk == prm.nblk - 1);
+            const int nl = quarter * 32 + lane;
 #pragma unroll 1
-            for (int mt = 0; mt < NST / 128; ++mt) {
-                const int n = n0 + 128 * mt;
-                float hin[32];
-                if (blk == 0) {
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int p = half * 32 + jj;
-                        hin[jj] = prm.init ? prm.init[fs_base + static_cast<size_t>(p) * NST + n] : 0.f;
-                    }
-                } else {
-                    load_words(mt);
-                    uint32_t missing = 0;
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj)
-                        if (static_cast<uint32_t>(w[jj] >> 32) != want) missing |= 1u << jj;
-                    if (missing) {
-                        // the previous block is still writing (or failed): poll the missing
-                        // words until they carry the expected tag, a poison tag, or time runs out
-                        const uint64_t t_start = ptx::globaltimer_ns();
-                        bool poisoned = false;
-                        while (missing && !poisoned) {
-                            if (ptx::globaltimer_ns() - t_start > prm.chain_wait_ns) break;
-                            __nanosleep(32);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                if (missing & (3u << (2 * i))) {
-                                    ptx::ld_relaxed_2xb64(prev + (static_cast<size_t>(16 * half + i) * NST + n) * 2,
-                                                          w[2 * i], w[2 * i + 1]);
-#pragma unroll
-                                    for (int e = 0; e < 2; ++e) {
-                                        const uint32_t tg = static_cast<uint32_t>(w[2 * i + e] >> 32);
-                                        if (tg == want) missing &= ~(1u << (2 * i + e));
-                                        poisoned |= (tg == kPoison);
-                                    }
-                                }
-                            }
-                        }
-                        if (missing) my_ok = false;
-                    }
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) hin[jj] = __uint_as_float(static_cast<uint32_t>(w[jj]));
-                }
+            for (int mt = 0; mt < K::MT; ++mt) {
+                const uint32_t pst = static_cast<uint32_t>(it * K::MT + mt) & 1;
+                wait_local(bar_st, pst, prm.status);
+                chain_ok = (sInfo[3 + slot] == 0);
+                const bool zero_in = !chain_ok || (blk == 0 && !prm.init);
                 if (mt == 0) {
                     wait_local(bar_s, ph, prm.status);
-                    if (K::SH == K::SM) wait_local(bar_d, ph, prm.status);  // sH shares sM with k5a's operand
-                    ptx::tc_fence_after();
+                    if (K::SH != K::SW) wait_local(bar_d, ph, prm.status);  // sH overlays k5a's sX
                 }
+                ptx::tc_fence_after();
                 uint32_t r[32];
                 ptx::tmem_ld32(tmem + lane_base + K::col_s(slot) + 64 * mt + half * 32, r);
                 ptx::tmem_wait_ld(r);
-                const uint64_t tag_hi = static_cast<uint64_t>(my_ok ? mine_tag : kPoison) << 32;
+                float hin[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float o0 = fmaf(a_blk, hin[2 * i], __uint_as_float(r[2 * i]));
-                    const float o1 = fmaf(a_blk, hin[2 * i + 1], __uint_as_float(r[2 * i + 1]));
-                    ptx::st_relaxed_2xb64(mine + (static_cast<size_t>(16 * half + i) * NST + n) * 2,
-                                          tag_hi | __float_as_uint(o0), tag_hi | __float_as_uint(o1));
-                    if (last && prm.final_state) {
-                        prm.final_state[fs_base + static_cast<size_t>(32 * half + 2 * i) * NST + n] = o0;
-                        prm.final_state[fs_base + static_cast<size_t>(32 * half + 2 * i + 1) * NST + n] = o1;
-                    }
+                for (int jj = 0; jj < 32; ++jj) {
+                    float* cell = st_buf + (32 * half + jj) * 128 + nl;
+                    hin[jj] = zero_in ? 0.f : *cell;
+                    *cell = fmaf(a_blk, hin[jj], __uint_as_float(r[jj]));
                 }
+                const int n = nl + 128 * mt;
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     uint4 o;
@@ -524,36 +609,35 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
                     o.w = pack_bf16x2(hin[8 * jj + 6], hin[8 * jj + 7]);
                     *reinterpret_cast<uint4*>(slot_base + K::SH + ptx::swz128(n, half * 4 + jj)) = o;
                 }
+                ptx::fence_proxy_async_smem();  // the agent's bulk store and k5b read what was written
+                ptx::tc_fence_before();
+                ptx::named_sync(1 + slot, 256);
+                if (leader) ptx::mbar_arrive(bar_pub);
             }
         }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        const bool chain_ok = ptx::named_sync_and(1 + slot, 256, my_ok);
-        if (leader && !chain_ok) atomicOr(prm.status, 1u);
 
-        // (g) leader: k5b Yo = C . s_in^T (M = t, N = p, K = n; A K-major, B MN-major)
-        // into S's columns; refill sX for the slot's next head once k5a has read it.
+        // (g) k5b is issued by the MMA warp (skipped when the chain failed);
+        // refill sX for the slot's next head once k5a has read it
         if (leader) {
-            if (chain_ok) {
-                ptx::tc_fence_after();
-                const uint64_t dsc_c_k = ptx::desc_sw128(sbase + K::OFF_C, 16, 1024);     // C, K-major
-                const uint64_t dsc_h = ptx::desc_sw128(slot_addr + K::SH, kTile, 1024);  // s_in^T, MN-major
-#pragma unroll
-                for (int k = 0; k < NST / 16; ++k)
-                    ptx::mma_bf16(tmem + K::col_o(slot), dsc_c_k + kmaj(k), dsc_h + mnmaj(k), IDESC_O, k > 0);
-                ptx::mma_commit(bar_o);
-            }
-            wait_local(bar_d, ph, prm.status);
-            if (j + K::SLOTS < hpu) {
-                ptx::mbar_arrive_expect_tx(bar_x, kTile);
-                ptx::tma_load_4d(slot_base + K::SX, &tm_x, bar_x, 0, h + K::SLOTS, t0, b);
+            sInfo[1 + slot] = chain_ok ? 0 : 1;
+            ptx::mbar_arrive(req_o);
+            if (K::SH == K::SW) {
+                wait_local(bar_d, ph, prm.status);
+                if (j + K::SLOTS < hpu) {
+                    ptx::mbar_arrive_expect_tx(bar_x, kTile);
+                    ptx::tma_load_4d(slot_base + K::SX, &tm_x, bar_x, 0, h + K::SLOTS, t0, b);
+                }
             }
         }
 
         // (h) epilogue: y = e^{cs_t} Yo + u_t Yd' (u_t = 1 for exact quarters), staged in sY, TMA store
         wait_local(bar_d, ph, prm.status);
+        wait_local(bar_o, ph, prm.status);  // also when k5b was skipped: sH is free once this completes
+        if (leader && K::SH != K::SW && j + K::SLOTS < hpu) {
+            ptx::mbar_arrive_expect_tx(bar_x, kTile);
+            ptx::tma_load_4d(slot_base + K::SX, &tm_x, bar_x, 0, h + K::SLOTS, t0, b);
+        }
         if (chain_ok) {
-            wait_local(bar_o, ph, prm.status);
             ptx::tc_fence_after();
             const int t = quarter * 32 + lane;
             const float e_t = tEt[j * kT + t];
@@ -587,7 +671,7 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
     }
     if (leader) ptx::bulk_wait_group_read0();
     ptx::tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // every slot is done, the MMA warp has committed its last group, the agents are idle
     ptx::tc_fence_after();
     if (warp == 0) ptx::tmem_dealloc(tmem, K::TMEM_COLS);
 }
@@ -624,9 +708,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t tc_counters_bytes(const ssd_dims&) { return kWorkspaceAlign; }
-
-std::atomic<uint32_t> g_epoch{0};
+// Work ticket, then one flag per (chain, parity); cleared before every launch.
+size_t tc_counters_bytes(const ssd_dims& d) {
+    return align_up(sizeof(uint32_t) * static_cast<size_t>(1 + 2 * d.batch * d.nheads), kWorkspaceAlign);
+}
 
 // Heads per unit: the largest of 8, 4, 2, 1 that divides the heads of one group.
 int heads_per_unit(const ssd_dims& d) {
@@ -656,8 +741,8 @@ ssd_status launch(const FwdArgs& a, void* ws) {
     p.init = a.init;
     p.final_state = a.final_state;
     p.ticket = static_cast<uint32_t*>(ws);
-    p.slots = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + counters);
-    p.epoch = g_epoch.fetch_add(1, std::memory_order_relaxed);
+    p.flags = p.ticket + 1;
+    p.slots = reinterpret_cast<float*>(static_cast<char*>(ws) + counters);
     p.status = a.status_word;
     p.batch = static_cast<int>(d.batch);
     p.H = static_cast<int>(d.nheads);
@@ -684,14 +769,13 @@ bool tc_supported(const ssd_dims& d, ssd_dtype io, int chunk_len) {
     if (d.dstate != 128 && d.dstate != 256) return false;
     if (chunk_len != 128 && chunk_len != 256) return false;
     const long long nblk = (d.seqlen + kT - 1) / kT;
-    if (nblk >= 65535) return false;  // state tags carry the block index in 16 bits
     if (nblk * d.batch * d.nheads >= (1ll << 31)) return false;
     if (d.seqlen >= (1ll << 31) || d.batch >= (1ll << 31) || d.nheads >= (1 << 20)) return false;
     return true;
 }
 
 size_t tc_workspace_bytes(const ssd_dims& d, int /*chunk_len*/) {
-    const size_t slots = sizeof(uint64_t) * static_cast<size_t>(d.batch * d.nheads) * 2 * kP * d.dstate;
+    const size_t slots = sizeof(float) * static_cast<size_t>(d.batch * d.nheads) * 2 * kP * d.dstate;
     return tc_counters_bytes(d) + align_up(slots, kWorkspaceAlign);
 }
 

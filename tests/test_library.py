@@ -123,12 +123,13 @@ def test_path_selection(lib):
 
 
 def test_workspace_sizes(lib):
-    # tensor-core path: a work counter + two state slots per (batch, head) of
-    # 64-bit tagged words (fp32 value and 32-bit tag)
+    # tensor-core path: a work counter, two ready flags per (batch, head) and
+    # two fp32 state slots per (batch, head)
     b, h, p, n = 4, 80, 64, 128
     need = pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, n, "bf16", 256, "tc")
-    slots = 8 * b * h * 2 * p * n
-    assert slots <= need <= slots + 4096
+    slots = 4 * b * h * 2 * p * n
+    counters = 4 * (1 + 2 * b * h)
+    assert slots + counters <= need <= slots + counters + 4096
     # SIMT path: one fp32 state per chunk
     need = pkg.ssd_fwd_workspace_bytes(1, 256, 4, 16, 1, 16, "f32", 64, "simt")
     assert need >= 4 * 1 * 4 * 4 * 16 * 16

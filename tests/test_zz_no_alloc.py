@@ -74,7 +74,7 @@ def test_noalloc_matches_ssd_fwd_on_two_calls(lib):
 
 def test_noalloc_rejects_work_beyond_its_scratch(lib):
     import mamba_ssd_chunked_gb300 as pkg
-    # 4 x 80 chains at dstate 128 need 40 MiB of scratch, more than the 16 MiB array
+    # 4 x 80 chains at dstate 128 need 20 MiB of scratch, more than the 16 MiB array
     dims = pkg.Dims(4, 256, 80, 64, 1, 128)
     assert pkg.ssd_fwd_workspace_bytes(4, 256, 80, 64, 1, 128, "bf16", 256, "tc") > SCRATCH_BYTES
     fake = 1 << 16
