@@ -66,12 +66,20 @@ typedef enum {
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
 /* Which kernels compute the forward.
- *   SSD_PATH_AUTO: tensor-core path when supported, else the SIMT path.
- *   SSD_PATH_SIMT: fp32 CUDA-core kernels, any supported shape, the five
- *                  stages at exactly chunk_len (chunk states in workspace).
- *   SSD_PATH_TC:   fused tcgen05/TMA kernel (bf16 io, headdim 64,
- *                  dstate 128 or 256, chunk_len 128 or 256). */
-typedef enum { SSD_PATH_AUTO = 0, SSD_PATH_SIMT = 1, SSD_PATH_TC = 2 } ssd_path;
+ *   SSD_PATH_AUTO:  SSD_PATH_TC when supported, else SSD_PATH_CHAIN when
+ *                   supported, else the SIMT path.
+ *   SSD_PATH_SIMT:  fp32 CUDA-core kernels, any supported shape, the five
+ *                   stages at exactly chunk_len (chunk states in workspace).
+ *   SSD_PATH_TC:    fused tcgen05/TMA kernel, one CTA per (128-token block,
+ *                   head group), chunk states chained through workspace
+ *                   (bf16 io, headdim 64, dstate 128 or 256, chunk_len 128
+ *                   or 256).
+ *   SSD_PATH_CHAIN: fused tcgen05/TMA kernel, one persistent CTA per SM that
+ *                   walks whole chains block by block with the chunk state
+ *                   kept in tensor memory (bf16 io, headdim 64, dstate 128,
+ *                   chunk_len 128 or 256). Its workspace depends on the
+ *                   current device's SM count. */
+typedef enum { SSD_PATH_AUTO = 0, SSD_PATH_SIMT = 1, SSD_PATH_TC = 2, SSD_PATH_CHAIN = 3 } ssd_path;
 
 typedef struct {
     int64_t batch, seqlen, nheads, headdim, ngroups, dstate;
@@ -121,7 +129,7 @@ SSD_API ssd_status ssd_fwd_ws(const ssd_dims* dims, ssd_dtype io_dtype,
 /* Workspace bytes ssd_fwd_ws needs for these arguments (0 if they are invalid). */
 SSD_API size_t ssd_fwd_workspace_bytes(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len, ssd_path path);
 
-/* The path SSD_PATH_AUTO picks for these arguments: SSD_PATH_TC or SSD_PATH_SIMT. */
+/* The path SSD_PATH_AUTO picks for these arguments (never SSD_PATH_AUTO). */
 SSD_API ssd_path ssd_select_path(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len);
 
 /*

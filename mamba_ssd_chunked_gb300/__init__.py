@@ -28,7 +28,7 @@ LIBRARY = os.path.join(_HERE, "libssd.so")
 
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_CUDA",
           4: "SSD_ERR_DEVICE_TIMEOUT", 5: "SSD_ERR_WORKSPACE"}
-PATHS = {"auto": 0, "simt": 1, "tc": 2}
+PATHS = {"auto": 0, "simt": 1, "tc": 2, "chain": 3}
 DTYPES = {"f32": 0, "bf16": 1}
 
 

@@ -87,18 +87,23 @@ ssd_status check_pointers(const void* x, const float* dt, const float* dt_bias, 
 }
 
 ssd_path resolve_path(const ssd_dims& d, ssd_dtype io, int chunk_len, ssd_path want) {
-    if (want == SSD_PATH_AUTO) return tc_supported(d, io, chunk_len) ? SSD_PATH_TC : SSD_PATH_SIMT;
-    return want;
+    if (want != SSD_PATH_AUTO) return want;
+    if (tc_supported(d, io, chunk_len)) return SSD_PATH_TC;
+    if (chain_supported(d, io, chunk_len)) return SSD_PATH_CHAIN;
+    return SSD_PATH_SIMT;
 }
 
 bool path_supported(const ssd_dims& d, ssd_dtype io, int chunk_len, ssd_path path) {
     if (path == SSD_PATH_TC) return tc_supported(d, io, chunk_len);
+    if (path == SSD_PATH_CHAIN) return chain_supported(d, io, chunk_len);
     if (path == SSD_PATH_SIMT) return simt_supported(d, chunk_len);
     return false;
 }
 
 size_t workspace_for(const ssd_dims& d, int chunk_len, ssd_path path) {
-    return path == SSD_PATH_TC ? tc_workspace_bytes(d, chunk_len) : simt_workspace_bytes(d, chunk_len);
+    if (path == SSD_PATH_TC) return tc_workspace_bytes(d, chunk_len);
+    if (path == SSD_PATH_CHAIN) return chain_workspace_bytes(d);
+    return simt_workspace_bytes(d, chunk_len);
 }
 
 ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* dt, const float* dt_bias,
@@ -107,7 +112,8 @@ ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* d
                void* stream) {
     ssd_status st = check_dims(dims, io, chunk_len, ngroups);
     if (st != SSD_OK) return st;
-    if (path != SSD_PATH_AUTO && path != SSD_PATH_SIMT && path != SSD_PATH_TC) return SSD_ERR_INVALID_ARG;
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_SIMT && path != SSD_PATH_TC && path != SSD_PATH_CHAIN)
+        return SSD_ERR_INVALID_ARG;
     st = check_pointers(x, dt, dt_bias, A, B, C, D, init, y, fs);
     if (st != SSD_OK) return st;
     const ssd_path p = resolve_path(*dims, io, chunk_len, path);
@@ -161,7 +167,9 @@ ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* d
     a.stream = static_cast<cudaStream_t>(stream);
     a.status_word = status;
     a.wait_limit_ns = wait_limit_ns();
-    return p == SSD_PATH_TC ? tc_forward(a, ws, ws_bytes) : simt_forward(a, ws, ws_bytes);
+    if (p == SSD_PATH_TC) return tc_forward(a, ws, ws_bytes);
+    if (p == SSD_PATH_CHAIN) return chain_forward(a, ws, ws_bytes);
+    return simt_forward(a, ws, ws_bytes);
 }
 
 size_t elem_bytes(ssd_dtype io) { return io == SSD_F32 ? 4 : 2; }
@@ -221,7 +229,7 @@ ssd_status ssd_fwd_ws(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, c
 
 size_t ssd_fwd_workspace_bytes(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len, ssd_path path) {
     if (check_dims(dims, io_dtype, chunk_len, dims ? static_cast<int>(dims->ngroups) : 0) != SSD_OK) return 0;
-    if (path != SSD_PATH_AUTO && path != SSD_PATH_SIMT && path != SSD_PATH_TC) return 0;
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_SIMT && path != SSD_PATH_TC && path != SSD_PATH_CHAIN) return 0;
     const ssd_path p = resolve_path(*dims, io_dtype, chunk_len, path);
     if (!path_supported(*dims, io_dtype, chunk_len, p)) return 0;
     return workspace_for(*dims, chunk_len, p);

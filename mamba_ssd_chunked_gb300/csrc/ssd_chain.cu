@@ -1,0 +1,1037 @@
+// Chain-local fused forward (tcgen05/TMA, bf16 io, dstate 128, headdim 64).
+//
+// A persistent CTA per SM walks a contiguous range of the flattened
+// (chain, block) index space, where a chain is HG heads (1 or 2) of one batch
+// row that read the same B/C group, and a block is 128 tokens. Along a chain
+// the blocks are processed in order by the same CTA, so the chunk state stays
+// in tensor memory from one block to the next; only where a CTA's range
+// starts or ends inside a chain is a state handed to the neighbouring CTA
+// through global memory (once per CTA boundary, not once per block).
+// A CTA processes the tail of its range first (a chain start, which waits on
+// nothing and publishes the hand-off early) and the head of its range last
+// (the continuation that consumes the previous CTA's hand-off).
+//
+// Per block and head the five stages of the chunked SSD (burn-mamba
+// "mamba2/ssd/serial.rs" k1..k5; fla "mamba2.py" naive chunked SSD) are
+// rewritten around one reference log-decay per (block, head):
+//
+//   dt_t = softplus(dt_raw + dt_bias), cs_t = inclusive cumsum of dt*A in the block,
+//   c    = cs_end / 2 (midpoint reference),
+//   W_s  = X_s dt_s e^{c - cs_s}                      (bf16, B operand of k3 and k5a)
+//   z    = e^{c} s_in                                  (fp32 in TMEM, bf16 copy H for k5b)
+//   k3   z += B^T W          ->  z = e^{c - cs_end} s_out  (the state stays scaled in TMEM)
+//   k5   Y = L W + C H^T     with L = C.B^T masked to s <= t (the same for every head)
+//   y_t  = e^{cs_t - c} Y_t + D x_t,  D x_t = e^{cs_t - c} (D / dt_t) W_t
+//
+// since e^{cs_t - cs_s} dt_s X_s = e^{cs_t - c} (e^{c - cs_s} dt_s X_s) and
+// e^{cs_t} C_t s_in = e^{cs_t - c} C_t (e^{c} s_in). The masked matrix L does not
+// depend on the head, so the MMAs of both heads of a chain run as one N = 128
+// operation (k3, k5a and k5b each: eight K=16 steps for the pair). Every factor
+// lies in [e^{-d/2}, e^{d/2}] for a block decay d = -cs_end, so this
+// "reference" mode is used for d <= kRefMaxDecay. Blocks that decay faster
+// use "exact" mode, per head:
+//
+//   W_s  = X_s dt_s e^{cs_end - cs_s}  (k3),   z = e^{cs_end} s_in,  H = s_in,
+//   C'_t = e^{cs_t} C_t (A operand in TMEM),   k5b: Y = C' H^T,
+//   Me[t][s] = C_t.B_s e^{cs_t - cs_s} dt_s (s < t), C_t.B_t dt_t + D (s = t),
+//   k5a: Y += Me X,  y_t = Y_t,
+//
+// where every factor is at most 1 (underflow only drops negligible terms).
+//
+// Roles (20 warps):
+//   warp 0       TMA producer: B, C (one buffer each), X (ring of three); and the
+//                MMA issuer of the state path (k3), polled with the loads
+//   warp 1       MMA issuer, output path: C.B^T, k5b, k5a
+//   warps 2..3   tables: dt, cumsum and per-token factors, one head each
+//   warps 4..7   masks into TMEM: L (shared), and per exact-mode head C', Me
+//   warps 8..11  W from X
+//   warps 12..15 state: rescale z in TMEM, write H; load / store states at segment ends
+//   warps 16..19 epilogue: y from TMEM (+ D x from W), stored straight to global memory
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "ptx.cuh"
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kT = 128;                // tokens per block
+constexpr int kP = 64;                 // headdim
+constexpr int kN = 128;                // dstate
+constexpr uint32_t kTile = 16384;      // 128 rows x 128 bytes, 128-byte swizzle
+constexpr float kRefMaxDecay = 140.f;  // reference mode while the block decay stays within this
+constexpr unsigned long long kLocalWaitNs = 2000000000ull;
+constexpr int kNX = 3;                 // X ring depth
+constexpr int kNumTab = 3;             // per-token tables per (block, head)
+constexpr int kTabSlots = 4;           // table ring depth (jobs)
+enum Tab { TAB_W = 0, TAB_DT = 1, TAB_CS = 2 };
+constexpr int kThreads = 640;
+
+template <int HG>
+struct ChainCfg {
+    static constexpr uint32_t OFF_B = 0;                          // B [t][n] as two 64-column tiles
+    static constexpr uint32_t OFF_C = OFF_B + 2 * kTile;          // C, same layout
+    static constexpr uint32_t OFF_X = OFF_C + 2 * kTile;          // X ring
+    static constexpr uint32_t OFF_W = OFF_X + kNX * kTile;        // W [2 buffers][HG heads], adjacent heads
+    static constexpr uint32_t OFF_H = OFF_W + 2 * HG * kTile;     // H [n][p] per head, adjacent heads
+    static constexpr uint32_t OFF_TAB = OFF_H + HG * kTile;       // [slots][HG][kNumTab][128] floats
+    static constexpr uint32_t TAB_BYTES = kTabSlots * HG * kNumTab * kT * 4;
+    static constexpr uint32_t OFF_SCAL = OFF_TAB + TAB_BYTES;     // [slots][HG][4] floats
+    static constexpr uint32_t OFF_BAR = OFF_SCAL + kTabSlots * HG * 4 * 4;
+    static constexpr int NBAR = 48;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;      // tmem address, ticket, flags
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static constexpr int NH = 64 * HG;                            // N of the batched MMAs
+    // TMEM columns
+    static constexpr uint32_t COL_CB = 0;       // C.B^T, fp32, 128 columns
+    static constexpr uint32_t COL_S = 128;      // scaled state per head, fp32, 64 columns each
+    static constexpr uint32_t COL_R0 = 256;     // region 0: L (or an exact head's C' / Me), bf16 pairs
+    static constexpr uint32_t COL_R1 = 320;     // region 1: an exact head's C' / Me
+    static constexpr uint32_t COL_Y = 384;      // output accumulator per head, fp32, 64 columns each
+};
+
+// mbarrier indices
+enum Bar {
+    B_B_FULL = 0, B_B_EMPTY, B_C_FULL, B_C_EMPTY,
+    B_X_FULL0, B_X_FULL1, B_X_FULL2, B_X_EMPTY0, B_X_EMPTY1, B_X_EMPTY2,
+    B_CB_FULL, B_CB_EMPTY,
+    B_R_FULL0, B_R_FULL1, B_R_EMPTY0, B_R_EMPTY1,
+    B_Y_FULL, B_Y_EMPTY,
+    B_TAB_FULL0, B_TAB_FULL1, B_TAB_FULL2, B_TAB_FULL3, B_TAB_EMPTY0, B_TAB_EMPTY1, B_TAB_EMPTY2, B_TAB_EMPTY3,
+    B_W_FULL0, B_W_FULL1, B_W_EMPTY0, B_W_EMPTY1,
+    B_SCALED, B_S_DONE, B_H_EMPTY,
+    B_DRAIN_A, B_DRAIN_B, B_K3_DONE0, B_K3_DONE1,
+    B_COUNT
+};
+static_assert(B_COUNT <= 48, "barrier budget");
+
+struct ChainParams {
+    const float* dt;
+    const float* dt_bias;
+    const float* A;
+    const float* D;
+    const float* init;
+    float* final_state;
+    __nv_bfloat16* y;
+    float* handoff;        // [nCTA][HG][P][N] fp32 states handed from CTA i to CTA i + 1
+    uint32_t* ticket;      // CTA order counter
+    uint32_t* flags;       // [nCTA]: 1 once CTA i's hand-off state is in place
+    uint32_t* status;
+    int batch, H, G, nblk, nchains, ncta;
+    long long L, total;    // total = nchains * nblk jobs
+    unsigned long long chain_wait_ns;
+};
+
+// A job is one block of one chain. The CTA's jobs, in processing order (all
+// indices fit 31 bits: the host only launches when chains * blocks < 2^31).
+struct JobList {
+    int first, last;   // flat range [first, last) = chain * nblk + block
+    int nblk;
+    int cF, cL;        // first and last chain touched
+    int nE, nM;        // lengths of the tail part (processed first) and of the full chains
+    __device__ int count() const { return last - first; }
+    // chain and block of the J-th job; seg_lo / seg_hi: the segment's block range
+    __device__ __forceinline__ void at(int J, int& chain, int& blk, int& seg_lo, int& seg_hi) const {
+        if (cF == cL) {
+            chain = cF;
+            seg_lo = first - cF * nblk;
+            blk = seg_lo + J;
+            seg_hi = last - cF * nblk;
+        } else if (J < nE) {
+            chain = cL;
+            blk = J;
+            seg_lo = 0;
+            seg_hi = nE;
+        } else if (J < nE + nM) {
+            const unsigned r = static_cast<unsigned>(J - nE);
+            chain = cF + 1 + static_cast<int>(r / static_cast<unsigned>(nblk));
+            blk = static_cast<int>(r % static_cast<unsigned>(nblk));
+            seg_lo = 0;
+            seg_hi = nblk;
+        } else {
+            chain = cF;
+            seg_lo = first - cF * nblk;
+            blk = seg_lo + (J - nE - nM);
+            seg_hi = nblk;
+        }
+    }
+};
+
+__device__ __forceinline__ JobList make_jobs(const ChainParams& p, int cta) {
+    JobList jl;
+    jl.first = static_cast<int>(p.total * cta / p.ncta);
+    jl.last = static_cast<int>(p.total * (cta + 1) / p.ncta);
+    jl.nblk = p.nblk;
+    jl.cF = jl.first / p.nblk;
+    jl.cL = (jl.last - 1) / p.nblk;
+    jl.nE = jl.last - jl.cL * p.nblk;
+    jl.nM = (jl.cF == jl.cL) ? 0 : (jl.cL - jl.cF - 1) * p.nblk;
+    return jl;
+}
+
+
+// Everything a role needs to know about its J-th job (out of line: one copy of
+// the index arithmetic serves every role).
+struct JobPos {
+    int blk, lo, hi;  // block, and the block range of the job's segment
+    int b, h0, g;     // batch row, first head, B/C group
+};
+
+__device__ __noinline__ JobPos job_pos(const JobList& jobs, int J, int chains_per_b, int HG, int HperG) {
+    JobPos jp;
+    int chain;
+    jobs.at(J, chain, jp.blk, jp.lo, jp.hi);
+    jp.b = chain / chains_per_b;
+    jp.h0 = (chain - jp.b * chains_per_b) * HG;
+    jp.g = jp.h0 / HperG;
+    return jp;
+}
+
+__device__ __noinline__ float softplus_f(float v) {
+    return v > 0.f ? v + log1pf(expf(-v)) : log1pf(expf(v));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&v);
+    return __bfloat1622float2(b);
+}
+
+// Bounded wait on this CTA's own pipeline. A timeout sets bit 1 of the status
+// word and the CTA's abort flag; after that no role waits on the pipeline any
+// more, so every loop runs out quickly (the results are then invalid and the
+// host is told). Copies and MMAs already issued are still drained before exit.
+__device__ __noinline__ void wait_bar(uint64_t* bar, uint32_t parity, uint32_t* status, volatile uint32_t* abort) {
+    if (*abort) return;
+    if (!ptx::mbar_wait(bar, parity, kLocalWaitNs)) {
+        atomicOr(status, 2u);
+        *abort = 1u;
+    }
+}
+
+// Per-warp arrival: every lane's prior writes are ordered before lane 0's arrive.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar);
+}
+
+// Which TMEM region an exact-mode head uses: region 1, unless both heads of a
+// pair are exact (then head 0 takes region 0, which L does not need).
+__device__ __forceinline__ int exact_region(int nexact, int j, int HG) {
+    return (HG == 2 && nexact == 2 && j == 0) ? 0 : 1;
+}
+
+
+// C'_t = e^{cs_t} C_t into 64 TMEM columns of this thread's lane (row t):
+// pairs of n as bf16, the A operand of an exact-mode k5b. C is [t][n] in two
+// 128-byte-swizzled tiles of 64 columns.
+__device__ __noinline__ void build_cprime(uint32_t dst, const uint8_t* c_tiles, int t, float e_t) {
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {  // 16 TMEM columns = 32 values of n per step
+        uint32_t pk[16];
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+            const int chunk = 4 * (ch & 1) + c8;  // 16-byte chunk within the 64-column tile
+            const uint4 v = *reinterpret_cast<const uint4*>(c_tiles + (ch >> 1) * kTile + ptx::swz128(t, chunk));
+            const float2 a0 = unpack_bf16x2(v.x), a1 = unpack_bf16x2(v.y), a2 = unpack_bf16x2(v.z),
+                         a3 = unpack_bf16x2(v.w);
+            pk[4 * c8 + 0] = pack_bf16x2(a0.x * e_t, a0.y * e_t);
+            pk[4 * c8 + 1] = pack_bf16x2(a1.x * e_t, a1.y * e_t);
+            pk[4 * c8 + 2] = pack_bf16x2(a2.x * e_t, a2.y * e_t);
+            pk[4 * c8 + 3] = pack_bf16x2(a3.x * e_t, a3.y * e_t);
+        }
+        ptx::tmem_st16(dst + 16 * ch, pk);
+    }
+}
+
+// Exact-mode masked matrix of one head into 64 TMEM columns of this thread's
+// lane (row t = 32 q + lane): Me[t][s] = CB[t][s] e^{cs_t - cs_s} dt_s for
+// s < t, CB[t][t] dt_t + D on the diagonal, zero above. Every tile is written.
+__device__ __noinline__ void build_exact_mask(uint32_t dst, uint32_t cb, int q, int lane, const float* csv,
+                                              const float* dtv, float D) {
+    const int t = 32 * q + lane;
+    const float cs_t = csv[t];
+#pragma unroll 1
+    for (int tile = 0; tile < 4; ++tile) {
+        uint32_t pk[16];
+        if (tile > q) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+        } else {
+            uint32_t rr[32];
+            ptx::tmem_ld32(cb + 32 * tile, rr);
+            ptx::tmem_wait_ld(rr);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                float m2[2];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c = 2 * e + h2, s = 32 * tile + c;
+                    const float cbv = __uint_as_float(rr[c]);
+                    const float below = cbv * __expf(fminf(cs_t - csv[s], 0.f)) * dtv[s];
+                    m2[h2] = (tile < q || c < lane) ? below : (c == lane ? fmaf(cbv, dtv[s], D) : 0.f);
+                }
+                pk[e] = pack_bf16x2(m2[0], m2[1]);
+            }
+        }
+        ptx::tmem_st16(dst + 16 * tile, pk);
+    }
+}
+
+
+// K = 128 in eight tcgen05.mma steps of K = 16. SS: both operands in shared
+// memory (K-major operand: +32 bytes per step inside a 64-column tile, next
+// tile after four steps; MN-major operand: +2048 bytes, 16 rows of 128 bytes).
+// TS: A (bf16, K-major) in tensor memory, 8 columns per step. Out of line and
+// rolled: the issue rate (one MMA per ~100 cycles per issuing thread) does
+// not need unrolling, and one copy keeps the instruction cache warm.
+__device__ __noinline__ void mma8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool a_kmajor, bool b_kmajor,
+                                     bool acc) {
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+        const uint64_t kk = static_cast<uint64_t>((((k >> 2) * kTile + (k & 3) * 32) >> 4));
+        const uint64_t mn = static_cast<uint64_t>((k * 2048) >> 4);
+        ptx::mma_bf16(d, a + (a_kmajor ? kk : mn), b + (b_kmajor ? kk : mn), idesc, (acc || k > 0) ? 1u : 0u);
+    }
+}
+
+__device__ __noinline__ void mma8_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc) {
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k)
+        ptx::mma_bf16_ta(d, a_tmem + 8 * k, b + static_cast<uint64_t>((k * 2048) >> 4), idesc, (acc || k > 0) ? 1u : 0u);
+}
+
+template <int HG>
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_chain_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
+                    const ChainParams prm) {
+    using K = ChainCfg<HG>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* tab = reinterpret_cast<float*>(smem + K::OFF_TAB);
+    float* scal = reinterpret_cast<float*>(smem + K::OFF_SCAL);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + K::OFF_MISC);
+    const uint32_t sbase = ptx::smem_u32(smem);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wg = warp >> 2, q = warp & 3;  // warpgroup, TMEM lane quarter
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+
+    auto T = [&](int slot, int j, int arr) { return tab + ((slot * HG + j) * kNumTab + arr) * kT; };
+    auto S = [&](int slot, int j) { return scal + (slot * HG + j) * 4; };  // exact?, c, cs_end
+
+    if (tid == 0) {
+        misc[1] = atomicAdd(prm.ticket, 1u);
+        uint32_t counts[B_COUNT];
+        for (int i = 0; i < B_COUNT; ++i) counts[i] = 1;
+        counts[B_B_EMPTY] = 2;                                  // C.B^T commit + k3 commit
+        counts[B_CB_EMPTY] = 4;                                 // mask warps
+        counts[B_R_FULL0] = counts[B_R_FULL1] = 4;              // mask warps
+        counts[B_Y_EMPTY] = 4;                                  // epilogue warps
+        for (int i = 0; i < kTabSlots; ++i) {
+            counts[B_TAB_FULL0 + i] = HG;                       // table warps
+            counts[B_TAB_EMPTY0 + i] = 4;                       // epilogue warps
+        }
+        counts[B_W_FULL0] = counts[B_W_FULL1] = 4;              // W warps
+        counts[B_W_EMPTY0] = counts[B_W_EMPTY1] = 3;            // k3 commit + k5a commit + y store drained
+        counts[B_SCALED] = 4;                                   // state warps
+        for (int i = 0; i < B_COUNT; ++i) ptx::mbar_init(&bars[i], counts[i]);
+        misc[3] = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(misc, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const int cta = static_cast<int>(misc[1]);
+    volatile uint32_t* abort_flag = misc + 3;
+    auto WB = [&](int bar, uint32_t parity) { wait_bar(&bars[bar], parity, prm.status, abort_flag); };
+    const JobList jobs = make_jobs(prm, cta);
+    const int njobs = jobs.count();
+    const int HperG = prm.H / prm.G;
+    const int chains_per_b = prm.H / HG;
+    auto chain_coords = [&](int chain, int& b, int& h0, int& g) {
+        b = chain / chains_per_b;
+        h0 = (chain % chains_per_b) * HG;
+        g = h0 / HperG;
+    };
+    auto count_exact = [&](int ts) {
+        int n = 0;
+        for (int j = 0; j < HG; ++j) n += S(ts, j)[0] != 0.f ? 1 : 0;
+        return n;
+    };
+
+    constexpr uint32_t IDESC_CB = ptx::idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, K::NH, true, true);
+    constexpr uint32_t IDESC_Y = ptx::idesc_bf16_f32(128, K::NH, false, true);
+    constexpr uint32_t IDESC_Y1 = ptx::idesc_bf16_f32(128, 64, false, true);
+    auto kmaj = [](int k) { return static_cast<uint64_t>(((k >> 2) * kTile + (k & 3) * 32) >> 4); };
+    auto mnmaj = [](int k) { return static_cast<uint64_t>((k * 2048) >> 4); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer and k3 issuer
+        if (lane == 0) {
+            int jb = 0, jc = 0, jx = 0;  // next job for B, next job for C, next X index (job * HG + head)
+            int jk = 0;                  // next job for k3
+            const int nx = njobs * HG;
+            const uint64_t dsc_bt = ptx::desc_sw128(sbase + K::OFF_B, kTile, 1024);
+            uint64_t idle_since = ptx::globaltimer_ns();
+            while (jb < njobs || jc < njobs || jx < nx || jk < njobs) {
+                bool progressed = false;
+                // k3 of job jk: z += B^T W, once W is built, z rescaled and B landed
+                if (jk < njobs && ptx::mbar_test_wait(&bars[B_W_FULL0 + (jk & 1)], (jk >> 1) & 1) &&
+                    ptx::mbar_test_wait(&bars[B_SCALED], jk & 1) && ptx::mbar_test_wait(&bars[B_B_FULL], jk & 1)) {
+                    ptx::tc_fence_after();
+                    const uint64_t dsc_w = ptx::desc_sw128(sbase + K::OFF_W + (jk & 1) * HG * kTile, kTile, 1024);
+                    mma8_ss(tmem + K::COL_S, dsc_bt, dsc_w, IDESC_S, false, false, true);
+                    ptx::mma_commit(&bars[B_S_DONE]);
+                    ptx::mma_commit(&bars[B_W_EMPTY0 + (jk & 1)]);
+                    ptx::mma_commit(&bars[B_K3_DONE0 + (jk & 1)]);
+                    ptx::mma_commit(&bars[B_B_EMPTY]);
+                    ++jk;
+                    progressed = true;
+                }
+                if (jb < njobs && (jb == 0 || ptx::mbar_test_wait(&bars[B_B_EMPTY], (jb - 1) & 1))) {
+                    const JobPos jp_ = job_pos(jobs, jb, chains_per_b, HG, HperG);
+                    const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
+                    (void)lo; (void)hi; (void)g; (void)h0; (void)b;
+                    ptx::mbar_arrive_expect_tx(&bars[B_B_FULL], 2 * kTile);
+                    ptx::tma_load_4d(smem + K::OFF_B, &tm_b, &bars[B_B_FULL], 0, g, blk * kT, b);
+                    ptx::tma_load_4d(smem + K::OFF_B + kTile, &tm_b, &bars[B_B_FULL], 64, g, blk * kT, b);
+                    ++jb;
+                    progressed = true;
+                }
+                if (jc < njobs && (jc == 0 || ptx::mbar_test_wait(&bars[B_C_EMPTY], (jc - 1) & 1))) {
+                    const JobPos jp_ = job_pos(jobs, jc, chains_per_b, HG, HperG);
+                    const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
+                    (void)lo; (void)hi; (void)g; (void)h0; (void)b;
+                    ptx::mbar_arrive_expect_tx(&bars[B_C_FULL], 2 * kTile);
+                    ptx::tma_load_4d(smem + K::OFF_C, &tm_c, &bars[B_C_FULL], 0, g, blk * kT, b);
+                    ptx::tma_load_4d(smem + K::OFF_C + kTile, &tm_c, &bars[B_C_FULL], 64, g, blk * kT, b);
+                    ++jc;
+                    progressed = true;
+                }
+                if (jx < nx) {
+                    const int slot = jx % kNX, use = jx / kNX;
+                    if (use == 0 || ptx::mbar_test_wait(&bars[B_X_EMPTY0 + slot], (use - 1) & 1)) {
+                        const JobPos jp_ = job_pos(jobs, jx / HG, chains_per_b, HG, HperG);
+                        const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
+                        (void)lo; (void)hi; (void)g; (void)h0; (void)b;
+                        uint64_t* fb = &bars[B_X_FULL0 + slot];
+                        ptx::mbar_arrive_expect_tx(fb, kTile);
+                        ptx::tma_load_4d(smem + K::OFF_X + slot * kTile, &tm_x, fb, 0, h0 + jx % HG, blk * kT, b);
+                        ++jx;
+                        progressed = true;
+                    }
+                }
+                const uint64_t now = ptx::globaltimer_ns();
+                if (*abort_flag) break;
+                if (progressed) {
+                    idle_since = now;
+                } else if (now - idle_since > 2 * kLocalWaitNs) {
+                    atomicOr(prm.status, 2u);
+                    *abort_flag = 1u;
+                    break;
+                }
+            }
+            // no copy into this CTA's shared memory may be left in flight at exit:
+            // wait for the last load of each buffer (earlier ones completed before
+            // their buffer was refilled), whether or not the CTA gave up
+            if (jb > 0) ptx::mbar_wait(&bars[B_B_FULL], (jb - 1) & 1, kLocalWaitNs);
+            if (jc > 0) ptx::mbar_wait(&bars[B_C_FULL], (jc - 1) & 1, kLocalWaitNs);
+            for (int c = 0; c < kNX && c < jx; ++c) {
+                const int xl = jx - 1 - c;
+                ptx::mbar_wait(&bars[B_X_FULL0 + xl % kNX], (xl / kNX) & 1, kLocalWaitNs);
+            }
+            // and every k3 must have completed before the tensor memory is released
+            ptx::mma_commit(&bars[B_DRAIN_B]);
+            ptx::mbar_wait(&bars[B_DRAIN_B], 0, kLocalWaitNs);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer: C.B^T, k5b, k5a
+        if (lane == 0) {
+            uint32_t rreads0 = 0, rreads1 = 0;  // fills of each TMEM region consumed so far
+            auto rwait = [&](int r) {
+                uint32_t& c = r ? rreads1 : rreads0;
+                WB(B_R_FULL0 + r, c & 1);
+                ++c;
+            };
+            const uint64_t dsc_c = ptx::desc_sw128(sbase + K::OFF_C, 16, 1024);
+            const uint64_t dsc_b = ptx::desc_sw128(sbase + K::OFF_B, 16, 1024);
+            const uint64_t dsc_h = ptx::desc_sw128(sbase + K::OFF_H, kTile, 1024);
+            for (int J = 0; J < njobs; ++J) {
+                const int ts = J & (kTabSlots - 1), wb = J & 1;
+                WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
+                WB(B_B_FULL, J & 1);
+                WB(B_C_FULL, J & 1);
+                if (J > 0) WB(B_CB_EMPTY, (J - 1) & 1);
+                ptx::tc_fence_after();
+                const int nexact = count_exact(ts);
+                mma8_ss(tmem + K::COL_CB, dsc_c, dsc_b, IDESC_CB, true, true, false);
+                ptx::mma_commit(&bars[B_CB_FULL]);
+                ptx::mma_commit(&bars[B_B_EMPTY]);
+                // k5b: Y = C H^T (reference heads), C' H^T (exact heads)
+                WB(B_SCALED, J & 1);
+                if (J > 0) WB(B_Y_EMPTY, (J - 1) & 1);
+                ptx::tc_fence_after();
+                if (nexact == 0) {
+                    mma8_ss(tmem + K::COL_Y, dsc_c, dsc_h, IDESC_Y, true, false, false);
+                } else {
+                    for (int j = 0; j < HG; ++j) {
+                        const uint64_t dh = ptx::desc_sw128(sbase + K::OFF_H + j * kTile, kTile, 1024);
+                        if (S(ts, j)[0] == 0.f) {
+                            mma8_ss(tmem + K::COL_Y + 64 * j, dsc_c, dh, IDESC_Y1, true, false, false);
+                        } else {
+                            const int r = exact_region(nexact, j, HG);
+                            rwait(r);
+                            ptx::tc_fence_after();
+                            const uint32_t ra = tmem + (r ? K::COL_R1 : K::COL_R0);
+                            mma8_ts(tmem + K::COL_Y + 64 * j, ra, dh, IDESC_Y1, false);
+                            ptx::mma_commit(&bars[B_R_EMPTY0 + r]);
+                        }
+                    }
+                }
+                ptx::mma_commit(&bars[B_H_EMPTY]);
+                ptx::mma_commit(&bars[B_C_EMPTY]);
+                // k5a: Y += L W (reference heads), Me X (exact heads)
+                const uint64_t dsc_w = ptx::desc_sw128(sbase + K::OFF_W + wb * HG * kTile, kTile, 1024);
+                // W built (and, through the W warps' waits, every X tile of this job landed)
+                WB(B_W_FULL0 + wb, (J >> 1) & 1);
+                if (nexact < HG) {
+                    rwait(0);
+                    ptx::tc_fence_after();
+                    if (nexact == 0) {
+                        mma8_ts(tmem + K::COL_Y, tmem + K::COL_R0, dsc_w, IDESC_Y, true);
+                    } else {
+                        for (int j = 0; j < HG; ++j) {
+                            if (S(ts, j)[0] != 0.f) continue;
+                            const uint64_t dw = dsc_w + ((j * kTile) >> 4);
+                            mma8_ts(tmem + K::COL_Y + 64 * j, tmem + K::COL_R0, dw, IDESC_Y1, true);
+                        }
+                    }
+                    ptx::mma_commit(&bars[B_R_EMPTY0]);
+                }
+                for (int j = 0; j < HG && nexact > 0; ++j) {
+                    if (S(ts, j)[0] == 0.f) continue;
+                    const int r = exact_region(nexact, j, HG);
+                    rwait(r);
+                    ptx::tc_fence_after();
+                    const int xs = (J * HG + j) % kNX;
+                    const uint64_t dx = ptx::desc_sw128(sbase + K::OFF_X + xs * kTile, kTile, 1024);
+                    const uint32_t ra = tmem + (r ? K::COL_R1 : K::COL_R0);
+                    mma8_ts(tmem + K::COL_Y + 64 * j, ra, dx, IDESC_Y1, true);
+                    ptx::mma_commit(&bars[B_R_EMPTY0 + r]);
+                    ptx::mma_commit(&bars[B_X_EMPTY0 + xs]);
+                }
+                ptx::mma_commit(&bars[B_W_EMPTY0 + wb]);
+                ptx::mma_commit(&bars[B_Y_FULL]);
+            }
+            ptx::mma_commit(&bars[B_DRAIN_A]);
+            ptx::mbar_wait(&bars[B_DRAIN_A], 0, kLocalWaitNs);
+        }
+        __syncwarp();
+    } else if (warp < 2 + HG) {
+        // ------------------------------------------------------------ tables for head j
+        const int j = warp - 2;
+        float pre[4];  // raw dt of the next job, loaded one job ahead
+        auto load_dt = [&](int J, float (&v)[4]) {
+            const JobPos jp_ = job_pos(jobs, J, chains_per_b, HG, HperG);
+            const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
+            (void)lo; (void)hi; (void)g; (void)h0; (void)b;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const long long t = static_cast<long long>(blk) * kT + 32 * i + lane;
+                v[i] = t < prm.L ? prm.dt[(static_cast<long long>(b) * prm.L + t) * prm.H + h0 + j] : 0.f;
+            }
+        };
+        if (njobs > 0) load_dt(0, pre);
+        for (int J = 0; J < njobs; ++J) {
+            const int ts = J & (kTabSlots - 1);
+            const JobPos jp_ = job_pos(jobs, J, chains_per_b, HG, HperG);
+            const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
+            (void)lo; (void)hi; (void)g; (void)h0; (void)b;
+            const int h = h0 + j;
+            float raw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) raw[i] = pre[i];
+            if (J + 1 < njobs) load_dt(J + 1, pre);
+            const float bias = prm.dt_bias[h], Ah = prm.A[h], Dh = prm.D ? prm.D[h] : 0.f;
+            float dtv[4], cs[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const long long t = static_cast<long long>(blk) * kT + 32 * i + lane;
+                dtv[i] = t < prm.L ? softplus_f(raw[i] + bias) : 0.f;
+                float v = dtv[i] * Ah;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, v, off);
+                    if (lane >= off) v += o;
+                }
+                cs[i] = v;
+            }
+            float run = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                cs[i] += run;
+                run = __shfl_sync(0xffffffffu, cs[i], 31);
+            }
+            const float cs_end = run;
+            const bool exact = -cs_end > kRefMaxDecay;
+            const float c = 0.5f * cs_end;
+            if (J >= kTabSlots) WB(B_TAB_EMPTY0 + ts, ((J / kTabSlots) - 1) & 1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = 32 * i + lane;
+                const float d = dtv[i];
+                T(ts, j, TAB_W)[t] = exact ? d * __expf(cs_end - cs[i]) : d * __expf(c - cs[i]);
+                T(ts, j, TAB_DT)[t] = d;
+                T(ts, j, TAB_CS)[t] = cs[i];
+            }
+            if (lane == 0) {
+                S(ts, j)[0] = exact ? 1.f : 0.f;
+                S(ts, j)[1] = c;
+                S(ts, j)[2] = cs_end;
+                S(ts, j)[3] = Dh;
+            }
+            warp_arrive(&bars[B_TAB_FULL0 + ts], lane);
+        }
+    } else if (warp < 4) {
+        // idle table warp (one head per chain)
+    } else if (wg == 1) {
+        // ------------------------------------------------------------ masks into TMEM
+        const int t = 32 * q + lane;
+        uint32_t writes0 = 0, writes1 = 0;  // fills of each region so far
+        bool dirty0 = true, dirty1 = true;  // tiles above this warp's diagonal are not known to be zero
+        auto claim = [&](int r) {
+            uint32_t& w = r ? writes1 : writes0;
+            if (w > 0) WB(B_R_EMPTY0 + r, (w - 1) & 1);
+            ++w;
+            ptx::tc_fence_after();
+        };
+        auto publish = [&](int r) {
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            warp_arrive(&bars[B_R_FULL0 + r], lane);
+        };
+        for (int J = 0; J < njobs; ++J) {
+            const int ts = J & (kTabSlots - 1);
+            WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
+            WB(B_C_FULL, J & 1);
+            WB(B_CB_FULL, J & 1);
+            ptx::tc_fence_after();
+            const int nexact = count_exact(ts);
+            // (a) C'_t = e^{cs_t} C_t for each exact-mode head (k5b reads it first)
+            for (int j = 0; j < HG && nexact > 0; ++j) {
+                if (S(ts, j)[0] == 0.f) continue;
+                const int r = exact_region(nexact, j, HG);
+                claim(r);
+                build_cprime(tmem + lane_base + (r ? K::COL_R1 : K::COL_R0), smem + K::OFF_C, t,
+                             __expf(T(ts, j, TAB_CS)[t]));
+                (r ? dirty1 : dirty0) = true;
+                publish(r);
+            }
+            // (b) L = C.B^T masked to s <= t, shared by the reference-mode heads
+            if (nexact < HG) {
+                claim(0);
+                const uint32_t dst = tmem + lane_base + K::COL_R0;
+#pragma unroll 1
+                for (int tile = 0; tile < 4; ++tile) {
+                    if (tile > q) {
+                        if (dirty0) {
+                            uint32_t z[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) z[e] = 0u;
+                            ptx::tmem_st16(dst + 16 * tile, z);
+                        }
+                        continue;
+                    }
+                    uint32_t rr[32];
+                    ptx::tmem_ld32(tmem + lane_base + K::COL_CB + 32 * tile, rr);
+                    ptx::tmem_wait_ld(rr);
+                    uint32_t pk[16];
+                    if (tile < q) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack_bf16x2(2 * e <= lane ? __uint_as_float(rr[2 * e]) : 0.f,
+                                                2 * e + 1 <= lane ? __uint_as_float(rr[2 * e + 1]) : 0.f);
+                    }
+                    ptx::tmem_st16(dst + 16 * tile, pk);
+                }
+                dirty0 = false;
+                publish(0);
+            }
+            // (c) Me for each exact-mode head, once k5b has read its C'
+            for (int j = 0; j < HG && nexact > 0; ++j) {
+                if (S(ts, j)[0] == 0.f) continue;
+                const int r = exact_region(nexact, j, HG);
+                claim(r);
+                build_exact_mask(tmem + lane_base + (r ? K::COL_R1 : K::COL_R0), tmem + lane_base + K::COL_CB, q, lane,
+                                 T(ts, j, TAB_CS), T(ts, j, TAB_DT), S(ts, j)[3]);
+                (r ? dirty1 : dirty0) = false;
+                publish(r);
+            }
+            warp_arrive(&bars[B_CB_EMPTY], lane);  // every C.B^T read of this job has completed
+        }
+    } else if (wg == 2) {
+        // ------------------------------------------------------------ W from X
+        const int wt = tid - 256;  // 0..127
+        for (int J = 0; J < njobs; ++J) {
+            const int ts = J & (kTabSlots - 1), wb = J & 1;
+            WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
+            if (J >= 2) WB(B_W_EMPTY0 + wb, ((J >> 1) - 1) & 1);
+#pragma unroll 1
+            for (int j = 0; j < HG; ++j) {
+                const int ix = J * HG + j, xs = ix % kNX;
+                const bool exact = S(ts, j)[0] != 0.f;
+                WB(B_X_FULL0 + xs, (ix / kNX) & 1);
+                const float* wf = T(ts, j, TAB_W);
+                const uint8_t* xb = smem + K::OFF_X + xs * kTile;
+                uint8_t* wbuf = smem + K::OFF_W + (wb * HG + j) * kTile;
+#pragma unroll 2
+                for (int i = 0; i < 8; ++i) {
+                    const int chunk = wt + 128 * i;  // 16-byte chunk; its row is chunk / 8 in either tile
+                    const int row = chunk >> 3;
+                    const uint4 v = *reinterpret_cast<const uint4*>(xb + chunk * 16);
+                    const float2 f0 = unpack_bf16x2(v.x), f1 = unpack_bf16x2(v.y), f2 = unpack_bf16x2(v.z),
+                                 f3 = unpack_bf16x2(v.w);
+                    const float w = wf[row];
+                    uint4 o;
+                    o.x = pack_bf16x2(f0.x * w, f0.y * w);
+                    o.y = pack_bf16x2(f1.x * w, f1.y * w);
+                    o.z = pack_bf16x2(f2.x * w, f2.y * w);
+                    o.w = pack_bf16x2(f3.x * w, f3.y * w);
+                    *reinterpret_cast<uint4*>(wbuf + chunk * 16) = o;
+                }
+                if (!exact) {
+                    // the X slot is free once all four warps have read it (exact mode:
+                    // k5a reads X, and its completion frees the slot)
+                    ptx::named_sync(1, 128);
+                    if (wt == 0) ptx::mbar_arrive(&bars[B_X_EMPTY0 + xs]);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            warp_arrive(&bars[B_W_FULL0 + wb], lane);
+        }
+    } else if (wg == 3) {
+        // ------------------------------------------------------------ state
+        const int n = 32 * q + lane;
+        const int st = tid - 384;  // 0..127
+        float sigma0 = 1.f, sigma1 = 1.f;  // per head: TMEM holds sigma * s
+        uint32_t sdone = 0;
+        for (int J = 0; J < njobs; ++J) {
+            const int ts = J & (kTabSlots - 1);
+            const JobPos jp_ = job_pos(jobs, J, chains_per_b, HG, HperG);
+            const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
+            (void)lo; (void)hi; (void)g; (void)h0; (void)b;
+            const bool seg_start = (blk == lo), seg_end = (blk == hi - 1);
+            if (seg_start && lo > 0) {
+                // wait for the previous CTA's hand-off of this chain's state
+                if (st == 0) {
+                    const uint32_t* f = prm.flags + (cta - 1);
+                    uint32_t v = ptx::ld_acquire_gpu(f);
+                    const uint64_t t0 = ptx::globaltimer_ns();
+                    while (v == 0u) {
+                        if (ptx::globaltimer_ns() - t0 > prm.chain_wait_ns) break;
+                        __nanosleep(256);
+                        v = ptx::ld_acquire_gpu(f);
+                    }
+                    misc[2] = (v == 0u) ? 1u : 0u;
+                    if (v == 0u) atomicOr(prm.status, 1u);
+                }
+                ptx::named_sync(2, 128);
+                ptx::fence_acquire_gpu();
+            }
+            WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
+            if (!seg_start) {
+                WB(B_S_DONE, sdone & 1);
+                ++sdone;
+                ptx::tc_fence_after();
+            }
+            if (J > 0) WB(B_H_EMPTY, (J - 1) & 1);
+#pragma unroll 1
+            for (int j = 0; j < HG; ++j) {
+                const int h = h0 + j;
+                const bool exact = S(ts, j)[0] != 0.f;
+                const float c = S(ts, j)[1], cs_end = S(ts, j)[2];
+                const float* src = nullptr;  // segment start: the incoming state, [p][n] rows of 128 floats
+                if (seg_start) {
+                    if (lo > 0)
+                        src = misc[2] ? nullptr : prm.handoff + (static_cast<size_t>(cta - 1) * HG + j) * kP * kN;
+                    else if (prm.init)
+                        src = prm.init + (static_cast<size_t>(b) * prm.H + h) * kP * kN;
+                    if (j) sigma1 = 1.f; else sigma0 = 1.f;
+                }
+                const float inv_sigma = 1.f / (j ? sigma1 : sigma0);
+                const float phi = (exact ? __expf(cs_end) : __expf(c)) * inv_sigma;  // z = phi * v
+                const float eta = exact ? inv_sigma : phi;                           // H = eta * v
+                uint8_t* hb = smem + K::OFF_H + j * kTile;
+                const uint32_t scol = tmem + lane_base + K::COL_S + 64 * j;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[32];
+                    if (seg_start) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            r[e] = __float_as_uint(src ? src[(32 * half + e) * kN + n] : 0.f);
+                    } else {
+                        ptx::tmem_ld32(scol + 32 * half, r);
+                        ptx::tmem_wait_ld(r);
+                    }
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(r[8 * c8 + 0]) * eta, __uint_as_float(r[8 * c8 + 1]) * eta);
+                        o.y = pack_bf16x2(__uint_as_float(r[8 * c8 + 2]) * eta, __uint_as_float(r[8 * c8 + 3]) * eta);
+                        o.z = pack_bf16x2(__uint_as_float(r[8 * c8 + 4]) * eta, __uint_as_float(r[8 * c8 + 5]) * eta);
+                        o.w = pack_bf16x2(__uint_as_float(r[8 * c8 + 6]) * eta, __uint_as_float(r[8 * c8 + 7]) * eta);
+                        *reinterpret_cast<uint4*>(hb + ptx::swz128(n, 4 * half + c8)) = o;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * phi);
+                    ptx::tmem_st32(scol + 32 * half, r);
+                }
+                const float sg = exact ? 1.f : __expf(c - cs_end);
+                if (j) sigma1 = sg; else sigma0 = sg;
+            }
+            ptx::tmem_wait_st();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            warp_arrive(&bars[B_SCALED], lane);
+            if (seg_end) {
+                // the chain's state after this block: final state, or the hand-off to CTA + 1
+                const bool to_final = (hi == prm.nblk);
+                WB(B_S_DONE, sdone & 1);
+                ++sdone;
+                ptx::tc_fence_after();
+#pragma unroll 1
+                for (int j = 0; j < HG; ++j) {
+                    const int h = h0 + j;
+                    float* dst = to_final
+                                     ? (prm.final_state ? prm.final_state + (static_cast<size_t>(b) * prm.H + h) * kP * kN
+                                                        : nullptr)
+                                     : prm.handoff + (static_cast<size_t>(cta) * HG + j) * kP * kN;
+                    const float inv_sigma = 1.f / (j ? sigma1 : sigma0);
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t r[32];
+                        ptx::tmem_ld32(tmem + lane_base + K::COL_S + 64 * j + 32 * half, r);
+                        ptx::tmem_wait_ld(r);
+                        if (dst) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) dst[(32 * half + e) * kN + n] = __uint_as_float(r[e]) * inv_sigma;
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                if (!to_final) {
+                    __threadfence();
+                    ptx::named_sync(2, 128);
+                    if (st == 0) ptx::st_release_gpu(prm.flags + cta, 1u);
+                }
+            }
+        }
+    } else if (wg == 4) {
+        // ------------------------------------------------------------ epilogue
+        // y is computed row by row into the job's W buffer (each thread reads its
+        // row of W for the D term, then overwrites the same bytes with y), so
+        // the accumulator is released as soon as it has been read, and y leaves
+        // through TMA stores of whole tiles.
+        const int t = 32 * q + lane;
+        const int et = tid - 512;  // 0..127
+        for (int J = 0; J < njobs; ++J) {
+            const int ts = J & (kTabSlots - 1), wb = J & 1;
+            const JobPos jp_ = job_pos(jobs, J, chains_per_b, HG, HperG);
+            const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
+            (void)lo; (void)hi; (void)g; (void)h0; (void)b;
+            WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
+            WB(B_K3_DONE0 + wb, (J >> 1) & 1);  // k3 no longer reads this W buffer
+            WB(B_Y_FULL, J & 1);
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int jh = 0; jh < 2 * HG; ++jh) {  // (head, 32-column half)
+                const int j = jh >> 1, half = jh & 1;
+                // row factor e^{cs_t - c} and D x_t = e^{cs_t - c} (D / dt_t) W_t (reference mode only)
+                const bool exact = S(ts, j)[0] != 0.f;
+                const float dtt = T(ts, j, TAB_DT)[t];
+                const float u = exact ? 1.f : __expf(T(ts, j, TAB_CS)[t] - S(ts, j)[1]);
+                const float du = (exact || dtt <= 0.f) ? 0.f : u * (S(ts, j)[3] / dtt);
+                uint8_t* wrow = smem + K::OFF_W + (wb * HG + j) * kTile;
+                uint32_t r[32];
+                ptx::tmem_ld32(tmem + lane_base + K::COL_Y + 32 * jh, r);
+                ptx::tmem_wait_ld(r);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint4* cell = reinterpret_cast<uint4*>(wrow + ptx::swz128(t, 4 * half + c8));
+                    const uint4 wv = *cell;
+                    const float2 w0 = unpack_bf16x2(wv.x), w1 = unpack_bf16x2(wv.y), w2 = unpack_bf16x2(wv.z),
+                                 w3 = unpack_bf16x2(wv.w);
+                    const float* yv = reinterpret_cast<const float*>(r) + 8 * c8;
+                    uint4 o;
+                    o.x = pack_bf16x2(fmaf(u, yv[0], du * w0.x), fmaf(u, yv[1], du * w0.y));
+                    o.y = pack_bf16x2(fmaf(u, yv[2], du * w1.x), fmaf(u, yv[3], du * w1.y));
+                    o.z = pack_bf16x2(fmaf(u, yv[4], du * w2.x), fmaf(u, yv[5], du * w2.y));
+                    o.w = pack_bf16x2(fmaf(u, yv[6], du * w3.x), fmaf(u, yv[7], du * w3.y));
+                    *cell = o;
+                }
+            }
+            ptx::tc_fence_before();
+            warp_arrive(&bars[B_Y_EMPTY], lane);         // the accumulator has been read
+            warp_arrive(&bars[B_TAB_EMPTY0 + ts], lane); // so have this job's tables
+            ptx::fence_proxy_async_smem();
+            ptx::named_sync(3, 128);
+            if (et == 0) {
+                for (int j = 0; j < HG; ++j)
+                    ptx::tma_store_4d(&tm_y, smem + K::OFF_W + (wb * HG + j) * kTile, 0, h0 + j, blk * kT, b);
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group_read0();            // the W buffer may be rebuilt once read
+                ptx::mbar_arrive(&bars[B_W_EMPTY0 + wb]);
+            }
+        }
+        if (et == 0) ptx::bulk_wait_group0();            // y is in global memory before the CTA exits
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 0) ptx::tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- host side
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+struct ChainPlan {
+    int hg;
+    int ncta;
+    long long nchains, nblk, total;
+};
+
+// Heads per chain and CTA count. Two heads share B, C and C.B^T, but halve the
+// number of chains; a chain split across CTAs serialises its blocks, so the
+// choice minimises max(jobs per CTA, blocks per chain) x relative job cost.
+ChainPlan plan(const ssd_dims& d, int nsm) {
+    ChainPlan p;
+    p.nblk = (d.seqlen + kT - 1) / kT;
+    const bool pair_ok = (d.nheads / d.ngroups) % 2 == 0;
+    double best = 1e300;
+    p.hg = 1;
+    for (int hg = 1; hg <= (pair_ok ? 2 : 1); ++hg) {
+        const long long chains = d.batch * d.nheads / hg;
+        const long long total = chains * p.nblk;
+        const double per_cta = static_cast<double>(total) / std::min<long long>(nsm, total);
+        const double cost = std::max(per_cta, static_cast<double>(p.nblk)) * (hg == 2 ? 1.5 : 1.0);
+        if (cost < best) {
+            best = cost;
+            p.hg = hg;
+        }
+    }
+    p.nchains = d.batch * d.nheads / p.hg;
+    p.total = p.nchains * p.nblk;
+    p.ncta = static_cast<int>(std::min<long long>(nsm, p.total));
+    return p;
+}
+
+size_t counters_bytes(int ncta) { return align_up(sizeof(uint32_t) * (1 + static_cast<size_t>(ncta)), kWorkspaceAlign); }
+
+template <int HG>
+ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
+    using K = ChainCfg<HG>;
+    const ssd_dims& d = a.d;
+    CUtensorMap tx, tb, tc, ty;
+    if (!make_map_bf16(&tx, a.x, d.headdim, d.nheads, d.seqlen, d.batch) ||
+        !make_map_bf16(&tb, a.B, d.dstate, d.ngroups, d.seqlen, d.batch) ||
+        !make_map_bf16(&tc, a.C, d.dstate, d.ngroups, d.seqlen, d.batch) ||
+        !make_map_bf16(&ty, a.y, d.headdim, d.nheads, d.seqlen, d.batch))
+        return SSD_ERR_CUDA;
+    const size_t counters = counters_bytes(pl.ncta);
+    if (cudaMemsetAsync(ws, 0, counters, a.stream) != cudaSuccess) return SSD_ERR_CUDA;
+    ChainParams p;
+    p.dt = a.dt;
+    p.dt_bias = a.dt_bias;
+    p.A = a.A;
+    p.D = a.D;
+    p.init = a.init;
+    p.final_state = a.final_state;
+    p.y = static_cast<__nv_bfloat16*>(a.y);
+    p.ticket = static_cast<uint32_t*>(ws);
+    p.flags = p.ticket + 1;
+    p.handoff = reinterpret_cast<float*>(static_cast<char*>(ws) + counters);
+    p.status = a.status_word;
+    p.batch = static_cast<int>(d.batch);
+    p.H = static_cast<int>(d.nheads);
+    p.G = static_cast<int>(d.ngroups);
+    p.nblk = static_cast<int>(pl.nblk);
+    p.nchains = static_cast<int>(pl.nchains);
+    p.ncta = pl.ncta;
+    p.L = d.seqlen;
+    p.total = pl.total;
+    p.chain_wait_ns = a.wait_limit_ns;
+    if (cudaFuncSetAttribute(ssd_chain_fused<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(K::SMEM_BYTES)) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    ssd_chain_fused<HG><<<static_cast<unsigned>(pl.ncta), kThreads, K::SMEM_BYTES, a.stream>>>(tx, tb, tc, ty, p);
+    note_launches(1);
+    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // namespace
+
+bool chain_supported(const ssd_dims& d, ssd_dtype io, int chunk_len) {
+    if (io != SSD_BF16) return false;
+    if (d.headdim != kP || d.dstate != kN) return false;
+    if (chunk_len != 128 && chunk_len != 256) return false;
+    if (d.seqlen >= (1ll << 31) || d.batch >= (1ll << 20) || d.nheads >= (1 << 20)) return false;
+    const long long nblk = (d.seqlen + kT - 1) / kT;
+    if (nblk * d.batch * d.nheads >= (1ll << 31)) return false;  // job indices are 32-bit
+    return true;
+}
+
+size_t chain_workspace_bytes(const ssd_dims& d) {
+    const int nsm = sm_count();
+    if (nsm <= 0) {
+        // no device to ask: size for the largest CTA count a device may have
+        const size_t cta = 1024;
+        return counters_bytes(static_cast<int>(cta)) + align_up(cta * 2 * kP * kN * sizeof(float), kWorkspaceAlign);
+    }
+    const ChainPlan pl = plan(d, nsm);
+    return counters_bytes(pl.ncta) +
+           align_up(static_cast<size_t>(pl.ncta) * pl.hg * kP * kN * sizeof(float), kWorkspaceAlign);
+}
+
+ssd_status chain_forward(const FwdArgs& a, void* ws, size_t ws_bytes) {
+    const int nsm = sm_count();
+    if (nsm <= 0) return SSD_ERR_CUDA;
+    const ChainPlan pl = plan(a.d, nsm);
+    if (ws_bytes < counters_bytes(pl.ncta) + align_up(static_cast<size_t>(pl.ncta) * pl.hg * kP * kN * sizeof(float),
+                                                      kWorkspaceAlign))
+        return SSD_ERR_WORKSPACE;
+    for (const void* p : {a.x, static_cast<const void*>(a.B), static_cast<const void*>(a.C),
+                          static_cast<const void*>(a.y)})
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return SSD_ERR_UNSUPPORTED;
+    return pl.hg == 2 ? launch_chain<2>(a, ws, pl) : launch_chain<1>(a, ws, pl);
+}
+
+}  // namespace ssd

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ssd.h"
@@ -39,6 +40,15 @@ ssd_status simt_forward(const FwdArgs& a, void* ws, size_t ws_bytes);
 bool tc_supported(const ssd_dims& d, ssd_dtype io, int chunk_len);
 size_t tc_workspace_bytes(const ssd_dims& d, int chunk_len);
 ssd_status tc_forward(const FwdArgs& a, void* ws, size_t ws_bytes);
+
+// Chain-local fused tcgen05/TMA path (dstate 128): persistent CTAs, state kept on chip.
+bool chain_supported(const ssd_dims& d, ssd_dtype io, int chunk_len);
+size_t chain_workspace_bytes(const ssd_dims& d);
+ssd_status chain_forward(const FwdArgs& a, void* ws, size_t ws_bytes);
+
+// 4-D bf16 TMA map over a row-major [outer, rows, mid, inner] tensor, box
+// {64, 1, 128, 1}, 128-byte swizzle, zero fill out of bounds.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t rows, uint64_t outer);
 
 // Launch bookkeeping (every kernel launch of the library goes through it).
 void note_launches(uint64_t n);

@@ -695,19 +695,6 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 4-D bf16 map over a [outer, rows, mid, inner] row-major tensor, box {64, 1, 128, 1}.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t rows, uint64_t outer) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[4] = {inner, mid, rows, outer};
-    const cuuint64_t strides[3] = {inner * 2, mid * inner * 2, rows * mid * inner * 2};
-    const cuuint32_t box[4] = {64, 1, kT, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Work ticket, then one flag per (chain, parity); cleared before every launch.
 size_t tc_counters_bytes(const ssd_dims& d) {
     return align_up(sizeof(uint32_t) * static_cast<size_t>(1 + 2 * d.batch * d.nheads), kWorkspaceAlign);
@@ -726,10 +713,10 @@ ssd_status launch(const FwdArgs& a, void* ws) {
     using K = Cfg<NST>;
     const ssd_dims& d = a.d;
     CUtensorMap tx, tb, tc, ty;
-    if (!make_map(&tx, a.x, d.headdim, d.nheads, d.seqlen, d.batch) ||
-        !make_map(&tb, a.B, d.dstate, d.ngroups, d.seqlen, d.batch) ||
-        !make_map(&tc, a.C, d.dstate, d.ngroups, d.seqlen, d.batch) ||
-        !make_map(&ty, a.y, d.headdim, d.nheads, d.seqlen, d.batch))
+    if (!make_map_bf16(&tx, a.x, d.headdim, d.nheads, d.seqlen, d.batch) ||
+        !make_map_bf16(&tb, a.B, d.dstate, d.ngroups, d.seqlen, d.batch) ||
+        !make_map_bf16(&tc, a.C, d.dstate, d.ngroups, d.seqlen, d.batch) ||
+        !make_map_bf16(&ty, a.y, d.headdim, d.nheads, d.seqlen, d.batch))
         return SSD_ERR_CUDA;
     const size_t counters = tc_counters_bytes(d);
     if (cudaMemsetAsync(ws, 0, counters, a.stream) != cudaSuccess) return SSD_ERR_CUDA;
@@ -762,6 +749,18 @@ ssd_status launch(const FwdArgs& a, void* ws) {
 }
 
 }  // namespace
+
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t rows, uint64_t outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {inner, mid, rows, outer};
+    const cuuint64_t strides[3] = {inner * 2, mid * inner * 2, rows * mid * inner * 2};
+    const cuuint32_t box[4] = {64, 1, kT, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool tc_supported(const ssd_dims& d, ssd_dtype io, int chunk_len) {
     if (io != SSD_BF16) return false;

@@ -1,0 +1,158 @@
+"""GPU parity of the chain-local tensor-core path (SSD_PATH_CHAIN) against the
+fp64 oracle.
+
+The cases cover: one tile, a single token, lengths one below / above a tile,
+ragged lengths, one head per chain (odd heads per group) and head pairs;
+chains split across CTAs (a hand-off at every block, and hand-offs in the
+middle of long chains); blocks whose decay selects the exact mode, the
+reference mode, and both within one head pair; absent D / initial state /
+final state; and agreement with the per-block tensor-core path.
+Tolerance: max|delta| / max|ref| <= 2e-2 on y and on the final state (bf16 io).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from forms import rel_err
+from gpu_util import TOL, check_against_oracle, check_sampled, oracle_full, run_gpu, to_device
+from mamba_ssd_chunked_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mamba_ssd_chunked_gb300 import build
+    build.build()
+
+
+CHAIN_SHAPES = [
+    # b, L, h, p, g, n
+    (1, 128, 1, 64, 1, 128),      # one tile, one head
+    (1, 1, 2, 64, 1, 128),        # a single token
+    (2, 127, 4, 64, 2, 128),      # one below a tile
+    (2, 129, 4, 64, 1, 128),      # one above a tile
+    (2, 300, 4, 64, 2, 128),      # ragged, several tiles
+    (1, 1000, 3, 64, 3, 128),     # one head per group: one head per chain
+    (3, 513, 8, 64, 2, 128),
+    (1, 2000, 2, 64, 1, 128),     # one chain spread over many CTAs: a hand-off at every block
+    (2, 4100, 6, 64, 1, 128),     # long chains split across CTAs mid-chain
+]
+
+
+@pytest.mark.parametrize("shape", CHAIN_SHAPES)
+@pytest.mark.parametrize("chunk_len", [128, 256])
+def test_chain_path_matches_oracle(shape, chunk_len):
+    check_against_oracle(shape, "bf16", chunk_len, "chain", seed=sum(shape) + chunk_len + 1)
+
+
+@pytest.mark.parametrize("dt_shift,A_scale", [(3.0, 4.0), (1.0, 2.0), (-2.0, 0.25), (0.0, 1.0)])
+def test_chain_path_strong_and_weak_decay(dt_shift, A_scale):
+    """Uniformly strong decay (every block in exact mode), moderate, weak."""
+    inp = make_inputs(2, 1100, 8, 64, 2, 128, io_dtype="bf16", init="normal", seed=43)
+    inp["dt"] = (inp["dt"] + dt_shift).astype(np.float32)
+    inp["A"] = (inp["A"] * A_scale).astype(np.float32)
+    t = to_device(inp, "bf16")
+    y, fs = run_gpu(t, 256, "chain")
+    y_ref, f_ref = oracle_full(inp)
+    assert rel_err(y.float().cpu().numpy(), y_ref) < 2e-2
+    assert rel_err(fs.cpu().numpy(), f_ref) < 2e-2
+
+
+def test_chain_path_mixed_modes_within_a_pair():
+    """Heads of one pair alternate between the exact and the reference mode,
+    and a head's blocks switch modes along the chain (dt bursts)."""
+    b, L, h = 2, 1500, 4
+    inp = make_inputs(b, L, h, 64, 1, 128, io_dtype="bf16", init="normal", seed=47)
+    inp["A"] = np.array([-0.5, -12.0, -2.0, -16.0], dtype=np.float32)
+    dt = inp["dt"]
+    dt[:, 300:420, :] += 3.0          # a burst: strong decay in a few blocks only
+    dt[:, 900:1000, 0] += 4.0
+    inp["dt"] = dt.astype(np.float32)
+    t = to_device(inp, "bf16")
+    y, fs = run_gpu(t, 256, "chain")
+    y_ref, f_ref = oracle_full(inp)
+    assert rel_err(y.float().cpu().numpy(), y_ref) < 2e-2
+    assert rel_err(fs.cpu().numpy(), f_ref) < 2e-2
+
+
+@pytest.mark.parametrize("init,with_D", [("zero", True), ("normal", False), ("zero", False)])
+def test_chain_path_optional_inputs(init, with_D):
+    check_against_oracle((2, 400, 4, 64, 2, 128), "bf16", 256, "chain", init=init, with_D=with_D, seed=8)
+
+
+def test_chain_path_final_state_optional():
+    inp = make_inputs(1, 300, 2, 64, 1, 128, io_dtype="bf16", init="normal", seed=20)
+    t = to_device(inp, "bf16")
+    y, fs = run_gpu(t, 256, "chain", return_final_state=False)
+    assert fs is None
+    y_ref, _ = oracle_full(inp)
+    assert rel_err(y.float().cpu().numpy(), y_ref) < 2e-2
+
+
+@pytest.mark.parametrize("split", [256, 200])
+def test_chain_path_split_sequence_carries_state(split):
+    L = 900
+    inp = make_inputs(2, L, 4, 64, 2, 128, io_dtype="bf16", init="normal", seed=14)
+    t = to_device(inp, "bf16")
+    y, fs = run_gpu(t, 256, "chain")
+    first = {k: (v[:, :split].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in t.items()}
+    second = {k: (v[:, split:].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in t.items()}
+    y1, f1 = run_gpu(first, 256, "chain")
+    second["init_state"] = f1
+    y2, f2 = run_gpu(second, 256, "chain")
+    y_cat = torch.cat([y1, y2], dim=1).float().cpu().numpy()
+    assert rel_err(y_cat, y.float().cpu().numpy()) < TOL["bf16"]
+    assert rel_err(f2.cpu().numpy(), fs.cpu().numpy()) < TOL["bf16"]
+
+
+def test_chain_path_repeat_runs_are_bitwise_identical():
+    inp = make_inputs(2, 2900, 8, 64, 2, 128, io_dtype="bf16", init="normal", seed=18)
+    t = to_device(inp, "bf16")
+    y1, f1 = run_gpu(t, 256, "chain")
+    y2, f2 = run_gpu(t, 256, "chain")
+    assert torch.equal(y1, y2) and torch.equal(f1, f2)
+
+
+def test_chain_and_per_block_paths_agree():
+    inp = make_inputs(2, 1600, 6, 64, 2, 128, io_dtype="bf16", init="normal", seed=10)
+    t = to_device(inp, "bf16")
+    y1, f1 = run_gpu(t, 256, "chain")
+    y2, f2 = run_gpu(t, 256, "tc")
+    assert rel_err(y1.float().cpu().numpy(), y2.float().cpu().numpy()) < 2e-2
+    assert rel_err(f1.cpu().numpy(), f2.cpu().numpy()) < 2e-2
+
+
+def test_chain_path_headline_strongest_heads():
+    """The Mamba2-2.7B layer shape, checked on the heads with the strongest and
+    the weakest decay (exact mode in most blocks / reference mode throughout)."""
+    from mamba_ssd_chunked_gb300.inputs import workload_inputs
+    inp = workload_inputs("mamba2_2p7b_layer")
+    t = to_device(inp, "bf16")
+    y, fs = run_gpu(t, 256, "chain")
+    dt = np.logaddexp(0.0, inp["dt"].astype(np.float64) + inp["dt_bias"])
+    rate = (dt * -inp["A"]).mean(axis=(0, 1))
+    order = np.argsort(rate)
+    heads = [int(order[-1]), int(order[-2]), int(order[0])]
+    chains = sorted({(bi, hi) for bi in (0, 3) for hi in heads})
+    check_sampled(inp, y, fs, chains, "bf16")
+
+
+@pytest.mark.parametrize("name", ["mamba2_130m_layer", "grouped_ragged"])
+def test_chain_path_full_size_workloads(name):
+    """Full-size workloads with dstate 128 through the chain path, on a seeded
+    sample of (batch, head) chains plus the strongest-decay head."""
+    from gpu_util import sampled_chains
+    from mamba_ssd_chunked_gb300.inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS[name]
+    inp = workload_inputs(name)
+    t = to_device(inp, "bf16")
+    y, fs = run_gpu(t, w.chunk_len, "chain")
+    dt = np.logaddexp(0.0, inp["dt"].astype(np.float64) + inp["dt_bias"])
+    strongest = int(np.argmax((dt * -inp["A"]).mean(axis=(0, 1))))
+    chains = sorted(set(sampled_chains(w.batch, w.nheads, 8, seed=w.seed)) | {(0, strongest), (w.batch - 1, strongest)})
+    check_sampled(inp, y, fs, chains, "bf16")
+    assert torch.isfinite(y.float()).all() and torch.isfinite(fs).all()

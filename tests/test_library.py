@@ -115,6 +115,7 @@ def test_workspace_too_small(lib):
 
 def test_path_selection(lib):
     assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 256) == "tc"
+    assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 128) == "tc"
     assert pkg.ssd_select_path(1, 131072, 64, 64, 1, 256, "bf16", 256) == "tc"
     assert pkg.ssd_select_path(1, 256, 4, 16, 1, 16, "f32", 64) == "simt"
     assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "f32", 256) == "simt"
@@ -134,6 +135,11 @@ def test_workspace_sizes(lib):
     need = pkg.ssd_fwd_workspace_bytes(1, 256, 4, 16, 1, 16, "f32", 64, "simt")
     assert need >= 4 * 1 * 4 * 4 * 16 * 16
     assert pkg.ssd_fwd_workspace_bytes(1, 256, 4, 16, 1, 16, "f32", 64, "tc") == 0
+    # chain path: a counter and flag per CTA, one hand-off state per CTA; without a
+    # device to ask for its SM count it sizes for 1024 CTAs of two heads
+    need = pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, n, "bf16", 256, "chain")
+    assert need >= 1024 * 2 * p * n * 4
+    assert pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, 256, "bf16", 256, "chain") == 0
 
 
 def test_kernel_counter_starts_without_launches(lib):
