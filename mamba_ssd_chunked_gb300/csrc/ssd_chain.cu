@@ -32,9 +32,9 @@
 // use "exact" mode, per head:
 //
 //   W_s  = X_s dt_s e^{cs_end - cs_s}  (k3),   z = e^{cs_end} s_in,  H = s_in,
-//   C'_t = e^{cs_t} C_t (A operand in TMEM),   k5b: Y = C' H^T,
+//   k5b: Yo = C H^T (into the C.B^T columns, free once the masks are built),
 //   Me[t][s] = C_t.B_s e^{cs_t - cs_s} dt_s (s < t), C_t.B_t dt_t + D (s = t),
-//   k5a: Y += Me X,  y_t = Y_t,
+//   k5a: Y = Me X,  y_t = Y_t + e^{cs_t} Yo_t,
 //
 // where every factor is at most 1 (underflow only drops negligible terms).
 //
@@ -43,7 +43,7 @@
 //                MMA issuer of the state path (k3), polled with the loads
 //   warp 1       MMA issuer, output path: C.B^T, k5b, k5a
 //   warps 2..3   tables: dt, cumsum and per-token factors, one head each
-//   warps 4..7   masks into TMEM: L (shared), and per exact-mode head C', Me
+//   warps 4..7   masks into TMEM: L (shared), and Me per exact-mode head
 //   warps 8..11  W from X
 //   warps 12..15 state: rescale z in TMEM, write H; load / store states at segment ends
 //   warps 16..19 epilogue: y from TMEM (+ D x from W), stored straight to global memory
@@ -100,7 +100,7 @@ enum Bar {
     B_X_FULL0, B_X_FULL1, B_X_FULL2, B_X_EMPTY0, B_X_EMPTY1, B_X_EMPTY2,
     B_CB_FULL, B_CB_EMPTY,
     B_R_FULL0, B_R_FULL1, B_R_EMPTY0, B_R_EMPTY1,
-    B_Y_FULL, B_Y_EMPTY,
+    B_Y_FULL, B_Y_EMPTY, B_YO_FREE,
     B_TAB_FULL0, B_TAB_FULL1, B_TAB_FULL2, B_TAB_FULL3, B_TAB_EMPTY0, B_TAB_EMPTY1, B_TAB_EMPTY2, B_TAB_EMPTY3,
     B_W_FULL0, B_W_FULL1, B_W_EMPTY0, B_W_EMPTY1,
     B_SCALED, B_S_DONE, B_H_EMPTY,
@@ -230,28 +230,6 @@ __device__ __forceinline__ int exact_region(int nexact, int j, int HG) {
 }
 
 
-// C'_t = e^{cs_t} C_t into 64 TMEM columns of this thread's lane (row t):
-// pairs of n as bf16, the A operand of an exact-mode k5b. C is [t][n] in two
-// 128-byte-swizzled tiles of 64 columns.
-__device__ __noinline__ void build_cprime(uint32_t dst, const uint8_t* c_tiles, int t, float e_t) {
-#pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {  // 16 TMEM columns = 32 values of n per step
-        uint32_t pk[16];
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-            const int chunk = 4 * (ch & 1) + c8;  // 16-byte chunk within the 64-column tile
-            const uint4 v = *reinterpret_cast<const uint4*>(c_tiles + (ch >> 1) * kTile + ptx::swz128(t, chunk));
-            const float2 a0 = unpack_bf16x2(v.x), a1 = unpack_bf16x2(v.y), a2 = unpack_bf16x2(v.z),
-                         a3 = unpack_bf16x2(v.w);
-            pk[4 * c8 + 0] = pack_bf16x2(a0.x * e_t, a0.y * e_t);
-            pk[4 * c8 + 1] = pack_bf16x2(a1.x * e_t, a1.y * e_t);
-            pk[4 * c8 + 2] = pack_bf16x2(a2.x * e_t, a2.y * e_t);
-            pk[4 * c8 + 3] = pack_bf16x2(a3.x * e_t, a3.y * e_t);
-        }
-        ptx::tmem_st16(dst + 16 * ch, pk);
-    }
-}
-
 // Exact-mode masked matrix of one head into 64 TMEM columns of this thread's
 // lane (row t = 32 q + lane): Me[t][s] = CB[t][s] e^{cs_t - cs_s} dt_s for
 // s < t, CB[t][t] dt_t + D on the diagonal, zero above. Every tile is written.
@@ -338,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         counts[B_CB_EMPTY] = 4;                                 // mask warps
         counts[B_R_FULL0] = counts[B_R_FULL1] = 4;              // mask warps
         counts[B_Y_EMPTY] = 4;                                  // epilogue warps
+        counts[B_YO_FREE] = 4;                                  // epilogue warps (jobs with exact heads)
         for (int i = 0; i < kTabSlots; ++i) {
             counts[B_TAB_FULL0 + i] = HG;                       // table warps
             counts[B_TAB_EMPTY0 + i] = 4;                       // epilogue warps
@@ -474,18 +453,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dsc_c = ptx::desc_sw128(sbase + K::OFF_C, 16, 1024);
             const uint64_t dsc_b = ptx::desc_sw128(sbase + K::OFF_B, 16, 1024);
             const uint64_t dsc_h = ptx::desc_sw128(sbase + K::OFF_H, kTile, 1024);
+            bool prev_exact = false;  // the previous job left Yo of exact heads in the C.B^T columns
+            uint32_t yo_uses = 0;
             for (int J = 0; J < njobs; ++J) {
                 const int ts = J & (kTabSlots - 1), wb = J & 1;
                 WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
                 WB(B_B_FULL, J & 1);
                 WB(B_C_FULL, J & 1);
                 if (J > 0) WB(B_CB_EMPTY, (J - 1) & 1);
+                if (prev_exact) {
+                    WB(B_YO_FREE, yo_uses & 1);
+                    ++yo_uses;
+                }
                 ptx::tc_fence_after();
                 const int nexact = count_exact(ts);
                 mma8_ss(tmem + K::COL_CB, dsc_c, dsc_b, IDESC_CB, true, true, false);
                 ptx::mma_commit(&bars[B_CB_FULL]);
                 ptx::mma_commit(&bars[B_B_EMPTY]);
-                // k5b: Y = C H^T (reference heads), C' H^T (exact heads)
+                // k5b: Y = C H^T for reference heads (H = e^{c} s_in); for exact heads
+                // Yo = C H^T (H = s_in) into the C.B^T columns once the masks have read them
                 WB(B_SCALED, J & 1);
                 if (J > 0) WB(B_Y_EMPTY, (J - 1) & 1);
                 ptx::tc_fence_after();
@@ -493,22 +479,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma8_ss(tmem + K::COL_Y, dsc_c, dsc_h, IDESC_Y, true, false, false);
                 } else {
                     for (int j = 0; j < HG; ++j) {
+                        if (S(ts, j)[0] != 0.f) continue;
                         const uint64_t dh = ptx::desc_sw128(sbase + K::OFF_H + j * kTile, kTile, 1024);
-                        if (S(ts, j)[0] == 0.f) {
-                            mma8_ss(tmem + K::COL_Y + 64 * j, dsc_c, dh, IDESC_Y1, true, false, false);
-                        } else {
-                            const int r = exact_region(nexact, j, HG);
-                            rwait(r);
-                            ptx::tc_fence_after();
-                            const uint32_t ra = tmem + (r ? K::COL_R1 : K::COL_R0);
-                            mma8_ts(tmem + K::COL_Y + 64 * j, ra, dh, IDESC_Y1, false);
-                            ptx::mma_commit(&bars[B_R_EMPTY0 + r]);
-                        }
+                        mma8_ss(tmem + K::COL_Y + 64 * j, dsc_c, dh, IDESC_Y1, true, false, false);
+                    }
+                    WB(B_CB_EMPTY, J & 1);
+                    ptx::tc_fence_after();
+                    for (int j = 0; j < HG; ++j) {
+                        if (S(ts, j)[0] == 0.f) continue;
+                        const uint64_t dh = ptx::desc_sw128(sbase + K::OFF_H + j * kTile, kTile, 1024);
+                        mma8_ss(tmem + K::COL_CB + 64 * j, dsc_c, dh, IDESC_Y1, true, false, false);
                     }
                 }
                 ptx::mma_commit(&bars[B_H_EMPTY]);
                 ptx::mma_commit(&bars[B_C_EMPTY]);
-                // k5a: Y += L W (reference heads), Me X (exact heads)
+                // k5a: Y += L W (reference heads); Y = Me X (exact heads)
                 const uint64_t dsc_w = ptx::desc_sw128(sbase + K::OFF_W + wb * HG * kTile, kTile, 1024);
                 // W built (and, through the W warps' waits, every X tile of this job landed)
                 WB(B_W_FULL0 + wb, (J >> 1) & 1);
@@ -534,12 +519,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int xs = (J * HG + j) % kNX;
                     const uint64_t dx = ptx::desc_sw128(sbase + K::OFF_X + xs * kTile, kTile, 1024);
                     const uint32_t ra = tmem + (r ? K::COL_R1 : K::COL_R0);
-                    mma8_ts(tmem + K::COL_Y + 64 * j, ra, dx, IDESC_Y1, true);
+                    mma8_ts(tmem + K::COL_Y + 64 * j, ra, dx, IDESC_Y1, false);
                     ptx::mma_commit(&bars[B_R_EMPTY0 + r]);
                     ptx::mma_commit(&bars[B_X_EMPTY0 + xs]);
                 }
                 ptx::mma_commit(&bars[B_W_EMPTY0 + wb]);
                 ptx::mma_commit(&bars[B_Y_FULL]);
+                prev_exact = nexact > 0;
             }
             ptx::mma_commit(&bars[B_DRAIN_A]);
             ptx::mbar_wait(&bars[B_DRAIN_A], 0, kLocalWaitNs);
@@ -631,20 +617,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int J = 0; J < njobs; ++J) {
             const int ts = J & (kTabSlots - 1);
             WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
-            WB(B_C_FULL, J & 1);
             WB(B_CB_FULL, J & 1);
             ptx::tc_fence_after();
             const int nexact = count_exact(ts);
-            // (a) C'_t = e^{cs_t} C_t for each exact-mode head (k5b reads it first)
-            for (int j = 0; j < HG && nexact > 0; ++j) {
-                if (S(ts, j)[0] == 0.f) continue;
-                const int r = exact_region(nexact, j, HG);
-                claim(r);
-                build_cprime(tmem + lane_base + (r ? K::COL_R1 : K::COL_R0), smem + K::OFF_C, t,
-                             __expf(T(ts, j, TAB_CS)[t]));
-                (r ? dirty1 : dirty0) = true;
-                publish(r);
-            }
             // (b) L = C.B^T masked to s <= t, shared by the reference-mode heads
             if (nexact < HG) {
                 claim(0);
@@ -679,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dirty0 = false;
                 publish(0);
             }
-            // (c) Me for each exact-mode head, once k5b has read its C'
+            // (c) Me for each exact-mode head
             for (int j = 0; j < HG && nexact > 0; ++j) {
                 if (S(ts, j)[0] == 0.f) continue;
                 const int r = exact_region(nexact, j, HG);
@@ -780,9 +755,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         src = prm.init + (static_cast<size_t>(b) * prm.H + h) * kP * kN;
                     if (j) sigma1 = 1.f; else sigma0 = 1.f;
                 }
+                // s = v / sigma is the true state; z = s e^{c} (reference) or s e^{cs_end} (exact).
+                // The two factors are applied one after the other: their product
+                // e^{c} / sigma can fall below the fp32 range when consecutive
+                // blocks both decay strongly, while s and z stay representable.
                 const float inv_sigma = 1.f / (j ? sigma1 : sigma0);
-                const float phi = (exact ? __expf(cs_end) : __expf(c)) * inv_sigma;  // z = phi * v
-                const float eta = exact ? inv_sigma : phi;                           // H = eta * v
+                const float f = exact ? __expf(cs_end) : __expf(c);
                 uint8_t* hb = smem + K::OFF_H + j * kTile;
                 const uint32_t scol = tmem + lane_base + K::COL_S + 64 * j;
 #pragma unroll 1
@@ -797,16 +775,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tmem_wait_ld(r);
                     }
 #pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * inv_sigma);  // s
+                    // H = bf16(z) (reference) or bf16(s) (exact)
+                    const float hf = exact ? 1.f : f;
+#pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
                         uint4 o;
-                        o.x = pack_bf16x2(__uint_as_float(r[8 * c8 + 0]) * eta, __uint_as_float(r[8 * c8 + 1]) * eta);
-                        o.y = pack_bf16x2(__uint_as_float(r[8 * c8 + 2]) * eta, __uint_as_float(r[8 * c8 + 3]) * eta);
-                        o.z = pack_bf16x2(__uint_as_float(r[8 * c8 + 4]) * eta, __uint_as_float(r[8 * c8 + 5]) * eta);
-                        o.w = pack_bf16x2(__uint_as_float(r[8 * c8 + 6]) * eta, __uint_as_float(r[8 * c8 + 7]) * eta);
+                        o.x = pack_bf16x2(__uint_as_float(r[8 * c8 + 0]) * hf, __uint_as_float(r[8 * c8 + 1]) * hf);
+                        o.y = pack_bf16x2(__uint_as_float(r[8 * c8 + 2]) * hf, __uint_as_float(r[8 * c8 + 3]) * hf);
+                        o.z = pack_bf16x2(__uint_as_float(r[8 * c8 + 4]) * hf, __uint_as_float(r[8 * c8 + 5]) * hf);
+                        o.w = pack_bf16x2(__uint_as_float(r[8 * c8 + 6]) * hf, __uint_as_float(r[8 * c8 + 7]) * hf);
                         *reinterpret_cast<uint4*>(hb + ptx::swz128(n, 4 * half + c8)) = o;
                     }
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * phi);
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);  // z
                     ptx::tmem_st32(scol + 32 * half, r);
                 }
                 const float sg = exact ? 1.f : __expf(c - cs_end);
@@ -878,6 +860,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[32];
                 ptx::tmem_ld32(tmem + lane_base + K::COL_Y + 32 * jh, r);
                 ptx::tmem_wait_ld(r);
+                if (exact) {
+                    // state term of an exact-mode head: e^{cs_t} (C s_in^T)_t, from the C.B^T columns
+                    uint32_t ro[32];
+                    ptx::tmem_ld32(tmem + lane_base + K::COL_CB + 32 * jh, ro);
+                    ptx::tmem_wait_ld(ro);
+                    const float e_t = __expf(T(ts, j, TAB_CS)[t]);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(fmaf(e_t, __uint_as_float(ro[e]), __uint_as_float(r[e])));
+                }
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
                     uint4* cell = reinterpret_cast<uint4*>(wrow + ptx::swz128(t, 4 * half + c8));
@@ -895,6 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tc_fence_before();
             warp_arrive(&bars[B_Y_EMPTY], lane);         // the accumulator has been read
+            if (count_exact(ts) > 0) warp_arrive(&bars[B_YO_FREE], lane);  // and Yo in the C.B^T columns
             warp_arrive(&bars[B_TAB_EMPTY0 + ts], lane); // so have this job's tables
             ptx::fence_proxy_async_smem();
             ptx::named_sync(3, 128);
