@@ -34,7 +34,11 @@ METRIC = "SSD fwd tokens/s and % of roofline (Mamba2-2.7B layer shape), 1 GB300"
 UNIT = "tokens/s"
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["mamba_ssd_chunked_gb300/csrc/ssd_tc.cu", "mamba_ssd_chunked_gb300/csrc/ptx.cuh"]
+# the source file of each fused kernel: a committed ncu summary's DRAM traffic is
+# reported only while the kernel source it was taken on is unchanged
+KERNEL_SOURCES = {"tc": ["mamba_ssd_chunked_gb300/csrc/ssd_tc.cu"],
+                  "chain": ["mamba_ssd_chunked_gb300/csrc/ssd_chain.cu"]}
+PROFILE_NAMES = {"tc": "ssd_tc_fused", "chain": "ssd_chain_fused"}
 
 
 # ----------------------------------------------------------------------------- roofline arithmetic
@@ -70,18 +74,20 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(path: str = "tc") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[path]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, kpath: str = "tc"):
     """DRAM bytes per launch of the fused kernel from the committed ncu
     summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"ssd_tc_fused_{workload}.md")
+    if kpath not in PROFILE_NAMES:
+        return None
+    path = os.path.join(ROOT, "profiles", f"{PROFILE_NAMES[kpath]}_{workload}.md")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -90,7 +96,7 @@ def profiled_traffic(workload: str):
             if line.startswith("traffic_bytes_per_launch:") or line.startswith("kernel_source_hash:"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_hash") != kernel_source_hash():
+    if vals.get("kernel_source_hash") != kernel_source_hash(kpath):
         return None
     try:
         return int(vals["traffic_bytes_per_launch"])
@@ -263,6 +269,9 @@ def config_dict(w: Workload):
             "l2": "flushed between timed steps (256 MiB write); inputs also exceed L2"}
 
 
+KERNEL_NAMES = {"tc": "ssd_tc_fused", "chain": "ssd_chain_fused", "simt": "simt (3 kernels)"}
+
+
 def run_ours(args, w: Workload, world, rank, local, pg):
     import torch
 
@@ -291,9 +300,22 @@ def run_ours(args, w: Workload, world, rank, local, pg):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    ws = None
+    if args.path != "auto":
+        need = pkg.ssd_fwd_workspace_bytes(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.io_dtype,
+                                           w.chunk_len, args.path)
+        if need == 0 and args.path != "simt":
+            raise RuntimeError(f"path {args.path} does not support workload {w.name}")
+        ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
+
     def step():
-        pkg.ssd_fwd(d["x"], d["dt"], d["dt_bias"], d["A"], d["B"], d["C"], d["D"], d["init_state"],
-                    chunk_len=w.chunk_len, y=y, final_state=fs, stream=stream.cuda_stream)
+        if ws is None:
+            pkg.ssd_fwd(d["x"], d["dt"], d["dt_bias"], d["A"], d["B"], d["C"], d["D"], d["init_state"],
+                        chunk_len=w.chunk_len, y=y, final_state=fs, stream=stream.cuda_stream)
+        else:
+            pkg.ssd_fwd(d["x"], d["dt"], d["dt_bias"], d["A"], d["B"], d["C"], d["D"], d["init_state"],
+                        chunk_len=w.chunk_len, y=y, final_state=fs, stream=stream.cuda_stream, path=args.path,
+                        workspace=ws)
 
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     ids = [v.strip() for v in visible.split(",") if v.strip()]
@@ -367,13 +389,13 @@ def run_ours(args, w: Workload, world, rank, local, pg):
     t_bytes = abytes / (peaks["hbm_gbs"] * 1e9)
     t_flops = aflops / (peaks["bf16_tflops"] * 1e12)
     bound = "hbm" if t_bytes >= t_flops else "tensor"
-    path = pkg.ssd_select_path(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.io_dtype,
-                               w.chunk_len)
+    path = args.path if args.path != "auto" else pkg.ssd_select_path(
+        w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.io_dtype, w.chunk_len)
     if bound == "hbm":
         achieved, peak, unit = abytes / mean_step / 1e9, peaks["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = aflops / mean_step / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-    traffic = profiled_traffic(w.name) if path == "tc" else None
+    traffic = profiled_traffic(w.name, path)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -397,7 +419,7 @@ def run_ours(args, w: Workload, world, rank, local, pg):
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_src} (burst)",
                      "algorithmic_bytes": abytes, "algorithmic_flops": aflops,
-                     "kernel": "ssd_tc_fused" if path == "tc" else "simt (3 kernels)",
+                     "kernel": KERNEL_NAMES[path],
                      "timing": "CUDA events around each ssd_fwd call on its stream (includes the 4-byte-per-chain "
                                "counter reset memset)"},
         "cpu_baseline": cpu,
@@ -416,6 +438,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="auto", choices=["auto", "tc", "chain", "simt"],
+                    help="kernel path of the timed step (auto: the library's choice)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing for cpu_baseline")

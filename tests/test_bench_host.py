@@ -80,5 +80,5 @@ def test_reference_arm_is_silent_on_other_ranks():
 
 
 def test_profiled_traffic_is_dropped_when_the_kernel_changed(tmp_path, monkeypatch):
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "not-the-profiled-source")
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda *a: "not-the-profiled-source")
     assert bench.profiled_traffic("mamba2_2p7b_layer") is None
