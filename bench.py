@@ -431,6 +431,87 @@ def run_ours(args, w: Workload, world, rank, local, pg):
     }
 
 
+# ----------------------------------------------------------------------------- decode step (--step)
+STEP_WORKLOAD = {"name": "mamba2_2p7b_decode_b64", "batch": 64, "nheads": 80, "headdim": 64, "ngroups": 1,
+                 "dstate": 128, "io_dtype": "bf16", "seed": 1240}
+
+
+def step_algorithmic_bytes(sw) -> int:
+    """HBM bytes one decode step must move: the fp32 state read and written,
+    x and y, B and C, dt, and the per-head parameters."""
+    b, h, p, g, n = sw["batch"], sw["nheads"], sw["headdim"], sw["ngroups"], sw["dstate"]
+    e = 2 if sw["io_dtype"] == "bf16" else 4
+    return 2 * b * h * p * n * 4 + 2 * b * h * p * e + 2 * b * g * n * e + b * h * 4 + 3 * h * 4
+
+
+def run_step(args):
+    """Time ssd_step (one decode token per sequence, state updated in place)."""
+    import torch
+
+    import mamba_ssd_chunked_gb300 as pkg
+    from mamba_ssd_chunked_gb300 import build as pkg_build
+
+    if not os.path.exists(pkg.LIBRARY):
+        pkg_build.build()
+    sw = STEP_WORKLOAD
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    b, h, p, g, n = sw["batch"], sw["nheads"], sw["headdim"], sw["ngroups"], sw["dstate"]
+    inp = make_inputs(b, 1, h, p, g, n, io_dtype=sw["io_dtype"], init="normal", seed=sw["seed"])
+    tdt = torch.bfloat16 if sw["io_dtype"] == "bf16" else torch.float32
+    d = {}
+    for k, v in inp.items():
+        if v is None:
+            d[k] = None
+            continue
+        t = torch.from_numpy(v).to(dev)
+        if k in ("x", "B", "C"):
+            t = t.to(tdt)
+        if k in ("x", "dt", "B", "C"):
+            t = t[:, 0].contiguous()
+        d[k] = t
+    state = d["init_state"]
+    y = torch.empty_like(d["x"])
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkg.ssd_step(d["x"], d["dt"], d["dt_bias"], d["A"], d["B"], d["C"], d["D"], state, y=y,
+                     stream=stream.cuda_stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = pkg.ssd_kernel_launches()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = pkg.ssd_kernel_launches() - launches0
+    per = [s_.elapsed_time(e_) / 1e3 for s_, e_ in zip(starts, ends)]
+    mean = sum(per) / len(per)
+    peaks, peak_src = load_peaks()
+    abytes = step_algorithmic_bytes(sw)
+    achieved = abytes / mean / 1e9
+    return {
+        "metric": "SSD decode step tokens/s (one token per sequence, Mamba2-2.7B layer heads), 1 GB300",
+        "value": b / mean, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+        "us_per_step": mean * 1e6, "higher_is_better": True, "dtype": sw["io_dtype"], "data": "synthetic",
+        "config": {"workload": sw["name"], "batch": b, "nheads": h, "headdim": p, "ngroups": g, "dstate": n,
+                   "l2": "flushed between timed steps (256 MiB write); the 168 MB state also exceeds L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "algorithmic_bytes": abytes,
+                     "peak_source": f"{peak_src} (burst)", "kernel": "ssd_step_rows4"},
+        "gpu_launches": launches,
+        "step_us": {"min": min(per) * 1e6, "median": statistics.median(per) * 1e6, "max": max(per) * 1e6},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,9 +524,14 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing for cpu_baseline")
+    ap.add_argument("--step", action="store_true",
+                    help="time the decode step (ssd_step) on its own workload instead of the forward")
     args = ap.parse_args(argv)
     if args.steps < 1:
         ap.error("--steps must be >= 1")
+    if args.step:
+        print(json.dumps(run_step(args)), flush=True)
+        return
     w = WORKLOADS[args.workload]
     world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":

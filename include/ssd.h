@@ -186,6 +186,30 @@ SSD_API ssd_status ssd_fwd_noalloc(const ssd_dims* dims, ssd_dtype io_dtype,
                                    const void* B, const void* C, const float* D, const float* init_state,
                                    int chunk_len, int ngroups, void* y, float* final_state, void* stream);
 
+/*
+ * ssd_step -- one decode step: a single new token per sequence, applied to a
+ * carried SSM state (fla "mamba2.py", Mamba2.torch_forward, cached-decode
+ * branch; its fast path is selective_state_update):
+ *
+ *   dt'  = softplus(dt + dt_bias[h])
+ *   state[b,h,p,n] = exp(dt' A[h]) state[b,h,p,n] + dt' x[b,h,p] B[b,g,n]
+ *   y[b,h,p]       = sum_n state[b,h,p,n] C[b,g,n] + D[h] x[b,h,p]
+ *
+ * with g = h / (nheads / ngroups), the same step as ssd_fwd over one token.
+ * dims->seqlen must be 1 (SSD_ERR_INVALID_ARG otherwise); the other dims are
+ * those of ssd_fwd. Layouts (dense, row-major, device pointers): x and y
+ * [b, h, p] in io_dtype; dt [b, h] fp32 (before bias and softplus); B and C
+ * [b, g, n] in io_dtype; dt_bias, A, D [h] fp32 (D nullable); state
+ * [b, h, p, n] fp32, read and overwritten in place (required). Pointers must
+ * be 16-byte aligned (SSD_ERR_UNSUPPORTED). The caller owns every buffer; the
+ * call is asynchronous on `stream` and needs no workspace. Arguments are
+ * checked on the host before anything is launched.
+ */
+SSD_API ssd_status ssd_step(const ssd_dims* dims, ssd_dtype io_dtype,
+                            const void* x, const float* dt, const float* dt_bias, const float* A,
+                            const void* B, const void* C, const float* D, float* state,
+                            int ngroups, void* y, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,7 @@ from typing import Optional, Tuple
 
 __all__ = [
     "SsdError", "library", "ssd_fwd", "ssd_fwd_host", "ssd_device_status", "ssd_fwd_workspace_bytes",
-    "ssd_select_path", "ssd_kernel_launches", "ssd_release", "Dims", "PATHS", "STATUS",
+    "ssd_select_path", "ssd_kernel_launches", "ssd_release", "ssd_step", "Dims", "PATHS", "STATUS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +73,8 @@ def library() -> ctypes.CDLL:
     lib.ssd_kernel_launches.argtypes = []
     lib.ssd_release.restype = None
     lib.ssd_release.argtypes = []
+    lib.ssd_step.restype = i
+    lib.ssd_step.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, vp, vp]
     _lib = lib
     return lib
 
@@ -207,6 +209,43 @@ def ssd_fwd_host(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: in
     if rc != 0:
         raise SsdError(rc, "ssd_fwd_host")
     return y, final_state
+
+
+def ssd_step(x, dt, dt_bias, A, B, C, D=None, state=None, ngroups: Optional[int] = None, y=None, stream=None):
+    """One decode step through ssd_step: x [b, h, p], dt [b, h], B/C [b, g, n]
+    (CUDA tensors, x/B/C bf16 or fp32 alike), state [b, h, p, n] fp32 updated in
+    place. Returns y [b, h, p] (x's dtype). Asynchronous on `stream`."""
+    torch = _torch()
+    if x.dim() != 3 or B.dim() != 3:
+        raise ValueError("x must be [b, h, p] and B [b, g, n]")
+    if state is None:
+        raise ValueError("state is required (it is updated in place)")
+    b, h, p = x.shape
+    g, n = B.shape[1], B.shape[2]
+    io = x.dtype
+    _check(x, "x", (b, h, p), io, "cuda")
+    _check(B, "B", (b, g, n), io, "cuda")
+    _check(C, "C", (b, g, n), io, "cuda")
+    f32 = torch.float32
+    _check(dt, "dt", (b, h), f32, "cuda")
+    _check(dt_bias, "dt_bias", (h,), f32, "cuda")
+    _check(A, "A", (h,), f32, "cuda")
+    _check(D, "D", (h,), f32, "cuda", optional=True)
+    _check(state, "state", (b, h, p, n), f32, "cuda")
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _check(y, "y", (b, h, p), io, "cuda")
+    if ngroups is None:
+        ngroups = g
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    dims = Dims(b, 1, h, p, g, n)
+    rc = library().ssd_step(ctypes.byref(dims), _io_code(x), _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B),
+                            _ptr(C), _ptr(D), _ptr(state), int(ngroups), _ptr(y), stream)
+    if rc != 0:
+        raise SsdError(rc, "ssd_step")
+    return y
 
 
 def ssd_device_status(stream=None) -> int:

@@ -391,4 +391,33 @@ ssd_status ssd_fwd_noalloc(const ssd_dims* dims, ssd_dtype io_dtype, const void*
     return tc_forward(a, scratch, kNoAllocScratchBytes);
 }
 
+ssd_status ssd_step(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, const float* dt, const float* dt_bias,
+                    const float* A, const void* B, const void* C, const float* D, float* state, int ngroups, void* y,
+                    void* stream) {
+    ssd_status st = check_dims(dims, io_dtype, 1, ngroups);
+    if (st != SSD_OK) return st;
+    if (dims->seqlen != 1) return SSD_ERR_INVALID_ARG;
+    if (!state) return SSD_ERR_INVALID_ARG;
+    st = check_pointers(x, dt, dt_bias, A, B, C, D, nullptr, y, state);
+    if (st != SSD_OK) return st;
+    if (!step_supported(*dims)) return SSD_ERR_UNSUPPORTED;
+    int dev = 0;
+    st = current_device(&dev);
+    if (st != SSD_OK) return st;
+    StepArgs a;
+    a.d = *dims;
+    a.io = io_dtype;
+    a.x = x;
+    a.dt = dt;
+    a.dt_bias = dt_bias;
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.D = D;
+    a.state = state;
+    a.y = y;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return step_forward(a);
+}
+
 }  // extern "C"

@@ -600,7 +600,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // idle table warp (one head per chain)
     } else if (wg == 1) {
         // ------------------------------------------------------------ masks into TMEM
-        const int t = 32 * q + lane;
         uint32_t writes0 = 0, writes1 = 0;  // fills of each region so far
         bool dirty0 = true, dirty1 = true;  // tiles above this warp's diagonal are not known to be zero
         auto claim = [&](int r) {

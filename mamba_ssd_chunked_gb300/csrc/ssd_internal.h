@@ -50,6 +50,24 @@ ssd_status chain_forward(const FwdArgs& a, void* ws, size_t ws_bytes);
 // {64, 1, 128, 1}, 128-byte swizzle, zero fill out of bounds.
 bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t rows, uint64_t outer);
 
+// One decode step on a carried state (ssd_step), arguments already validated.
+struct StepArgs {
+    ssd_dims d;
+    ssd_dtype io;
+    const void* x;
+    const float* dt;
+    const float* dt_bias;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    float* state;
+    void* y;
+    cudaStream_t stream;
+};
+bool step_supported(const ssd_dims& d);
+ssd_status step_forward(const StepArgs& a);
+
 // Launch bookkeeping (every kernel launch of the library goes through it).
 void note_launches(uint64_t n);
 

@@ -5,6 +5,9 @@ leg may import this package. It shares no code with the CUDA path: the
 arithmetic lives in ``ssd_oracle.c`` (token-by-token recurrence, fp64), built
 with the host C compiler into ``libssd_oracle.so`` beside it.
 
+``step`` (one decode step on a carried state) is the recurrence over one
+token with that state as the initial state.
+
 Parity status: pinned. The recurrence is checked (tests/test_oracle_pins.py)
 against a brute-force semiseparable-matrix product, an independent fp64
 five-stage chunked form at several chunk lengths, closed forms, the
@@ -113,3 +116,26 @@ def recurrence(
     if want_y:
         y = y_sel.reshape(b, h, L, p).transpose(0, 2, 1, 3).copy()
     return y, final_sel.reshape(b, h, p, n)
+
+
+def step(
+    x: np.ndarray,
+    dt: np.ndarray,
+    dt_bias: np.ndarray,
+    A: np.ndarray,
+    B: np.ndarray,
+    C: np.ndarray,
+    D: Optional[np.ndarray],
+    state: np.ndarray,
+    nthreads: Optional[int] = None,
+) -> Tuple[np.ndarray, np.ndarray]:
+    """One decode step on a carried state: the recurrence over a single token
+    with the state as its initial state (fla "mamba2.py", Mamba2.torch_forward,
+    cached-decode branch, computes exactly this step).
+
+    Shapes: x [b,h,p], dt [b,h] (raw), B/C [b,g,n], state [b,h,p,n]. Returns
+    y [b,h,p] and the new state [b,h,p,n] (fp64).
+    """
+    b, h, p = x.shape
+    y, final = recurrence(x[:, None], dt[:, None], dt_bias, A, B[:, None], C[:, None], D, state, nthreads=nthreads)
+    return y[:, 0], final

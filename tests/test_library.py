@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_documented_entry_points():
     names = declared_functions()
     for n in ("ssd_fwd", "ssd_fwd_ws", "ssd_fwd_host", "ssd_fwd_workspace_bytes", "ssd_device_status",
-              "ssd_status_string", "ssd_kernel_launches", "ssd_release", "ssd_select_path"):
+              "ssd_status_string", "ssd_kernel_launches", "ssd_release", "ssd_select_path", "ssd_step"):
         assert n in names
 
 
@@ -144,3 +144,12 @@ def test_workspace_sizes(lib):
 
 def test_kernel_counter_starts_without_launches(lib):
     assert lib.ssd_kernel_launches() >= 0
+
+
+def test_step_rejects_bad_arguments_on_host(lib):
+    d = pkg.Dims(2, 2, 4, 64, 2, 128)   # seqlen must be 1
+    assert lib.ssd_step(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 2, FAKE, None) == 1
+    d = pkg.Dims(2, 1, 4, 64, 2, 128)
+    assert lib.ssd_step(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 2, FAKE, None) == 1
+    assert lib.ssd_step(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, FAKE, None) == 1
+    assert lib.ssd_step(ctypes.byref(d), 1, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 2, FAKE, None) == 2

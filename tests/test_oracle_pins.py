@@ -257,3 +257,64 @@ def test_invalid_arguments_are_rejected():
     bad["B"] = np.zeros((1, 4, 2, 2), np.float32)  # 3 heads, 2 groups
     with pytest.raises(RuntimeError):
         _run(bad)
+
+
+def test_decode_step_matches_its_closed_form():
+    """oracle.step against the single-token update written out with numpy:
+    s' = e^{dA} s + d x B^T, y = s' C + D x (d = softplus(dt + dt_bias))."""
+    rng = np.random.Generator(np.random.PCG64(77))
+    b, h, p, g, n = 2, 6, 5, 3, 7
+    x = rng.standard_normal((b, h, p)).astype(np.float32)
+    dt = rng.standard_normal((b, h)).astype(np.float32)
+    dt_bias = rng.standard_normal(h).astype(np.float32)
+    A = -np.exp(rng.uniform(0, 2, h)).astype(np.float32)
+    B = rng.standard_normal((b, g, n)).astype(np.float32)
+    C = rng.standard_normal((b, g, n)).astype(np.float32)
+    D = rng.standard_normal(h).astype(np.float32)
+    s0 = rng.standard_normal((b, h, p, n)).astype(np.float32)
+    y, s1 = oracle.step(x, dt, dt_bias, A, B, C, D, s0)
+    hg = np.arange(h) // (h // g)
+    d = np.log1p(np.exp(dt.astype(np.float64) + dt_bias))
+    decay = np.exp(d * A)[..., None, None]
+    Bh = B.astype(np.float64)[:, hg]             # [b,h,n]
+    Ch = C.astype(np.float64)[:, hg]
+    s_ref = decay * s0 + (d[..., None] * x)[..., None] * Bh[:, :, None, :]
+    y_ref = np.einsum("bhpn,bhn->bhp", s_ref, Ch) + D.astype(np.float64)[None, :, None] * x.astype(np.float64)
+    assert np.max(np.abs(s1 - s_ref)) < 1e-12 * max(1.0, np.max(np.abs(s_ref)))
+    assert np.max(np.abs(y - y_ref)) < 1e-12 * max(1.0, np.max(np.abs(y_ref)))
+
+
+def test_decode_step_special_cases():
+    """Two reductions of the single-token update (fla Mamba2.torch_forward,
+    cached-decode branch): from a zero state the new state is the outer
+    product d x B^T, so y = x (d <B, C> + D) per row; with x = 0 the state
+    only decays, s' = e^{d A} s, and y = s' C. A dropped decay, a transposed
+    outer product or a wrong group map fails one of them."""
+    rng = np.random.Generator(np.random.PCG64(78))
+    b, h, p, g, n = 3, 4, 6, 2, 9
+    x = rng.standard_normal((b, h, p)).astype(np.float32)
+    dt = rng.standard_normal((b, h)).astype(np.float32)
+    dt_bias = rng.standard_normal(h).astype(np.float32)
+    A = -np.exp(rng.uniform(0, 2, h)).astype(np.float32)
+    B = rng.standard_normal((b, g, n)).astype(np.float32)
+    C = rng.standard_normal((b, g, n)).astype(np.float32)
+    D = rng.standard_normal(h).astype(np.float32)
+    d = np.log1p(np.exp(dt.astype(np.float64) + dt_bias))       # [b, h]
+    # zero state: y[b,h,p] = x (d <B_g, C_g> + D_h), g = h // (h / g)
+    y, s1 = oracle.step(x, dt, dt_bias, A, B, C, D, np.zeros((b, h, p, n), np.float32))
+    for bi in range(b):
+        for hi in range(h):
+            gi = hi // (h // g)
+            bc = float(np.dot(B[bi, gi].astype(np.float64), C[bi, gi].astype(np.float64)))
+            want = x[bi, hi].astype(np.float64) * (d[bi, hi] * bc + float(D[hi]))
+            assert np.allclose(y[bi, hi], want, rtol=1e-12, atol=1e-12)
+            assert np.allclose(s1[bi, hi], d[bi, hi] * np.outer(x[bi, hi].astype(np.float64), B[bi, gi].astype(np.float64)), rtol=1e-12, atol=1e-12)
+    # x = 0: pure decay of the carried state
+    s0 = rng.standard_normal((b, h, p, n)).astype(np.float32)
+    y, s1 = oracle.step(np.zeros_like(x), dt, dt_bias, A, B, C, D, s0)
+    for bi in range(b):
+        for hi in range(h):
+            gi = hi // (h // g)
+            decayed = np.exp(d[bi, hi] * float(A[hi])) * s0[bi, hi].astype(np.float64)
+            assert np.allclose(s1[bi, hi], decayed, rtol=1e-12, atol=1e-300)
+            assert np.allclose(y[bi, hi], decayed @ C[bi, gi].astype(np.float64), rtol=1e-11, atol=1e-12)
