@@ -37,8 +37,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the source file of each fused kernel: a committed ncu summary's DRAM traffic is
 # reported only while the kernel source it was taken on is unchanged
 KERNEL_SOURCES = {"tc": ["mamba_ssd_chunked_gb300/csrc/ssd_tc.cu"],
-                  "chain": ["mamba_ssd_chunked_gb300/csrc/ssd_chain.cu"]}
-PROFILE_NAMES = {"tc": "ssd_tc_fused", "chain": "ssd_chain_fused"}
+                  "chain": ["mamba_ssd_chunked_gb300/csrc/ssd_chain.cu"],
+                  "step": ["mamba_ssd_chunked_gb300/csrc/ssd_step.cu"]}
+PROFILE_NAMES = {"tc": "ssd_tc_fused", "chain": "ssd_chain_fused", "step": "ssd_step_rows4"}
 
 
 # ----------------------------------------------------------------------------- roofline arithmetic
@@ -479,6 +480,11 @@ def run_step(args):
         pkg.ssd_step(d["x"], d["dt"], d["dt_bias"], d["A"], d["B"], d["C"], d["D"], state, y=y,
                      stream=stream.cuda_stream)
 
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in visible.split(",") if v.strip()]
+    clocks = ClockSampler(ids[0] if ids else "0")
+    clocks.start()
+    time.sleep(0.3)
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         step()
@@ -486,13 +492,17 @@ def run_step(args):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     launches0 = pkg.ssd_kernel_launches()
+    t_wall0 = clocks.mark()
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
+    t_wall1 = clocks.mark()
     launches = pkg.ssd_kernel_launches() - launches0
+    time.sleep(0.3)
+    clocks.stop()
     per = [s_.elapsed_time(e_) / 1e3 for s_, e_ in zip(starts, ends)]
     mean = sum(per) / len(per)
     peaks, peak_src = load_peaks()
@@ -505,9 +515,11 @@ def run_step(args):
         "config": {"workload": sw["name"], "batch": b, "nheads": h, "headdim": p, "ngroups": g, "dstate": n,
                    "l2": "flushed between timed steps (256 MiB write); the 168 MB state also exceeds L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "algorithmic_bytes": abytes,
-                     "peak_source": f"{peak_src} (burst)", "kernel": "ssd_step_rows4"},
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(sw["name"], "step"),
+                     "algorithmic_bytes": abytes, "peak_source": f"{peak_src} (burst)",
+                     "kernel": "ssd_step_rows4"},
         "gpu_launches": launches,
+        "clocks": clocks.summary(t_wall0, t_wall1),
         "step_us": {"min": min(per) * 1e6, "median": statistics.median(per) * 1e6, "max": max(per) * 1e6},
     }
 
