@@ -6,7 +6,9 @@ arithmetic lives in ``ssd_oracle.c`` (token-by-token recurrence, fp64), built
 with the host C compiler into ``libssd_oracle.so`` beside it.
 
 ``step`` (one decode step on a carried state) is the recurrence over one
-token with that state as the initial state.
+token with that state as the initial state. ``layer_ops`` holds the causal
+conv1d + SiLU before the scan, its decode step, and the gated RMSNorm after
+it (fp64 numpy).
 
 Parity status: pinned. The recurrence is checked (tests/test_oracle_pins.py)
 against a brute-force semiseparable-matrix product, an independent fp64
@@ -139,3 +141,8 @@ def step(
     b, h, p = x.shape
     y, final = recurrence(x[:, None], dt[:, None], dt_bias, A, B[:, None], C[:, None], D, state, nthreads=nthreads)
     return y[:, 0], final
+
+
+# The per-token operations before and after the scan (causal conv1d + SiLU,
+# its decode step, the gated RMSNorm), in fp64 numpy.
+from .layer_ops import conv1d_silu, conv1d_step, gated_rmsnorm, silu  # noqa: E402,F401

@@ -318,3 +318,96 @@ def test_decode_step_special_cases():
             decayed = np.exp(d[bi, hi] * float(A[hi])) * s0[bi, hi].astype(np.float64)
             assert np.allclose(s1[bi, hi], decayed, rtol=1e-12, atol=1e-300)
             assert np.allclose(y[bi, hi], decayed @ C[bi, gi].astype(np.float64), rtol=1e-11, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- conv1d + SiLU, gated RMSNorm
+def _silu_lib(v):
+    """SiLU through scipy's logistic function (independent of the oracle's formula)."""
+    from scipy.special import expit
+    return v * expit(v)
+
+
+def test_conv1d_matches_numpy_convolve():
+    """The causal depthwise conv (fla Mamba2.__init__, nn.Conv1d with groups = conv_dim and
+    padding K - 1, cropped to seq_len) equals numpy's full convolution of each channel with the
+    reversed taps, first seq_len outputs; then bias and SiLU."""
+    rng = np.random.Generator(np.random.PCG64(91))
+    b, L, d_inner, gn, K = 2, 37, 12, 4, 4
+    cd = d_inner + 2 * gn
+    xbc = rng.standard_normal((b, L, cd))
+    w = rng.standard_normal((cd, K))
+    bias = rng.standard_normal(cd)
+    x, Bo, Co, state = oracle.conv1d_silu(xbc, w, bias, d_inner, gn)
+    full = np.concatenate([x, Bo, Co], axis=-1)
+    for bi in range(b):
+        for c in range(cd):
+            pre = np.convolve(xbc[bi, :, c], w[c, ::-1])[:L] + bias[c]
+            assert np.allclose(full[bi, :, c], _silu_lib(pre), rtol=1e-12, atol=1e-12)
+    # the conv state is the last K inputs, channel-major
+    assert np.array_equal(state, xbc[:, L - K:, :].transpose(0, 2, 1))
+
+
+def test_conv1d_single_taps_and_short_sequences():
+    """Only the last tap set: out = silu(x + bias) (no shift); only the first tap: the input delayed
+    by K - 1 steps with zeros before the sequence; seq_len < K pads the conv state with zeros."""
+    rng = np.random.Generator(np.random.PCG64(92))
+    b, L, d_inner, gn, K = 1, 9, 4, 2, 4
+    cd = d_inner + 2 * gn
+    xbc = rng.standard_normal((b, L, cd))
+    last = np.zeros((cd, K)); last[:, K - 1] = 1.0
+    x, Bo, Co, _ = oracle.conv1d_silu(xbc, last, None, d_inner, gn)
+    assert np.allclose(np.concatenate([x, Bo, Co], -1), _silu_lib(xbc), rtol=1e-13, atol=1e-15)
+    first = np.zeros((cd, K)); first[:, 0] = 1.0
+    x, Bo, Co, _ = oracle.conv1d_silu(xbc, first, None, d_inner, gn, activation=False)
+    got = np.concatenate([x, Bo, Co], -1)
+    assert np.array_equal(got[:, :K - 1], np.zeros((b, K - 1, cd)))
+    assert np.array_equal(got[:, K - 1:], xbc[:, :L - K + 1])
+    short = xbc[:, :2]
+    _, _, _, st = oracle.conv1d_silu(short, last, None, d_inner, gn)
+    assert np.array_equal(st[:, :, :K - 2], np.zeros((b, cd, K - 2)))
+    assert np.array_equal(st[:, :, K - 2:], short.transpose(0, 2, 1))
+
+
+def test_conv1d_decode_steps_reproduce_the_prefill():
+    """The cached-decode branch (roll the conv state, append the token, dot with the taps), run
+    token by token from a zero state, gives the prefill's outputs and its final conv state."""
+    rng = np.random.Generator(np.random.PCG64(93))
+    b, L, d_inner, gn, K = 2, 11, 6, 2, 4
+    cd = d_inner + 2 * gn
+    xbc = rng.standard_normal((b, L, cd))
+    w = rng.standard_normal((cd, K))
+    bias = rng.standard_normal(cd)
+    x, Bo, Co, st = oracle.conv1d_silu(xbc, w, bias, d_inner, gn)
+    state = np.zeros((b, cd, K))
+    for t in range(L):
+        xs, bs, cs, state = oracle.conv1d_step(xbc[:, t], state, w, bias, d_inner, gn)
+        assert np.allclose(xs, x[:, t], rtol=1e-12, atol=1e-13)
+        assert np.allclose(bs, Bo[:, t], rtol=1e-12, atol=1e-13)
+        assert np.allclose(cs, Co[:, t], rtol=1e-12, atol=1e-13)
+    assert np.array_equal(state, st)
+
+
+def test_gated_rmsnorm_against_torch_rms_norm_and_closed_forms():
+    """norm_before_gate=False: out = rms_norm(y * silu(z)) * w. Checked against torch's fp64
+    rms_norm of the gated product, a constant row (c / sqrt(c^2 + eps)), a zero gate (output 0),
+    and groups (each group normalised on its own)."""
+    import torch
+    rng = np.random.Generator(np.random.PCG64(94))
+    rows, d, eps = 7, 48, 1e-5
+    y = rng.standard_normal((rows, d))
+    z = rng.standard_normal((rows, d))
+    w = rng.standard_normal(d)
+    got = oracle.gated_rmsnorm(y, z, w, eps)
+    v = torch.from_numpy(y) * torch.nn.functional.silu(torch.from_numpy(z))
+    ref = torch.nn.functional.rms_norm(v, (d,), torch.from_numpy(w), eps).numpy()
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-13)
+    const = np.full((1, d), 0.3)
+    out = oracle.gated_rmsnorm(const, None, np.ones(d), eps)
+    assert np.allclose(out, 0.3 / np.sqrt(0.09 + eps), rtol=1e-14)
+    assert np.array_equal(oracle.gated_rmsnorm(y, np.zeros_like(z), w, eps), np.zeros_like(y))
+    gs = 16
+    grouped = oracle.gated_rmsnorm(y, z, w, eps, group_size=gs)
+    for gi in range(d // gs):
+        sl = slice(gi * gs, (gi + 1) * gs)
+        ref_g = torch.nn.functional.rms_norm(v[:, sl], (gs,), torch.from_numpy(w[sl]), eps).numpy()
+        assert np.allclose(grouped[:, sl], ref_g, rtol=1e-12, atol=1e-13)
