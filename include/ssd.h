@@ -210,6 +210,89 @@ SSD_API ssd_status ssd_step(const ssd_dims* dims, ssd_dtype io_dtype,
                             const void* B, const void* C, const float* D, float* state,
                             int ngroups, void* y, void* stream);
 
+/* ------------------------------------------------------------------------
+ * The per-token operations around the scan in a Mamba-2 layer (fla
+ * "mamba2.py", Mamba2.torch_forward, steps 2 and 3). They read and write
+ * each element once: HBM-bound streaming kernels, fp32 arithmetic.
+ */
+
+/* Shapes of the conv over xBC: conv_dim = d_inner + 2 * ngroups * dstate
+ * channels per token (x first, then B, then C), kernel_size taps (1..8). */
+typedef struct {
+    int64_t batch, seqlen, d_inner, ngroups, dstate, kernel_size;
+} ssd_conv_dims;
+
+/*
+ * ssd_conv1d_silu -- causal depthwise conv1d over time plus SiLU, split into
+ * the scan's inputs (fla "mamba2.py": Mamba2.__init__ builds
+ * nn.Conv1d(conv_dim, conv_dim, kernel_size, groups=conv_dim,
+ * padding=kernel_size - 1); Mamba2.torch_forward step 2 keeps the first
+ * seqlen outputs, applies SiLU and splits x / B / C):
+ *
+ *   o[b,t,c] = bias[c] + sum_{k<K} weight[c,k] * xbc[b, t-(K-1)+k, c]   (zero before t = 0)
+ *   x[b,t,:] = act(o[b,t,0:d_inner]); B[b,t,:] = act(o[b,t,d_inner:d_inner+G]);
+ *   C[b,t,:] = act(o[b,t,d_inner+G:]),  G = ngroups*dstate, act = SiLU or identity
+ *
+ * xbc             device [batch, seqlen, *] io dtype; token t of sequence b
+ *                 starts at xbc + (b*seqlen + t) * xbc_row_stride elements
+ *                 (xbc_row_stride >= conv_dim, e.g. the in_proj row length,
+ *                 so the slice can be read in place).
+ * weight          device [conv_dim, kernel_size] fp32; bias [conv_dim] fp32 or NULL.
+ * activation      1: SiLU; 0: none.
+ * x, B, C         device outputs, dense: x [batch, seqlen, d_inner] (the
+ *                 scan's [b, L, h, p]), B and C [batch, seqlen, ngroups, dstate].
+ * conv_state      device output [batch, conv_dim, kernel_size] io dtype, or
+ *                 NULL: the last kernel_size inputs of each channel, zeros
+ *                 in front when seqlen < kernel_size (what the layer caches).
+ * Pointers need the element alignment; 16-byte aligned pointers and strides
+ * with d_inner, G multiples of 8 (bf16) / 4 (fp32) take the vector path.
+ * Errors: SSD_ERR_INVALID_ARG (NULL, dims < 1, stride < conv_dim),
+ * SSD_ERR_UNSUPPORTED (kernel_size > 8, misaligned pointer, sizes beyond the
+ * indexing limits). Asynchronous on `stream`; no workspace.
+ */
+SSD_API ssd_status ssd_conv1d_silu(const ssd_conv_dims* dims, ssd_dtype io_dtype,
+                                   const void* xbc, int64_t xbc_row_stride,
+                                   const float* weight, const float* bias, int activation,
+                                   void* x, void* B, void* C, void* conv_state, void* stream);
+
+/*
+ * ssd_conv1d_step -- the cached-decode form of the same conv (fla
+ * "mamba2.py", Mamba2.torch_forward step 2, cache_position > 0): per
+ * sequence the conv state shifts left by one token, the new token enters at
+ * the right, and o[c] = bias[c] + sum_k state[c,k] * weight[c,k].
+ * dims->seqlen must be 1. xbc: [batch, *] with row stride xbc_row_stride;
+ * conv_state [batch, conv_dim, kernel_size] io dtype, updated in place
+ * (required); x [batch, d_inner], B and C [batch, ngroups*dstate].
+ * Errors and alignment as ssd_conv1d_silu.
+ */
+SSD_API ssd_status ssd_conv1d_step(const ssd_conv_dims* dims, ssd_dtype io_dtype,
+                                   const void* xbc, int64_t xbc_row_stride,
+                                   const float* weight, const float* bias, int activation,
+                                   void* conv_state, void* x, void* B, void* C, void* stream);
+
+/*
+ * ssd_gated_rmsnorm -- RMSNormGated(dim, eps, norm_before_gate=False) applied
+ * as norm(y, z) after the scan (fla "mamba2.py", step 3): per row and per
+ * group of group_size consecutive channels,
+ *
+ *   v = y * silu(z)          (v = y when z == NULL)
+ *   out = v / sqrt(mean(v^2 over the group) + eps) * weight
+ *
+ * y, z, out       device [rows, *] io dtype with the given row strides
+ *                 (elements, >= dim); z may be NULL.
+ * weight          device [dim] fp32.
+ * group_size      channels per normalisation group; <= 0 means dim (one
+ *                 group); dim % group_size == 0; at most 64 groups.
+ * Errors: SSD_ERR_INVALID_ARG (NULL, sizes < 1, strides < dim, dim not a
+ * multiple of group_size, eps < 0), SSD_ERR_UNSUPPORTED (more than 64
+ * groups, misaligned pointers, sizes beyond the indexing limits).
+ * Asynchronous on `stream`; no workspace.
+ */
+SSD_API ssd_status ssd_gated_rmsnorm(ssd_dtype io_dtype, int64_t rows, int64_t dim, int64_t group_size,
+                                     const void* y, int64_t y_row_stride, const void* z, int64_t z_row_stride,
+                                     const float* weight, float eps, void* out, int64_t out_row_stride,
+                                     void* stream);
+
 #ifdef __cplusplus
 }
 #endif

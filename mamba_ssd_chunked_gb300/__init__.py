@@ -20,7 +20,8 @@ from typing import Optional, Tuple
 
 __all__ = [
     "SsdError", "library", "ssd_fwd", "ssd_fwd_host", "ssd_device_status", "ssd_fwd_workspace_bytes",
-    "ssd_select_path", "ssd_kernel_launches", "ssd_release", "ssd_step", "Dims", "PATHS", "STATUS",
+    "ssd_select_path", "ssd_kernel_launches", "ssd_release", "ssd_step", "ssd_conv1d_silu", "ssd_conv1d_step",
+    "ssd_gated_rmsnorm", "Dims", "ConvDims", "PATHS", "STATUS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +35,10 @@ DTYPES = {"f32": 0, "bf16": 1}
 
 class Dims(ctypes.Structure):
     _fields_ = [(k, ctypes.c_int64) for k in ("batch", "seqlen", "nheads", "headdim", "ngroups", "dstate")]
+
+
+class ConvDims(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_int64) for k in ("batch", "seqlen", "d_inner", "ngroups", "dstate", "kernel_size")]
 
 
 class SsdError(RuntimeError):
@@ -75,6 +80,13 @@ def library() -> ctypes.CDLL:
     lib.ssd_release.argtypes = []
     lib.ssd_step.restype = i
     lib.ssd_step.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, vp, vp]
+    pconv = ctypes.POINTER(ConvDims)
+    lib.ssd_conv1d_silu.restype = i
+    lib.ssd_conv1d_silu.argtypes = [pconv, i, vp, i64, fp, fp, i, vp, vp, vp, vp, vp]
+    lib.ssd_conv1d_step.restype = i
+    lib.ssd_conv1d_step.argtypes = [pconv, i, vp, i64, fp, fp, i, vp, vp, vp, vp, vp]
+    lib.ssd_gated_rmsnorm.restype = i
+    lib.ssd_gated_rmsnorm.argtypes = [i, i64, i64, i64, vp, i64, vp, i64, fp, ctypes.c_float, vp, i64, vp]
     _lib = lib
     return lib
 
@@ -246,6 +258,114 @@ def ssd_step(x, dt, dt_bias, A, B, C, D=None, state=None, ngroups: Optional[int]
     if rc != 0:
         raise SsdError(rc, "ssd_step")
     return y
+
+
+def _row_view(t, name, rows_shape, io):
+    """Row stride (elements) of a CUDA tensor whose last dim is contiguous and
+    whose leading dims are packed rows of that stride (e.g. a slice of the
+    in_proj output along its last dimension)."""
+    if t.dtype != io:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {io}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape[:-1]) != tuple(rows_shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, leading dims must be {tuple(rows_shape)}")
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name} must be contiguous in its last dimension")
+    rs = t.stride(-2) if t.dim() >= 2 else t.shape[-1]
+    expect = rs
+    for k in range(t.dim() - 2, -1, -1):
+        if t.shape[k] > 1 and t.stride(k) != expect:
+            raise ValueError(f"{name}: leading dimensions must be packed rows of stride {rs}")
+        expect *= t.shape[k]
+    return rs
+
+
+def ssd_conv1d_silu(xbc, weight, bias, d_inner: int, ngroups: int, dstate: int, activation: bool = True,
+                    return_state: bool = False, stream=None):
+    """Causal depthwise conv1d (+ SiLU) of xbc [b, L, >= conv_dim] (a CUDA
+    tensor, bf16 or fp32, last dim contiguous, e.g. a slice of the in_proj
+    output) with weight [conv_dim, K] fp32 and bias [conv_dim] fp32 or None.
+    Returns x [b, L, d_inner], B [b, L, ngroups, dstate], C [b, L, ngroups, dstate]
+    and, with return_state, the conv state [b, conv_dim, K] (else None)."""
+    torch = _torch()
+    b, L = xbc.shape[0], xbc.shape[1]
+    io = xbc.dtype
+    cd = d_inner + 2 * ngroups * dstate
+    if xbc.shape[2] < cd:
+        raise ValueError(f"xbc has {xbc.shape[2]} channels, need at least conv_dim = {cd}")
+    rs = _row_view(xbc, "xbc", (b, L), io)
+    K = weight.shape[1]
+    _check(weight, "weight", (cd, K), torch.float32, "cuda")
+    _check(bias, "bias", (cd,), torch.float32, "cuda", optional=True)
+    x = torch.empty((b, L, d_inner), dtype=io, device=xbc.device)
+    Bo = torch.empty((b, L, ngroups, dstate), dtype=io, device=xbc.device)
+    Co = torch.empty_like(Bo)
+    st = torch.empty((b, cd, K), dtype=io, device=xbc.device) if return_state else None
+    if stream is None:
+        stream = torch.cuda.current_stream(xbc.device).cuda_stream
+    dims = ConvDims(b, L, d_inner, ngroups, dstate, K)
+    rc = library().ssd_conv1d_silu(ctypes.byref(dims), _io_code(xbc), _ptr(xbc), int(rs), _ptr(weight), _ptr(bias),
+                                   1 if activation else 0, _ptr(x), _ptr(Bo), _ptr(Co), _ptr(st), stream)
+    if rc != 0:
+        raise SsdError(rc, "ssd_conv1d_silu")
+    return x, Bo, Co, st
+
+
+def ssd_conv1d_step(xbc, conv_state, weight, bias, d_inner: int, ngroups: int, dstate: int,
+                    activation: bool = True, stream=None):
+    """One decode token through the conv: xbc [b, >= conv_dim] (last dim
+    contiguous), conv_state [b, conv_dim, K] (xbc's dtype, contiguous) updated
+    in place. Returns x [b, d_inner], B [b, ngroups, dstate], C [b, ngroups, dstate]."""
+    torch = _torch()
+    b = xbc.shape[0]
+    io = xbc.dtype
+    cd = d_inner + 2 * ngroups * dstate
+    if xbc.shape[1] < cd:
+        raise ValueError(f"xbc has {xbc.shape[1]} channels, need at least conv_dim = {cd}")
+    rs = _row_view(xbc, "xbc", (b,), io)
+    K = weight.shape[1]
+    _check(weight, "weight", (cd, K), torch.float32, "cuda")
+    _check(bias, "bias", (cd,), torch.float32, "cuda", optional=True)
+    _check(conv_state, "conv_state", (b, cd, K), io, "cuda")
+    x = torch.empty((b, d_inner), dtype=io, device=xbc.device)
+    Bo = torch.empty((b, ngroups, dstate), dtype=io, device=xbc.device)
+    Co = torch.empty_like(Bo)
+    if stream is None:
+        stream = torch.cuda.current_stream(xbc.device).cuda_stream
+    dims = ConvDims(b, 1, d_inner, ngroups, dstate, K)
+    rc = library().ssd_conv1d_step(ctypes.byref(dims), _io_code(xbc), _ptr(xbc), int(rs), _ptr(weight), _ptr(bias),
+                                   1 if activation else 0, _ptr(conv_state), _ptr(x), _ptr(Bo), _ptr(Co), stream)
+    if rc != 0:
+        raise SsdError(rc, "ssd_conv1d_step")
+    return x, Bo, Co
+
+
+def ssd_gated_rmsnorm(y, z, weight, eps: float = 1e-5, group_size: Optional[int] = None, out=None, stream=None):
+    """Gated RMSNorm (norm_before_gate=False) over the last dimension: y and z
+    [..., dim] CUDA tensors of one dtype (last dim contiguous, leading dims
+    packed rows; z may be None or a strided slice), weight [dim] fp32.
+    Returns out [..., dim] (y's dtype, contiguous unless given)."""
+    torch = _torch()
+    dim = y.shape[-1]
+    lead = tuple(y.shape[:-1])
+    rows = 1
+    for v in lead:
+        rows *= v
+    io = y.dtype
+    ys = _row_view(y, "y", lead, io)
+    zs = _row_view(z, "z", lead, io) if z is not None else 0
+    _check(weight, "weight", (dim,), torch.float32, "cuda")
+    if out is None:
+        out = torch.empty(y.shape, dtype=io, device=y.device)
+    os_ = _row_view(out, "out", lead, io)
+    if stream is None:
+        stream = torch.cuda.current_stream(y.device).cuda_stream
+    rc = library().ssd_gated_rmsnorm(_io_code(y), int(rows), int(dim), int(group_size or 0), _ptr(y), int(ys), _ptr(z),
+                                     int(zs), _ptr(weight), float(eps), _ptr(out), int(os_), stream)
+    if rc != 0:
+        raise SsdError(rc, "ssd_gated_rmsnorm")
+    return out
 
 
 def ssd_device_status(stream=None) -> int:

@@ -138,3 +138,43 @@ def workload_inputs(name: str) -> Dict[str, Optional[np.ndarray]]:
     w = WORKLOADS[name]
     return make_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate,
                        io_dtype=w.io_dtype, init=w.init, seed=w.seed)
+
+
+# ----------------------------------------------------------------------------- around the scan
+# Recipes for the operations before and after the scan (same rules: one PCG64
+# stream per seed, values rounded to the io dtype where the tensor is io).
+#   in_proj output zxbcdt [b, L, 2 d_inner + 2 g n + h] ~ N(0, 1) (io dtype); xBC
+#       is its slice [d_inner, 2 d_inner + 2 g n) and the gate z its first d_inner
+#       channels (fla "mamba2.py" split order: gate, xBC, dt when d_mlp = 0)
+#   conv weight [conv_dim, K] and bias [conv_dim] ~ U(-1/sqrt(K), 1/sqrt(K)) fp32
+#       (the bound of nn.Conv1d's default init for a depthwise kernel of K taps)
+#   norm weight [d_inner] = 1 + N(0, 0.1^2) fp32 (RMSNorm weights start at one)
+#   scan output y [b, L, d_inner] ~ N(0, 1) (io dtype) when the norm is tested alone
+
+CONV_WORKLOAD = {"name": "mamba2_2p7b_conv", "batch": 4, "seqlen": 4096, "d_inner": 5120, "ngroups": 1,
+                 "dstate": 128, "nheads": 80, "kernel_size": 4, "io_dtype": "bf16", "seed": 1241}
+NORM_WORKLOAD = {"name": "mamba2_2p7b_gated_norm", "batch": 4, "seqlen": 4096, "d_inner": 5120, "ngroups": 1,
+                 "dstate": 128, "nheads": 80, "io_dtype": "bf16", "eps": 1e-5, "seed": 1242}
+
+
+def _io_round(a: np.ndarray, io_dtype: str) -> np.ndarray:
+    if io_dtype not in ("f32", "bf16"):
+        raise ValueError(f"io_dtype must be 'f32' or 'bf16', got {io_dtype!r}")
+    return round_to_bf16(a) if io_dtype == "bf16" else np.ascontiguousarray(a, dtype=np.float32)
+
+
+def make_layer_inputs(batch: int, seqlen: int, d_inner: int, ngroups: int, dstate: int, nheads: int,
+                      kernel_size: int = 4, io_dtype: str = "bf16", seed: int = 0) -> Dict[str, np.ndarray]:
+    """zxbcdt [b, L, 2 d_inner + 2 g n + h], conv weight [conv_dim, K], conv
+    bias [conv_dim], norm weight [d_inner], y [b, L, d_inner] (all float32
+    arrays; io tensors hold io-representable values)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    f32 = np.float32
+    cd = d_inner + 2 * ngroups * dstate
+    zxbcdt = _io_round(rng.standard_normal((batch, seqlen, d_inner + cd + nheads), dtype=f32), io_dtype)
+    bound = 1.0 / np.sqrt(kernel_size)
+    conv_w = rng.uniform(-bound, bound, size=(cd, kernel_size)).astype(f32)
+    conv_b = rng.uniform(-bound, bound, size=cd).astype(f32)
+    norm_w = (1.0 + 0.1 * rng.standard_normal(d_inner)).astype(f32)
+    y = _io_round(rng.standard_normal((batch, seqlen, d_inner), dtype=f32), io_dtype)
+    return {"zxbcdt": zxbcdt, "conv_w": conv_w, "conv_b": conv_b, "norm_w": norm_w, "y": y}

@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_documented_entry_points():
     names = declared_functions()
     for n in ("ssd_fwd", "ssd_fwd_ws", "ssd_fwd_host", "ssd_fwd_workspace_bytes", "ssd_device_status",
-              "ssd_status_string", "ssd_kernel_launches", "ssd_release", "ssd_select_path", "ssd_step"):
+              "ssd_status_string", "ssd_kernel_launches", "ssd_release", "ssd_select_path", "ssd_step",
+              "ssd_conv1d_silu", "ssd_conv1d_step", "ssd_gated_rmsnorm"):
         assert n in names
 
 
@@ -153,3 +154,28 @@ def test_step_rejects_bad_arguments_on_host(lib):
     assert lib.ssd_step(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 2, FAKE, None) == 1
     assert lib.ssd_step(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, FAKE, None) == 1
     assert lib.ssd_step(ctypes.byref(d), 1, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 2, FAKE, None) == 2
+
+
+def test_conv_rejects_bad_arguments_on_host(lib):
+    d = pkg.ConvDims(2, 16, 64, 1, 16, 4)           # conv_dim = 96
+    call = lib.ssd_conv1d_silu
+    assert call(None, 1, FAKE, 96, FAKE, None, 1, FAKE, FAKE, FAKE, None, None) == 1
+    assert call(ctypes.byref(d), 1, None, 96, FAKE, None, 1, FAKE, FAKE, FAKE, None, None) == 1
+    assert call(ctypes.byref(d), 1, FAKE, 95, FAKE, None, 1, FAKE, FAKE, FAKE, None, None) == 1   # stride < conv_dim
+    assert call(ctypes.byref(d), 3, FAKE, 96, FAKE, None, 1, FAKE, FAKE, FAKE, None, None) == 1   # dtype
+    big = pkg.ConvDims(2, 16, 64, 1, 16, 9)          # more than 8 taps
+    assert call(ctypes.byref(big), 1, FAKE, 96, FAKE, None, 1, FAKE, FAKE, FAKE, None, None) == 2
+    assert call(ctypes.byref(d), 1, FAKE + 1, 96, FAKE, None, 1, FAKE, FAKE, FAKE, None, None) == 2  # misaligned
+    assert lib.ssd_conv1d_step(ctypes.byref(d), 1, FAKE, 96, FAKE, None, 1, FAKE, FAKE, FAKE, FAKE, None) == 1
+    one = pkg.ConvDims(2, 1, 64, 1, 16, 4)
+    assert lib.ssd_conv1d_step(ctypes.byref(one), 1, FAKE, 96, FAKE, None, 1, None, FAKE, FAKE, FAKE, None) == 1
+
+
+def test_norm_rejects_bad_arguments_on_host(lib):
+    f = lib.ssd_gated_rmsnorm
+    assert f(1, 4, 64, 0, None, 64, None, 0, FAKE, 1e-5, FAKE, 64, None) == 1            # y NULL
+    assert f(1, 4, 64, 0, FAKE, 63, None, 0, FAKE, 1e-5, FAKE, 64, None) == 1            # stride < dim
+    assert f(1, 4, 64, 24, FAKE, 64, None, 0, FAKE, 1e-5, FAKE, 64, None) == 1           # 64 % 24 != 0
+    assert f(1, 4, 64, 0, FAKE, 64, None, 0, FAKE, -1.0, FAKE, 64, None) == 1            # eps < 0
+    assert f(1, 4, 130, 1, FAKE, 130, None, 0, FAKE, 1e-5, FAKE, 130, None) == 2         # > 64 groups
+    assert f(1, 4, 64, 0, FAKE + 2, 64, None, 0, FAKE, 1e-5, FAKE, 64, None) == 2        # misaligned
