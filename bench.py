@@ -38,8 +38,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # reported only while the kernel source it was taken on is unchanged
 KERNEL_SOURCES = {"tc": ["mamba_ssd_chunked_gb300/csrc/ssd_tc.cu"],
                   "chain": ["mamba_ssd_chunked_gb300/csrc/ssd_chain.cu"],
-                  "step": ["mamba_ssd_chunked_gb300/csrc/ssd_step.cu"]}
-PROFILE_NAMES = {"tc": "ssd_tc_fused", "chain": "ssd_chain_fused", "step": "ssd_step_rows4"}
+                  "step": ["mamba_ssd_chunked_gb300/csrc/ssd_step.cu"],
+                  "conv": ["mamba_ssd_chunked_gb300/csrc/ssd_layer.cu"],
+                  "norm": ["mamba_ssd_chunked_gb300/csrc/ssd_layer.cu"]}
+PROFILE_NAMES = {"tc": "ssd_tc_fused", "chain": "ssd_chain_fused", "step": "ssd_step_rows4",
+                 "conv": "conv1d_fwd", "norm": "gated_rmsnorm"}
 
 
 # ----------------------------------------------------------------------------- roofline arithmetic
@@ -445,15 +448,72 @@ def step_algorithmic_bytes(sw) -> int:
     return 2 * b * h * p * n * 4 + 2 * b * h * p * e + 2 * b * g * n * e + b * h * 4 + 3 * h * 4
 
 
-def run_step(args):
-    """Time ssd_step (one decode token per sequence, state updated in place)."""
+def _time_op(args, dev, stream, op):
+    """Warm up, then time args.steps calls of op() on `stream` with CUDA events
+    (L2 flushed before each call, clocks sampled during the timed region).
+    Returns (seconds per call, library launches in the timed region, clocks)."""
     import torch
 
+    import mamba_ssd_chunked_gb300 as pkg
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in visible.split(",") if v.strip()]
+    clocks = ClockSampler(ids[0] if ids else "0")
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        op()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = pkg.ssd_kernel_launches()
+    t_wall0 = clocks.mark()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        op()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = clocks.mark()
+    launches = pkg.ssd_kernel_launches() - launches0
+    time.sleep(0.3)
+    clocks.stop()
+    per = [s_.elapsed_time(e_) / 1e3 for s_, e_ in zip(starts, ends)]
+    return per, launches, clocks.summary(t_wall0, t_wall1)
+
+
+def _op_line(args, metric, units_per_call, unit, per, launches, ck, cfg, abytes, kpath, kernel, dtype):
+    peaks, peak_src = load_peaks()
+    mean = sum(per) / len(per)
+    achieved = abytes / mean / 1e9
+    return {
+        "metric": metric, "value": units_per_call / mean, "unit": unit, "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "us_per_step": mean * 1e6, "higher_is_better": True, "dtype": dtype,
+        "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(cfg["workload"], kpath),
+                     "algorithmic_bytes": abytes, "peak_source": f"{peak_src} (burst)", "kernel": kernel},
+        "gpu_launches": launches, "clocks": ck,
+        "step_us": {"min": min(per) * 1e6, "median": statistics.median(per) * 1e6, "max": max(per) * 1e6},
+    }
+
+
+def _load_pkg():
     import mamba_ssd_chunked_gb300 as pkg
     from mamba_ssd_chunked_gb300 import build as pkg_build
 
     if not os.path.exists(pkg.LIBRARY):
         pkg_build.build()
+    return pkg
+
+
+def run_step(args):
+    """Time ssd_step (one decode token per sequence, state updated in place)."""
+    import torch
+
+    pkg = _load_pkg()
     sw = STEP_WORKLOAD
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -473,55 +533,81 @@ def run_step(args):
         d[k] = t
     state = d["init_state"]
     y = torch.empty_like(d["x"])
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def op():
         pkg.ssd_step(d["x"], d["dt"], d["dt_bias"], d["A"], d["B"], d["C"], d["D"], state, y=y,
                      stream=stream.cuda_stream)
 
-    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-    ids = [v.strip() for v in visible.split(",") if v.strip()]
-    clocks = ClockSampler(ids[0] if ids else "0")
-    clocks.start()
-    time.sleep(0.3)
-    for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    launches0 = pkg.ssd_kernel_launches()
-    t_wall0 = clocks.mark()
-    for i in range(args.steps):
-        flush.zero_()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    t_wall1 = clocks.mark()
-    launches = pkg.ssd_kernel_launches() - launches0
-    time.sleep(0.3)
-    clocks.stop()
-    per = [s_.elapsed_time(e_) / 1e3 for s_, e_ in zip(starts, ends)]
-    mean = sum(per) / len(per)
-    peaks, peak_src = load_peaks()
-    abytes = step_algorithmic_bytes(sw)
-    achieved = abytes / mean / 1e9
-    return {
-        "metric": "SSD decode step tokens/s (one token per sequence, Mamba2-2.7B layer heads), 1 GB300",
-        "value": b / mean, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
-        "us_per_step": mean * 1e6, "higher_is_better": True, "dtype": sw["io_dtype"], "data": "synthetic",
-        "config": {"workload": sw["name"], "batch": b, "nheads": h, "headdim": p, "ngroups": g, "dstate": n,
-                   "l2": "flushed between timed steps (256 MiB write); the 168 MB state also exceeds L2"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(sw["name"], "step"),
-                     "algorithmic_bytes": abytes, "peak_source": f"{peak_src} (burst)",
-                     "kernel": "ssd_step_rows4"},
-        "gpu_launches": launches,
-        "clocks": clocks.summary(t_wall0, t_wall1),
-        "step_us": {"min": min(per) * 1e6, "median": statistics.median(per) * 1e6, "max": max(per) * 1e6},
-    }
+    per, launches, ck = _time_op(args, dev, stream, op)
+    cfg = {"workload": sw["name"], "batch": b, "nheads": h, "headdim": p, "ngroups": g, "dstate": n,
+           "l2": "flushed between timed steps (256 MiB write); the 168 MB state also exceeds L2"}
+    return _op_line(args, "SSD decode step tokens/s (one token per sequence, Mamba2-2.7B layer heads), 1 GB300",
+                    b, "tokens/s", per, launches, ck, cfg, step_algorithmic_bytes(sw), "step", "ssd_step_rows4",
+                    sw["io_dtype"])
+
+
+def conv_algorithmic_bytes(cw) -> int:
+    """xBC read once and x/B/C written once (io dtype), plus the taps and bias."""
+    es = 2 if cw["io_dtype"] == "bf16" else 4
+    cd = cw["d_inner"] + 2 * cw["ngroups"] * cw["dstate"]
+    tokens = cw["batch"] * cw["seqlen"]
+    return 2 * tokens * cd * es + cd * (cw["kernel_size"] + 1) * 4
+
+
+def norm_algorithmic_bytes(nw) -> int:
+    """y and z read once, out written once (io dtype), plus the weight."""
+    es = 2 if nw["io_dtype"] == "bf16" else 4
+    tokens = nw["batch"] * nw["seqlen"]
+    return 3 * tokens * nw["d_inner"] * es + nw["d_inner"] * 4
+
+
+def run_layer_op(args, which):
+    """Time ssd_conv1d_silu or ssd_gated_rmsnorm on the 2.7B-layer shape, reading
+    xBC / the gate in place from a synthetic in_proj output."""
+    import torch
+
+    from mamba_ssd_chunked_gb300.inputs import CONV_WORKLOAD, NORM_WORKLOAD, make_layer_inputs
+
+    pkg = _load_pkg()
+    cw = CONV_WORKLOAD if which == "conv" else NORM_WORKLOAD
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    b, L, di, g, n, h = cw["batch"], cw["seqlen"], cw["d_inner"], cw["ngroups"], cw["dstate"], cw["nheads"]
+    K = cw.get("kernel_size", 4)
+    inp = make_layer_inputs(b, L, di, g, n, h, kernel_size=K, io_dtype=cw["io_dtype"], seed=cw["seed"])
+    tdt = torch.bfloat16 if cw["io_dtype"] == "bf16" else torch.float32
+    zx = torch.from_numpy(inp["zxbcdt"]).to(dev).to(tdt)
+    cd = di + 2 * g * n
+    stream = torch.cuda.current_stream(dev)
+    cfg = {"workload": cw["name"], "batch": b, "seqlen": L, "d_inner": di, "ngroups": g, "dstate": n,
+           "in_proj_row": int(zx.shape[-1]),
+           "l2": "flushed between timed steps (256 MiB write); the inputs also exceed L2"}
+    if which == "conv":
+        w = torch.from_numpy(inp["conv_w"]).to(dev)
+        bias = torch.from_numpy(inp["conv_b"]).to(dev)
+        xbc = zx[..., di:di + cd]
+        cfg["kernel_size"] = K
+
+        def op():
+            pkg.ssd_conv1d_silu(xbc, w, bias, di, g, n, stream=stream.cuda_stream)
+
+        per, launches, ck = _time_op(args, dev, stream, op)
+        return _op_line(args, "causal conv1d + SiLU tokens/s (Mamba2-2.7B layer xBC), 1 GB300", b * L, "tokens/s",
+                        per, launches, ck, cfg, conv_algorithmic_bytes(cw), "conv", "conv1d_fwd", cw["io_dtype"])
+    y = torch.from_numpy(inp["y"]).to(dev).to(tdt)
+    z = zx[..., :di]
+    nw = torch.from_numpy(inp["norm_w"]).to(dev)
+    out = torch.empty_like(y)
+    cfg["eps"] = cw["eps"]
+
+    def op():
+        pkg.ssd_gated_rmsnorm(y, z, nw, eps=cw["eps"], out=out, stream=stream.cuda_stream)
+
+    per, launches, ck = _time_op(args, dev, stream, op)
+    return _op_line(args, "gated RMSNorm tokens/s (Mamba2-2.7B layer, norm_before_gate=False), 1 GB300", b * L,
+                    "tokens/s", per, launches, ck, cfg, norm_algorithmic_bytes(cw), "norm", "gated_rmsnorm",
+                    cw["io_dtype"])
 
 
 def main(argv=None):
@@ -538,11 +624,16 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing for cpu_baseline")
     ap.add_argument("--step", action="store_true",
                     help="time the decode step (ssd_step) on its own workload instead of the forward")
+    ap.add_argument("--conv", action="store_true", help="time the causal conv1d + SiLU (ssd_conv1d_silu)")
+    ap.add_argument("--norm", action="store_true", help="time the gated RMSNorm (ssd_gated_rmsnorm)")
     args = ap.parse_args(argv)
     if args.steps < 1:
         ap.error("--steps must be >= 1")
     if args.step:
         print(json.dumps(run_step(args)), flush=True)
+        return
+    if args.conv or args.norm:
+        print(json.dumps(run_layer_op(args, "conv" if args.conv else "norm")), flush=True)
         return
     w = WORKLOADS[args.workload]
     world, rank, local, pg = dist_setup(args)

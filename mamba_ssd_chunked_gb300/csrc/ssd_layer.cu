@@ -82,7 +82,85 @@ __device__ __forceinline__ void store_n(T* p, const float* f) {
     }
 }
 
-__device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
+__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.f + __expf(-v)); }
+
+// SiLU with one MUFU op: v * sigmoid(v) = h + h * tanh(h), h = v / 2. tanh.approx
+// has a relative error near 2^-11, far below bf16 rounding; fp32 outputs use silu_f.
+__device__ __forceinline__ float silu_tanh(float v) {
+    const float h = 0.5f * v;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
+
+template <typename T>
+__device__ __forceinline__ float silu_io(float v) {
+    if constexpr (sizeof(T) == 2) {
+        return silu_tanh(v);
+    } else {
+        return silu_f(v);
+    }
+}
+
+// V raw elements of T, moved with one access of V * sizeof(T) bytes when that
+// is 4, 8 or 16 (the pointer is then aligned to it), else element by element.
+template <typename T, int V>
+struct Raw {
+    static constexpr int kBytes = V * static_cast<int>(sizeof(T));
+    static constexpr int kWords = kBytes >= 4 ? kBytes / 4 : 1;
+    uint32_t w[kWords];
+    __device__ __forceinline__ void load(const T* p) {
+        if constexpr (kBytes == 16) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p);
+            w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+        } else if constexpr (kBytes == 8) {
+            const uint2 v = *reinterpret_cast<const uint2*>(p);
+            w[0] = v.x, w[1] = v.y;
+        } else if constexpr (kBytes == 4) {
+            w[0] = *reinterpret_cast<const uint32_t*>(p);
+        } else {
+            w[0] = *reinterpret_cast<const uint16_t*>(p);
+        }
+    }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < kWords; ++i) w[i] = 0u;
+    }
+    __device__ __forceinline__ float get(int i) const {
+        if constexpr (sizeof(T) == 2) {
+            const uint32_t u = w[i >> 1];
+            return __uint_as_float((i & 1) ? (u & 0xFFFF0000u) : (u << 16));
+        } else {
+            return __uint_as_float(w[i]);
+        }
+    }
+};
+
+template <typename T, int V>
+__device__ __forceinline__ void store_raw(T* p, const float* f) {
+    constexpr int kBytes = V * static_cast<int>(sizeof(T));
+    if constexpr (sizeof(T) == 2 && (kBytes == 16 || kBytes == 8 || kBytes == 4)) {
+        uint32_t w[kBytes / 4];
+#pragma unroll
+        for (int i = 0; i < kBytes / 4; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        if constexpr (kBytes == 16)
+            *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        else if constexpr (kBytes == 8)
+            *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+        else
+            *reinterpret_cast<uint32_t*>(p) = w[0];
+    } else if constexpr (sizeof(T) == 4 && kBytes == 16) {
+        *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+    } else if constexpr (sizeof(T) == 4 && kBytes == 8) {
+        *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) Io<T>::st(p + i, f[i]);
+    }
+}
 
 struct ConvShape {
     long long L, stride;  // tokens, elements between consecutive tokens of xBC
@@ -90,21 +168,27 @@ struct ConvShape {
     int act;              // 1: SiLU
 };
 
-// Output channel c of token row `row` goes to x, B or C (c is V-aligned and the
-// three ranges are multiples of V, so a vector never straddles two of them).
+// Output channel c goes to x, B or C (c is V-aligned and the three ranges are
+// multiples of V, so a vector never straddles two of them): base and row length.
 template <typename T>
-__device__ __forceinline__ T* out_ptr(T* x, T* B, T* C, const ConvShape& s, long long row, int c) {
-    if (c < s.d_inner) return x + row * s.d_inner + c;
+__device__ __forceinline__ T* out_base(T* x, T* B, T* C, const ConvShape& s, int c, int* row) {
+    if (c < s.d_inner) {
+        *row = s.d_inner;
+        return x + c;
+    }
     c -= s.d_inner;
-    if (c < s.gn) return B + row * s.gn + c;
-    return C + row * s.gn + (c - s.gn);
+    *row = s.gn;
+    return c < s.gn ? B + c : C + (c - s.gn);
 }
 
 constexpr int kConvThreads = 128;
 constexpr int kConvRun = 32;  // tokens per thread
+constexpr int kConvGroup = 8; // tokens loaded together; the next group is in flight during compute
 
-// One thread: V consecutive channels of one batch row over kConvRun tokens,
-// the previous K - 1 inputs kept in registers as a sliding window.
+// One thread: V consecutive channels of one batch row over kConvRun tokens. The
+// previous K - 1 inputs stay in registers (raw io values) as a sliding window,
+// and the loads of the next kConvGroup tokens are issued before the current
+// group is computed.
 template <typename T, int V, int K>
 __global__ void __launch_bounds__(kConvThreads)
     conv1d_fwd(const T* __restrict__ xbc, const float* __restrict__ w, const float* __restrict__ bias,
@@ -112,8 +196,11 @@ __global__ void __launch_bounds__(kConvThreads)
     const int c = (blockIdx.x * kConvThreads + threadIdx.x) * V;
     if (c >= s.cd) return;
     const long long b = blockIdx.z;
-    const long long t0 = static_cast<long long>(blockIdx.y) * kConvRun;
+    const int t0 = static_cast<int>(blockIdx.y) * kConvRun;
+    const int t1 = static_cast<int>(t0 + kConvRun < s.L ? t0 + kConvRun : s.L);
     const T* in = xbc + b * s.L * s.stride + c;
+    int orow;
+    T* out = out_base(x, B, C, s, c, &orow) + b * s.L * orow;
     float wk[K][V], bv[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) {
@@ -121,58 +208,55 @@ __global__ void __launch_bounds__(kConvThreads)
         for (int k = 0; k < K; ++k) wk[k][i] = w[(c + i) * K + k];
         bv[i] = bias ? bias[c + i] : 0.f;
     }
-    float win[K][V];  // win[k] = input at token t - (K - 1) + k
+    Raw<T, V> win[K];  // win[k]: input at token t - (K - 1) + k while token t is computed
 #pragma unroll
     for (int k = 0; k < K - 1; ++k) {
-        const long long t = t0 - (K - 1) + k;
-        if (t >= 0) {
-            load_n<T, V>(in + t * s.stride, win[k]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < V; ++i) win[k][i] = 0.f;
-        }
+        const int t = t0 - (K - 1) + k;
+        if (t >= 0)
+            win[k].load(in + static_cast<long long>(t) * s.stride);
+        else
+            win[k].zero();
     }
-    const long long t1 = t0 + kConvRun < s.L ? t0 + kConvRun : s.L;
-    constexpr int kAhead = 4;  // loads in flight per thread
-    for (long long tb = t0; tb < t1; tb += kAhead) {
-        float nxt[kAhead][V];
+    Raw<T, V> cur[kConvGroup], nxt[kConvGroup];
 #pragma unroll
-        for (int a = 0; a < kAhead; ++a)
-            if (tb + a < t1) load_n<T, V>(in + (tb + a) * s.stride, nxt[a]);
+    for (int a = 0; a < kConvGroup; ++a)
+        if (t0 + a < t1) cur[a].load(in + static_cast<long long>(t0 + a) * s.stride);
+    for (int tb = t0; tb < t1; tb += kConvGroup) {
 #pragma unroll
-        for (int a = 0; a < kAhead; ++a) {
-            if (tb + a >= t1) break;
+        for (int a = 0; a < kConvGroup; ++a)
+            if (tb + kConvGroup + a < t1) nxt[a].load(in + static_cast<long long>(tb + kConvGroup + a) * s.stride);
 #pragma unroll
-            for (int i = 0; i < V; ++i) win[K - 1][i] = nxt[a][i];
-            float o[V];
+        for (int a = 0; a < kConvGroup; ++a) {
+            if (tb + a < t1) {
+                win[K - 1] = cur[a];
+                float o[V];
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-                float acc = bv[i];
+                for (int i = 0; i < V; ++i) {
+                    float acc = bv[i];
 #pragma unroll
-                for (int k = 0; k < K; ++k) acc = fmaf(wk[k][i], win[k][i], acc);
-                o[i] = s.act ? silu_f(acc) : acc;
+                    for (int k = 0; k < K; ++k) acc = fmaf(wk[k][i], win[k].get(i), acc);
+                    o[i] = s.act ? silu_io<T>(acc) : acc;
+                }
+                store_raw<T, V>(out + static_cast<long long>(tb + a) * orow, o);
+#pragma unroll
+                for (int k = 0; k < K - 1; ++k) win[k] = win[k + 1];
             }
-            store_n<T, V>(out_ptr(x, B, C, s, b * s.L + tb + a, c), o);
-#pragma unroll
-            for (int k = 0; k < K - 1; ++k)
-#pragma unroll
-                for (int i = 0; i < V; ++i) win[k][i] = win[k + 1][i];
         }
+#pragma unroll
+        for (int a = 0; a < kConvGroup; ++a) cur[a] = nxt[a];
     }
     // conv state: the last K inputs, channel-major [b][cd][K], zeros before the sequence
     if (state && t1 == s.L) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const long long t = s.L - K + k;
-            float v[V];
-            if (t >= 0) {
-                load_n<T, V>(in + t * s.stride, v);
-            } else {
+            Raw<T, V> v;
+            if (t >= 0)
+                v.load(in + t * s.stride);
+            else
+                v.zero();
 #pragma unroll
-                for (int i = 0; i < V; ++i) v[i] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < V; ++i) Io<T>::st(state + (b * s.cd + c + i) * K + k, v[i]);
+            for (int i = 0; i < V; ++i) Io<T>::st(state + (b * s.cd + c + i) * K + k, v.get(i));
         }
     }
 }
@@ -185,8 +269,8 @@ __global__ void __launch_bounds__(kConvThreads)
     const int c = (blockIdx.x * kConvThreads + threadIdx.x) * V;
     if (c >= s.cd) return;
     const long long b = blockIdx.y;
-    float cur[V];
-    load_n<T, V>(xbc + b * s.stride + c, cur);
+    Raw<T, V> cur;
+    cur.load(xbc + b * s.stride + c);
     float o[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) {
@@ -194,13 +278,15 @@ __global__ void __launch_bounds__(kConvThreads)
         float acc = bias ? bias[c + i] : 0.f;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-            const float v = k + 1 < K ? Io<T>::ld(st + k + 1) : cur[i];
+            const float v = k + 1 < K ? Io<T>::ld(st + k + 1) : cur.get(i);
             acc = fmaf(w[(c + i) * K + k], v, acc);
             Io<T>::st(st + k, v);
         }
-        o[i] = s.act ? silu_f(acc) : acc;
+        o[i] = s.act ? silu_io<T>(acc) : acc;
     }
-    store_n<T, V>(out_ptr(x, B, C, s, b, c), o);
+    int orow;
+    T* out = out_base(x, B, C, s, c, &orow) + b * orow;
+    store_raw<T, V>(out, o);
 }
 
 template <typename T, int V>
@@ -258,6 +344,7 @@ __global__ void __launch_bounds__(kNormThreads)
     const T* zr = z ? z + row * s.zstride : nullptr;
     T* orow = out + row * s.ostride;
     const int ngroups = static_cast<int>(s.dim / s.group);
+    const int group = static_cast<int>(s.group);  // dim < 2^30: 32-bit channel indices
     const int nvec = static_cast<int>(s.dim / V);
     for (int g = threadIdx.x; g < ngroups; g += kNormThreads) sums[g] = 0.f;
     __syncthreads();
@@ -268,7 +355,7 @@ __global__ void __launch_bounds__(kNormThreads)
             float g[V];
             load_n<T, V>(zr + static_cast<long long>(vi) * V, g);
 #pragma unroll
-            for (int i = 0; i < V; ++i) v[i] *= silu_f(g[i]);
+            for (int i = 0; i < V; ++i) v[i] *= silu_io<T>(g[i]);
         }
     };
     // pass 1: gated values and their squares summed per group
@@ -281,7 +368,7 @@ __global__ void __launch_bounds__(kNormThreads)
         if (ngroups == 1)
             tot += ss;
         else
-            atomicAdd(&sums[static_cast<int>(static_cast<long long>(vi) * V / s.group)], ss);
+            atomicAdd(&sums[vi * V / group], ss);
     };
     if constexpr (R > 0) {
 #pragma unroll
@@ -314,12 +401,24 @@ __global__ void __launch_bounds__(kNormThreads)
     __syncthreads();
     // pass 2: scale by the group's 1/rms and the weight
     const float inv_group = 1.f / static_cast<float>(s.group);
+    const float rstd0 = rsqrtf(fmaf(sums[0], inv_group, s.eps));
     auto emit = [&](int vi, const float* v) {
-        const int g = static_cast<int>(static_cast<long long>(vi) * V / s.group);
-        const float rstd = rsqrtf(fmaf(sums[g], inv_group, s.eps));
+        const float rstd = ngroups == 1 ? rstd0 : rsqrtf(fmaf(sums[vi * V / group], inv_group, s.eps));
+        float wv[V];
+        if constexpr (V % 4 == 0) {
+            const float4* w4 = reinterpret_cast<const float4*>(w + static_cast<long long>(vi) * V);
+#pragma unroll
+            for (int i = 0; i < V / 4; ++i) {
+                const float4 q = w4[i];
+                wv[4 * i] = q.x, wv[4 * i + 1] = q.y, wv[4 * i + 2] = q.z, wv[4 * i + 3] = q.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) wv[i] = w[static_cast<long long>(vi) * V + i];
+        }
         float o[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) o[i] = v[i] * rstd * w[static_cast<long long>(vi) * V + i];
+        for (int i = 0; i < V; ++i) o[i] = v[i] * rstd * wv[i];
         store_n<T, V>(orow + static_cast<long long>(vi) * V, o);
     };
     if constexpr (R > 0) {
@@ -345,14 +444,23 @@ ssd_status launch_norm(long long rows, const void* y, const void* z, const float
     const T* zi = static_cast<const T*>(z);
     T* o = static_cast<T*>(out);
     const unsigned grid = static_cast<unsigned>(rows);
-    if (per_thread <= 2)
-        gated_rmsnorm<T, V, 2><<<grid, kNormThreads, 0, stream>>>(yi, zi, w, o, s);
-    else if (per_thread <= 4)
-        gated_rmsnorm<T, V, 4><<<grid, kNormThreads, 0, stream>>>(yi, zi, w, o, s);
-    else if (per_thread <= 8)
-        gated_rmsnorm<T, V, 8><<<grid, kNormThreads, 0, stream>>>(yi, zi, w, o, s);
-    else
-        gated_rmsnorm<T, V, 0><<<grid, kNormThreads, 0, stream>>>(yi, zi, w, o, s);
+    switch (per_thread) {
+#define SSD_NORM_CASE(RR) \
+    case RR:              \
+        gated_rmsnorm<T, V, RR><<<grid, kNormThreads, 0, stream>>>(yi, zi, w, o, s); \
+        break;
+        SSD_NORM_CASE(1)
+        SSD_NORM_CASE(2)
+        SSD_NORM_CASE(3)
+        SSD_NORM_CASE(4)
+        SSD_NORM_CASE(5)
+        SSD_NORM_CASE(6)
+        SSD_NORM_CASE(7)
+        SSD_NORM_CASE(8)
+#undef SSD_NORM_CASE
+        default:
+            gated_rmsnorm<T, V, 0><<<grid, kNormThreads, 0, stream>>>(yi, zi, w, o, s);
+    }
     note_launches(1);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
@@ -377,13 +485,16 @@ ssd_status check_conv(const ssd_conv_dims* d, ssd_dtype io, const void* xbc, int
     return SSD_OK;
 }
 
-// The 16-byte path needs every row start and every x/B/C boundary on 16 bytes.
+// The vector path moves 4 channels per access (8 bytes bf16, 16 bytes fp32): every
+// row start and every x/B/C boundary must sit on that access size. Four bf16
+// channels per thread measured faster than eight (fewer registers per thread,
+// more warps per SM).
 bool conv_vec_ok(const ssd_conv_dims* d, ssd_dtype io, const void* xbc, int64_t stride, const void* x,
                  const void* B, const void* C) {
-    const int64_t v = io == SSD_BF16 ? 8 : 4;
+    const size_t bytes = io == SSD_BF16 ? 8 : 16;
     const int64_t gn = d->ngroups * d->dstate;
-    return d->d_inner % v == 0 && gn % v == 0 && stride % v == 0 && aligned(xbc, 16) && aligned(x, 16) &&
-           aligned(B, 16) && aligned(C, 16);
+    return d->d_inner % 4 == 0 && gn % 4 == 0 && stride % 4 == 0 && aligned(xbc, bytes) && aligned(x, bytes) &&
+           aligned(B, bytes) && aligned(C, bytes);
 }
 
 ssd_status run_conv(bool step, const ssd_conv_dims* d, ssd_dtype io, const void* xbc, int64_t stride,
@@ -400,7 +511,7 @@ ssd_status run_conv(bool step, const ssd_conv_dims* d, ssd_dtype io, const void*
     const int K = static_cast<int>(d->kernel_size);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (io == SSD_BF16)
-        return vec ? launch_conv<__nv_bfloat16, 8>(step, K, xbc, w, bias, x, B, C, state, s, d->batch, st)
+        return vec ? launch_conv<__nv_bfloat16, 4>(step, K, xbc, w, bias, x, B, C, state, s, d->batch, st)
                    : launch_conv<__nv_bfloat16, 1>(step, K, xbc, w, bias, x, B, C, state, s, d->batch, st);
     return vec ? launch_conv<float, 4>(step, K, xbc, w, bias, x, B, C, state, s, d->batch, st)
                : launch_conv<float, 1>(step, K, xbc, w, bias, x, B, C, state, s, d->batch, st);
@@ -455,7 +566,8 @@ ssd_status ssd_gated_rmsnorm(ssd_dtype io_dtype, int64_t rows, int64_t dim, int6
         if (p && !aligned(p, es < 4 ? 4 : es)) return SSD_ERR_UNSUPPORTED;
     const int64_t v = io_dtype == SSD_BF16 ? 8 : 4;
     const bool vec = dim % v == 0 && gs % v == 0 && y_row_stride % v == 0 && out_row_stride % v == 0 &&
-                     (!z || z_row_stride % v == 0) && aligned(y, 16) && aligned(out, 16) && (!z || aligned(z, 16));
+                     (!z || z_row_stride % v == 0) && aligned(y, 16) && aligned(out, 16) && (!z || aligned(z, 16)) &&
+                     aligned(weight, 16);
     NormShape s;
     s.dim = dim;
     s.group = gs;
