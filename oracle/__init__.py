@@ -45,7 +45,7 @@ def _load(path: str) -> ctypes.CDLL:
     f = lib.ssd_oracle_recurrence
     f.restype = ctypes.c_int
     i64, fp = ctypes.c_int64, ctypes.c_void_p
-    f.argtypes = [i64] * 6 + [fp] * 8 + [i64, fp, fp, fp, fp, ctypes.c_int]
+    f.argtypes = [i64] * 6 + [fp] * 8 + [i64, fp, fp, fp, fp, ctypes.c_int, ctypes.c_double, ctypes.c_double]
     return lib
 
 
@@ -82,8 +82,12 @@ def recurrence(
     nthreads: Optional[int] = None,
     want_y: bool = True,
     lib: Optional[ctypes.CDLL] = None,
+    dt_limit: Tuple[float, float] = (0.0, float("inf")),
 ) -> Tuple[Optional[np.ndarray], np.ndarray]:
     """Run the fp64 recurrence.
+
+    ``dt_limit`` = (lo, hi) clamps softplus(dt + dt_bias) like torch.clamp
+    (fla "mamba2.py", the time_step_limit clamp; (0, inf) is no clamp).
 
     Shapes: x [b,L,h,p], dt [b,L,h] (raw), dt_bias [h], A [h], B/C [b,L,g,n],
     D [h] or None, init_state [b,h,p,n] or None.
@@ -109,7 +113,8 @@ def recurrence(
     rc = (lib or library()).ssd_oracle_recurrence(
         b, L, h, p, g, n,
         _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
-        k, _ptr(sel_b), _ptr(sel_h), _ptr(y_sel), _ptr(final_sel), int(nthreads))
+        k, _ptr(sel_b), _ptr(sel_h), _ptr(y_sel), _ptr(final_sel), int(nthreads),
+        float(dt_limit[0]), float(dt_limit[1]))
     if rc != 0:
         raise RuntimeError(f"ssd_oracle_recurrence failed with code {rc}")
     if not full:
@@ -130,6 +135,7 @@ def step(
     D: Optional[np.ndarray],
     state: np.ndarray,
     nthreads: Optional[int] = None,
+    dt_limit: Tuple[float, float] = (0.0, float("inf")),
 ) -> Tuple[np.ndarray, np.ndarray]:
     """One decode step on a carried state: the recurrence over a single token
     with the state as its initial state (fla "mamba2.py", Mamba2.torch_forward,
@@ -139,7 +145,8 @@ def step(
     y [b,h,p] and the new state [b,h,p,n] (fp64).
     """
     b, h, p = x.shape
-    y, final = recurrence(x[:, None], dt[:, None], dt_bias, A, B[:, None], C[:, None], D, state, nthreads=nthreads)
+    y, final = recurrence(x[:, None], dt[:, None], dt_bias, A, B[:, None], C[:, None], D, state, nthreads=nthreads,
+                          dt_limit=dt_limit)
     return y[:, 0], final
 
 

@@ -10,7 +10,7 @@
  *
  *   s_{-1}  = init_state[b,h]                 (zeros when init_state is NULL)
  *   for t = 0 .. L-1:
- *     delta_t = softplus(dt[b,t,h] + dt_bias[h])
+ *     delta_t = clamp(softplus(dt[b,t,h] + dt_bias[h]), dt_min, dt_max)
  *     s_t     = exp(delta_t * A[h]) * s_{t-1} + delta_t * x[b,t,h,:] (outer) B[b,t,g,:]
  *     y[b,t,h,:] = s_t . C[b,t,g,:] + D[h] * x[b,t,h,:]
  *   final_state[b,h] = s_{L-1}
@@ -22,8 +22,10 @@
  *     discretisation exp(delta*A) for the decay and delta*B*u for the input.
  *   - flash-linear-attention "fla/layers/mamba2.py", Mamba2.torch_forward,
  *     single-token branch: state*exp(dt*A) + dt*B*x, readout state.C + D*x;
- *     dt = softplus(dt + dt_bias), the clamp to time_step_limit = (0, inf)
- *     being a no-op (no clamp is applied here).
+ *     dt = softplus(dt + dt_bias), then torch.clamp to time_step_limit
+ *     (lower bound first, then upper; the default (0, inf) changes nothing),
+ *     the same clamp the naive chunked branch applies and the fused branch
+ *     passes on as dt_limit.
  *   - Group map head -> group = head / (nheads/ngroups): burn-mamba
  *     "mamba2/ssd/serial.rs", ssd_serial (heads_per_group).
  *
@@ -40,6 +42,7 @@
 typedef struct {
     int64_t batch, seqlen, nheads, headdim, ngroups, dstate;
     const float *x, *dt, *dt_bias, *A, *B, *C, *D, *init_state;
+    double dt_min, dt_max;
     int64_t nsel;
     const int64_t *sel_b, *sel_h;
     double *y_sel;      /* [nsel, seqlen, headdim] */
@@ -70,7 +73,9 @@ static void run_chain(const oracle_job *j, int64_t k, double *s) {
 
     double *y = j->y_sel ? j->y_sel + k * L * P : NULL;
     for (int64_t t = 0; t < L; ++t) {
-        const double delta = softplus((double)j->dt[(b * L + t) * H + h] + bias_h);
+        double delta = softplus((double)j->dt[(b * L + t) * H + h] + bias_h);
+        if (delta < j->dt_min) delta = j->dt_min;
+        if (delta > j->dt_max) delta = j->dt_max;
         const double decay = exp(delta * a_h);
         const float *xt = j->x + ((b * L + t) * H + h) * P;
         const float *Bt = j->B + ((b * L + t) * G + g) * N;
@@ -106,7 +111,8 @@ static void *worker(void *arg) {
 }
 
 /*
- * Runs the recurrence for the selected (b, h) chains (every token of each).
+ * Runs the recurrence for the selected (b, h) chains (every token of each),
+ * with softplus(dt + dt_bias) clamped to [dt_min, dt_max] (0, INFINITY: none).
  * Returns 0 on success, -1 on invalid arguments, -2 on allocation/thread failure.
  * y_sel or final_sel may be NULL to skip that output.
  */
@@ -116,7 +122,8 @@ int ssd_oracle_recurrence(int64_t batch, int64_t seqlen, int64_t nheads, int64_t
                           const float *B, const float *C, const float *D,
                           const float *init_state,
                           int64_t nsel, const int64_t *sel_b, const int64_t *sel_h,
-                          double *y_sel, double *final_sel, int nthreads) {
+                          double *y_sel, double *final_sel, int nthreads,
+                          double dt_min, double dt_max) {
     if (batch < 1 || seqlen < 1 || nheads < 1 || headdim < 1 || ngroups < 1 || dstate < 1)
         return -1;
     if (nheads % ngroups != 0) return -1;
@@ -130,6 +137,7 @@ int ssd_oracle_recurrence(int64_t batch, int64_t seqlen, int64_t nheads, int64_t
     j.ngroups = ngroups; j.dstate = dstate;
     j.x = x; j.dt = dt; j.dt_bias = dt_bias; j.A = A; j.B = B; j.C = C; j.D = D;
     j.init_state = init_state;
+    j.dt_min = dt_min; j.dt_max = dt_max;
     j.nsel = nsel; j.sel_b = sel_b; j.sel_h = sel_h;
     j.y_sel = y_sel; j.final_sel = final_sel;
     j.next = 0;

@@ -41,12 +41,15 @@ def _expand_groups(M: np.ndarray, nheads: int) -> np.ndarray:
     return np.repeat(M, r, axis=2)
 
 
-def quadratic(x, dt, dt_bias, A, B, C, D=None, init_state=None) -> Tuple[np.ndarray, np.ndarray]:
-    """Brute-force semiseparable form in fp64 (O(L^2) per chain: tiny inputs only)."""
+def quadratic(x, dt, dt_bias, A, B, C, D=None, init_state=None, dt_limit=None) -> Tuple[np.ndarray, np.ndarray]:
+    """Brute-force semiseparable form in fp64 (O(L^2) per chain: tiny inputs only).
+    dt_limit = (lo, hi) bounds the softplus output with np.clip."""
     x = np.asarray(x, np.float64)
     b, L, h, p = x.shape
     n = B.shape[3]
     delta = softplus(np.asarray(dt, np.float64) + np.asarray(dt_bias, np.float64)[None, None, :])
+    if dt_limit is not None:
+        delta = np.clip(delta, dt_limit[0], dt_limit[1])
     Bh = _expand_groups(np.asarray(B, np.float64), h)
     Ch = _expand_groups(np.asarray(C, np.float64), h)
     A = np.asarray(A, np.float64)

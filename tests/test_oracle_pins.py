@@ -411,3 +411,69 @@ def test_gated_rmsnorm_against_torch_rms_norm_and_closed_forms():
         sl = slice(gi * gs, (gi + 1) * gs)
         ref_g = torch.nn.functional.rms_norm(v[:, sl], (gs,), torch.from_numpy(w[sl]), eps).numpy()
         assert np.allclose(grouped[:, sl], ref_g, rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- dt_limit
+def _inverse_softplus64(v):
+    return v + np.log(-np.expm1(-v))
+
+
+def test_dt_limit_equals_a_shifted_raw_dt():
+    """clamp(softplus(dt + bias), lo, hi) (fla Mamba2.torch_forward, time_step_limit) is the same
+    discretisation as an unclamped run on the raw dt that softplus maps onto the clamped value, so
+    the clamped oracle must match the unclamped oracle on that raw dt (up to its fp32 rounding)."""
+    inp = make_inputs(2, 40, 4, 3, 2, 5, io_dtype="f32", init="normal", seed=41)
+    lo, hi = 0.02, 0.3
+    y, fs = _run(inp, dt_limit=(lo, hi))
+    delta = softplus(inp["dt"].astype(np.float64) + inp["dt_bias"].astype(np.float64))
+    assert (delta < lo).any() and (delta > hi).any(), "the draw must hit both bounds"
+    raw = (_inverse_softplus64(np.clip(delta, lo, hi)) - inp["dt_bias"].astype(np.float64)).astype(np.float32)
+    shifted = dict(inp, dt=raw)
+    y2, f2 = _run(shifted)
+    assert rel_err(y, y2) < 1e-5 and rel_err(fs, f2) < 1e-5
+    # and the brute-force form with the clip agrees to fp64 rounding
+    yq, fq = quadratic(*_forms_args(inp), dt_limit=(lo, hi))
+    assert rel_err(y, yq) < TIGHT and rel_err(fs, fq) < TIGHT
+
+
+def test_default_dt_limit_is_no_clamp_and_a_point_limit_is_constant_dt():
+    """(0, inf) leaves every result bit-identical; lo == hi == c makes every step dt = c, which
+    the brute-force form reproduces with a constant delta."""
+    inp = make_inputs(1, 17, 3, 2, 1, 4, io_dtype="f32", init="normal", seed=42)
+    y0, f0 = _run(inp)
+    y1, f1 = _run(inp, dt_limit=(0.0, float("inf")))
+    assert np.array_equal(y0, y1) and np.array_equal(f0, f1)
+    c = 0.05
+    y, fs = _run(inp, dt_limit=(c, c))
+    raw = np.full_like(inp["dt"], 0.0)
+    bias = _inverse_softplus64(np.full(3, c)).astype(np.float64)
+    yq, fq = quadratic(inp["x"], raw, bias, inp["A"], inp["B"], inp["C"], inp["D"], inp["init_state"])
+    assert rel_err(y, yq) < 1e-12 and rel_err(fs, fq) < 1e-12
+
+
+CLAMP_MUTANTS = {
+    "clamp_lower_dropped": ("if (delta < j->dt_min) delta = j->dt_min;", ""),
+    "clamp_upper_dropped": ("if (delta > j->dt_max) delta = j->dt_max;", ""),
+    "clamp_before_softplus": (
+        "double delta = softplus((double)j->dt[(b * L + t) * H + h] + bias_h);\n"
+        "        if (delta < j->dt_min) delta = j->dt_min;\n"
+        "        if (delta > j->dt_max) delta = j->dt_max;",
+        "double delta = (double)j->dt[(b * L + t) * H + h] + bias_h;\n"
+        "        if (delta < j->dt_min) delta = j->dt_min;\n"
+        "        if (delta > j->dt_max) delta = j->dt_max;\n"
+        "        delta = softplus(delta);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CLAMP_MUTANTS))
+def test_dt_limit_pins_reject_planted_mistake(name, tmp_path):
+    old, new = CLAMP_MUTANTS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation target for {name} not found exactly once"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    so = oracle.compile_oracle(str(mutated), str(tmp_path / "mutant.so"))
+    inp = make_inputs(2, 12, 4, 3, 2, 5, io_dtype="f32", init="normal", seed=43)
+    y, fs = _run(inp, lib=oracle.library(so), dt_limit=(0.02, 0.3))
+    yq, fq = quadratic(*_forms_args(inp), dt_limit=(0.02, 0.3))
+    assert rel_err(y, yq) > 1e-6 or rel_err(fs, fq) > 1e-6, f"pins missed mutant {name}"
