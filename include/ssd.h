@@ -4,7 +4,7 @@
  *
  * The operation (the same one, whatever path computes it):
  *
- *   delta[b,t,h] = softplus(dt[b,t,h] + dt_bias[h])            (no clamp)
+ *   delta[b,t,h] = softplus(dt[b,t,h] + dt_bias[h])   (ssd_fwd_ex / ssd_step_ex: clamped, ssd_dt_limit)
  *   s_{-1}       = init_state[b,h]        (zeros when init_state == NULL)
  *   s_t          = exp(delta[b,t,h] A[h]) s_{t-1} + delta[b,t,h] x[b,t,h,:] (outer) B[b,t,g(h),:]
  *   y[b,t,h,:]   = s_t C[b,t,g(h),:] + D[h] x[b,t,h,:]           (D == NULL: no skip)
@@ -85,6 +85,16 @@ typedef struct {
     int64_t batch, seqlen, nheads, headdim, ngroups, dstate;
 } ssd_dims;
 
+/* Clamp of the discretisation step: delta = min(max(softplus(dt + dt_bias),
+ * dt_min), dt_max), torch.clamp's order (fla "mamba2.py", Mamba2.torch_forward:
+ * the time_step_limit clamp after softplus; the fused branch passes it as
+ * dt_limit). Requires 0 <= dt_min <= dt_max; dt_max may be +INFINITY.
+ * {0, INFINITY} (or a NULL pointer where one is taken) changes nothing.
+ * Padded steps past the sequence end keep delta = 0. */
+typedef struct {
+    float dt_min, dt_max;
+} ssd_dt_limit;
+
 /*
  * ssd_fwd -- the SSD chunked-scan forward (the five stages of burn-mamba
  * "serial.rs" ssd_serial / fla "mamba2.py" naive chunked SSD).
@@ -125,6 +135,20 @@ SSD_API ssd_status ssd_fwd_ws(const ssd_dims* dims, ssd_dtype io_dtype,
                       const void* B, const void* C, const float* D, const float* init_state,
                       int chunk_len, int ngroups, void* y, float* final_state,
                       ssd_path path, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * ssd_fwd_ex -- ssd_fwd with a dt limit and an optional explicit path and
+ * workspace: dt_limit NULL means no clamp (SSD_ERR_INVALID_ARG when
+ * dt_min < 0, dt_max < dt_min or either is NaN); workspace NULL means the
+ * library-owned workspace (as ssd_fwd, path honoured), else a caller
+ * workspace under the rules of ssd_fwd_ws. Everything else as ssd_fwd.
+ */
+SSD_API ssd_status ssd_fwd_ex(const ssd_dims* dims, ssd_dtype io_dtype,
+                              const void* x, const float* dt, const float* dt_bias, const float* A,
+                              const void* B, const void* C, const float* D, const float* init_state,
+                              int chunk_len, int ngroups, void* y, float* final_state,
+                              const ssd_dt_limit* dt_limit, ssd_path path,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes ssd_fwd_ws needs for these arguments (0 if they are invalid). */
 SSD_API size_t ssd_fwd_workspace_bytes(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len, ssd_path path);
@@ -209,6 +233,12 @@ SSD_API ssd_status ssd_step(const ssd_dims* dims, ssd_dtype io_dtype,
                             const void* x, const float* dt, const float* dt_bias, const float* A,
                             const void* B, const void* C, const float* D, float* state,
                             int ngroups, void* y, void* stream);
+
+/* ssd_step_ex -- ssd_step with a dt limit (NULL: none; see ssd_dt_limit). */
+SSD_API ssd_status ssd_step_ex(const ssd_dims* dims, ssd_dtype io_dtype,
+                               const void* x, const float* dt, const float* dt_bias, const float* A,
+                               const void* B, const void* C, const float* D, float* state,
+                               int ngroups, void* y, const ssd_dt_limit* dt_limit, void* stream);
 
 /* ------------------------------------------------------------------------
  * The per-token operations around the scan in a Mamba-2 layer (fla

@@ -21,7 +21,7 @@ from typing import Optional, Tuple
 __all__ = [
     "SsdError", "library", "ssd_fwd", "ssd_fwd_host", "ssd_device_status", "ssd_fwd_workspace_bytes",
     "ssd_select_path", "ssd_kernel_launches", "ssd_release", "ssd_step", "ssd_conv1d_silu", "ssd_conv1d_step",
-    "ssd_gated_rmsnorm", "Dims", "ConvDims", "PATHS", "STATUS",
+    "ssd_gated_rmsnorm", "Dims", "ConvDims", "DtLimit", "PATHS", "STATUS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -35,6 +35,10 @@ DTYPES = {"f32": 0, "bf16": 1}
 
 class Dims(ctypes.Structure):
     _fields_ = [(k, ctypes.c_int64) for k in ("batch", "seqlen", "nheads", "headdim", "ngroups", "dstate")]
+
+
+class DtLimit(ctypes.Structure):
+    _fields_ = [("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float)]
 
 
 class ConvDims(ctypes.Structure):
@@ -80,6 +84,12 @@ def library() -> ctypes.CDLL:
     lib.ssd_release.argtypes = []
     lib.ssd_step.restype = i
     lib.ssd_step.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, vp, vp]
+    plim = ctypes.POINTER(DtLimit)
+    lib.ssd_fwd_ex.restype = i
+    lib.ssd_fwd_ex.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, i, vp, fp, plim, i, vp, ctypes.c_size_t,
+                               vp]
+    lib.ssd_step_ex.restype = i
+    lib.ssd_step_ex.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, vp, plim, vp]
     pconv = ctypes.POINTER(ConvDims)
     lib.ssd_conv1d_silu.restype = i
     lib.ssd_conv1d_silu.argtypes = [pconv, i, vp, i64, fp, fp, i, vp, vp, vp, vp, vp]
@@ -150,8 +160,10 @@ def _check_all(x, dt, dt_bias, A, B, C, D, init_state, device_type):
 
 def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: int = 256,
             ngroups: Optional[int] = None, y=None, final_state=None, return_final_state: bool = True,
-            path: str = "auto", workspace=None, stream=None) -> Tuple[object, Optional[object]]:
-    """Run the SSD forward on the GPU through ssd_fwd / ssd_fwd_ws.
+            path: str = "auto", workspace=None, stream=None,
+            dt_limit: Optional[Tuple[float, float]] = None) -> Tuple[object, Optional[object]]:
+    """Run the SSD forward on the GPU through ssd_fwd / ssd_fwd_ws (ssd_fwd_ex
+    when a dt_limit = (lo, hi) clamp of softplus(dt + dt_bias) is given).
 
     Returns (y, final_state); final_state is None when return_final_state is
     False. With path != "auto" or an explicit workspace (a uint8 CUDA tensor)
@@ -179,7 +191,14 @@ def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: int = 2
     if stream is None:
         stream = torch.cuda.current_stream(x.device).cuda_stream
     io = _io_code(x)
-    if path == "auto" and workspace is None:
+    if dt_limit is not None:
+        lim = DtLimit(float(dt_limit[0]), float(dt_limit[1]))
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_len = workspace.numel() if workspace is not None else 0
+        rc = lib.ssd_fwd_ex(ctypes.byref(dims), io, _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
+                            _ptr(D), _ptr(init_state), int(chunk_len), int(ngroups), _ptr(y), _ptr(final_state),
+                            ctypes.byref(lim), PATHS[path], ws_ptr, ws_len, stream)
+    elif path == "auto" and workspace is None:
         rc = lib.ssd_fwd(ctypes.byref(dims), io, _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
                          _ptr(D), _ptr(init_state), int(chunk_len), int(ngroups), _ptr(y), _ptr(final_state),
                          stream)
@@ -223,10 +242,12 @@ def ssd_fwd_host(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: in
     return y, final_state
 
 
-def ssd_step(x, dt, dt_bias, A, B, C, D=None, state=None, ngroups: Optional[int] = None, y=None, stream=None):
-    """One decode step through ssd_step: x [b, h, p], dt [b, h], B/C [b, g, n]
-    (CUDA tensors, x/B/C bf16 or fp32 alike), state [b, h, p, n] fp32 updated in
-    place. Returns y [b, h, p] (x's dtype). Asynchronous on `stream`."""
+def ssd_step(x, dt, dt_bias, A, B, C, D=None, state=None, ngroups: Optional[int] = None, y=None, stream=None,
+             dt_limit: Optional[Tuple[float, float]] = None):
+    """One decode step through ssd_step (ssd_step_ex with a dt_limit): x [b, h, p],
+    dt [b, h], B/C [b, g, n] (CUDA tensors, x/B/C bf16 or fp32 alike), state
+    [b, h, p, n] fp32 updated in place. Returns y [b, h, p] (x's dtype).
+    Asynchronous on `stream`."""
     torch = _torch()
     if x.dim() != 3 or B.dim() != 3:
         raise ValueError("x must be [b, h, p] and B [b, g, n]")
@@ -253,8 +274,14 @@ def ssd_step(x, dt, dt_bias, A, B, C, D=None, state=None, ngroups: Optional[int]
     if stream is None:
         stream = torch.cuda.current_stream(x.device).cuda_stream
     dims = Dims(b, 1, h, p, g, n)
-    rc = library().ssd_step(ctypes.byref(dims), _io_code(x), _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B),
-                            _ptr(C), _ptr(D), _ptr(state), int(ngroups), _ptr(y), stream)
+    if dt_limit is None:
+        rc = library().ssd_step(ctypes.byref(dims), _io_code(x), _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B),
+                                _ptr(C), _ptr(D), _ptr(state), int(ngroups), _ptr(y), stream)
+    else:
+        lim = DtLimit(float(dt_limit[0]), float(dt_limit[1]))
+        rc = library().ssd_step_ex(ctypes.byref(dims), _io_code(x), _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A),
+                                   _ptr(B), _ptr(C), _ptr(D), _ptr(state), int(ngroups), _ptr(y), ctypes.byref(lim),
+                                   stream)
     if rc != 0:
         raise SsdError(rc, "ssd_step")
     return y

@@ -109,7 +109,7 @@ size_t workspace_for(const ssd_dims& d, int chunk_len, ssd_path path) {
 ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* dt, const float* dt_bias,
                const float* A, const void* B, const void* C, const float* D, const float* init, int chunk_len,
                int ngroups, void* y, float* fs, ssd_path path, void* ws, size_t ws_bytes, bool own_ws,
-               void* stream) {
+               void* stream, float dt_min = 0.f, float dt_max = __builtin_inff()) {
     ssd_status st = check_dims(dims, io, chunk_len, ngroups);
     if (st != SSD_OK) return st;
     if (path != SSD_PATH_AUTO && path != SSD_PATH_SIMT && path != SSD_PATH_TC && path != SSD_PATH_CHAIN)
@@ -167,12 +167,25 @@ ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* d
     a.stream = static_cast<cudaStream_t>(stream);
     a.status_word = status;
     a.wait_limit_ns = wait_limit_ns();
+    a.dt_min = dt_min;
+    a.dt_max = dt_max;
     if (p == SSD_PATH_TC) return tc_forward(a, ws, ws_bytes);
     if (p == SSD_PATH_CHAIN) return chain_forward(a, ws, ws_bytes);
     return simt_forward(a, ws, ws_bytes);
 }
 
 size_t elem_bytes(ssd_dtype io) { return io == SSD_F32 ? 4 : 2; }
+
+// A dt limit is 0 <= dt_min <= dt_max (dt_max may be +inf); NULL means none.
+bool dt_limit_ok(const ssd_dt_limit* lim, float* lo, float* hi) {
+    *lo = 0.f;
+    *hi = __builtin_inff();
+    if (!lim) return true;
+    if (!(lim->dt_min >= 0.f) || !(lim->dt_max >= lim->dt_min)) return false;  // also rejects NaN
+    *lo = lim->dt_min;
+    *hi = lim->dt_max;
+    return true;
+}
 
 // ---- fixed scratch for ssd_fwd_noalloc
 // Some callers must not allocate device memory (see ssd_fwd_noalloc in
@@ -225,6 +238,18 @@ ssd_status ssd_fwd_ws(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, c
                       ssd_path path, void* workspace, size_t workspace_bytes, void* stream) {
     return run(dims, io_dtype, x, dt, dt_bias, A, B, C, D, init_state, chunk_len, ngroups, y, final_state, path,
                workspace, workspace_bytes, false, stream);
+}
+
+ssd_status ssd_fwd_ex(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, const float* dt,
+                      const float* dt_bias, const float* A, const void* B, const void* C, const float* D,
+                      const float* init_state, int chunk_len, int ngroups, void* y, float* final_state,
+                      const ssd_dt_limit* dt_limit, ssd_path path, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    float lo, hi;
+    if (!dt_limit_ok(dt_limit, &lo, &hi)) return SSD_ERR_INVALID_ARG;
+    const bool own = workspace == nullptr;
+    return run(dims, io_dtype, x, dt, dt_bias, A, B, C, D, init_state, chunk_len, ngroups, y, final_state, path,
+               workspace, workspace_bytes, own, stream, lo, hi);
 }
 
 size_t ssd_fwd_workspace_bytes(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len, ssd_path path) {
@@ -394,6 +419,14 @@ ssd_status ssd_fwd_noalloc(const ssd_dims* dims, ssd_dtype io_dtype, const void*
 ssd_status ssd_step(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, const float* dt, const float* dt_bias,
                     const float* A, const void* B, const void* C, const float* D, float* state, int ngroups, void* y,
                     void* stream) {
+    return ssd_step_ex(dims, io_dtype, x, dt, dt_bias, A, B, C, D, state, ngroups, y, nullptr, stream);
+}
+
+ssd_status ssd_step_ex(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, const float* dt,
+                       const float* dt_bias, const float* A, const void* B, const void* C, const float* D,
+                       float* state, int ngroups, void* y, const ssd_dt_limit* dt_limit, void* stream) {
+    float lo, hi;
+    if (!dt_limit_ok(dt_limit, &lo, &hi)) return SSD_ERR_INVALID_ARG;
     ssd_status st = check_dims(dims, io_dtype, 1, ngroups);
     if (st != SSD_OK) return st;
     if (dims->seqlen != 1) return SSD_ERR_INVALID_ARG;
@@ -417,6 +450,8 @@ ssd_status ssd_step(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, con
     a.state = state;
     a.y = y;
     a.stream = static_cast<cudaStream_t>(stream);
+    a.dt_min = lo;
+    a.dt_max = hi;
     return step_forward(a);
 }
 

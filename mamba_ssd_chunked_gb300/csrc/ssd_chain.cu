@@ -124,6 +124,7 @@ struct ChainParams {
     int batch, H, G, nblk, nchains, ncta;
     long long L, total;    // total = nchains * nblk jobs
     unsigned long long chain_wait_ns;
+    float dt_min, dt_max;  // clamp of softplus(dt + dt_bias)
 };
 
 // A job is one block of one chain. The CTA's jobs, in processing order (all
@@ -561,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const long long t = static_cast<long long>(blk) * kT + 32 * i + lane;
-                dtv[i] = t < prm.L ? softplus_f(raw[i] + bias) : 0.f;
+                dtv[i] = t < prm.L ? fminf(fmaxf(softplus_f(raw[i] + bias), prm.dt_min), prm.dt_max) : 0.f;
                 float v = dtv[i] * Ah;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -980,6 +981,8 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     p.L = d.seqlen;
     p.total = pl.total;
     p.chain_wait_ns = a.wait_limit_ns;
+    p.dt_min = a.dt_min;
+    p.dt_max = a.dt_max;
     if (cudaFuncSetAttribute(ssd_chain_fused<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(K::SMEM_BYTES)) != cudaSuccess)
         return SSD_ERR_CUDA;

@@ -29,6 +29,8 @@ struct FwdArgs {
     cudaStream_t stream;
     unsigned* status_word;             // device word: bit 0 = a bounded wait timed out
     unsigned long long wait_limit_ns;  // per-wait wall-clock limit on the device
+    float dt_min = 0.f;                // softplus(dt + dt_bias) is clamped to [dt_min, dt_max]
+    float dt_max = __builtin_inff();
 };
 
 // CUDA-core path: the five stages at exactly chunk_len, chunk states in workspace.
@@ -64,6 +66,8 @@ struct StepArgs {
     float* state;
     void* y;
     cudaStream_t stream;
+    float dt_min = 0.f;  // softplus(dt + dt_bias) is clamped to [dt_min, dt_max]
+    float dt_max = __builtin_inff();
 };
 bool step_supported(const ssd_dims& d);
 ssd_status step_forward(const StepArgs& a);

@@ -2,7 +2,7 @@
 // sequence): fla "mamba2.py", Mamba2.torch_forward, cached-decode branch
 // (the fast path calls selective_state_update):
 //
-//   dt' = softplus(dt + dt_bias[h])
+//   dt' = clamp(softplus(dt + dt_bias[h]), dt_min, dt_max)   ((0, inf) by default)
 //   state[p][n] = e^{dt' A[h]} state[p][n] + dt' x[p] B[n]     (in place, fp32)
 //   y[p] = sum_n state[p][n] C[n] + D[h] x[p]
 //
@@ -36,12 +36,12 @@ __global__ void __launch_bounds__(kStepThreads)
     ssd_step_vec4(const T* __restrict__ x, const float* __restrict__ dt, const float* __restrict__ dt_bias,
                   const float* __restrict__ A, const T* __restrict__ B, const T* __restrict__ C,
                   const float* __restrict__ D, float* __restrict__ state, T* __restrict__ y, int H, int G, int P,
-                  int N) {
+                  int N, float2 lim) {
     const int bh = blockIdx.x;
     const int b = bh / H, h = bh % H;
     const int g = h / (H / G);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float d = softplus_step(dt[bh] + dt_bias[h]);
+    const float d = fminf(fmaxf(softplus_step(dt[bh] + dt_bias[h]), lim.x), lim.y);
     const float decay = expf(d * A[h]);
     const float Dh = D ? D[h] : 0.f;
     const long long bg = static_cast<long long>(b) * G + g;
@@ -76,13 +76,13 @@ template <typename T, int NV>
 __global__ void __launch_bounds__(kStepThreads)
     ssd_step_rows4(const T* __restrict__ x, const float* __restrict__ dt, const float* __restrict__ dt_bias,
                    const float* __restrict__ A, const T* __restrict__ B, const T* __restrict__ C,
-                   const float* __restrict__ D, float* __restrict__ state, T* __restrict__ y, int H, int G, int P) {
+                   const float* __restrict__ D, float* __restrict__ state, T* __restrict__ y, int H, int G, int P, float2 lim) {
     constexpr int N = 128 * NV, N4 = N / 4;
     const int bh = blockIdx.x;
     const int b = bh / H, h = bh % H;
     const int g = h / (H / G);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float d = softplus_step(dt[bh] + dt_bias[h]);
+    const float d = fminf(fmaxf(softplus_step(dt[bh] + dt_bias[h]), lim.x), lim.y);
     const float decay = expf(d * A[h]);
     const float Dh = D ? D[h] : 0.f;
     const long long bg = static_cast<long long>(b) * G + g;
@@ -143,12 +143,12 @@ __global__ void __launch_bounds__(kStepThreads)
     ssd_step_scalar(const T* __restrict__ x, const float* __restrict__ dt, const float* __restrict__ dt_bias,
                     const float* __restrict__ A, const T* __restrict__ B, const T* __restrict__ C,
                     const float* __restrict__ D, float* __restrict__ state, T* __restrict__ y, int H, int G, int P,
-                    int N) {
+                    int N, float2 lim) {
     const int bh = blockIdx.x;
     const int b = bh / H, h = bh % H;
     const int g = h / (H / G);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float d = softplus_step(dt[bh] + dt_bias[h]);
+    const float d = fminf(fmaxf(softplus_step(dt[bh] + dt_bias[h]), lim.x), lim.y);
     const float decay = expf(d * A[h]);
     const float Dh = D ? D[h] : 0.f;
     const long long bg = static_cast<long long>(b) * G + g;
@@ -178,15 +178,16 @@ ssd_status launch_step(const StepArgs& a) {
     const T* B = static_cast<const T*>(a.B);
     const T* C = static_cast<const T*>(a.C);
     T* y = static_cast<T*>(a.y);
+    const float2 lim = make_float2(a.dt_min, a.dt_max);
     if (N == 128)
-        ssd_step_rows4<T, 1><<<grid, kStepThreads, 0, a.stream>>>(x, a.dt, a.dt_bias, a.A, B, C, a.D, a.state, y, H, G, P);
+        ssd_step_rows4<T, 1><<<grid, kStepThreads, 0, a.stream>>>(x, a.dt, a.dt_bias, a.A, B, C, a.D, a.state, y, H, G, P, lim);
     else if (N == 256)
-        ssd_step_rows4<T, 2><<<grid, kStepThreads, 0, a.stream>>>(x, a.dt, a.dt_bias, a.A, B, C, a.D, a.state, y, H, G, P);
+        ssd_step_rows4<T, 2><<<grid, kStepThreads, 0, a.stream>>>(x, a.dt, a.dt_bias, a.A, B, C, a.D, a.state, y, H, G, P, lim);
     else if (N % 4 == 0)
-        ssd_step_vec4<T><<<grid, kStepThreads, 0, a.stream>>>(x, a.dt, a.dt_bias, a.A, B, C, a.D, a.state, y, H, G, P, N);
+        ssd_step_vec4<T><<<grid, kStepThreads, 0, a.stream>>>(x, a.dt, a.dt_bias, a.A, B, C, a.D, a.state, y, H, G, P, N, lim);
     else
         ssd_step_scalar<T><<<grid, kStepThreads, 0, a.stream>>>(x, a.dt, a.dt_bias, a.A, B, C, a.D, a.state, y, H, G,
-                                                                P, N);
+                                                                P, N, lim);
     note_launches(1);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

@@ -124,6 +124,7 @@ struct TcParams {
     int batch, H, G, nblk, hpu, ngrp;  // hpu heads per unit, ngrp = H / hpu head groups
     long long L;
     unsigned long long chain_wait_ns;  // limit on waiting for the previous block's state
+    float dt_min, dt_max;              // clamp of softplus(dt + dt_bias)
 };
 
 __device__ __forceinline__ float softplus_f(float v) {
@@ -232,7 +233,10 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
         const int h = h0 + j;
         const long long t = static_cast<long long>(t0) + 32 * c4 + lane;
         float dtv = 0.f;
-        if (t < L) dtv = softplus_f(prm.dt[(static_cast<long long>(b) * L + t) * prm.H + h] + prm.dt_bias[h]);
+        if (t < L)
+            dtv = fminf(fmaxf(softplus_f(prm.dt[(static_cast<long long>(b) * L + t) * prm.H + h] + prm.dt_bias[h]),
+                              prm.dt_min),
+                        prm.dt_max);
         float v = dtv * prm.A[h];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -739,6 +743,8 @@ ssd_status launch(const FwdArgs& a, void* ws) {
     p.ngrp = p.H / p.hpu;
     p.L = d.seqlen;
     p.chain_wait_ns = a.wait_limit_ns;
+    p.dt_min = a.dt_min;
+    p.dt_max = a.dt_max;
     if (cudaFuncSetAttribute(ssd_tc_fused<NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(K::SMEM_BYTES)) != cudaSuccess)
         return SSD_ERR_CUDA;

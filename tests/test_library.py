@@ -29,7 +29,7 @@ def test_header_declares_the_documented_entry_points():
     names = declared_functions()
     for n in ("ssd_fwd", "ssd_fwd_ws", "ssd_fwd_host", "ssd_fwd_workspace_bytes", "ssd_device_status",
               "ssd_status_string", "ssd_kernel_launches", "ssd_release", "ssd_select_path", "ssd_step",
-              "ssd_conv1d_silu", "ssd_conv1d_step", "ssd_gated_rmsnorm"):
+              "ssd_conv1d_silu", "ssd_conv1d_step", "ssd_gated_rmsnorm", "ssd_fwd_ex", "ssd_step_ex"):
         assert n in names
 
 
@@ -179,3 +179,14 @@ def test_norm_rejects_bad_arguments_on_host(lib):
     assert f(1, 4, 64, 0, FAKE, 64, None, 0, FAKE, -1.0, FAKE, 64, None) == 1            # eps < 0
     assert f(1, 4, 130, 1, FAKE, 130, None, 0, FAKE, 1e-5, FAKE, 130, None) == 2         # > 64 groups
     assert f(1, 4, 64, 0, FAKE + 2, 64, None, 0, FAKE, 1e-5, FAKE, 64, None) == 2        # misaligned
+
+
+@pytest.mark.parametrize("lo,hi", [(-0.1, 1.0), (0.5, 0.1), (float("nan"), 1.0), (0.0, float("nan"))])
+def test_bad_dt_limit_rejected_on_host(lib, lo, hi):
+    d = pkg.Dims(1, 8, 2, 64, 1, 128)
+    lim = pkg.DtLimit(lo, hi)
+    assert lib.ssd_fwd_ex(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 1, FAKE, None,
+                          ctypes.byref(lim), 0, None, 0, None) == 1
+    d1 = pkg.Dims(1, 1, 2, 64, 1, 128)
+    assert lib.ssd_step_ex(ctypes.byref(d1), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, FAKE,
+                           ctypes.byref(lim), None) == 1
