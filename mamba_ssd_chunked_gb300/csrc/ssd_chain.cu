@@ -1,52 +1,51 @@
-// Chain-local fused forward (tcgen05/TMA, bf16 io, dstate 128, headdim 64).
+// Chain-local fused forward, head-pair-major form (tcgen05/TMA, bf16 io,
+// dstate 128, headdim 64).
 //
 // A persistent CTA per SM walks a contiguous range of the flattened
-// (chain, block) index space, where a chain is HG heads (1 or 2) of one batch
-// row that read the same B/C group, and a block is 128 tokens. Along a chain
-// the blocks are processed in order by the same CTA, so the chunk state stays
-// in tensor memory from one block to the next; only where a CTA's range
-// starts or ends inside a chain is a state handed to the neighbouring CTA
-// through global memory (once per CTA boundary, not once per block).
-// A CTA processes the tail of its range first (a chain start, which waits on
-// nothing and publishes the hand-off early) and the head of its range last
-// (the continuation that consumes the previous CTA's hand-off).
+// (chain, block) index space. A chain is a pair of heads of one batch row that
+// read the same B/C group; a block is 128 tokens. Along a chain the blocks are
+// processed in order by the same CTA, so the chunk state stays in tensor memory
+// from block to block; only where a CTA's range starts or ends inside a chain
+// is a state handed to the neighbouring CTA through global memory. A CTA
+// processes the tail of its range (a chain start) first and the head of its
+// range (the continuation that consumes the previous CTA's hand-off) last.
 //
-// Per block and head the five stages of the chunked SSD (burn-mamba
-// "mamba2/ssd/serial.rs" k1..k5; fla "mamba2.py" naive chunked SSD) are
-// rewritten around one reference log-decay per (block, head):
+// Per block the chunked SSD (burn-mamba "mamba2/ssd/serial.rs" k1..k5; fla
+// "mamba2.py" naive chunked SSD) is computed with every MMA's M dimension
+// running over (head, p) of the pair, 128 rows:
 //
-//   dt_t = softplus(dt_raw + dt_bias), cs_t = inclusive cumsum of dt*A in the block,
-//   c    = cs_end / 2 (midpoint reference),
-//   W_s  = X_s dt_s e^{c - cs_s}                      (bf16, B operand of k3 and k5a)
-//   z    = e^{c} s_in                                  (fp32 in TMEM, bf16 copy H for k5b)
-//   k3   z += B^T W          ->  z = e^{c - cs_end} s_out  (the state stays scaled in TMEM)
-//   k5   Y = L W + C H^T     with L = C.B^T masked to s <= t (the same for every head)
-//   y_t  = e^{cs_t - c} Y_t + D x_t,  D x_t = e^{cs_t - c} (D / dt_t) W_t
+//   dt_t = clamp(softplus(dt_raw + dt_bias)), cs_t = cumsum of dt*A over the sub-block,
+//   c    = cs_end / 2 (a reference log-decay per sub-block and head),
+//   W_s  = X_s dt_s e^{c - cs_s}                  (bf16, built in place over X)
+//   Z    = e^{c} s_in                              (fp32 state in TMEM, rows (h, p), columns n)
+//   k3   Z += W^T B            ->  Z = e^{c - cs_end} s_out
+//   Y^T  = D x_t e^{c - cs_t}   (preloaded into the accumulator from the X tile)
+//   k5a  Y^T += W^T L^T        with L = C.B^T masked to s <= t (shared by the heads)
+//   k5b  Y^T += H C^T          with H = bf16(e^{c} s_in), read by the MMA from TMEM
+//   y_t  = e^{cs_t - c} Y_t
 //
 // since e^{cs_t - cs_s} dt_s X_s = e^{cs_t - c} (e^{c - cs_s} dt_s X_s) and
-// e^{cs_t} C_t s_in = e^{cs_t - c} C_t (e^{c} s_in). The masked matrix L does not
-// depend on the head, so the MMAs of both heads of a chain run as one N = 128
-// operation (k3, k5a and k5b each: eight K=16 steps for the pair). Every factor
-// lies in [e^{-d/2}, e^{d/2}] for a block decay d = -cs_end, so this
-// "reference" mode is used for d <= kRefMaxDecay. Blocks that decay faster
-// use "exact" mode, per head:
+// e^{cs_t} C_t s_in = e^{cs_t - c} C_t (e^{c} s_in). Every factor stays within
+// e^{+-d/2} for a sub-block decay d, so a block whose decay exceeds
+// kMaxSubDecay is split into 2, 4 or 8 sub-blocks (64, 32 or 16 tokens) that
+// each pass the state on like a block. A 16-token sub-block that still decays
+// faster ("extreme") keeps the state path (with its reference moved to
+// cs_end + kExtremeRef) and C s_in with reference 0, and the epilogue adds its
+// intra-block sum with per-entry decays on the CUDA cores.
 //
-//   W_s  = X_s dt_s e^{cs_end - cs_s}  (k3),   z = e^{cs_end} s_in,  H = s_in,
-//   k5b: Yo = C H^T (into the C.B^T columns, free once the masks are built),
-//   Me[t][s] = C_t.B_s e^{cs_t - cs_s} dt_s (s < t), C_t.B_t dt_t + D (s = t),
-//   k5a: Y = Me X,  y_t = Y_t + e^{cs_t} Yo_t,
+// L for every (batch, block, group) is computed once by a small kernel
+// (chain_masks) into the workspace, and so is every job's table record (dt,
+// sub-block split, per-token factors; chain_tables); the chain kernel streams
+// both like inputs.
 //
-// where every factor is at most 1 (underflow only drops negligible terms).
-//
-// Roles (20 warps):
-//   warp 0       TMA producer: B, C (one buffer each), X (ring of three); and the
-//                MMA issuer of the state path (k3), polled with the loads
-//   warp 1       MMA issuer, output path: C.B^T, k5b, k5a
-//   warps 2..3   tables: dt, cumsum and per-token factors, one head each
-//   warps 4..7   masks into TMEM: L (shared), and Me per exact-mode head
-//   warps 8..11  W from X
-//   warps 12..15 state: rescale z in TMEM, write H; load / store states at segment ends
-//   warps 16..19 epilogue: y from TMEM (+ D x from W), stored straight to global memory
+// Roles (16 warps):
+//   warp 0       TMA producer: L, B and C through a ring of four slots
+//   warp 1       MMA issuer, state path: k3
+//   warp 2       MMA issuer, output path: k5a, k5b
+//   warp 3       TMA producer: X (2 job slots of two heads) and each job's table record
+//   warps 4..7   preload Y^T with the D term from X, then W from X in place
+//   warps 8..11  state: rescale Z, write H; load / store states at segment ends
+//   warps 12..15 epilogue: y = u Y from TMEM, stored to global
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -58,56 +57,61 @@
 namespace ssd {
 namespace {
 
-constexpr int kT = 128;                // tokens per block
-constexpr int kP = 64;                 // headdim
-constexpr int kN = 128;                // dstate
-constexpr uint32_t kTile = 16384;      // 128 rows x 128 bytes, 128-byte swizzle
-constexpr float kRefMaxDecay = 140.f;  // reference mode while the block decay stays within this
+constexpr int kT = 128;                 // tokens per block
+constexpr int kP = 64;                  // headdim
+constexpr int kN = 128;                 // dstate
+constexpr int kHG = 2;                  // heads per chain
+constexpr uint32_t kTile = 16384;       // 128 rows x 128 bytes, 128-byte swizzle
+constexpr float kMaxSubDecay = 150.f;   // a sub-block decaying at most this keeps factors within e^{+-75}
+constexpr float kExtremeRef = 75.f;     // extreme sub-blocks: state reference cs_end + this
 constexpr unsigned long long kLocalWaitNs = 2000000000ull;
-constexpr int kNX = 3;                 // X ring depth
-constexpr int kNumTab = 3;             // per-token tables per (block, head)
-constexpr int kTabSlots = 4;           // table ring depth (jobs)
-enum Tab { TAB_W = 0, TAB_DT = 1, TAB_CS = 2 };
-constexpr int kThreads = 640;
+constexpr int kTabSlots = 2;            // table ring depth (jobs)
+constexpr int kYRows = 16;              // tokens per y staging buffer
+constexpr int kYBufs = 4;               // y staging buffers
+constexpr int kNumTab = 5;              // per-token tables per (job, head), 128 floats each
+// TAB_UD holds float2 {u_t, 1 / u_t} per token (0 for extreme sub-blocks) and spans two table rows
+enum Tab { TAB_WF = 0, TAB_UD = 1, TAB_CS = 3, TAB_DT = 4 };
+constexpr int kScal = 32;               // scalars per (job, head): ec[8], hs[8], is[8], D
+enum Scal { SC_EC = 0, SC_HS = 8, SC_IS = 16, SC_D = 24 };
+constexpr int kThreads = 512;
+constexpr int kRing = 4;                // slots of the L / B / C ring
+// Per-job table record, the same in the workspace and in a shared-memory slot:
+// [2 heads][kNumTab][128] floats, [2 heads][kScal] floats, {nq, extreme, 0, 0}.
+constexpr uint32_t kRecTab = kHG * kNumTab * kT * 4;
+constexpr uint32_t kRecScal = kHG * kScal * 4;
+constexpr uint32_t kRecBytes = kRecTab + kRecScal + 16;
+static_assert(kRecBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+enum RingKind { RK_L = 0, RK_B = 1, RK_C = 2 };
 
-template <int HG>
-struct ChainCfg {
-    static constexpr uint32_t OFF_B = 0;                          // B [t][n] as two 64-column tiles
-    static constexpr uint32_t OFF_C = OFF_B + 2 * kTile;          // C, same layout
-    static constexpr uint32_t OFF_X = OFF_C + 2 * kTile;          // X ring
-    static constexpr uint32_t OFF_W = OFF_X + kNX * kTile;        // W [2 buffers][HG heads], adjacent heads
-    static constexpr uint32_t OFF_H = OFF_W + 2 * HG * kTile;     // H [n][p] per head, adjacent heads
-    static constexpr uint32_t OFF_TAB = OFF_H + HG * kTile;       // [slots][HG][kNumTab][128] floats
-    static constexpr uint32_t TAB_BYTES = kTabSlots * HG * kNumTab * kT * 4;
-    static constexpr uint32_t OFF_SCAL = OFF_TAB + TAB_BYTES;     // [slots][HG][4] floats
-    static constexpr uint32_t OFF_BAR = OFF_SCAL + kTabSlots * HG * 4 * 4;
-    static constexpr int NBAR = 48;
-    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;      // tmem address, ticket, flags
+struct Cfg {
+    // ring of kRing 32 KB slots ([t][128] as two 64-column tiles) holding, in
+    // consumption order, L, B and C of each job: ring position 3J + kind
+    static constexpr uint32_t OFF_RING = 0;
+    static constexpr uint32_t OFF_XW = 8 * kTile;        // 2 job slots x 2 heads, X then W then y
+    static constexpr uint32_t OFF_YS = 12 * kTile;       // y staging: kYBufs buffers x 2 heads x [16 t][64 p]
+    static constexpr uint32_t YS_HEAD = kYRows * 128, YS_BUF = kHG * YS_HEAD;
+    static constexpr uint32_t OFF_TAB = OFF_YS + kYBufs * YS_BUF;  // [slots] table records
+    static constexpr uint32_t OFF_BAR = (OFF_TAB + kTabSlots * kRecBytes + 7) & ~7u;
+    static constexpr int NBAR = 40;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    static constexpr int NH = 64 * HG;                            // N of the batched MMAs
-    // TMEM columns
-    static constexpr uint32_t COL_CB = 0;       // C.B^T, fp32, 128 columns
-    static constexpr uint32_t COL_S = 128;      // scaled state per head, fp32, 64 columns each
-    static constexpr uint32_t COL_R0 = 256;     // region 0: L (or an exact head's C' / Me), bf16 pairs
-    static constexpr uint32_t COL_R1 = 320;     // region 1: an exact head's C' / Me
-    static constexpr uint32_t COL_Y = 384;      // output accumulator per head, fp32, 64 columns each
+    static constexpr uint32_t COL_Z = 0;     // state, fp32, 128 columns (n)
+    static constexpr uint32_t COL_H = 128;   // 2 x 64 columns, bf16 pairs
+    static constexpr uint32_t COL_Y = 256;   // 2 x 128 columns (t)
 };
 
-// mbarrier indices
 enum Bar {
-    B_B_FULL = 0, B_B_EMPTY, B_C_FULL, B_C_EMPTY,
-    B_X_FULL0, B_X_FULL1, B_X_FULL2, B_X_EMPTY0, B_X_EMPTY1, B_X_EMPTY2,
-    B_CB_FULL, B_CB_EMPTY,
-    B_R_FULL0, B_R_FULL1, B_R_EMPTY0, B_R_EMPTY1,
-    B_Y_FULL, B_Y_EMPTY, B_YO_FREE,
-    B_TAB_FULL0, B_TAB_FULL1, B_TAB_FULL2, B_TAB_FULL3, B_TAB_EMPTY0, B_TAB_EMPTY1, B_TAB_EMPTY2, B_TAB_EMPTY3,
-    B_W_FULL0, B_W_FULL1, B_W_EMPTY0, B_W_EMPTY1,
-    B_SCALED, B_S_DONE, B_H_EMPTY,
-    B_DRAIN_A, B_DRAIN_B, B_K3_DONE0, B_K3_DONE1,
+    B_R_FULL0 = 0, B_R_FULL1, B_R_FULL2, B_R_FULL3, B_R_EMPTY0, B_R_EMPTY1, B_R_EMPTY2, B_R_EMPTY3,
+    B_X_FULL0, B_X_FULL1, B_XW_FREE0, B_XW_FREE1,
+    B_TAB_FULL0, B_TAB_FULL1, B_TAB_EMPTY0, B_TAB_EMPTY1,
+    B_W_FULL0, B_W_FULL1, B_YI_FULL0, B_YI_FULL1,
+    B_SCALED, B_S_DONE, B_H_FULL0, B_H_FULL1, B_H_EMPTY0, B_H_EMPTY1,
+    B_Y_FULL0, B_Y_FULL1, B_Y_EMPTY0, B_Y_EMPTY1,
+    B_DRAIN_K3, B_DRAIN_Y,
     B_COUNT
 };
-static_assert(B_COUNT <= 48, "barrier budget");
+static_assert(B_COUNT <= Cfg::NBAR, "barrier budget");
 
 struct ChainParams {
     const float* dt;
@@ -116,15 +120,18 @@ struct ChainParams {
     const float* D;
     const float* init;
     float* final_state;
+    const __nv_bfloat16* x;
     __nv_bfloat16* y;
-    float* handoff;        // [nCTA][HG][P][N] fp32 states handed from CTA i to CTA i + 1
-    uint32_t* ticket;      // CTA order counter
-    uint32_t* flags;       // [nCTA]: 1 once CTA i's hand-off state is in place
+    const __nv_bfloat16* masks;  // [b][nblk][G][t][s] bf16 L tiles (read again by the extreme path)
+    const uint8_t* tables;       // [chain * nblk + block] table records
+    float* handoff;              // [nCTA][2][P][N] fp32 states handed from CTA i to CTA i + 1
+    uint32_t* ticket;            // CTA order counter
+    uint32_t* flags;             // [nCTA]: 1 once CTA i's hand-off state is in place
     uint32_t* status;
     int batch, H, G, nblk, nchains, ncta;
-    long long L, total;    // total = nchains * nblk jobs
+    long long L, total;          // total = nchains * nblk jobs
     unsigned long long chain_wait_ns;
-    float dt_min, dt_max;  // clamp of softplus(dt + dt_bias)
+    float dt_min, dt_max;        // clamp of softplus(dt + dt_bias)
 };
 
 // A job is one block of one chain. The CTA's jobs, in processing order (all
@@ -135,7 +142,6 @@ struct JobList {
     int cF, cL;        // first and last chain touched
     int nE, nM;        // lengths of the tail part (processed first) and of the full chains
     __device__ int count() const { return last - first; }
-    // chain and block of the J-th job; seg_lo / seg_hi: the segment's block range
     __device__ __forceinline__ void at(int J, int& chain, int& blk, int& seg_lo, int& seg_hi) const {
         if (cF == cL) {
             chain = cF;
@@ -174,25 +180,22 @@ __device__ __forceinline__ JobList make_jobs(const ChainParams& p, int cta) {
     return jl;
 }
 
-
-// Everything a role needs to know about its J-th job (out of line: one copy of
-// the index arithmetic serves every role).
 struct JobPos {
     int blk, lo, hi;  // block, and the block range of the job's segment
     int b, h0, g;     // batch row, first head, B/C group
 };
 
-__device__ __noinline__ JobPos job_pos(const JobList& jobs, int J, int chains_per_b, int HG, int HperG) {
+__device__ __noinline__ JobPos job_pos(const JobList& jobs, int J, int chains_per_b, int HperG) {
     JobPos jp;
     int chain;
     jobs.at(J, chain, jp.blk, jp.lo, jp.hi);
     jp.b = chain / chains_per_b;
-    jp.h0 = (chain - jp.b * chains_per_b) * HG;
+    jp.h0 = (chain - jp.b * chains_per_b) * kHG;
     jp.g = jp.h0 / HperG;
     return jp;
 }
 
-__device__ __noinline__ float softplus_f(float v) {
+__device__ __forceinline__ float softplus_f(float v) {
     return v > 0.f ? v + log1pf(expf(-v)) : log1pf(expf(v));
 }
 
@@ -218,113 +221,103 @@ __device__ __noinline__ void wait_bar(uint64_t* bar, uint32_t parity, uint32_t* 
     }
 }
 
-// Per-warp arrival: every lane's prior writes are ordered before lane 0's arrive.
 __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(bar);
 }
 
-// Which TMEM region an exact-mode head uses: region 1, unless both heads of a
-// pair are exact (then head 0 takes region 0, which L does not need).
-__device__ __forceinline__ int exact_region(int nexact, int j, int HG) {
-    return (HG == 2 && nexact == 2 && j == 0) ? 0 : 1;
+// Operand offsets (descriptor units of 16 bytes) of K step k (16 elements):
+// K-major [rows][64] tiles: +32 B inside a tile, the next 64-column tile after
+// four steps; MN-major tiles (rows along K): +16 rows of 128 B.
+__device__ __forceinline__ uint64_t kmaj(int k) {
+    return static_cast<uint64_t>((((k >> 2) * kTile + (k & 3) * 32) >> 4));
+}
+__device__ __forceinline__ uint64_t mnmaj(int k) { return static_cast<uint64_t>((k * 2048) >> 4); }
+
+// k3 of one sub-block: Z += W^T B over its K steps [k0, k0 + nk).
+__device__ __noinline__ void mma_k3(uint32_t z, uint64_t a_w, uint64_t b_b, uint32_t idesc, int k0, int nk) {
+#pragma unroll 1
+    for (int k = k0; k < k0 + nk; ++k) ptx::mma_bf16(z, a_w + mnmaj(k), b_b + mnmaj(k), idesc, 1u);
 }
 
-
-// Exact-mode masked matrix of one head into 64 TMEM columns of this thread's
-// lane (row t = 32 q + lane): Me[t][s] = CB[t][s] e^{cs_t - cs_s} dt_s for
-// s < t, CB[t][t] dt_t + D on the diagonal, zero above. Every tile is written.
-__device__ __noinline__ void build_exact_mask(uint32_t dst, uint32_t cb, int q, int lane, const float* csv,
-                                              const float* dtv, float D) {
-    const int t = 32 * q + lane;
-    const float cs_t = csv[t];
+// k5a of one sub-block: Y^T[:, t0 : t0 + QS] += W^T L^T over s in the sub-block
+// (L rows from t0, K steps [k0, k0 + nk)).
+__device__ __noinline__ void mma_k5a(uint32_t y, uint64_t a_w, uint64_t b_l, uint32_t idesc, int k0, int nk) {
 #pragma unroll 1
-    for (int tile = 0; tile < 4; ++tile) {
-        uint32_t pk[16];
-        if (tile > q) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) pk[e] = 0u;
-        } else {
-            uint32_t rr[32];
-            ptx::tmem_ld32(cb + 32 * tile, rr);
-            ptx::tmem_wait_ld(rr);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                float m2[2];
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int c = 2 * e + h2, s = 32 * tile + c;
-                    const float cbv = __uint_as_float(rr[c]);
-                    const float below = cbv * __expf(fminf(cs_t - csv[s], 0.f)) * dtv[s];
-                    m2[h2] = (tile < q || c < lane) ? below : (c == lane ? fmaf(cbv, dtv[s], D) : 0.f);
-                }
-                pk[e] = pack_bf16x2(m2[0], m2[1]);
-            }
+    for (int k = k0; k < k0 + nk; ++k) ptx::mma_bf16(y, a_w + mnmaj(k), b_l + kmaj(k), idesc, 1u);
+}
+
+// k5b of one sub-block: Y^T[:, t0 : t0 + QS] += H C^T, H from TMEM (8 columns per step).
+__device__ __noinline__ void mma_k5b(uint32_t y, uint32_t h_tmem, uint64_t b_c, uint32_t idesc) {
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) ptx::mma_bf16_ta(y, h_tmem + 8 * k, b_c + kmaj(k), idesc, 1u);
+}
+
+__device__ __forceinline__ uint32_t idesc_n(int n, bool a_mn, bool b_mn) {
+    return ptx::idesc_bf16_f32(128, n, a_mn, b_mn);
+}
+
+// The tokens of extreme sub-blocks for one (head, p) (rare; out of line): y_t
+// = u_t Y_t + D x_t + the intra-block sum over s in [s0, t] with per-entry
+// decays (every factor e^{cs_t - cs_s} <= 1). Y comes again from TMEM, x and L
+// from global memory, cumsum, dt and u from the job's tables.
+__device__ __noinline__ void extreme_tokens(uint32_t ycol, uint32_t extreme, int qs, int tn, const float2* ud,
+                                            const float* cs, const float* dtv, float Dh, const __nv_bfloat16* xg,
+                                            __nv_bfloat16* yg, long long x_tstride, const __nv_bfloat16* lg) {
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+        uint32_t r[32];
+        ptx::tmem_ld32(ycol + 32 * k, r);
+        ptx::tmem_wait_ld(r);
+#pragma unroll 1
+        for (int e = 0; e < 32; ++e) {
+            const int t = 32 * k + e;
+            if (t >= tn || !((extreme >> (t / qs)) & 1u)) continue;
+            float acc = fmaf(ud[t].x, __uint_as_float(r[e]), Dh * __bfloat162float(xg[t * x_tstride]));
+            for (int s = (t / qs) * qs; s <= t; ++s)
+                acc = fmaf(__bfloat162float(lg[t * kT + s]) * __expf(cs[t] - cs[s]) * dtv[s],
+                           __bfloat162float(xg[s * x_tstride]), acc);
+            yg[t * x_tstride] = __float2bfloat16_rn(acc);
         }
-        ptx::tmem_st16(dst + 16 * tile, pk);
     }
 }
 
-
-// K = 128 in eight tcgen05.mma steps of K = 16. SS: both operands in shared
-// memory (K-major operand: +32 bytes per step inside a 64-column tile, next
-// tile after four steps; MN-major operand: +2048 bytes, 16 rows of 128 bytes).
-// TS: A (bf16, K-major) in tensor memory, 8 columns per step. Out of line and
-// rolled: the issue rate (one MMA per ~100 cycles per issuing thread) does
-// not need unrolling, and one copy keeps the instruction cache warm.
-__device__ __noinline__ void mma8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool a_kmajor, bool b_kmajor,
-                                     bool acc) {
-#pragma unroll 1
-    for (int k = 0; k < 8; ++k) {
-        const uint64_t kk = static_cast<uint64_t>((((k >> 2) * kTile + (k & 3) * 32) >> 4));
-        const uint64_t mn = static_cast<uint64_t>((k * 2048) >> 4);
-        ptx::mma_bf16(d, a + (a_kmajor ? kk : mn), b + (b_kmajor ? kk : mn), idesc, (acc || k > 0) ? 1u : 0u);
-    }
-}
-
-__device__ __noinline__ void mma8_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc) {
-#pragma unroll 1
-    for (int k = 0; k < 8; ++k)
-        ptx::mma_bf16_ta(d, a_tmem + 8 * k, b + static_cast<uint64_t>((k * 2048) >> 4), idesc, (acc || k > 0) ? 1u : 0u);
-}
-
-template <int HG>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chain_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
-                    const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
-                    const ChainParams prm) {
-    using K = ChainCfg<HG>;
+                    const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_l,
+                    const __grid_constant__ CUtensorMap tm_y, const ChainParams prm) {
+    using K = Cfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* tab = reinterpret_cast<float*>(smem + K::OFF_TAB);
-    float* scal = reinterpret_cast<float*>(smem + K::OFF_SCAL);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + K::OFF_MISC);
     const uint32_t sbase = ptx::smem_u32(smem);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wg = warp >> 2, q = warp & 3;  // warpgroup, TMEM lane quarter
-    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int q4 = warp & 3;  // TMEM lane quarter
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
 
-    auto T = [&](int slot, int j, int arr) { return tab + ((slot * HG + j) * kNumTab + arr) * kT; };
-    auto S = [&](int slot, int j) { return scal + (slot * HG + j) * 4; };  // exact?, c, cs_end
+    auto T = [&](int slot, int j, int arr) {
+        return reinterpret_cast<float*>(smem + K::OFF_TAB + slot * kRecBytes) + (j * kNumTab + arr) * kT;
+    };
+    auto S = [&](int slot, int j) {
+        return reinterpret_cast<float*>(smem + K::OFF_TAB + slot * kRecBytes + kRecTab) + j * kScal;
+    };
+    auto JW = [&](int slot) {
+        return reinterpret_cast<uint32_t*>(smem + K::OFF_TAB + slot * kRecBytes + kRecTab + kRecScal);
+    };
 
     if (tid == 0) {
         misc[1] = atomicAdd(prm.ticket, 1u);
         uint32_t counts[B_COUNT];
         for (int i = 0; i < B_COUNT; ++i) counts[i] = 1;
-        counts[B_B_EMPTY] = 2;                                  // C.B^T commit + k3 commit
-        counts[B_CB_EMPTY] = 4;                                 // mask warps
-        counts[B_R_FULL0] = counts[B_R_FULL1] = 4;              // mask warps
-        counts[B_Y_EMPTY] = 4;                                  // epilogue warps
-        counts[B_YO_FREE] = 4;                                  // epilogue warps (jobs with exact heads)
-        for (int i = 0; i < kTabSlots; ++i) {
-            counts[B_TAB_FULL0 + i] = HG;                       // table warps
-            counts[B_TAB_EMPTY0 + i] = 4;                       // epilogue warps
-        }
-        counts[B_W_FULL0] = counts[B_W_FULL1] = 4;              // W warps
-        counts[B_W_EMPTY0] = counts[B_W_EMPTY1] = 3;            // k3 commit + k5a commit + y store drained
-        counts[B_SCALED] = 4;                                   // state warps
+        for (int i = 0; i < kTabSlots; ++i) counts[B_TAB_EMPTY0 + i] = 5;  // epilogue warps, k3 issuer
+        counts[B_W_FULL0] = counts[B_W_FULL1] = 4;                          // W warps
+        counts[B_YI_FULL0] = counts[B_YI_FULL1] = 4;                        // W warps
+        counts[B_SCALED] = 4;                                               // state warps
+        counts[B_H_FULL0] = counts[B_H_FULL1] = 4;                          // state warps
+        counts[B_Y_EMPTY0] = counts[B_Y_EMPTY1] = 4;                        // epilogue warps
+        counts[B_XW_FREE0] = counts[B_XW_FREE1] = 2;                        // k3 and k5a commits
         for (int i = 0; i < B_COUNT; ++i) ptx::mbar_init(&bars[i], counts[i]);
         misc[3] = 0u;
         ptx::fence_mbar_init();
@@ -343,382 +336,220 @@ __global__ void __launch_bounds__(kThreads, 1)
     const JobList jobs = make_jobs(prm, cta);
     const int njobs = jobs.count();
     const int HperG = prm.H / prm.G;
-    const int chains_per_b = prm.H / HG;
-    auto chain_coords = [&](int chain, int& b, int& h0, int& g) {
-        b = chain / chains_per_b;
-        h0 = (chain % chains_per_b) * HG;
-        g = h0 / HperG;
-    };
-    auto count_exact = [&](int ts) {
-        int n = 0;
-        for (int j = 0; j < HG; ++j) n += S(ts, j)[0] != 0.f ? 1 : 0;
-        return n;
-    };
-
-    constexpr uint32_t IDESC_CB = ptx::idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, K::NH, true, true);
-    constexpr uint32_t IDESC_Y = ptx::idesc_bf16_f32(128, K::NH, false, true);
-    constexpr uint32_t IDESC_Y1 = ptx::idesc_bf16_f32(128, 64, false, true);
-    auto kmaj = [](int k) { return static_cast<uint64_t>(((k >> 2) * kTile + (k & 3) * 32) >> 4); };
-    auto mnmaj = [](int k) { return static_cast<uint64_t>((k * 2048) >> 4); };
+    const int chains_per_b = prm.H / kHG;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer and k3 issuer
+        // ------------------------------------------------------------ TMA producer: L, B, C ring
         if (lane == 0) {
-            int jb = 0, jc = 0, jx = 0;  // next job for B, next job for C, next X index (job * HG + head)
-            int jk = 0;                  // next job for k3
-            const int nx = njobs * HG;
-            const uint64_t dsc_bt = ptx::desc_sw128(sbase + K::OFF_B, kTile, 1024);
-            uint64_t idle_since = ptx::globaltimer_ns();
-            while (jb < njobs || jc < njobs || jx < nx || jk < njobs) {
-                bool progressed = false;
-                // k3 of job jk: z += B^T W, once W is built, z rescaled and B landed
-                if (jk < njobs && ptx::mbar_test_wait(&bars[B_W_FULL0 + (jk & 1)], (jk >> 1) & 1) &&
-                    ptx::mbar_test_wait(&bars[B_SCALED], jk & 1) && ptx::mbar_test_wait(&bars[B_B_FULL], jk & 1)) {
-                    ptx::tc_fence_after();
-                    const uint64_t dsc_w = ptx::desc_sw128(sbase + K::OFF_W + (jk & 1) * HG * kTile, kTile, 1024);
-                    mma8_ss(tmem + K::COL_S, dsc_bt, dsc_w, IDESC_S, false, false, true);
-                    ptx::mma_commit(&bars[B_S_DONE]);
-                    ptx::mma_commit(&bars[B_W_EMPTY0 + (jk & 1)]);
-                    ptx::mma_commit(&bars[B_K3_DONE0 + (jk & 1)]);
-                    ptx::mma_commit(&bars[B_B_EMPTY]);
-                    ++jk;
-                    progressed = true;
-                }
-                if (jb < njobs && (jb == 0 || ptx::mbar_test_wait(&bars[B_B_EMPTY], (jb - 1) & 1))) {
-                    const JobPos jp_ = job_pos(jobs, jb, chains_per_b, HG, HperG);
-                    const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
-                    (void)lo; (void)hi; (void)g; (void)h0; (void)b;
-                    ptx::mbar_arrive_expect_tx(&bars[B_B_FULL], 2 * kTile);
-                    ptx::tma_load_4d(smem + K::OFF_B, &tm_b, &bars[B_B_FULL], 0, g, blk * kT, b);
-                    ptx::tma_load_4d(smem + K::OFF_B + kTile, &tm_b, &bars[B_B_FULL], 64, g, blk * kT, b);
-                    ++jb;
-                    progressed = true;
-                }
-                if (jc < njobs && (jc == 0 || ptx::mbar_test_wait(&bars[B_C_EMPTY], (jc - 1) & 1))) {
-                    const JobPos jp_ = job_pos(jobs, jc, chains_per_b, HG, HperG);
-                    const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
-                    (void)lo; (void)hi; (void)g; (void)h0; (void)b;
-                    ptx::mbar_arrive_expect_tx(&bars[B_C_FULL], 2 * kTile);
-                    ptx::tma_load_4d(smem + K::OFF_C, &tm_c, &bars[B_C_FULL], 0, g, blk * kT, b);
-                    ptx::tma_load_4d(smem + K::OFF_C + kTile, &tm_c, &bars[B_C_FULL], 64, g, blk * kT, b);
-                    ++jc;
-                    progressed = true;
-                }
-                if (jx < nx) {
-                    const int slot = jx % kNX, use = jx / kNX;
-                    if (use == 0 || ptx::mbar_test_wait(&bars[B_X_EMPTY0 + slot], (use - 1) & 1)) {
-                        const JobPos jp_ = job_pos(jobs, jx / HG, chains_per_b, HG, HperG);
-                        const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
-                        (void)lo; (void)hi; (void)g; (void)h0; (void)b;
-                        uint64_t* fb = &bars[B_X_FULL0 + slot];
-                        ptx::mbar_arrive_expect_tx(fb, kTile);
-                        ptx::tma_load_4d(smem + K::OFF_X + slot * kTile, &tm_x, fb, 0, h0 + jx % HG, blk * kT, b);
-                        ++jx;
-                        progressed = true;
-                    }
-                }
-                const uint64_t now = ptx::globaltimer_ns();
+            const int npos = 3 * njobs;
+            int pr = 0;
+            for (; pr < npos; ++pr) {
+                const int rs = pr % kRing, ru = pr / kRing;
+                if (ru > 0) WB(B_R_EMPTY0 + rs, (ru - 1) & 1);
                 if (*abort_flag) break;
-                if (progressed) {
-                    idle_since = now;
-                } else if (now - idle_since > 2 * kLocalWaitNs) {
-                    atomicOr(prm.status, 2u);
-                    *abort_flag = 1u;
-                    break;
+                const int J = pr / 3, kind = pr - 3 * J;
+                const JobPos jp = job_pos(jobs, J, chains_per_b, HperG);
+                uint64_t* fb = &bars[B_R_FULL0 + rs];
+                uint8_t* dst = smem + K::OFF_RING + rs * 2 * kTile;
+                ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
+                if (kind == RK_L) {
+                    const int tile = (jp.b * prm.nblk + jp.blk) * prm.G + jp.g;
+                    ptx::tma_load_4d(dst, &tm_l, fb, 0, 0, 0, tile);
+                    ptx::tma_load_4d(dst + kTile, &tm_l, fb, 64, 0, 0, tile);
+                } else {
+                    const CUtensorMap* m = kind == RK_B ? &tm_b : &tm_c;
+                    ptx::tma_load_4d(dst, m, fb, 0, jp.g, jp.blk * kT, jp.b);
+                    ptx::tma_load_4d(dst + kTile, m, fb, 64, jp.g, jp.blk * kT, jp.b);
                 }
             }
-            // no copy into this CTA's shared memory may be left in flight at exit:
-            // wait for the last load of each buffer (earlier ones completed before
-            // their buffer was refilled), whether or not the CTA gave up
-            if (jb > 0) ptx::mbar_wait(&bars[B_B_FULL], (jb - 1) & 1, kLocalWaitNs);
-            if (jc > 0) ptx::mbar_wait(&bars[B_C_FULL], (jc - 1) & 1, kLocalWaitNs);
-            for (int c = 0; c < kNX && c < jx; ++c) {
-                const int xl = jx - 1 - c;
-                ptx::mbar_wait(&bars[B_X_FULL0 + xl % kNX], (xl / kNX) & 1, kLocalWaitNs);
+            // no copy into shared memory may be left in flight at exit: wait for the
+            // last load of each slot (earlier ones completed before their reuse)
+            for (int i = 0; i < kRing && i < pr; ++i) {
+                const int P = pr - 1 - i;
+                ptx::mbar_wait(&bars[B_R_FULL0 + P % kRing], (P / kRing) & 1, kLocalWaitNs);
             }
-            // and every k3 must have completed before the tensor memory is released
-            ptx::mma_commit(&bars[B_DRAIN_B]);
-            ptx::mbar_wait(&bars[B_DRAIN_B], 0, kLocalWaitNs);
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer: C.B^T, k5b, k5a
+        // ------------------------------------------------------------ MMA issuer: k3
         if (lane == 0) {
-            uint32_t rreads0 = 0, rreads1 = 0;  // fills of each TMEM region consumed so far
-            auto rwait = [&](int r) {
-                uint32_t& c = r ? rreads1 : rreads0;
-                WB(B_R_FULL0 + r, c & 1);
-                ++c;
-            };
-            const uint64_t dsc_c = ptx::desc_sw128(sbase + K::OFF_C, 16, 1024);
-            const uint64_t dsc_b = ptx::desc_sw128(sbase + K::OFF_B, 16, 1024);
-            const uint64_t dsc_h = ptx::desc_sw128(sbase + K::OFF_H, kTile, 1024);
-            bool prev_exact = false;  // the previous job left Yo of exact heads in the C.B^T columns
-            uint32_t yo_uses = 0;
+            const uint32_t idesc = idesc_n(128, true, true);
+            uint32_t u = 0;  // sub-blocks so far
             for (int J = 0; J < njobs; ++J) {
-                const int ts = J & (kTabSlots - 1), wb = J & 1;
+                const int ts = J & (kTabSlots - 1), xs = J & 1;
                 WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
-                WB(B_B_FULL, J & 1);
-                WB(B_C_FULL, J & 1);
-                if (J > 0) WB(B_CB_EMPTY, (J - 1) & 1);
-                if (prev_exact) {
-                    WB(B_YO_FREE, yo_uses & 1);
-                    ++yo_uses;
-                }
-                ptx::tc_fence_after();
-                const int nexact = count_exact(ts);
-                mma8_ss(tmem + K::COL_CB, dsc_c, dsc_b, IDESC_CB, true, true, false);
-                ptx::mma_commit(&bars[B_CB_FULL]);
-                ptx::mma_commit(&bars[B_B_EMPTY]);
-                // k5b: Y = C H^T for reference heads (H = e^{c} s_in); for exact heads
-                // Yo = C H^T (H = s_in) into the C.B^T columns once the masks have read them
-                WB(B_SCALED, J & 1);
-                if (J > 0) WB(B_Y_EMPTY, (J - 1) & 1);
-                ptx::tc_fence_after();
-                if (nexact == 0) {
-                    mma8_ss(tmem + K::COL_Y, dsc_c, dsc_h, IDESC_Y, true, false, false);
-                } else {
-                    for (int j = 0; j < HG; ++j) {
-                        if (S(ts, j)[0] != 0.f) continue;
-                        const uint64_t dh = ptx::desc_sw128(sbase + K::OFF_H + j * kTile, kTile, 1024);
-                        mma8_ss(tmem + K::COL_Y + 64 * j, dsc_c, dh, IDESC_Y1, true, false, false);
-                    }
-                    WB(B_CB_EMPTY, J & 1);
+                const int nq = static_cast<int>(JW(ts)[0]);
+                const int ksub = 8 / nq;  // K steps per sub-block
+                ptx::mbar_arrive(&bars[B_TAB_EMPTY0 + ts]);  // this issuer is done with the record
+                const int pb = 3 * J + RK_B;
+                WB(B_W_FULL0 + xs, (J >> 1) & 1);
+                WB(B_R_FULL0 + pb % kRing, (pb / kRing) & 1);
+                const uint64_t a_w = ptx::desc_sw128(sbase + K::OFF_XW + xs * 2 * kTile, kTile, 1024);
+                const uint64_t b_b = ptx::desc_sw128(sbase + K::OFF_RING + (pb % kRing) * 2 * kTile, kTile, 1024);
+                for (int q = 0; q < nq; ++q, ++u) {
+                    WB(B_SCALED, u & 1);
                     ptx::tc_fence_after();
-                    for (int j = 0; j < HG; ++j) {
-                        if (S(ts, j)[0] == 0.f) continue;
-                        const uint64_t dh = ptx::desc_sw128(sbase + K::OFF_H + j * kTile, kTile, 1024);
-                        mma8_ss(tmem + K::COL_CB + 64 * j, dsc_c, dh, IDESC_Y1, true, false, false);
-                    }
+                    mma_k3(tmem + K::COL_Z, a_w, b_b, idesc, q * ksub, ksub);
+                    ptx::mma_commit(&bars[B_S_DONE]);
                 }
-                ptx::mma_commit(&bars[B_H_EMPTY]);
-                ptx::mma_commit(&bars[B_C_EMPTY]);
-                // k5a: Y += L W (reference heads); Y = Me X (exact heads)
-                const uint64_t dsc_w = ptx::desc_sw128(sbase + K::OFF_W + wb * HG * kTile, kTile, 1024);
-                // W built (and, through the W warps' waits, every X tile of this job landed)
-                WB(B_W_FULL0 + wb, (J >> 1) & 1);
-                if (nexact < HG) {
-                    rwait(0);
-                    ptx::tc_fence_after();
-                    if (nexact == 0) {
-                        mma8_ts(tmem + K::COL_Y, tmem + K::COL_R0, dsc_w, IDESC_Y, true);
-                    } else {
-                        for (int j = 0; j < HG; ++j) {
-                            if (S(ts, j)[0] != 0.f) continue;
-                            const uint64_t dw = dsc_w + ((j * kTile) >> 4);
-                            mma8_ts(tmem + K::COL_Y + 64 * j, tmem + K::COL_R0, dw, IDESC_Y1, true);
-                        }
-                    }
-                    ptx::mma_commit(&bars[B_R_EMPTY0]);
-                }
-                for (int j = 0; j < HG && nexact > 0; ++j) {
-                    if (S(ts, j)[0] == 0.f) continue;
-                    const int r = exact_region(nexact, j, HG);
-                    rwait(r);
-                    ptx::tc_fence_after();
-                    const int xs = (J * HG + j) % kNX;
-                    const uint64_t dx = ptx::desc_sw128(sbase + K::OFF_X + xs * kTile, kTile, 1024);
-                    const uint32_t ra = tmem + (r ? K::COL_R1 : K::COL_R0);
-                    mma8_ts(tmem + K::COL_Y + 64 * j, ra, dx, IDESC_Y1, false);
-                    ptx::mma_commit(&bars[B_R_EMPTY0 + r]);
-                    ptx::mma_commit(&bars[B_X_EMPTY0 + xs]);
-                }
-                ptx::mma_commit(&bars[B_W_EMPTY0 + wb]);
-                ptx::mma_commit(&bars[B_Y_FULL]);
-                prev_exact = nexact > 0;
+                ptx::mma_commit(&bars[B_R_EMPTY0 + pb % kRing]);
+                ptx::mma_commit(&bars[B_XW_FREE0 + xs]);
             }
-            ptx::mma_commit(&bars[B_DRAIN_A]);
-            ptx::mbar_wait(&bars[B_DRAIN_A], 0, kLocalWaitNs);
+            ptx::mma_commit(&bars[B_DRAIN_K3]);
+            ptx::mbar_wait(&bars[B_DRAIN_K3], 0, kLocalWaitNs);
         }
         __syncwarp();
-    } else if (warp < 2 + HG) {
-        // ------------------------------------------------------------ tables for head j
-        const int j = warp - 2;
-        float pre[4];  // raw dt of the next job, loaded one job ahead
-        auto load_dt = [&](int J, float (&v)[4]) {
-            const JobPos jp_ = job_pos(jobs, J, chains_per_b, HG, HperG);
-            const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
-            (void)lo; (void)hi; (void)g; (void)h0; (void)b;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const long long t = static_cast<long long>(blk) * kT + 32 * i + lane;
-                v[i] = t < prm.L ? prm.dt[(static_cast<long long>(b) * prm.L + t) * prm.H + h0 + j] : 0.f;
-            }
-        };
-        if (njobs > 0) load_dt(0, pre);
-        for (int J = 0; J < njobs; ++J) {
-            const int ts = J & (kTabSlots - 1);
-            const JobPos jp_ = job_pos(jobs, J, chains_per_b, HG, HperG);
-            const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
-            (void)lo; (void)hi; (void)g; (void)h0; (void)b;
-            const int h = h0 + j;
-            float raw[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) raw[i] = pre[i];
-            if (J + 1 < njobs) load_dt(J + 1, pre);
-            const float bias = prm.dt_bias[h], Ah = prm.A[h], Dh = prm.D ? prm.D[h] : 0.f;
-            float dtv[4], cs[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const long long t = static_cast<long long>(blk) * kT + 32 * i + lane;
-                dtv[i] = t < prm.L ? fminf(fmaxf(softplus_f(raw[i] + bias), prm.dt_min), prm.dt_max) : 0.f;
-                float v = dtv[i] * Ah;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float o = __shfl_up_sync(0xffffffffu, v, off);
-                    if (lane >= off) v += o;
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ MMA issuer: k5a, k5b
+        if (lane == 0) {
+            uint32_t u = 0;
+            for (int J = 0; J < njobs; ++J) {
+                const int ts = J & (kTabSlots - 1), xs = J & 1, yb = J & 1;
+                WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
+                const int nq = static_cast<int>(JW(ts)[0]);
+                const uint32_t extreme = JW(ts)[1];
+                const int qs = kT / nq, ksub = 8 / nq;
+                const uint32_t yc = tmem + K::COL_Y + 128 * yb;
+                const int pl = 3 * J + RK_L, pc = 3 * J + RK_C;
+                WB(B_YI_FULL0 + yb, (J >> 1) & 1);  // Y preloaded with D x / u
+                WB(B_W_FULL0 + xs, (J >> 1) & 1);
+                WB(B_R_FULL0 + pl % kRing, (pl / kRing) & 1);
+                ptx::tc_fence_after();
+                const uint64_t a_w = ptx::desc_sw128(sbase + K::OFF_XW + xs * 2 * kTile, kTile, 1024);
+                const uint32_t id_a = idesc_n(qs, true, false), id_b = idesc_n(qs, false, false);
+                for (int q = 0; q < nq; ++q) {
+                    if ((extreme >> q) & 1u) continue;
+                    const uint64_t b_l =
+                        ptx::desc_sw128(sbase + K::OFF_RING + (pl % kRing) * 2 * kTile + q * qs * 128, 16, 1024);
+                    mma_k5a(yc + q * qs, a_w, b_l, id_a, q * ksub, ksub);
                 }
-                cs[i] = v;
-            }
-            float run = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                cs[i] += run;
-                run = __shfl_sync(0xffffffffu, cs[i], 31);
-            }
-            const float cs_end = run;
-            const bool exact = -cs_end > kRefMaxDecay;
-            const float c = 0.5f * cs_end;
-            if (J >= kTabSlots) WB(B_TAB_EMPTY0 + ts, ((J / kTabSlots) - 1) & 1);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = 32 * i + lane;
-                const float d = dtv[i];
-                T(ts, j, TAB_W)[t] = exact ? d * __expf(cs_end - cs[i]) : d * __expf(c - cs[i]);
-                T(ts, j, TAB_DT)[t] = d;
-                T(ts, j, TAB_CS)[t] = cs[i];
-            }
-            if (lane == 0) {
-                S(ts, j)[0] = exact ? 1.f : 0.f;
-                S(ts, j)[1] = c;
-                S(ts, j)[2] = cs_end;
-                S(ts, j)[3] = Dh;
-            }
-            warp_arrive(&bars[B_TAB_FULL0 + ts], lane);
-        }
-    } else if (warp < 4) {
-        // idle table warp (one head per chain)
-    } else if (wg == 1) {
-        // ------------------------------------------------------------ masks into TMEM
-        uint32_t writes0 = 0, writes1 = 0;  // fills of each region so far
-        bool dirty0 = true, dirty1 = true;  // tiles above this warp's diagonal are not known to be zero
-        auto claim = [&](int r) {
-            uint32_t& w = r ? writes1 : writes0;
-            if (w > 0) WB(B_R_EMPTY0 + r, (w - 1) & 1);
-            ++w;
-            ptx::tc_fence_after();
-        };
-        auto publish = [&](int r) {
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            warp_arrive(&bars[B_R_FULL0 + r], lane);
-        };
-        for (int J = 0; J < njobs; ++J) {
-            const int ts = J & (kTabSlots - 1);
-            WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
-            WB(B_CB_FULL, J & 1);
-            ptx::tc_fence_after();
-            const int nexact = count_exact(ts);
-            // (b) L = C.B^T masked to s <= t, shared by the reference-mode heads
-            if (nexact < HG) {
-                claim(0);
-                const uint32_t dst = tmem + lane_base + K::COL_R0;
-#pragma unroll 1
-                for (int tile = 0; tile < 4; ++tile) {
-                    if (tile > q) {
-                        if (dirty0) {
-                            uint32_t z[16];
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) z[e] = 0u;
-                            ptx::tmem_st16(dst + 16 * tile, z);
-                        }
-                        continue;
-                    }
-                    uint32_t rr[32];
-                    ptx::tmem_ld32(tmem + lane_base + K::COL_CB + 32 * tile, rr);
-                    ptx::tmem_wait_ld(rr);
-                    uint32_t pk[16];
-                    if (tile < q) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            pk[e] = pack_bf16x2(2 * e <= lane ? __uint_as_float(rr[2 * e]) : 0.f,
-                                                2 * e + 1 <= lane ? __uint_as_float(rr[2 * e + 1]) : 0.f);
-                    }
-                    ptx::tmem_st16(dst + 16 * tile, pk);
+                ptx::mma_commit(&bars[B_R_EMPTY0 + pl % kRing]);
+                ptx::mma_commit(&bars[B_XW_FREE0 + xs]);
+                WB(B_R_FULL0 + pc % kRing, (pc / kRing) & 1);
+                for (int q = 0; q < nq; ++q, ++u) {
+                    const int hb = u & 1;
+                    WB(B_H_FULL0 + hb, (u >> 1) & 1);
+                    ptx::tc_fence_after();
+                    const uint64_t b_c =
+                        ptx::desc_sw128(sbase + K::OFF_RING + (pc % kRing) * 2 * kTile + q * qs * 128, 16, 1024);
+                    mma_k5b(yc + q * qs, tmem + K::COL_H + 64 * hb, b_c, id_b);
+                    ptx::mma_commit(&bars[B_H_EMPTY0 + hb]);
                 }
-                dirty0 = false;
-                publish(0);
+                ptx::mma_commit(&bars[B_R_EMPTY0 + pc % kRing]);
+                ptx::mma_commit(&bars[B_Y_FULL0 + yb]);
             }
-            // (c) Me for each exact-mode head
-            for (int j = 0; j < HG && nexact > 0; ++j) {
-                if (S(ts, j)[0] == 0.f) continue;
-                const int r = exact_region(nexact, j, HG);
-                claim(r);
-                build_exact_mask(tmem + lane_base + (r ? K::COL_R1 : K::COL_R0), tmem + lane_base + K::COL_CB, q, lane,
-                                 T(ts, j, TAB_CS), T(ts, j, TAB_DT), S(ts, j)[3]);
-                (r ? dirty1 : dirty0) = false;
-                publish(r);
-            }
-            warp_arrive(&bars[B_CB_EMPTY], lane);  // every C.B^T read of this job has completed
+            ptx::mma_commit(&bars[B_DRAIN_Y]);
+            ptx::mbar_wait(&bars[B_DRAIN_Y], 0, kLocalWaitNs);
         }
-    } else if (wg == 2) {
-        // ------------------------------------------------------------ W from X
-        const int wt = tid - 256;  // 0..127
+        __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ TMA producer: X
+        if (lane == 0) {
+            int jx = 0, ntab = 0;
+            for (; jx < njobs; ++jx) {
+                const int ts = jx & (kTabSlots - 1);
+                if (jx >= kTabSlots) WB(B_TAB_EMPTY0 + ts, ((jx / kTabSlots) - 1) & 1);
+                if (*abort_flag) break;
+                const JobPos jp = job_pos(jobs, jx, chains_per_b, HperG);
+                const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.h0 / kHG) * prm.nblk + jp.blk;
+                ptx::mbar_arrive_expect_tx(&bars[B_TAB_FULL0 + ts], kRecBytes);
+                ptx::bulk_load(smem + K::OFF_TAB + ts * kRecBytes, prm.tables + rec * kRecBytes, kRecBytes,
+                               &bars[B_TAB_FULL0 + ts]);
+                ++ntab;
+                if (jx >= 2) WB(B_XW_FREE0 + (jx & 1), ((jx >> 1) - 1) & 1);  // k3 and k5a of job jx - 2 are done
+                if (*abort_flag) break;
+                uint64_t* fb = &bars[B_X_FULL0 + (jx & 1)];
+                uint8_t* dst = smem + K::OFF_XW + (jx & 1) * 2 * kTile;
+                ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
+                ptx::tma_load_4d(dst, &tm_x, fb, 0, jp.h0, jp.blk * kT, jp.b);
+                ptx::tma_load_4d(dst + kTile, &tm_x, fb, 0, jp.h0 + 1, jp.blk * kT, jp.b);
+            }
+            for (int i = 0; i < 2 && i < jx; ++i) {
+                const int J = jx - 1 - i;
+                ptx::mbar_wait(&bars[B_X_FULL0 + (J & 1)], (J >> 1) & 1, kLocalWaitNs);
+            }
+
+            // table copies: the last one per slot
+            for (int i = 0; i < kTabSlots && i < ntab; ++i) {
+                const int J = ntab - 1 - i;
+                ptx::mbar_wait(&bars[B_TAB_FULL0 + (J & (kTabSlots - 1))], (J / kTabSlots) & 1, kLocalWaitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ W from X, in place
+        const int wt = tid - 128;  // 0..127; also TMEM lane (head j, p) for the preload
+        const int jl = wt >> 6, pl = wt & 63;
         for (int J = 0; J < njobs; ++J) {
-            const int ts = J & (kTabSlots - 1), wb = J & 1;
+            const int ts = J & (kTabSlots - 1), xs = J & 1, yb = J & 1;
             WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
-            if (J >= 2) WB(B_W_EMPTY0 + wb, ((J >> 1) - 1) & 1);
+            WB(B_X_FULL0 + xs, (J >> 1) & 1);
+            // Y^T[(j, p), t] = D_j x_t[p] / u_t, the D term in the accumulator's own scale
+            // (zero for extreme sub-blocks, whose epilogue adds D x itself)
+            if (J >= 2) WB(B_Y_EMPTY0 + yb, ((J >> 1) - 1) & 1);
+            {
+                const uint8_t* tile = smem + K::OFF_XW + (xs * kHG + jl) * kTile;
+                const float2* ud = reinterpret_cast<const float2*>(T(ts, jl, TAB_UD));
+                const float Dh = S(ts, jl)[SC_D];
+                const uint32_t pbyte = (pl & 7) * 2, pchunk = pl >> 3;
+                const uint32_t ycol = tmem + lane_base + K::COL_Y + 128 * yb;
 #pragma unroll 1
-            for (int j = 0; j < HG; ++j) {
-                const int ix = J * HG + j, xs = ix % kNX;
-                const bool exact = S(ts, j)[0] != 0.f;
-                WB(B_X_FULL0 + xs, (ix / kNX) & 1);
-                const float* wf = T(ts, j, TAB_W);
-                const uint8_t* xb = smem + K::OFF_X + xs * kTile;
-                uint8_t* wbuf = smem + K::OFF_W + (wb * HG + j) * kTile;
-#pragma unroll 2
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int t = 32 * k + e;
+                        const float xv =
+                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + ptx::swz128(t, pchunk) + pbyte));
+                        r[e] = __float_as_uint(Dh * xv * ud[t].y);
+                    }
+                    ptx::tmem_st32(ycol + 32 * k, r);
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::named_sync(1, 128);  // every thread has read its X column before W overwrites it
+                warp_arrive(&bars[B_YI_FULL0 + yb], lane);
+            }
+#pragma unroll 1
+            for (int j = 0; j < kHG; ++j) {
+                const float* wf = T(ts, j, TAB_WF);
+                uint8_t* tile = smem + K::OFF_XW + (xs * kHG + j) * kTile;
+                // all loads first, then the stores (see the epilogue)
+                uint4 v[8];
+                float w[8];
+#pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int chunk = wt + 128 * i;  // 16-byte chunk; its row is chunk / 8 in either tile
-                    const int row = chunk >> 3;
-                    const uint4 v = *reinterpret_cast<const uint4*>(xb + chunk * 16);
-                    const float2 f0 = unpack_bf16x2(v.x), f1 = unpack_bf16x2(v.y), f2 = unpack_bf16x2(v.z),
-                                 f3 = unpack_bf16x2(v.w);
-                    const float w = wf[row];
-                    uint4 o;
-                    o.x = pack_bf16x2(f0.x * w, f0.y * w);
-                    o.y = pack_bf16x2(f1.x * w, f1.y * w);
-                    o.z = pack_bf16x2(f2.x * w, f2.y * w);
-                    o.w = pack_bf16x2(f3.x * w, f3.y * w);
-                    *reinterpret_cast<uint4*>(wbuf + chunk * 16) = o;
+                    const int chunk = wt + 128 * i;  // 16-byte chunk; its row is chunk / 8
+                    v[i] = *reinterpret_cast<const uint4*>(tile + chunk * 16);
+                    w[i] = wf[chunk >> 3];
                 }
-                if (!exact) {
-                    // the X slot is free once all four warps have read it (exact mode:
-                    // k5a reads X, and its completion frees the slot)
-                    ptx::named_sync(1, 128);
-                    if (wt == 0) ptx::mbar_arrive(&bars[B_X_EMPTY0 + xs]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 f0 = unpack_bf16x2(v[i].x), f1 = unpack_bf16x2(v[i].y), f2 = unpack_bf16x2(v[i].z),
+                                 f3 = unpack_bf16x2(v[i].w);
+                    uint4 o;
+                    o.x = pack_bf16x2(f0.x * w[i], f0.y * w[i]);
+                    o.y = pack_bf16x2(f1.x * w[i], f1.y * w[i]);
+                    o.z = pack_bf16x2(f2.x * w[i], f2.y * w[i]);
+                    o.w = pack_bf16x2(f3.x * w[i], f3.y * w[i]);
+                    *reinterpret_cast<uint4*>(tile + (wt + 128 * i) * 16) = o;
                 }
             }
             ptx::fence_proxy_async_smem();
-            warp_arrive(&bars[B_W_FULL0 + wb], lane);
+            warp_arrive(&bars[B_W_FULL0 + xs], lane);
         }
-    } else if (wg == 3) {
+    } else if (warp < 12) {
         // ------------------------------------------------------------ state
-        const int n = 32 * q + lane;
-        const int st = tid - 384;  // 0..127
-        float sigma0 = 1.f, sigma1 = 1.f;  // per head: TMEM holds sigma * s
-        uint32_t sdone = 0;
+        const int st = tid - 256;    // TMEM lane = (head j, p)
+        const int j = st >> 6, p = st & 63;
+        float inv_prev = 1.f;        // Z = sigma s; 1 / sigma of the last sub-block
+        uint32_t sdone = 0, u = 0;
         for (int J = 0; J < njobs; ++J) {
             const int ts = J & (kTabSlots - 1);
-            const JobPos jp_ = job_pos(jobs, J, chains_per_b, HG, HperG);
-            const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
-            (void)lo; (void)hi; (void)g; (void)h0; (void)b;
-            const bool seg_start = (blk == lo), seg_end = (blk == hi - 1);
-            if (seg_start && lo > 0) {
+            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG);
+            const bool seg_start = (jp.blk == jp.lo), seg_end = (jp.blk == jp.hi - 1);
+            const int h = jp.h0 + j;
+            if (seg_start && jp.lo > 0) {
                 // wait for the previous CTA's hand-off of this chain's state
                 if (st == 0) {
                     const uint32_t* f = prm.flags + (cta - 1);
@@ -736,91 +567,92 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::fence_acquire_gpu();
             }
             WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
-            if (!seg_start) {
-                WB(B_S_DONE, sdone & 1);
-                ++sdone;
-                ptx::tc_fence_after();
+            const int nq = static_cast<int>(JW(ts)[0]);
+            const float* sc = S(ts, j);
+            const float* src = nullptr;  // segment start: the incoming state row [n]
+            if (seg_start) {
+                if (jp.lo > 0)
+                    src = misc[2] ? nullptr : prm.handoff + ((static_cast<size_t>(cta - 1) * kHG + j) * kP + p) * kN;
+                else if (prm.init)
+                    src = prm.init + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * kN;
+                inv_prev = 1.f;
             }
-            if (J > 0) WB(B_H_EMPTY, (J - 1) & 1);
-#pragma unroll 1
-            for (int j = 0; j < HG; ++j) {
-                const int h = h0 + j;
-                const bool exact = S(ts, j)[0] != 0.f;
-                const float c = S(ts, j)[1], cs_end = S(ts, j)[2];
-                const float* src = nullptr;  // segment start: the incoming state, [p][n] rows of 128 floats
-                if (seg_start) {
-                    if (lo > 0)
-                        src = misc[2] ? nullptr : prm.handoff + (static_cast<size_t>(cta - 1) * HG + j) * kP * kN;
-                    else if (prm.init)
-                        src = prm.init + (static_cast<size_t>(b) * prm.H + h) * kP * kN;
-                    if (j) sigma1 = 1.f; else sigma0 = 1.f;
+            for (int q = 0; q < nq; ++q, ++u) {
+                const bool from_src = seg_start && q == 0;
+                if (!from_src) {
+                    WB(B_S_DONE, sdone & 1);
+                    ++sdone;
                 }
-                // s = v / sigma is the true state; z = s e^{c} (reference) or s e^{cs_end} (exact).
-                // The two factors are applied one after the other: their product
-                // e^{c} / sigma can fall below the fp32 range when consecutive
-                // blocks both decay strongly, while s and z stay representable.
-                const float inv_sigma = 1.f / (j ? sigma1 : sigma0);
-                const float f = exact ? __expf(cs_end) : __expf(c);
-                uint8_t* hb = smem + K::OFF_H + j * kTile;
-                const uint32_t scol = tmem + lane_base + K::COL_S + 64 * j;
+                const int hb = u & 1;
+                if (u >= 2) WB(B_H_EMPTY0 + hb, ((u >> 1) - 1) & 1);
+                ptx::tc_fence_after();
+                const float ec = sc[SC_EC + q], hs = sc[SC_HS + q];
+                const uint32_t zcol = tmem + lane_base + K::COL_Z;
+                const uint32_t hcol = tmem + lane_base + K::COL_H + 64 * hb;
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
+                for (int k = 0; k < 4; ++k) {
                     uint32_t r[32];
-                    if (seg_start) {
+                    if (from_src) {
+                        if (src) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            r[e] = __float_as_uint(src ? src[(32 * half + e) * kN + n] : 0.f);
+                            for (int e = 0; e < 8; ++e) {
+                                const float4 v = *reinterpret_cast<const float4*>(src + 32 * k + 4 * e);
+                                r[4 * e] = __float_as_uint(v.x);
+                                r[4 * e + 1] = __float_as_uint(v.y);
+                                r[4 * e + 2] = __float_as_uint(v.z);
+                                r[4 * e + 3] = __float_as_uint(v.w);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) r[e] = 0u;
+                        }
                     } else {
-                        ptx::tmem_ld32(scol + 32 * half, r);
+                        ptx::tmem_ld32(zcol + 32 * k, r);
                         ptx::tmem_wait_ld(r);
                     }
+                    // s = Z / sigma_prev is the true state; the two factors of the new
+                    // scale are applied one after the other (their product can leave
+                    // the fp32 range when consecutive sub-blocks both decay strongly)
+                    uint32_t hp[16];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * inv_sigma);  // s
-                    // H = bf16(z) (reference) or bf16(s) (exact)
-                    const float hf = exact ? 1.f : f;
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        uint4 o;
-                        o.x = pack_bf16x2(__uint_as_float(r[8 * c8 + 0]) * hf, __uint_as_float(r[8 * c8 + 1]) * hf);
-                        o.y = pack_bf16x2(__uint_as_float(r[8 * c8 + 2]) * hf, __uint_as_float(r[8 * c8 + 3]) * hf);
-                        o.z = pack_bf16x2(__uint_as_float(r[8 * c8 + 4]) * hf, __uint_as_float(r[8 * c8 + 5]) * hf);
-                        o.w = pack_bf16x2(__uint_as_float(r[8 * c8 + 6]) * hf, __uint_as_float(r[8 * c8 + 7]) * hf);
-                        *reinterpret_cast<uint4*>(hb + ptx::swz128(n, 4 * half + c8)) = o;
+                    for (int e = 0; e < 16; ++e) {
+                        const float s0 = __uint_as_float(r[2 * e]) * inv_prev;
+                        const float s1 = __uint_as_float(r[2 * e + 1]) * inv_prev;
+                        hp[e] = pack_bf16x2(s0 * hs, s1 * hs);
+                        r[2 * e] = __float_as_uint(s0 * ec);
+                        r[2 * e + 1] = __float_as_uint(s1 * ec);
                     }
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);  // z
-                    ptx::tmem_st32(scol + 32 * half, r);
+                    ptx::tmem_st32(zcol + 32 * k, r);
+                    ptx::tmem_st16(hcol + 16 * k, hp);
                 }
-                const float sg = exact ? 1.f : __expf(c - cs_end);
-                if (j) sigma1 = sg; else sigma0 = sg;
+                inv_prev = sc[SC_IS + q];
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                warp_arrive(&bars[B_SCALED], lane);
+                warp_arrive(&bars[B_H_FULL0 + hb], lane);
             }
-            ptx::tmem_wait_st();
-            ptx::fence_proxy_async_smem();
-            ptx::tc_fence_before();
-            warp_arrive(&bars[B_SCALED], lane);
             if (seg_end) {
                 // the chain's state after this block: final state, or the hand-off to CTA + 1
-                const bool to_final = (hi == prm.nblk);
+                const bool to_final = (jp.hi == prm.nblk);
                 WB(B_S_DONE, sdone & 1);
                 ++sdone;
                 ptx::tc_fence_after();
+                float* dst = to_final ? (prm.final_state
+                                             ? prm.final_state + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * kN
+                                             : nullptr)
+                                      : prm.handoff + ((static_cast<size_t>(cta) * kHG + j) * kP + p) * kN;
 #pragma unroll 1
-                for (int j = 0; j < HG; ++j) {
-                    const int h = h0 + j;
-                    float* dst = to_final
-                                     ? (prm.final_state ? prm.final_state + (static_cast<size_t>(b) * prm.H + h) * kP * kN
-                                                        : nullptr)
-                                     : prm.handoff + (static_cast<size_t>(cta) * HG + j) * kP * kN;
-                    const float inv_sigma = 1.f / (j ? sigma1 : sigma0);
-#pragma unroll 1
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t r[32];
-                        ptx::tmem_ld32(tmem + lane_base + K::COL_S + 64 * j + 32 * half, r);
-                        ptx::tmem_wait_ld(r);
-                        if (dst) {
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t r[32];
+                    ptx::tmem_ld32(tmem + lane_base + K::COL_Z + 32 * k, r);
+                    ptx::tmem_wait_ld(r);
+                    if (dst) {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) dst[(32 * half + e) * kN + n] = __uint_as_float(r[e]) * inv_sigma;
-                        }
+                        for (int e = 0; e < 8; ++e)
+                            *reinterpret_cast<float4*>(dst + 32 * k + 4 * e) =
+                                make_float4(__uint_as_float(r[4 * e]) * inv_prev, __uint_as_float(r[4 * e + 1]) * inv_prev,
+                                            __uint_as_float(r[4 * e + 2]) * inv_prev,
+                                            __uint_as_float(r[4 * e + 3]) * inv_prev);
                     }
                 }
                 ptx::tc_fence_before();
@@ -831,80 +663,302 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (wg == 4) {
+    } else {
         // ------------------------------------------------------------ epilogue
-        // y is computed row by row into the job's W buffer (each thread reads its
-        // row of W for the D term, then overwrites the same bytes with y), so
-        // the accumulator is released as soon as it has been read, and y leaves
-        // through TMA stores of whole tiles.
-        const int t = 32 * q + lane;
-        const int et = tid - 512;  // 0..127
+        // Thread (head j, p) turns its row of Y^T into y[t, p] = u_t Y_t (the D term
+        // is in Y already), 16 tokens at a time, into one of kYBufs staging tiles
+        // that leave by TMA stores.
+        const int et = tid - 384;
+        const int j = et >> 6, p = et & 63;
+        const uint32_t pbyte = (p & 7) * 2, pchunk = p >> 3;
+        const long long x_tstride = static_cast<long long>(prm.H) * kP;
+        uint32_t nbuf = 0;  // staging tiles used so far
         for (int J = 0; J < njobs; ++J) {
-            const int ts = J & (kTabSlots - 1), wb = J & 1;
-            const JobPos jp_ = job_pos(jobs, J, chains_per_b, HG, HperG);
-            const int blk = jp_.blk, lo = jp_.lo, hi = jp_.hi, b = jp_.b, h0 = jp_.h0, g = jp_.g;
-            (void)lo; (void)hi; (void)g; (void)h0; (void)b;
+            const int ts = J & (kTabSlots - 1), yb = J & 1;
+            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG);
+            const long long t0 = static_cast<long long>(jp.blk) * kT;
+            const int tn = static_cast<int>(min(static_cast<long long>(kT), prm.L - t0));  // valid tokens
             WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
-            WB(B_K3_DONE0 + wb, (J >> 1) & 1);  // k3 no longer reads this W buffer
-            WB(B_Y_FULL, J & 1);
+            const float2* ud = reinterpret_cast<const float2*>(T(ts, j, TAB_UD));
+            const uint32_t extreme = JW(ts)[1];
+            const int qs = kT / static_cast<int>(JW(ts)[0]);
+            WB(B_Y_FULL0 + yb, (J >> 1) & 1);
             ptx::tc_fence_after();
+            const uint32_t ycol = tmem + lane_base + K::COL_Y + 128 * yb;
 #pragma unroll 1
-            for (int jh = 0; jh < 2 * HG; ++jh) {  // (head, 32-column half)
-                const int j = jh >> 1, half = jh & 1;
-                // row factor e^{cs_t - c} and D x_t = e^{cs_t - c} (D / dt_t) W_t (reference mode only)
-                const bool exact = S(ts, j)[0] != 0.f;
-                const float dtt = T(ts, j, TAB_DT)[t];
-                const float u = exact ? 1.f : __expf(T(ts, j, TAB_CS)[t] - S(ts, j)[1]);
-                const float du = (exact || dtt <= 0.f) ? 0.f : u * (S(ts, j)[3] / dtt);
-                uint8_t* wrow = smem + K::OFF_W + (wb * HG + j) * kTile;
+            for (int k = 0; k < 4; ++k) {
                 uint32_t r[32];
-                ptx::tmem_ld32(tmem + lane_base + K::COL_Y + 32 * jh, r);
+                ptx::tmem_ld32(ycol + 32 * k, r);
                 ptx::tmem_wait_ld(r);
-                if (exact) {
-                    // state term of an exact-mode head: e^{cs_t} (C s_in^T)_t, from the C.B^T columns
-                    uint32_t ro[32];
-                    ptx::tmem_ld32(tmem + lane_base + K::COL_CB + 32 * jh, ro);
-                    ptx::tmem_wait_ld(ro);
-                    const float e_t = __expf(T(ts, j, TAB_CS)[t]);
+                if (k == 3 && extreme == 0u) {
+                    ptx::tc_fence_before();
+                    warp_arrive(&bars[B_Y_EMPTY0 + yb], lane);  // the accumulator has been read
+                }
+                // every factor first (two tokens per 16-byte load), then the stores: the
+                // compiler cannot move a load past a shared-memory store it may alias
+                float uv[32];
+                const float4* ud4 = reinterpret_cast<const float4*>(ud) + 16 * k;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(fmaf(e_t, __uint_as_float(ro[e]), __uint_as_float(r[e])));
+                for (int e = 0; e < 16; ++e) {
+                    const float4 q = ud4[e];
+                    uv[2 * e] = q.x;
+                    uv[2 * e + 1] = q.z;
                 }
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint4* cell = reinterpret_cast<uint4*>(wrow + ptx::swz128(t, 4 * half + c8));
-                    const uint4 wv = *cell;
-                    const float2 w0 = unpack_bf16x2(wv.x), w1 = unpack_bf16x2(wv.y), w2 = unpack_bf16x2(wv.z),
-                                 w3 = unpack_bf16x2(wv.w);
-                    const float* yv = reinterpret_cast<const float*>(r) + 8 * c8;
-                    uint4 o;
-                    o.x = pack_bf16x2(fmaf(u, yv[0], du * w0.x), fmaf(u, yv[1], du * w0.y));
-                    o.y = pack_bf16x2(fmaf(u, yv[2], du * w1.x), fmaf(u, yv[3], du * w1.y));
-                    o.z = pack_bf16x2(fmaf(u, yv[4], du * w2.x), fmaf(u, yv[5], du * w2.y));
-                    o.w = pack_bf16x2(fmaf(u, yv[6], du * w3.x), fmaf(u, yv[7], du * w3.y));
-                    *cell = o;
+                for (int h2 = 0; h2 < 2; ++h2, ++nbuf) {
+                    // 16 tokens into buffer nbuf % kYBufs; its previous store (kYBufs
+                    // chunks ago) was waited for before the last barrier
+                    uint8_t* buf = smem + K::OFF_YS + (nbuf % kYBufs) * K::YS_BUF;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        *reinterpret_cast<__nv_bfloat16*>(buf + j * K::YS_HEAD + ptx::swz128(e, pchunk) + pbyte) =
+                            __float2bfloat16_rn(uv[16 * h2 + e] * __uint_as_float(r[16 * h2 + e]));
+                    ptx::fence_proxy_async_smem();
+                    // the next buffer's store (issued kYBufs - 1 chunks ago) has read it
+                    if (et == 0) ptx::bulk_wait_group_read<kYBufs - 2>();
+                    ptx::named_sync(3, 128);
+                    if (et == 0) {
+                        for (int jj = 0; jj < kHG; ++jj)
+                            ptx::tma_store_4d(&tm_y, buf + jj * K::YS_HEAD, 0, jp.h0 + jj,
+                                              static_cast<int>(t0) + 32 * k + 16 * h2, jp.b);
+                        ptx::bulk_commit_group();
+                    }
                 }
             }
-            ptx::tc_fence_before();
-            warp_arrive(&bars[B_Y_EMPTY], lane);         // the accumulator has been read
-            if (count_exact(ts) > 0) warp_arrive(&bars[B_YO_FREE], lane);  // and Yo in the C.B^T columns
-            warp_arrive(&bars[B_TAB_EMPTY0 + ts], lane); // so have this job's tables
-            ptx::fence_proxy_async_smem();
-            ptx::named_sync(3, 128);
-            if (et == 0) {
-                for (int j = 0; j < HG; ++j)
-                    ptx::tma_store_4d(&tm_y, smem + K::OFF_W + (wb * HG + j) * kTile, 0, h0 + j, blk * kT, b);
-                ptx::bulk_commit_group();
-                ptx::bulk_wait_group_read0();            // the W buffer may be rebuilt once read
-                ptx::mbar_arrive(&bars[B_W_EMPTY0 + wb]);
+            if (extreme != 0u) {
+                // tokens of extreme sub-blocks: overwrite the stored inter-block term with the full y
+                if (et == 0) {
+                    ptx::bulk_wait_group0();
+                    ptx::fence_proxy_async_global();
+                }
+                ptx::named_sync(3, 128);
+                const long long off = ((static_cast<long long>(jp.b) * prm.L + t0) * prm.H + jp.h0 + j) * kP + p;
+                const __nv_bfloat16* lg =
+                    prm.masks + static_cast<size_t>((jp.b * prm.nblk + jp.blk) * prm.G + jp.g) * kT * kT;
+                extreme_tokens(ycol, extreme, qs, tn, ud, T(ts, j, TAB_CS), T(ts, j, TAB_DT), S(ts, j)[SC_D],
+                               prm.x + off, prm.y + off, x_tstride, lg);
+                ptx::tc_fence_before();
+                warp_arrive(&bars[B_Y_EMPTY0 + yb], lane);
             }
+            warp_arrive(&bars[B_TAB_EMPTY0 + ts], lane);
         }
-        if (et == 0) ptx::bulk_wait_group0();            // y is in global memory before the CTA exits
+        if (et == 0) ptx::bulk_wait_group0();  // y is in global memory before the CTA exits
     }
 
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     if (warp == 0) ptx::tmem_dealloc(tmem, 512);
+}
+
+struct TableParams {
+    const float* dt;
+    const float* dt_bias;
+    const float* A;
+    const float* D;
+    uint8_t* out;  // [chain * nblk + block] table records
+    long long L;
+    int H, nblk, chains_per_b;
+    float dt_min, dt_max;
+};
+
+// The table record of one job (one block of one head pair): 128 threads, thread
+// t owns token t of the block for both heads. dt = clamp(softplus(dt_raw +
+// dt_bias)), the block cumsum of dt*A, the sub-block split (the largest of 128,
+// 64, 32, 16 tokens whose decays all stay within kMaxSubDecay; 16-token
+// sub-blocks beyond it are extreme), then per token the W factor, the epilogue
+// factor u and 1 / u, the sub-block-relative cumsum and dt, and per
+// sub-block the state scales e^{c}, the H scale and 1 / sigma.
+__global__ void __launch_bounds__(128) chain_tables(const TableParams prm) {
+    __shared__ float red[kHG * 4 + kHG * 8];  // warp totals, then the cumsum at tokens 16k + 15
+    const int wt = threadIdx.x, wl = wt & 31, ww = wt >> 5;
+    const long long job = blockIdx.x;
+    const int blk = static_cast<int>(job % prm.nblk);
+    const int chain = static_cast<int>(job / prm.nblk);
+    const int b = chain / prm.chains_per_b, h0 = (chain % prm.chains_per_b) * kHG;
+    uint8_t* rec = prm.out + job * kRecBytes;
+    float* tabs = reinterpret_cast<float*>(rec);
+    float* scal = reinterpret_cast<float*>(rec + kRecTab);
+    uint32_t* jw = reinterpret_cast<uint32_t*>(rec + kRecTab + kRecScal);
+    auto T = [&](int j, int arr) { return tabs + (j * kNumTab + arr) * kT; };
+    auto S = [&](int j) { return scal + j * kScal; };
+    const long long tg = static_cast<long long>(blk) * kT + wt;
+    const float2 raw2 = tg < prm.L
+                            ? *reinterpret_cast<const float2*>(prm.dt + (static_cast<long long>(b) * prm.L + tg) * prm.H + h0)
+                            : make_float2(0.f, 0.f);
+    const float raw[kHG] = {raw2.x, raw2.y};
+    float dtv[kHG], cs[kHG];
+#pragma unroll
+    for (int j = 0; j < kHG; ++j) {
+        const int h = h0 + j;
+        dtv[j] = tg < prm.L ? fminf(fmaxf(softplus_f(raw[j] + prm.dt_bias[h]), prm.dt_min), prm.dt_max) : 0.f;
+        float v = dtv[j] * prm.A[h];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, v, off);
+            if (wl >= off) v += o;
+        }
+        cs[j] = v;
+        if (wl == 31) red[j * 4 + ww] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kHG; ++j) {
+        float pre = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < 3; ++w2)
+            if (w2 < ww) pre += red[j * 4 + w2];
+        cs[j] += pre;
+        if ((wt & 15) == 15) red[kHG * 4 + j * 8 + (wt >> 4)] = cs[j];
+    }
+    __syncthreads();
+    float bnd[kHG][8];  // cumsum at token 16k + 15
+#pragma unroll
+    for (int j = 0; j < kHG; ++j)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) bnd[j][k] = red[kHG * 4 + j * 8 + k];
+    int nq = 8;
+#pragma unroll
+    for (int cand = 1; cand < 8; cand <<= 1) {
+        const int m = 8 / cand;  // 16-token units per sub-block
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < kHG; ++j)
+#pragma unroll
+            for (int r = 0; r < cand; ++r) {
+                const float lo_ = r > 0 ? bnd[j][r * m - 1] : 0.f;
+                ok = ok && (lo_ - bnd[j][(r + 1) * m - 1] <= kMaxSubDecay);
+            }
+        if (ok && nq == 8) nq = cand;
+    }
+    uint32_t extreme = 0u;
+    if (nq == 8) {
+#pragma unroll
+        for (int j = 0; j < kHG; ++j)
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float lo_ = r > 0 ? bnd[j][r - 1] : 0.f;
+                if (lo_ - bnd[j][r] > kMaxSubDecay) extreme |= 1u << r;
+            }
+    }
+    const int qs = kT / nq, m = qs / 16;
+    const int q = wt / qs;
+    const bool ext = (extreme >> q) & 1u;
+#pragma unroll
+    for (int j = 0; j < kHG; ++j) {
+        const int h = h0 + j;
+        const float Dh = prm.D ? prm.D[h] : 0.f;
+        // cumsum relative to the sub-block start, and the sub-block's end value
+        float base = 0.f, endv = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (q > 0 && k == q * m - 1) base = bnd[j][k];
+            if (k == (q + 1) * m - 1) endv = bnd[j][k];
+        }
+        const float csl = cs[j] - base, cse = endv - base;
+        const float c = (-cse <= kMaxSubDecay) ? 0.5f * cse : cse + kExtremeRef;
+        const float d = dtv[j];
+        T(j, TAB_WF)[wt] = d * __expf(c - csl);
+        const float uft = ext ? __expf(csl) : __expf(csl - c);
+        reinterpret_cast<float2*>(T(j, TAB_UD))[wt] = make_float2(uft, ext ? 0.f : __expf(c - csl));
+        T(j, TAB_CS)[wt] = csl;
+        T(j, TAB_DT)[wt] = d;
+        if (wt < nq) {
+            // the sub-block scalars: thread wt serves sub-block wt
+            float lo_ = 0.f, hi_ = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (wt > 0 && k == wt * m - 1) lo_ = bnd[j][k];
+                if (k == (wt + 1) * m - 1) hi_ = bnd[j][k];
+            }
+            const float se = hi_ - lo_;
+            const bool sext = (extreme >> wt) & 1u;
+            const float sc_ = (-se <= kMaxSubDecay) ? 0.5f * se : se + kExtremeRef;
+            S(j)[SC_EC + wt] = __expf(sc_);
+            S(j)[SC_HS + wt] = sext ? 1.f : __expf(sc_);
+            S(j)[SC_IS + wt] = __expf(se - sc_);
+        }
+        if (wt == 0) S(j)[SC_D] = Dh;
+    }
+    if (wt == 0) {
+        jw[0] = static_cast<uint32_t>(nq);
+        jw[1] = extreme;
+        jw[2] = 0u;
+        jw[3] = 0u;
+    }
+}
+
+// L = C.B^T masked to s <= t, in bf16, for one (batch, block, group): the matrix
+// every head of the group shares (burn-mamba k2_ssd_bmm plus the causal mask).
+// One CTA of 128 threads per tile; thread t writes row t.
+constexpr uint32_t kMaskSmem = 4 * kTile + 64 + 1024;
+
+__global__ void __launch_bounds__(128)
+    chain_masks(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
+                __nv_bfloat16* __restrict__ out, int nblk, int G, uint32_t* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 4 * kTile);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + 4 * kTile + 16);
+    const int tile = blockIdx.x;
+    const int g = tile % G, blk = (tile / G) % nblk, b = tile / (G * nblk);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (tid == 0) {
+        ptx::mbar_init(&bars[0], 1);
+        ptx::mbar_init(&bars[1], 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(misc, 128);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const uint32_t sbase = ptx::smem_u32(smem);
+    if (tid == 0) {
+        ptx::mbar_arrive_expect_tx(&bars[0], 4 * kTile);
+        ptx::tma_load_4d(smem, &tm_c, &bars[0], 0, g, blk * kT, b);
+        ptx::tma_load_4d(smem + kTile, &tm_c, &bars[0], 64, g, blk * kT, b);
+        ptx::tma_load_4d(smem + 2 * kTile, &tm_b, &bars[0], 0, g, blk * kT, b);
+        ptx::tma_load_4d(smem + 3 * kTile, &tm_b, &bars[0], 64, g, blk * kT, b);
+        if (ptx::mbar_wait(&bars[0], 0, kLocalWaitNs)) {
+            ptx::tc_fence_after();
+            const uint64_t a = ptx::desc_sw128(sbase, 16, 1024), bb = ptx::desc_sw128(sbase + 2 * kTile, 16, 1024);
+            const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
+            for (int k = 0; k < 8; ++k) ptx::mma_bf16(tmem, a + kmaj(k), bb + kmaj(k), idesc, k > 0 ? 1u : 0u);
+        } else {
+            atomicOr(status, 2u);
+        }
+        ptx::mma_commit(&bars[1]);  // arrives once the MMAs (if any) complete
+    }
+    __syncwarp();
+    if (!ptx::mbar_wait(&bars[1], 0, kLocalWaitNs)) atomicOr(status, 2u);
+    ptx::tc_fence_after();
+    const int t = tid;
+    __nv_bfloat16* row = out + (static_cast<size_t>(tile) * kT + t) * kT;
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32 * k, r);
+        ptx::tmem_wait_ld(r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int s = 32 * k + 2 * e;
+            pk[e] = pack_bf16x2(s <= t ? __uint_as_float(r[2 * e]) : 0.f,
+                                s + 1 <= t ? __uint_as_float(r[2 * e + 1]) : 0.f);
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<uint4*>(row + 32 * k + 8 * v) =
+                make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 0) ptx::tmem_dealloc(tmem, 128);
 }
 
 // ---------------------------------------------------------------- host side
@@ -916,50 +970,66 @@ int sm_count() {
 }
 
 struct ChainPlan {
-    int hg;
     int ncta;
-    long long nchains, nblk, total;
+    long long nchains, nblk, total, ntiles;
 };
 
-// Heads per chain and CTA count. Two heads share B, C and C.B^T, but halve the
-// number of chains; a chain split across CTAs serialises its blocks, so the
-// choice minimises max(jobs per CTA, blocks per chain) x relative job cost.
 ChainPlan plan(const ssd_dims& d, int nsm) {
     ChainPlan p;
     p.nblk = (d.seqlen + kT - 1) / kT;
-    const bool pair_ok = (d.nheads / d.ngroups) % 2 == 0;
-    double best = 1e300;
-    p.hg = 1;
-    for (int hg = 1; hg <= (pair_ok ? 2 : 1); ++hg) {
-        const long long chains = d.batch * d.nheads / hg;
-        const long long total = chains * p.nblk;
-        const double per_cta = static_cast<double>(total) / std::min<long long>(nsm, total);
-        const double cost = std::max(per_cta, static_cast<double>(p.nblk)) * (hg == 2 ? 1.5 : 1.0);
-        if (cost < best) {
-            best = cost;
-            p.hg = hg;
-        }
-    }
-    p.nchains = d.batch * d.nheads / p.hg;
+    p.nchains = d.batch * d.nheads / kHG;
     p.total = p.nchains * p.nblk;
     p.ncta = static_cast<int>(std::min<long long>(nsm, p.total));
+    p.ntiles = d.batch * p.nblk * d.ngroups;
     return p;
 }
 
-size_t counters_bytes(int ncta) { return align_up(sizeof(uint32_t) * (1 + static_cast<size_t>(ncta)), kWorkspaceAlign); }
+size_t counters_bytes(int ncta) {
+    return align_up(sizeof(uint32_t) * (1 + static_cast<size_t>(ncta)), kWorkspaceAlign);
+}
+size_t handoff_bytes(int ncta) {
+    return align_up(static_cast<size_t>(ncta) * kHG * kP * kN * sizeof(float), kWorkspaceAlign);
+}
+size_t masks_bytes(long long ntiles) { return align_up(static_cast<size_t>(ntiles) * kT * kT * 2, kWorkspaceAlign); }
+size_t tables_bytes(long long jobs) { return align_up(static_cast<size_t>(jobs) * kRecBytes, kWorkspaceAlign); }
+size_t chain_ws_bytes(const ChainPlan& pl) {
+    return counters_bytes(pl.ncta) + handoff_bytes(pl.ncta) + masks_bytes(pl.ntiles) + tables_bytes(pl.total);
+}
 
-template <int HG>
 ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
-    using K = ChainCfg<HG>;
     const ssd_dims& d = a.d;
-    CUtensorMap tx, tb, tc, ty;
+    const size_t counters = counters_bytes(pl.ncta);
+    float* handoff = reinterpret_cast<float*>(static_cast<char*>(ws) + counters);
+    __nv_bfloat16* masks =
+        reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + counters + handoff_bytes(pl.ncta));
+    uint8_t* tables =
+        static_cast<uint8_t*>(ws) + counters + handoff_bytes(pl.ncta) + masks_bytes(pl.ntiles);
+    CUtensorMap tx, tb, tc, tl, ty;
     if (!make_map_bf16(&tx, a.x, d.headdim, d.nheads, d.seqlen, d.batch) ||
         !make_map_bf16(&tb, a.B, d.dstate, d.ngroups, d.seqlen, d.batch) ||
         !make_map_bf16(&tc, a.C, d.dstate, d.ngroups, d.seqlen, d.batch) ||
-        !make_map_bf16(&ty, a.y, d.headdim, d.nheads, d.seqlen, d.batch))
+        !make_map_bf16(&tl, masks, kT, 1, kT, static_cast<uint64_t>(pl.ntiles)) ||
+        !make_map_bf16(&ty, a.y, d.headdim, d.nheads, d.seqlen, d.batch, kYRows))
         return SSD_ERR_CUDA;
-    const size_t counters = counters_bytes(pl.ncta);
     if (cudaMemsetAsync(ws, 0, counters, a.stream) != cudaSuccess) return SSD_ERR_CUDA;
+    if (cudaFuncSetAttribute(chain_masks, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kMaskSmem)) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    chain_masks<<<static_cast<unsigned>(pl.ntiles), 128, kMaskSmem, a.stream>>>(
+        tb, tc, masks, static_cast<int>(pl.nblk), static_cast<int>(d.ngroups), a.status_word);
+    TableParams tp;
+    tp.dt = a.dt;
+    tp.dt_bias = a.dt_bias;
+    tp.A = a.A;
+    tp.D = a.D;
+    tp.out = tables;
+    tp.L = d.seqlen;
+    tp.H = static_cast<int>(d.nheads);
+    tp.nblk = static_cast<int>(pl.nblk);
+    tp.chains_per_b = static_cast<int>(d.nheads / kHG);
+    tp.dt_min = a.dt_min;
+    tp.dt_max = a.dt_max;
+    chain_tables<<<static_cast<unsigned>(pl.total), 128, 0, a.stream>>>(tp);
     ChainParams p;
     p.dt = a.dt;
     p.dt_bias = a.dt_bias;
@@ -967,10 +1037,13 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     p.D = a.D;
     p.init = a.init;
     p.final_state = a.final_state;
+    p.x = static_cast<const __nv_bfloat16*>(a.x);
     p.y = static_cast<__nv_bfloat16*>(a.y);
+    p.masks = masks;
+    p.tables = tables;
     p.ticket = static_cast<uint32_t*>(ws);
     p.flags = p.ticket + 1;
-    p.handoff = reinterpret_cast<float*>(static_cast<char*>(ws) + counters);
+    p.handoff = handoff;
     p.status = a.status_word;
     p.batch = static_cast<int>(d.batch);
     p.H = static_cast<int>(d.nheads);
@@ -983,11 +1056,11 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     p.chain_wait_ns = a.wait_limit_ns;
     p.dt_min = a.dt_min;
     p.dt_max = a.dt_max;
-    if (cudaFuncSetAttribute(ssd_chain_fused<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(K::SMEM_BYTES)) != cudaSuccess)
+    if (cudaFuncSetAttribute(ssd_chain_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Cfg::SMEM_BYTES)) != cudaSuccess)
         return SSD_ERR_CUDA;
-    ssd_chain_fused<HG><<<static_cast<unsigned>(pl.ncta), kThreads, K::SMEM_BYTES, a.stream>>>(tx, tb, tc, ty, p);
-    note_launches(1);
+    ssd_chain_fused<<<static_cast<unsigned>(pl.ncta), kThreads, Cfg::SMEM_BYTES, a.stream>>>(tx, tb, tc, tl, ty, p);
+    note_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
@@ -997,35 +1070,30 @@ bool chain_supported(const ssd_dims& d, ssd_dtype io, int chunk_len) {
     if (io != SSD_BF16) return false;
     if (d.headdim != kP || d.dstate != kN) return false;
     if (chunk_len != 128 && chunk_len != 256) return false;
+    if ((d.nheads / d.ngroups) % kHG != 0) return false;  // a chain's two heads share a B/C group
     if (d.seqlen >= (1ll << 31) || d.batch >= (1ll << 20) || d.nheads >= (1 << 20)) return false;
     const long long nblk = (d.seqlen + kT - 1) / kT;
-    if (nblk * d.batch * d.nheads >= (1ll << 31)) return false;  // job indices are 32-bit
+    if (nblk * d.batch * d.nheads >= (1ll << 31)) return false;   // job indices are 32-bit
+    if (nblk * d.batch * d.ngroups >= (1ll << 31)) return false;  // so are mask tile indices
     return true;
 }
 
 size_t chain_workspace_bytes(const ssd_dims& d) {
-    const int nsm = sm_count();
-    if (nsm <= 0) {
-        // no device to ask: size for the largest CTA count a device may have
-        const size_t cta = 1024;
-        return counters_bytes(static_cast<int>(cta)) + align_up(cta * 2 * kP * kN * sizeof(float), kWorkspaceAlign);
-    }
+    int nsm = sm_count();
+    if (nsm <= 0) nsm = 1024;  // no device to ask: size for the largest CTA count a device may have
     const ChainPlan pl = plan(d, nsm);
-    return counters_bytes(pl.ncta) +
-           align_up(static_cast<size_t>(pl.ncta) * pl.hg * kP * kN * sizeof(float), kWorkspaceAlign);
+    return chain_ws_bytes(pl);
 }
 
 ssd_status chain_forward(const FwdArgs& a, void* ws, size_t ws_bytes) {
     const int nsm = sm_count();
     if (nsm <= 0) return SSD_ERR_CUDA;
     const ChainPlan pl = plan(a.d, nsm);
-    if (ws_bytes < counters_bytes(pl.ncta) + align_up(static_cast<size_t>(pl.ncta) * pl.hg * kP * kN * sizeof(float),
-                                                      kWorkspaceAlign))
-        return SSD_ERR_WORKSPACE;
+    if (ws_bytes < chain_ws_bytes(pl)) return SSD_ERR_WORKSPACE;
     for (const void* p : {a.x, static_cast<const void*>(a.B), static_cast<const void*>(a.C),
                           static_cast<const void*>(a.y)})
         if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return SSD_ERR_UNSUPPORTED;
-    return pl.hg == 2 ? launch_chain<2>(a, ws, pl) : launch_chain<1>(a, ws, pl);
+    return launch_chain(a, ws, pl);
 }
 
 }  // namespace ssd

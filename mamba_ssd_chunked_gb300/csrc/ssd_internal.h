@@ -49,8 +49,9 @@ size_t chain_workspace_bytes(const ssd_dims& d);
 ssd_status chain_forward(const FwdArgs& a, void* ws, size_t ws_bytes);
 
 // 4-D bf16 TMA map over a row-major [outer, rows, mid, inner] tensor, box
-// {64, 1, 128, 1}, 128-byte swizzle, zero fill out of bounds.
-bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t rows, uint64_t outer);
+// {64, 1, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t rows, uint64_t outer,
+                   uint32_t box_rows = 128);
 
 // One decode step on a carried state (ssd_step), arguments already validated.
 struct StepArgs {

@@ -756,12 +756,13 @@ ssd_status launch(const FwdArgs& a, void* ws) {
 
 }  // namespace
 
-bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t rows, uint64_t outer) {
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t rows, uint64_t outer,
+                   uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {inner, mid, rows, outer};
     const cuuint64_t strides[3] = {inner * 2, mid * inner * 2, rows * mid * inner * 2};
-    const cuuint32_t box[4] = {64, 1, kT, 1};
+    const cuuint32_t box[4] = {64, 1, box_rows, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

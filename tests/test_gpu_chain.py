@@ -2,11 +2,13 @@
 fp64 oracle.
 
 The cases cover: one tile, a single token, lengths one below / above a tile,
-ragged lengths, one head per chain (odd heads per group) and head pairs;
-chains split across CTAs (a hand-off at every block, and hand-offs in the
-middle of long chains); blocks whose decay selects the exact mode, the
-reference mode, and both within one head pair; absent D / initial state /
-final state; and agreement with the per-block tensor-core path.
+ragged lengths, head pairs of one or several groups; chains split across CTAs
+(a hand-off at every block, and hand-offs in the middle of long chains);
+blocks that run whole, blocks split into 64-, 32- and 16-token sub-blocks by
+their decay, and 16-token sub-blocks whose decay is still too strong
+("extreme", finished on the CUDA cores), mixed within one head pair; absent
+D / initial state / final state; the rejection of odd heads per group; and
+agreement with the per-block tensor-core path.
 Tolerance: max|delta| / max|ref| <= 2e-2 on y and on the final state (bf16 io).
 """
 import numpy as np
@@ -31,12 +33,12 @@ def _built():
 
 CHAIN_SHAPES = [
     # b, L, h, p, g, n
-    (1, 128, 1, 64, 1, 128),      # one tile, one head
+    (1, 128, 2, 64, 1, 128),      # one tile, one head pair
     (1, 1, 2, 64, 1, 128),        # a single token
     (2, 127, 4, 64, 2, 128),      # one below a tile
     (2, 129, 4, 64, 1, 128),      # one above a tile
     (2, 300, 4, 64, 2, 128),      # ragged, several tiles
-    (1, 1000, 3, 64, 3, 128),     # one head per group: one head per chain
+    (1, 1000, 6, 64, 3, 128),     # three groups of one pair each
     (3, 513, 8, 64, 2, 128),
     (1, 2000, 2, 64, 1, 128),     # one chain spread over many CTAs: a hand-off at every block
     (2, 4100, 6, 64, 1, 128),     # long chains split across CTAs mid-chain
@@ -51,7 +53,8 @@ def test_chain_path_matches_oracle(shape, chunk_len):
 
 @pytest.mark.parametrize("dt_shift,A_scale", [(3.0, 4.0), (1.0, 2.0), (-2.0, 0.25), (0.0, 1.0)])
 def test_chain_path_strong_and_weak_decay(dt_shift, A_scale):
-    """Uniformly strong decay (every block in exact mode), moderate, weak."""
+    """Uniformly strong decay (most 16-token sub-blocks extreme), moderate
+    (blocks split into sub-blocks), weak (whole blocks)."""
     inp = make_inputs(2, 1100, 8, 64, 2, 128, io_dtype="bf16", init="normal", seed=43)
     inp["dt"] = (inp["dt"] + dt_shift).astype(np.float32)
     inp["A"] = (inp["A"] * A_scale).astype(np.float32)
@@ -63,8 +66,8 @@ def test_chain_path_strong_and_weak_decay(dt_shift, A_scale):
 
 
 def test_chain_path_mixed_modes_within_a_pair():
-    """Heads of one pair alternate between the exact and the reference mode,
-    and a head's blocks switch modes along the chain (dt bursts)."""
+    """Heads of one pair decay at very different rates, and a head's blocks
+    switch between whole, split and extreme along the chain (dt bursts)."""
     b, L, h = 2, 1500, 4
     inp = make_inputs(b, L, h, 64, 1, 128, io_dtype="bf16", init="normal", seed=47)
     inp["A"] = np.array([-0.5, -12.0, -2.0, -16.0], dtype=np.float32)
@@ -118,7 +121,7 @@ def test_chain_path_repeat_runs_are_bitwise_identical():
 
 
 def test_chain_and_per_block_paths_agree():
-    inp = make_inputs(2, 1600, 6, 64, 2, 128, io_dtype="bf16", init="normal", seed=10)
+    inp = make_inputs(2, 1600, 8, 64, 2, 128, io_dtype="bf16", init="normal", seed=10)
     t = to_device(inp, "bf16")
     y1, f1 = run_gpu(t, 256, "chain")
     y2, f2 = run_gpu(t, 256, "tc")
@@ -159,8 +162,8 @@ def test_chain_path_full_size_workloads(name):
 
 
 def test_chain_path_consecutive_strong_reference_blocks():
-    """Every block decays by about 120 nats (below the exact-mode threshold), so
-    the rescaling from one block's scaled state to the next spans e^{-120}: the
+    """Every block decays by about 120 nats (below the split threshold), so the
+    rescaling from one block's scaled state to the next spans e^{-120}: the
     scale pass must not form that factor in one fp32 number (it underflows),
     or the state term of each block's first rows is lost."""
     b, L, h = 2, 1536, 4
@@ -180,3 +183,29 @@ def test_chain_path_consecutive_strong_reference_blocks():
     first = y_ref[:, ::128]
     got = y.float().cpu().numpy()[:, ::128]
     assert rel_err(got, first) < 2e-2
+
+
+@pytest.mark.parametrize("decay", [200.0, 400.0, 800.0, 3000.0])
+def test_chain_path_each_split_level(decay):
+    """A block decay of ~200 / 400 / 800 nats selects 64- / 32- / 16-token
+    sub-blocks, ~3000 makes every 16-token sub-block extreme."""
+    b, L, h = 1, 640, 2
+    inp = make_inputs(b, L, h, 64, 1, 128, io_dtype="bf16", init="normal", seed=61)
+    inp["A"] = np.array([-1.0, -0.5], dtype=np.float32)
+    target = (decay / 128.0) / -inp["A"]
+    inp["dt_bias"] = (target + np.log(-np.expm1(-target))).astype(np.float32)
+    inp["dt"] = (0.02 * inp["dt"]).astype(np.float32)
+    t = to_device(inp, "bf16")
+    y, fs = run_gpu(t, 256, "chain")
+    y_ref, f_ref = oracle_full(inp)
+    assert rel_err(y.float().cpu().numpy(), y_ref) < 2e-2
+    assert rel_err(fs.cpu().numpy(), f_ref) < 2e-2
+
+
+def test_chain_path_rejects_odd_heads_per_group():
+    import mamba_ssd_chunked_gb300 as pkg
+    inp = make_inputs(1, 256, 3, 64, 3, 128, io_dtype="bf16", init="zero", seed=3)
+    t = to_device(inp, "bf16")
+    assert pkg.ssd_fwd_workspace_bytes(1, 256, 3, 64, 3, 128, "bf16", 256, "chain") == 0
+    with pytest.raises(pkg.SsdError):
+        run_gpu(t, 256, "chain")
