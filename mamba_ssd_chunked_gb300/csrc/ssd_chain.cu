@@ -19,10 +19,9 @@
 //   W_s  = X_s dt_s e^{c - cs_s}                  (bf16, built in place over X)
 //   Z    = e^{c} s_in                              (fp32 state in TMEM, rows (h, p), columns n)
 //   k3   Z += W^T B            ->  Z = e^{c - cs_end} s_out
-//   Y^T  = D x_t e^{c - cs_t}   (preloaded into the accumulator from the X tile)
-//   k5a  Y^T += W^T L^T        with L = C.B^T masked to s <= t (shared by the heads)
+//   k5a  Y^T  = W^T L^T        with L = C.B^T masked to s <= t (shared by the heads)
 //   k5b  Y^T += H C^T          with H = bf16(e^{c} s_in), read by the MMA from TMEM
-//   y_t  = e^{cs_t - c} Y_t
+//   y_t  = e^{cs_t - c} Y_t + (D / wf_t) W_t     (= ... + D x_t, wf_t = dt_t e^{c - cs_t})
 //
 // since e^{cs_t - cs_s} dt_s X_s = e^{cs_t - c} (e^{c - cs_s} dt_s X_s) and
 // e^{cs_t} C_t s_in = e^{cs_t - c} C_t (e^{c} s_in). Every factor stays within
@@ -31,21 +30,26 @@
 // each pass the state on like a block. A 16-token sub-block that still decays
 // faster ("extreme") keeps the state path (with its reference moved to
 // cs_end + kExtremeRef) and C s_in with reference 0, and the epilogue adds its
-// intra-block sum with per-entry decays on the CUDA cores.
+// intra-block sum with per-entry decays on the CUDA cores. Tokens whose W factor is
+// so small that x wf may underflow bf16 take D x_t from x in global memory.
 //
 // L for every (batch, block, group) is computed once by a small kernel
 // (chain_masks) into the workspace, and so is every job's table record (dt,
 // sub-block split, per-token factors; chain_tables); the chain kernel streams
-// both like inputs.
+// both like inputs. The last table CTA also splits the jobs into one contiguous
+// range per chain CTA with equal estimated cost (a job costs more the more
+// sub-blocks it has), so that CTAs holding fast-decaying heads finish with the
+// rest.
 //
 // Roles (16 warps):
 //   warp 0       TMA producer: L, B and C through a ring of four slots
 //   warp 1       MMA issuer, state path: k3
 //   warp 2       MMA issuer, output path: k5a, k5b
 //   warp 3       TMA producer: X (2 job slots of two heads) and each job's table record
-//   warps 4..7   preload Y^T with the D term from X, then W from X in place
+//   warps 4..7   W from X in place
 //   warps 8..11  state: rescale Z, write H; load / store states at segment ends
-//   warps 12..15 epilogue: y = u Y from TMEM, stored to global
+//   warps 12..15 epilogue: y from Y (TMEM) and W (shared memory), written over W
+//                and stored from there by TMA
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -65,22 +69,26 @@ constexpr uint32_t kTile = 16384;       // 128 rows x 128 bytes, 128-byte swizzl
 constexpr float kMaxSubDecay = 150.f;   // a sub-block decaying at most this keeps factors within e^{+-75}
 constexpr float kExtremeRef = 75.f;     // extreme sub-blocks: state reference cs_end + this
 constexpr unsigned long long kLocalWaitNs = 2000000000ull;
-constexpr int kTabSlots = 2;            // table ring depth (jobs)
-constexpr int kYRows = 16;              // tokens per y staging buffer
-constexpr int kYBufs = 4;               // y staging buffers
-constexpr int kNumTab = 5;              // per-token tables per (job, head), 128 floats each
-// TAB_UD holds float2 {u_t, 1 / u_t} per token (0 for extreme sub-blocks) and spans two table rows
-enum Tab { TAB_WF = 0, TAB_UD = 1, TAB_CS = 3, TAB_DT = 4 };
+constexpr int kTabSlots = 4;            // table ring depth (jobs)
+constexpr int kNumTab = 3;              // per-token tables per (job, head) staged in shared memory
+enum Tab { TAB_WF = 0, TAB_U = 1, TAB_UG = 2 };  // W factor wf, epilogue factors u and D / wf
+// Tokens with wf below this take D x from x itself: above it (D / wf) W is off from
+// D x by at most |D| 5e-4 even where x wf is a bf16 subnormal (spacing 2^-133).
+constexpr float kTinyWF = 1e-37f;
+constexpr int kNumTabX = 2;             // per-token tables per (job, head) read from global only
+enum TabX { TABX_CS = 0, TABX_DT = 1 }; // sub-block cumsum and dt (extreme sub-blocks)
 constexpr int kScal = 32;               // scalars per (job, head): ec[8], hs[8], is[8], D
 enum Scal { SC_EC = 0, SC_HS = 8, SC_IS = 16, SC_D = 24 };
 constexpr int kThreads = 512;
 constexpr int kRing = 4;                // slots of the L / B / C ring
-// Per-job table record, the same in the workspace and in a shared-memory slot:
-// [2 heads][kNumTab][128] floats, [2 heads][kScal] floats, {nq, extreme, 0, 0}.
+// Per-job table record in the workspace: [2 heads][kNumTab][128] floats,
+// [2 heads][kScal] floats, {nq, extreme, 0, 0} (the part a shared-memory slot
+// holds), then [2 heads][kNumTabX][128] floats.
 constexpr uint32_t kRecTab = kHG * kNumTab * kT * 4;
 constexpr uint32_t kRecScal = kHG * kScal * 4;
-constexpr uint32_t kRecBytes = kRecTab + kRecScal + 16;
-static_assert(kRecBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+constexpr uint32_t kRecSmem = kRecTab + kRecScal + 16;
+constexpr uint32_t kRecBytes = kRecSmem + kHG * kNumTabX * kT * 4;
+static_assert(kRecSmem % 16 == 0 && kRecBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 enum RingKind { RK_L = 0, RK_B = 1, RK_C = 2 };
 
 struct Cfg {
@@ -88,13 +96,12 @@ struct Cfg {
     // consumption order, L, B and C of each job: ring position 3J + kind
     static constexpr uint32_t OFF_RING = 0;
     static constexpr uint32_t OFF_XW = 8 * kTile;        // 2 job slots x 2 heads, X then W then y
-    static constexpr uint32_t OFF_YS = 12 * kTile;       // y staging: kYBufs buffers x 2 heads x [16 t][64 p]
-    static constexpr uint32_t YS_HEAD = kYRows * 128, YS_BUF = kHG * YS_HEAD;
-    static constexpr uint32_t OFF_TAB = OFF_YS + kYBufs * YS_BUF;  // [slots] table records
-    static constexpr uint32_t OFF_BAR = (OFF_TAB + kTabSlots * kRecBytes + 7) & ~7u;
+    static constexpr uint32_t OFF_TAB = 12 * kTile;      // [slots] table records
+    static constexpr uint32_t OFF_BAR = (OFF_TAB + kTabSlots * kRecSmem + 7) & ~7u;
     static constexpr int NBAR = 40;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+    static constexpr uint32_t OFF_SCAN = OFF_MISC + 64;  // [kThreads / 32] u64, cta_range
+    static constexpr uint32_t SMEM_BYTES = OFF_SCAN + 128 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static constexpr uint32_t COL_Z = 0;     // state, fp32, 128 columns (n)
     static constexpr uint32_t COL_H = 128;   // 2 x 64 columns, bf16 pairs
@@ -103,15 +110,18 @@ struct Cfg {
 
 enum Bar {
     B_R_FULL0 = 0, B_R_FULL1, B_R_FULL2, B_R_FULL3, B_R_EMPTY0, B_R_EMPTY1, B_R_EMPTY2, B_R_EMPTY3,
-    B_X_FULL0, B_X_FULL1, B_XW_FREE0, B_XW_FREE1,
-    B_TAB_FULL0, B_TAB_FULL1, B_TAB_EMPTY0, B_TAB_EMPTY1,
-    B_W_FULL0, B_W_FULL1, B_YI_FULL0, B_YI_FULL1,
+    B_X_FULL0, B_X_FULL1, B_XW_FREE0, B_XW_FREE1, B_XW_EMPTY0, B_XW_EMPTY1,
+    B_TAB_FULL0, B_TAB_FULL3 = B_TAB_FULL0 + 3, B_TAB_EMPTY0, B_TAB_EMPTY3 = B_TAB_EMPTY0 + 3,
+    B_W_FULL0, B_W_FULL1,
     B_SCALED, B_S_DONE, B_H_FULL0, B_H_FULL1, B_H_EMPTY0, B_H_EMPTY1,
     B_Y_FULL0, B_Y_FULL1, B_Y_EMPTY0, B_Y_EMPTY1,
     B_DRAIN_K3, B_DRAIN_Y,
     B_COUNT
 };
 static_assert(B_COUNT <= Cfg::NBAR, "barrier budget");
+static_assert(B_TAB_FULL3 - B_TAB_FULL0 + 1 == kTabSlots && B_TAB_EMPTY3 - B_TAB_EMPTY0 + 1 == kTabSlots,
+              "one full and one empty barrier per table slot");
+static_assert((kTabSlots & (kTabSlots - 1)) == 0, "table slots are indexed by J & (kTabSlots - 1)");
 
 struct ChainParams {
     const float* dt;
@@ -124,6 +134,7 @@ struct ChainParams {
     __nv_bfloat16* y;
     const __nv_bfloat16* masks;  // [b][nblk][G][t][s] bf16 L tiles (read again by the extreme path)
     const uint8_t* tables;       // [chain * nblk + block] table records
+    const uint8_t* cost;         // [jobs] estimated job costs (cta_range); null: even split by count
     float* handoff;              // [nCTA][2][P][N] fp32 states handed from CTA i to CTA i + 1
     uint32_t* ticket;            // CTA order counter
     uint32_t* flags;             // [nCTA]: 1 once CTA i's hand-off state is in place
@@ -168,10 +179,10 @@ struct JobList {
     }
 };
 
-__device__ __forceinline__ JobList make_jobs(const ChainParams& p, int cta) {
+__device__ __forceinline__ JobList make_jobs(const ChainParams& p, int first, int last) {
     JobList jl;
-    jl.first = static_cast<int>(p.total * cta / p.ncta);
-    jl.last = static_cast<int>(p.total * (cta + 1) / p.ncta);
+    jl.first = first;
+    jl.last = last;
     jl.nblk = p.nblk;
     jl.cF = jl.first / p.nblk;
     jl.cL = (jl.last - 1) / p.nblk;
@@ -240,46 +251,123 @@ __device__ __noinline__ void mma_k3(uint32_t z, uint64_t a_w, uint64_t b_b, uint
     for (int k = k0; k < k0 + nk; ++k) ptx::mma_bf16(z, a_w + mnmaj(k), b_b + mnmaj(k), idesc, 1u);
 }
 
-// k5a of one sub-block: Y^T[:, t0 : t0 + QS] += W^T L^T over s in the sub-block
-// (L rows from t0, K steps [k0, k0 + nk)).
+// k5a of one sub-block: Y^T[:, t0 : t0 + QS] = W^T L^T over s in the sub-block
+// (L rows from t0, K steps [k0, k0 + nk)); the first step overwrites the columns.
 __device__ __noinline__ void mma_k5a(uint32_t y, uint64_t a_w, uint64_t b_l, uint32_t idesc, int k0, int nk) {
 #pragma unroll 1
-    for (int k = k0; k < k0 + nk; ++k) ptx::mma_bf16(y, a_w + mnmaj(k), b_l + kmaj(k), idesc, 1u);
+    for (int k = k0; k < k0 + nk; ++k) ptx::mma_bf16(y, a_w + mnmaj(k), b_l + kmaj(k), idesc, k > k0 ? 1u : 0u);
 }
 
-// k5b of one sub-block: Y^T[:, t0 : t0 + QS] += H C^T, H from TMEM (8 columns per step).
-__device__ __noinline__ void mma_k5b(uint32_t y, uint32_t h_tmem, uint64_t b_c, uint32_t idesc) {
+// k5b of one sub-block: Y^T[:, t0 : t0 + QS] (+)= H C^T, H from TMEM (8 columns per
+// step); it overwrites the columns of extreme sub-blocks, which have no k5a.
+__device__ __noinline__ void mma_k5b(uint32_t y, uint32_t h_tmem, uint64_t b_c, uint32_t idesc, uint32_t acc) {
 #pragma unroll 1
-    for (int k = 0; k < 8; ++k) ptx::mma_bf16_ta(y, h_tmem + 8 * k, b_c + kmaj(k), idesc, 1u);
+    for (int k = 0; k < 8; ++k) ptx::mma_bf16_ta(y, h_tmem + 8 * k, b_c + kmaj(k), idesc, (acc | k) ? 1u : 0u);
 }
 
 __device__ __forceinline__ uint32_t idesc_n(int n, bool a_mn, bool b_mn) {
     return ptx::idesc_bf16_f32(128, n, a_mn, b_mn);
 }
 
-// The tokens of extreme sub-blocks for one (head, p) (rare; out of line): y_t
-// = u_t Y_t + D x_t + the intra-block sum over s in [s0, t] with per-entry
-// decays (every factor e^{cs_t - cs_s} <= 1). Y comes again from TMEM, x and L
-// from global memory, cumsum, dt and u from the job's tables.
-__device__ __noinline__ void extreme_tokens(uint32_t ycol, uint32_t extreme, int qs, int tn, const float2* ud,
-                                            const float* cs, const float* dtv, float Dh, const __nv_bfloat16* xg,
-                                            __nv_bfloat16* yg, long long x_tstride, const __nv_bfloat16* lg) {
+// The rare tokens of one (head, p), out of line, rewritten in global memory
+// after the tile store: in extreme sub-blocks y_t = u_t Y_t + D x_t + the
+// intra-block sum over s in [s0, t] with per-entry decays (every factor
+// e^{cs_t - cs_s} <= 1); elsewhere, where wf_t < kTinyWF, y_t = u_t Y_t + D x_t.
+// Y comes again from TMEM, x and L from global memory, u and wf from the job's
+// tables, cumsum and dt from its record in global memory.
+__device__ __noinline__ void fixup_tokens(uint32_t ycol, uint32_t extreme, int qs, int tn, const float* uf,
+                                          const float* wf, const float* cs, const float* dtv, float Dh,
+                                          const __nv_bfloat16* xg, __nv_bfloat16* yg, long long x_tstride,
+                                          const __nv_bfloat16* lg) {
 #pragma unroll 1
     for (int k = 0; k < 4; ++k) {
         uint32_t r[32];
         ptx::tmem_ld32(ycol + 32 * k, r);
-        ptx::tmem_wait_ld(r);
-#pragma unroll 1
+        // x of the chunk's rare tokens, all loads in flight at once
+        uint32_t pick = 0u;
+        float xv[32];
+#pragma unroll
         for (int e = 0; e < 32; ++e) {
             const int t = 32 * k + e;
-            if (t >= tn || !((extreme >> (t / qs)) & 1u)) continue;
-            float acc = fmaf(ud[t].x, __uint_as_float(r[e]), Dh * __bfloat162float(xg[t * x_tstride]));
-            for (int s = (t / qs) * qs; s <= t; ++s)
-                acc = fmaf(__bfloat162float(lg[t * kT + s]) * __expf(cs[t] - cs[s]) * dtv[s],
-                           __bfloat162float(xg[s * x_tstride]), acc);
+            const bool on = t < tn && (((extreme >> (t / qs)) & 1u) || wf[t] < kTinyWF);
+            pick |= (on ? 1u : 0u) << e;
+            xv[e] = on ? __bfloat162float(xg[t * x_tstride]) : 0.f;
+        }
+        ptx::tmem_wait_ld(r);
+        if (pick == 0u) continue;
+#pragma unroll 1
+        for (int e = 0; e < 32; ++e) {
+            if (!((pick >> e) & 1u)) continue;
+            const int t = 32 * k + e;
+            float acc = fmaf(uf[t], __uint_as_float(r[e]), Dh * xv[e]);
+            if ((extreme >> (t / qs)) & 1u)
+                for (int s = (t / qs) * qs; s <= t; ++s)
+                    acc = fmaf(__bfloat162float(lg[t * kT + s]) * __expf(cs[t] - cs[s]) * dtv[s],
+                               __bfloat162float(xg[s * x_tstride]), acc);
             yg[t * x_tstride] = __float2bfloat16_rn(acc);
         }
     }
+}
+
+// This CTA's job range [first, last) when the jobs are split by estimated cost
+// (all kThreads threads; out[0..1] and sh[0..15] in shared memory). CTA c
+// starts after the job i whose cost interval (before, after] holds
+// T_c = ceil(c total / ncta), c in [1, ncta); T_c increases with c, so every
+// such c lands on exactly one job. With at least kBalanceMin jobs per CTA,
+// T_{c+1} - T_c >= 5 kBalanceMin - 1 exceeds any one job's cost (at most 46),
+// so no range is empty. Thread t sums the costs of a contiguous run of the
+// byte array, a block scan places each thread's run on the cost line, and the
+// thread whose run holds T_cta or T_cta+1 finds the job.
+__device__ __noinline__ void cta_range(const uint8_t* cost, long long njob, long long ncta, int cta,
+                                       unsigned long long* sh, uint32_t* out) {
+    const int t = threadIdx.x, l = t & 31, wp = t >> 5;
+    const long long nw = (njob + 3) / 4;  // 4-byte words (the array is padded to them)
+    const long long k = (nw + kThreads - 1) / kThreads;
+    const long long w0 = min(nw, t * k), w1 = min(nw, w0 + k);
+    const uint32_t* cw = reinterpret_cast<const uint32_t*>(cost);
+    auto word = [&](long long i) {
+        uint32_t v = __ldg(cw + i);
+        for (int b = 0; b < 4; ++b)
+            if (4 * i + b >= njob) v &= ~(0xffu << (8 * b));
+        return v;
+    };
+    auto bsum = [](uint32_t v) { return (v & 0xffu) + ((v >> 8) & 0xffu) + ((v >> 16) & 0xffu) + (v >> 24); };
+    unsigned long long sum = 0;
+    for (long long i = w0; i < w1; ++i) sum += bsum(word(i));
+    unsigned long long x = sum;  // inclusive scan over the block
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (l >= o) x += y;
+    }
+    if (l == 31) sh[wp] = x;
+    __syncthreads();
+    unsigned long long before = x - sum, total = 0;
+    for (int i = 0; i < kThreads / 32; ++i) {
+        if (i < wp) before += sh[i];
+        total += sh[i];
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const long long c = cta + e;
+        if (c == 0 || c == ncta) continue;
+        const unsigned long long tc = (c * total + ncta - 1) / ncta;
+        if (before < tc && tc <= before + sum) {
+            unsigned long long run = before;
+            for (long long i = w0; i < w1; ++i) {
+                const uint32_t v = word(i);
+                for (int b = 0; b < 4; ++b) {
+                    run += (v >> (8 * b)) & 0xffu;
+                    if (run >= tc) {
+                        out[e] = static_cast<uint32_t>(4 * i + b + 1);
+                        i = w1;
+                        break;
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -298,13 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
 
     auto T = [&](int slot, int j, int arr) {
-        return reinterpret_cast<float*>(smem + K::OFF_TAB + slot * kRecBytes) + (j * kNumTab + arr) * kT;
+        return reinterpret_cast<float*>(smem + K::OFF_TAB + slot * kRecSmem) + (j * kNumTab + arr) * kT;
     };
     auto S = [&](int slot, int j) {
-        return reinterpret_cast<float*>(smem + K::OFF_TAB + slot * kRecBytes + kRecTab) + j * kScal;
+        return reinterpret_cast<float*>(smem + K::OFF_TAB + slot * kRecSmem + kRecTab) + j * kScal;
     };
     auto JW = [&](int slot) {
-        return reinterpret_cast<uint32_t*>(smem + K::OFF_TAB + slot * kRecBytes + kRecTab + kRecScal);
+        return reinterpret_cast<uint32_t*>(smem + K::OFF_TAB + slot * kRecSmem + kRecTab + kRecScal);
     };
 
     if (tid == 0) {
@@ -313,11 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < B_COUNT; ++i) counts[i] = 1;
         for (int i = 0; i < kTabSlots; ++i) counts[B_TAB_EMPTY0 + i] = 5;  // epilogue warps, k3 issuer
         counts[B_W_FULL0] = counts[B_W_FULL1] = 4;                          // W warps
-        counts[B_YI_FULL0] = counts[B_YI_FULL1] = 4;                        // W warps
         counts[B_SCALED] = 4;                                               // state warps
         counts[B_H_FULL0] = counts[B_H_FULL1] = 4;                          // state warps
         counts[B_Y_EMPTY0] = counts[B_Y_EMPTY1] = 4;                        // epilogue warps
         counts[B_XW_FREE0] = counts[B_XW_FREE1] = 2;                        // k3 and k5a commits
+        // B_XW_EMPTY: one epilogue thread, once the y store has read the slot
         for (int i = 0; i < B_COUNT; ++i) ptx::mbar_init(&bars[i], counts[i]);
         misc[3] = 0u;
         ptx::fence_mbar_init();
@@ -333,7 +421,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cta = static_cast<int>(misc[1]);
     volatile uint32_t* abort_flag = misc + 3;
     auto WB = [&](int bar, uint32_t parity) { wait_bar(&bars[bar], parity, prm.status, abort_flag); };
-    const JobList jobs = make_jobs(prm, cta);
+    int first = static_cast<int>(prm.total * cta / prm.ncta), last = static_cast<int>(prm.total * (cta + 1) / prm.ncta);
+    if (prm.cost) {
+        uint32_t* out = misc + 4;
+        cta_range(prm.cost, prm.total, prm.ncta, cta, reinterpret_cast<unsigned long long*>(smem + K::OFF_SCAN), out);
+        first = cta == 0 ? 0 : static_cast<int>(out[0]);
+        last = cta == prm.ncta - 1 ? static_cast<int>(prm.total) : static_cast<int>(out[1]);
+    }
+    const JobList jobs = make_jobs(prm, first, last);
     const int njobs = jobs.count();
     const int HperG = prm.H / prm.G;
     const int chains_per_b = prm.H / kHG;
@@ -411,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int qs = kT / nq, ksub = 8 / nq;
                 const uint32_t yc = tmem + K::COL_Y + 128 * yb;
                 const int pl = 3 * J + RK_L, pc = 3 * J + RK_C;
-                WB(B_YI_FULL0 + yb, (J >> 1) & 1);  // Y preloaded with D x / u
+                if (J >= 2) WB(B_Y_EMPTY0 + yb, ((J >> 1) - 1) & 1);  // the epilogue has read job J - 2
                 WB(B_W_FULL0 + xs, (J >> 1) & 1);
                 WB(B_R_FULL0 + pl % kRing, (pl / kRing) & 1);
                 ptx::tc_fence_after();
@@ -432,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     const uint64_t b_c =
                         ptx::desc_sw128(sbase + K::OFF_RING + (pc % kRing) * 2 * kTile + q * qs * 128, 16, 1024);
-                    mma_k5b(yc + q * qs, tmem + K::COL_H + 64 * hb, b_c, id_b);
+                    mma_k5b(yc + q * qs, tmem + K::COL_H + 64 * hb, b_c, id_b, (~extreme >> q) & 1u);
                     ptx::mma_commit(&bars[B_H_EMPTY0 + hb]);
                 }
                 ptx::mma_commit(&bars[B_R_EMPTY0 + pc % kRing]);
@@ -452,11 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*abort_flag) break;
                 const JobPos jp = job_pos(jobs, jx, chains_per_b, HperG);
                 const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.h0 / kHG) * prm.nblk + jp.blk;
-                ptx::mbar_arrive_expect_tx(&bars[B_TAB_FULL0 + ts], kRecBytes);
-                ptx::bulk_load(smem + K::OFF_TAB + ts * kRecBytes, prm.tables + rec * kRecBytes, kRecBytes,
+                ptx::mbar_arrive_expect_tx(&bars[B_TAB_FULL0 + ts], kRecSmem);
+                ptx::bulk_load(smem + K::OFF_TAB + ts * kRecSmem, prm.tables + rec * kRecBytes, kRecSmem,
                                &bars[B_TAB_FULL0 + ts]);
                 ++ntab;
-                if (jx >= 2) WB(B_XW_FREE0 + (jx & 1), ((jx >> 1) - 1) & 1);  // k3 and k5a of job jx - 2 are done
+                if (jx >= 2) WB(B_XW_EMPTY0 + (jx & 1), ((jx >> 1) - 1) & 1);  // y of job jx - 2 has left
                 if (*abort_flag) break;
                 uint64_t* fb = &bars[B_X_FULL0 + (jx & 1)];
                 uint8_t* dst = smem + K::OFF_XW + (jx & 1) * 2 * kTile;
@@ -478,43 +573,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < 8) {
         // ------------------------------------------------------------ W from X, in place
-        const int wt = tid - 128;  // 0..127; also TMEM lane (head j, p) for the preload
-        const int jl = wt >> 6, pl = wt & 63;
+        const int wt = tid - 128;  // 0..127
         for (int J = 0; J < njobs; ++J) {
-            const int ts = J & (kTabSlots - 1), xs = J & 1, yb = J & 1;
+            const int ts = J & (kTabSlots - 1), xs = J & 1;
             WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
             WB(B_X_FULL0 + xs, (J >> 1) & 1);
-            // Y^T[(j, p), t] = D_j x_t[p] / u_t, the D term in the accumulator's own scale
-            // (zero for extreme sub-blocks, whose epilogue adds D x itself)
-            if (J >= 2) WB(B_Y_EMPTY0 + yb, ((J >> 1) - 1) & 1);
-            {
-                const uint8_t* tile = smem + K::OFF_XW + (xs * kHG + jl) * kTile;
-                const float2* ud = reinterpret_cast<const float2*>(T(ts, jl, TAB_UD));
-                const float Dh = S(ts, jl)[SC_D];
-                const uint32_t pbyte = (pl & 7) * 2, pchunk = pl >> 3;
-                const uint32_t ycol = tmem + lane_base + K::COL_Y + 128 * yb;
-#pragma unroll 1
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t r[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int t = 32 * k + e;
-                        const float xv =
-                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + ptx::swz128(t, pchunk) + pbyte));
-                        r[e] = __float_as_uint(Dh * xv * ud[t].y);
-                    }
-                    ptx::tmem_st32(ycol + 32 * k, r);
-                }
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                ptx::named_sync(1, 128);  // every thread has read its X column before W overwrites it
-                warp_arrive(&bars[B_YI_FULL0 + yb], lane);
-            }
 #pragma unroll 1
             for (int j = 0; j < kHG; ++j) {
                 const float* wf = T(ts, j, TAB_WF);
                 uint8_t* tile = smem + K::OFF_XW + (xs * kHG + j) * kTile;
-                // all loads first, then the stores (see the epilogue)
+                // all loads first, then the stores: the compiler cannot move a load past
+                // a shared-memory store it may alias
                 uint4 v[8];
                 float w[8];
 #pragma unroll
@@ -665,78 +734,98 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // Thread (head j, p) turns its row of Y^T into y[t, p] = u_t Y_t (the D term
-        // is in Y already), 16 tokens at a time, into one of kYBufs staging tiles
-        // that leave by TMA stores.
+        // Warp q4 owns TMEM lanes 32 q4 .. 32 q4 + 31: head j = q4 / 2, p in
+        // [32 (q4 % 2), +32), taken as two halves of 16 lanes. Y is read in the
+        // 16x256b fragment layout (a thread holds token pairs of two p), W in the
+        // same layout by ldmatrix.trans from the job's W tile, and
+        // y = u Y + (D / wf) W goes back over W by stmatrix.trans; the two tiles
+        // then leave by TMA stores and the slot is handed back to the X producer.
         const int et = tid - 384;
-        const int j = et >> 6, p = et & 63;
-        const uint32_t pbyte = (p & 7) * 2, pchunk = p >> 3;
+        const int j = q4 >> 1;
+        const int lq = lane & 3;  // token pair of the thread within an 8-token group
+        // ldmatrix / stmatrix row addresses: lane l serves row l % 8 of matrix l / 8
+        // (matrix m: tokens + 8 (m >> 1), p chunk + (m & 1))
+        const int mrow = lane & 7, mm = lane >> 3;
         const long long x_tstride = static_cast<long long>(prm.H) * kP;
-        uint32_t nbuf = 0;  // staging tiles used so far
         for (int J = 0; J < njobs; ++J) {
-            const int ts = J & (kTabSlots - 1), yb = J & 1;
-            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG);
-            const long long t0 = static_cast<long long>(jp.blk) * kT;
-            const int tn = static_cast<int>(min(static_cast<long long>(kT), prm.L - t0));  // valid tokens
+            const int ts = J & (kTabSlots - 1), yb = J & 1, xs = J & 1;
             WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
-            const float2* ud = reinterpret_cast<const float2*>(T(ts, j, TAB_UD));
+            const float2* u2 = reinterpret_cast<const float2*>(T(ts, j, TAB_U));
+            const float2* g2 = reinterpret_cast<const float2*>(T(ts, j, TAB_UG));
             const uint32_t extreme = JW(ts)[1];
-            const int qs = kT / static_cast<int>(JW(ts)[0]);
+            const bool rare = (extreme | JW(ts)[2]) != 0u;
             WB(B_Y_FULL0 + yb, (J >> 1) & 1);
+            WB(B_XW_FREE0 + xs, (J >> 1) & 1);  // k3 and k5a no longer read W
             ptx::tc_fence_after();
-            const uint32_t ycol = tmem + lane_base + K::COL_Y + 128 * yb;
+            const uint32_t tile = sbase + K::OFF_XW + (xs * kHG + j) * kTile;
 #pragma unroll 1
-            for (int k = 0; k < 4; ++k) {
-                uint32_t r[32];
-                ptx::tmem_ld32(ycol + 32 * k, r);
-                ptx::tmem_wait_ld(r);
-                if (k == 3 && extreme == 0u) {
-                    ptx::tc_fence_before();
-                    warp_arrive(&bars[B_Y_EMPTY0 + yb], lane);  // the accumulator has been read
-                }
-                // every factor first (two tokens per 16-byte load), then the stores: the
-                // compiler cannot move a load past a shared-memory store it may alias
-                float uv[32];
-                const float4* ud4 = reinterpret_cast<const float4*>(ud) + 16 * k;
+            for (int hf = 0; hf < 2; ++hf) {
+                const uint32_t ylane = tmem + (static_cast<uint32_t>(32 * q4 + 16 * hf) << 16) + K::COL_Y + 128 * yb;
+                const uint32_t pc = 4 * (q4 & 1) + 2 * hf + (mm & 1);  // 16-byte chunk of p in the row
+#pragma unroll 1
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t r[16];
+                    ptx::tmem_ld16x256_x4(ylane + 32 * k, r);
+                    ptx::tmem_wait_ld(r);
+                    if (hf == 1 && k == 3 && !rare) {
+                        ptx::tc_fence_before();
+                        warp_arrive(&bars[B_Y_EMPTY0 + yb], lane);  // the accumulator has been read
+                    }
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float4 q = ud4[e];
-                    uv[2 * e] = q.x;
-                    uv[2 * e + 1] = q.z;
-                }
+                    for (int c = 0; c < 2; ++c) {  // 16 tokens: groups g = 2c, 2c + 1
+                        const int tb = 32 * k + 16 * c;
+                        const int trow = tb + 8 * (mm >> 1) + mrow;
+                        const uint32_t addr = tile + trow * 128 + ((pc ^ (trow & 7)) << 4);
+                        uint32_t w[4];
+                        ptx::ldmatrix_x4_trans(addr, w);
+                        uint32_t o[4];
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2, ++nbuf) {
-                    // 16 tokens into buffer nbuf % kYBufs; its previous store (kYBufs
-                    // chunks ago) was waited for before the last barrier
-                    uint8_t* buf = smem + K::OFF_YS + (nbuf % kYBufs) * K::YS_BUF;
+                        for (int gg = 0; gg < 2; ++gg) {
+                            const int g = 2 * c + gg;
+                            const int tp = (tb + 8 * gg) / 2 + lq;  // token pair (t, t + 1) / 2
+                            const float2 u = u2[tp], gw = g2[tp];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        *reinterpret_cast<__nv_bfloat16*>(buf + j * K::YS_HEAD + ptx::swz128(e, pchunk) + pbyte) =
-                            __float2bfloat16_rn(uv[16 * h2 + e] * __uint_as_float(r[16 * h2 + e]));
-                    ptx::fence_proxy_async_smem();
-                    // the next buffer's store (issued kYBufs - 1 chunks ago) has read it
-                    if (et == 0) ptx::bulk_wait_group_read<kYBufs - 2>();
-                    ptx::named_sync(3, 128);
-                    if (et == 0) {
-                        for (int jj = 0; jj < kHG; ++jj)
-                            ptx::tma_store_4d(&tm_y, buf + jj * K::YS_HEAD, 0, jp.h0 + jj,
-                                              static_cast<int>(t0) + 32 * k + 16 * h2, jp.b);
-                        ptx::bulk_commit_group();
+                            for (int hp = 0; hp < 2; ++hp) {  // p = lr, p = 8 + lr
+                                const float2 wv = unpack_bf16x2(w[2 * gg + hp]);
+                                o[2 * gg + hp] = pack_bf16x2(fmaf(u.x, __uint_as_float(r[4 * g + 2 * hp]), gw.x * wv.x),
+                                                             fmaf(u.y, __uint_as_float(r[4 * g + 2 * hp + 1]), gw.y * wv.y));
+                            }
+                        }
+                        ptx::stmatrix_x4_trans(addr, o);
                     }
                 }
             }
-            if (extreme != 0u) {
-                // tokens of extreme sub-blocks: overwrite the stored inter-block term with the full y
+            ptx::fence_proxy_async_smem();
+            ptx::named_sync(3, 128);
+            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG);
+            if (et == 0) {
+                for (int jj = 0; jj < kHG; ++jj)
+                    ptx::tma_store_4d(&tm_y, smem + K::OFF_XW + (xs * kHG + jj) * kTile, 0, jp.h0 + jj,
+                                      jp.blk * kT, jp.b);
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group_read0();
+                ptx::mbar_arrive(&bars[B_XW_EMPTY0 + xs]);  // the slot may take the next X
+            }
+            if (rare) {
+                // extreme sub-blocks and tokens with a tiny W factor: rewrite them in
+                // global memory once the tile store has landed
                 if (et == 0) {
                     ptx::bulk_wait_group0();
                     ptx::fence_proxy_async_global();
                 }
                 ptx::named_sync(3, 128);
+                const int p = et & 63;
+                const long long t0 = static_cast<long long>(jp.blk) * kT;
+                const int tn = static_cast<int>(min(static_cast<long long>(kT), prm.L - t0));  // valid tokens
                 const long long off = ((static_cast<long long>(jp.b) * prm.L + t0) * prm.H + jp.h0 + j) * kP + p;
+                const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.h0 / kHG) * prm.nblk + jp.blk;
+                const float* xt = reinterpret_cast<const float*>(prm.tables + rec * kRecBytes + kRecSmem) +
+                                  j * kNumTabX * kT;
                 const __nv_bfloat16* lg =
                     prm.masks + static_cast<size_t>((jp.b * prm.nblk + jp.blk) * prm.G + jp.g) * kT * kT;
-                extreme_tokens(ycol, extreme, qs, tn, ud, T(ts, j, TAB_CS), T(ts, j, TAB_DT), S(ts, j)[SC_D],
-                               prm.x + off, prm.y + off, x_tstride, lg);
+                fixup_tokens(tmem + lane_base + K::COL_Y + 128 * yb, extreme, kT / static_cast<int>(JW(ts)[0]), tn,
+                             T(ts, j, TAB_U), T(ts, j, TAB_WF), xt + TABX_CS * kT, xt + TABX_DT * kT, S(ts, j)[SC_D],
+                             prm.x + off, prm.y + off, x_tstride, lg);
                 ptx::tc_fence_before();
                 warp_arrive(&bars[B_Y_EMPTY0 + yb], lane);
             }
@@ -756,135 +845,163 @@ struct TableParams {
     const float* dt_bias;
     const float* A;
     const float* D;
-    uint8_t* out;  // [chain * nblk + block] table records
+    uint8_t* out;      // [chain * nblk + block] table records
+    uint8_t* cost;     // [jobs, padded to kSplitRound] estimated job costs
     long long L;
-    int H, nblk, chains_per_b;
+    int H, nblk, chains_per_b, total;
     float dt_min, dt_max;
 };
 
-// The table record of one job (one block of one head pair): 128 threads, thread
-// t owns token t of the block for both heads. dt = clamp(softplus(dt_raw +
-// dt_bias)), the block cumsum of dt*A, the sub-block split (the largest of 128,
-// 64, 32, 16 tokens whose decays all stay within kMaxSubDecay; 16-token
-// sub-blocks beyond it are extreme), then per token the W factor, the epilogue
-// factor u and 1 / u, the sub-block-relative cumsum and dt, and per
-// sub-block the state scales e^{c}, the H scale and 1 / sigma.
+// Estimated cost of a job in the chain kernel: every sub-block beyond the first
+// adds a pass of the state path, an extreme one the CUDA-core intra-block sum,
+// tokens with a tiny W factor a fix-up pass. At most 5 + 7 + 32 + 2.
+__device__ __forceinline__ uint32_t job_cost(int nq, uint32_t extreme, int tiny) {
+    return 5u + static_cast<uint32_t>(nq - 1) + 4u * static_cast<uint32_t>(__popc(extreme)) + (tiny ? 2u : 0u);
+}
+
+constexpr int kBalanceMin = 20;  // cost balancing from this many jobs per chain CTA up (see cta_range)
+
+// The table record of one job (one block of one head pair), one warp per job:
+// lane l owns tokens 4l .. 4l + 3 of the block for both heads. dt =
+// clamp(softplus(dt_raw + dt_bias)), the block cumsum of dt*A, the sub-block
+// split (the largest of 128, 64, 32, 16 tokens whose decays all stay within
+// kMaxSubDecay; 16-token sub-blocks beyond it are extreme), then per token the
+// W factor, the epilogue factors u and D / wf, the sub-block-relative cumsum
+// and dt, and per sub-block the state scales e^{c}, the H scale and 1 / sigma.
 __global__ void __launch_bounds__(128) chain_tables(const TableParams prm) {
-    __shared__ float red[kHG * 4 + kHG * 8];  // warp totals, then the cumsum at tokens 16k + 15
-    const int wt = threadIdx.x, wl = wt & 31, ww = wt >> 5;
-    const long long job = blockIdx.x;
-    const int blk = static_cast<int>(job % prm.nblk);
-    const int chain = static_cast<int>(job / prm.nblk);
-    const int b = chain / prm.chains_per_b, h0 = (chain % prm.chains_per_b) * kHG;
-    uint8_t* rec = prm.out + job * kRecBytes;
-    float* tabs = reinterpret_cast<float*>(rec);
-    float* scal = reinterpret_cast<float*>(rec + kRecTab);
-    uint32_t* jw = reinterpret_cast<uint32_t*>(rec + kRecTab + kRecScal);
-    auto T = [&](int j, int arr) { return tabs + (j * kNumTab + arr) * kT; };
-    auto S = [&](int j) { return scal + j * kScal; };
-    const long long tg = static_cast<long long>(blk) * kT + wt;
-    const float2 raw2 = tg < prm.L
-                            ? *reinterpret_cast<const float2*>(prm.dt + (static_cast<long long>(b) * prm.L + tg) * prm.H + h0)
-                            : make_float2(0.f, 0.f);
-    const float raw[kHG] = {raw2.x, raw2.y};
-    float dtv[kHG], cs[kHG];
+    const int wl = threadIdx.x & 31;
+    const long long job = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);  // one warp per job
+    if (job < prm.total) {
+        const int blk = static_cast<int>(job % prm.nblk);
+        const int chain = static_cast<int>(job / prm.nblk);
+        const int b = chain / prm.chains_per_b, h0 = (chain % prm.chains_per_b) * kHG;
+        uint8_t* rec = prm.out + job * kRecBytes;
+        float* tabs = reinterpret_cast<float*>(rec);
+        float* scal = reinterpret_cast<float*>(rec + kRecTab);
+        uint32_t* jw = reinterpret_cast<uint32_t*>(rec + kRecTab + kRecScal);
+        float* tabx = reinterpret_cast<float*>(rec + kRecSmem);
+        auto T = [&](int j, int arr) { return reinterpret_cast<float4*>(tabs + (j * kNumTab + arr) * kT) + wl; };
+        auto TX = [&](int j, int arr) { return reinterpret_cast<float4*>(tabx + (j * kNumTabX + arr) * kT) + wl; };
+        auto S = [&](int j) { return scal + j * kScal; };
+        // lane wl owns tokens 4 wl .. 4 wl + 3 of the block (one 16-token unit)
+        const long long tg0 = static_cast<long long>(blk) * kT + 4 * wl;
+        float dtv[kHG][4], cs[kHG][4];
 #pragma unroll
-    for (int j = 0; j < kHG; ++j) {
-        const int h = h0 + j;
-        dtv[j] = tg < prm.L ? fminf(fmaxf(softplus_f(raw[j] + prm.dt_bias[h]), prm.dt_min), prm.dt_max) : 0.f;
-        float v = dtv[j] * prm.A[h];
+        for (int i = 0; i < 4; ++i) {
+            const long long tg = tg0 + i;
+            const float2 raw = tg < prm.L ? *reinterpret_cast<const float2*>(
+                                                prm.dt + (static_cast<long long>(b) * prm.L + tg) * prm.H + h0)
+                                          : make_float2(0.f, 0.f);
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(0xffffffffu, v, off);
-            if (wl >= off) v += o;
+            for (int j = 0; j < kHG; ++j)
+                dtv[j][i] = tg < prm.L ? fminf(fmaxf(softplus_f((j ? raw.y : raw.x) + prm.dt_bias[h0 + j]), prm.dt_min),
+                                               prm.dt_max)
+                                       : 0.f;
         }
-        cs[j] = v;
-        if (wl == 31) red[j * 4 + ww] = v;
-    }
-    __syncthreads();
+        float bnd[kHG][8];  // cumsum at token 16k + 15
 #pragma unroll
-    for (int j = 0; j < kHG; ++j) {
-        float pre = 0.f;
+        for (int j = 0; j < kHG; ++j) {
+            const float a = prm.A[h0 + j];
+            float run = 0.f;
 #pragma unroll
-        for (int w2 = 0; w2 < 3; ++w2)
-            if (w2 < ww) pre += red[j * 4 + w2];
-        cs[j] += pre;
-        if ((wt & 15) == 15) red[kHG * 4 + j * 8 + (wt >> 4)] = cs[j];
-    }
-    __syncthreads();
-    float bnd[kHG][8];  // cumsum at token 16k + 15
-#pragma unroll
-    for (int j = 0; j < kHG; ++j)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) bnd[j][k] = red[kHG * 4 + j * 8 + k];
-    int nq = 8;
-#pragma unroll
-    for (int cand = 1; cand < 8; cand <<= 1) {
-        const int m = 8 / cand;  // 16-token units per sub-block
-        bool ok = true;
-#pragma unroll
-        for (int j = 0; j < kHG; ++j)
-#pragma unroll
-            for (int r = 0; r < cand; ++r) {
-                const float lo_ = r > 0 ? bnd[j][r * m - 1] : 0.f;
-                ok = ok && (lo_ - bnd[j][(r + 1) * m - 1] <= kMaxSubDecay);
+            for (int i = 0; i < 4; ++i) {
+                run += dtv[j][i] * a;
+                cs[j][i] = run;
             }
-        if (ok && nq == 8) nq = cand;
-    }
-    uint32_t extreme = 0u;
-    if (nq == 8) {
+            float v = run;  // inclusive scan of the lane totals
 #pragma unroll
-        for (int j = 0; j < kHG; ++j)
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const float lo_ = r > 0 ? bnd[j][r - 1] : 0.f;
-                if (lo_ - bnd[j][r] > kMaxSubDecay) extreme |= 1u << r;
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, v, off);
+                if (wl >= off) v += o;
             }
-    }
-    const int qs = kT / nq, m = qs / 16;
-    const int q = wt / qs;
-    const bool ext = (extreme >> q) & 1u;
+            const float pre = v - run;
 #pragma unroll
-    for (int j = 0; j < kHG; ++j) {
-        const int h = h0 + j;
-        const float Dh = prm.D ? prm.D[h] : 0.f;
-        // cumsum relative to the sub-block start, and the sub-block's end value
-        float base = 0.f, endv = 0.f;
+            for (int i = 0; i < 4; ++i) cs[j][i] += pre;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if (q > 0 && k == q * m - 1) base = bnd[j][k];
-            if (k == (q + 1) * m - 1) endv = bnd[j][k];
+            for (int k = 0; k < 8; ++k) bnd[j][k] = __shfl_sync(0xffffffffu, v, 4 * k + 3);
         }
-        const float csl = cs[j] - base, cse = endv - base;
-        const float c = (-cse <= kMaxSubDecay) ? 0.5f * cse : cse + kExtremeRef;
-        const float d = dtv[j];
-        T(j, TAB_WF)[wt] = d * __expf(c - csl);
-        const float uft = ext ? __expf(csl) : __expf(csl - c);
-        reinterpret_cast<float2*>(T(j, TAB_UD))[wt] = make_float2(uft, ext ? 0.f : __expf(c - csl));
-        T(j, TAB_CS)[wt] = csl;
-        T(j, TAB_DT)[wt] = d;
-        if (wt < nq) {
-            // the sub-block scalars: thread wt serves sub-block wt
-            float lo_ = 0.f, hi_ = 0.f;
+        int nq = 8;
+#pragma unroll
+        for (int cand = 1; cand < 8; cand <<= 1) {
+            const int m = 8 / cand;  // 16-token units per sub-block
+            bool ok = true;
+#pragma unroll
+            for (int j = 0; j < kHG; ++j)
+#pragma unroll
+                for (int r = 0; r < cand; ++r) {
+                    const float lo_ = r > 0 ? bnd[j][r * m - 1] : 0.f;
+                    ok = ok && (lo_ - bnd[j][(r + 1) * m - 1] <= kMaxSubDecay);
+                }
+            if (ok && nq == 8) nq = cand;
+        }
+        uint32_t extreme = 0u;
+        if (nq == 8) {
+#pragma unroll
+            for (int j = 0; j < kHG; ++j)
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const float lo_ = r > 0 ? bnd[j][r - 1] : 0.f;
+                    if (lo_ - bnd[j][r] > kMaxSubDecay) extreme |= 1u << r;
+                }
+        }
+        const int qs = kT / nq, m = qs / 16;
+        const int q = 4 * wl / qs;  // the lane's sub-block
+        const bool ext = (extreme >> q) & 1u;
+        bool any_tiny = false;
+#pragma unroll
+        for (int j = 0; j < kHG; ++j) {
+            const float Dh = prm.D ? prm.D[h0 + j] : 0.f;
+            // cumsum relative to the sub-block start, and the sub-block's end value
+            float base = 0.f, endv = 0.f;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                if (wt > 0 && k == wt * m - 1) lo_ = bnd[j][k];
-                if (k == (wt + 1) * m - 1) hi_ = bnd[j][k];
+                if (q > 0 && k == q * m - 1) base = bnd[j][k];
+                if (k == (q + 1) * m - 1) endv = bnd[j][k];
             }
-            const float se = hi_ - lo_;
-            const bool sext = (extreme >> wt) & 1u;
-            const float sc_ = (-se <= kMaxSubDecay) ? 0.5f * se : se + kExtremeRef;
-            S(j)[SC_EC + wt] = __expf(sc_);
-            S(j)[SC_HS + wt] = sext ? 1.f : __expf(sc_);
-            S(j)[SC_IS + wt] = __expf(se - sc_);
+            const float cse = endv - base;
+            const float c = (-cse <= kMaxSubDecay) ? 0.5f * cse : cse + kExtremeRef;
+            float wf4[4], u4[4], g4[4], c4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float csl = cs[j][i] - base;
+                const float wfv = dtv[j][i] * __expf(c - csl);
+                const bool tiny = !ext && wfv < kTinyWF;  // D x from x itself (fixup_tokens)
+                any_tiny |= tiny && (tg0 + i < prm.L);
+                wf4[i] = wfv;
+                u4[i] = ext ? __expf(csl) : __expf(csl - c);
+                g4[i] = (ext || tiny) ? 0.f : Dh / wfv;
+                c4[i] = csl;
+            }
+            *T(j, TAB_WF) = make_float4(wf4[0], wf4[1], wf4[2], wf4[3]);
+            *T(j, TAB_U) = make_float4(u4[0], u4[1], u4[2], u4[3]);
+            *T(j, TAB_UG) = make_float4(g4[0], g4[1], g4[2], g4[3]);
+            *TX(j, TABX_CS) = make_float4(c4[0], c4[1], c4[2], c4[3]);
+            *TX(j, TABX_DT) = make_float4(dtv[j][0], dtv[j][1], dtv[j][2], dtv[j][3]);
+            if (wl < nq) {
+                // the sub-block scalars: lane wl serves sub-block wl
+                float lo_ = 0.f, hi_ = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (wl > 0 && k == wl * m - 1) lo_ = bnd[j][k];
+                    if (k == (wl + 1) * m - 1) hi_ = bnd[j][k];
+                }
+                const float se = hi_ - lo_;
+                const bool sext = (extreme >> wl) & 1u;
+                const float sc_ = (-se <= kMaxSubDecay) ? 0.5f * se : se + kExtremeRef;
+                S(j)[SC_EC + wl] = __expf(sc_);
+                S(j)[SC_HS + wl] = sext ? 1.f : __expf(sc_);
+                S(j)[SC_IS + wl] = __expf(se - sc_);
+            }
+            if (wl == 0) S(j)[SC_D] = Dh;
         }
-        if (wt == 0) S(j)[SC_D] = Dh;
-    }
-    if (wt == 0) {
-        jw[0] = static_cast<uint32_t>(nq);
-        jw[1] = extreme;
-        jw[2] = 0u;
-        jw[3] = 0u;
+        any_tiny = __any_sync(0xffffffffu, any_tiny);
+        if (wl == 0) {
+            jw[0] = static_cast<uint32_t>(nq);
+            jw[1] = extreme;
+            jw[2] = any_tiny ? 1u : 0u;  // some valid token has wf < kTinyWF
+            jw[3] = 0u;
+            prm.cost[job] = static_cast<uint8_t>(job_cost(nq, extreme, any_tiny));
+        }
     }
 }
 
@@ -984,6 +1101,7 @@ ChainPlan plan(const ssd_dims& d, int nsm) {
     return p;
 }
 
+// ticket, flags [ncta]
 size_t counters_bytes(int ncta) {
     return align_up(sizeof(uint32_t) * (1 + static_cast<size_t>(ncta)), kWorkspaceAlign);
 }
@@ -992,8 +1110,10 @@ size_t handoff_bytes(int ncta) {
 }
 size_t masks_bytes(long long ntiles) { return align_up(static_cast<size_t>(ntiles) * kT * kT * 2, kWorkspaceAlign); }
 size_t tables_bytes(long long jobs) { return align_up(static_cast<size_t>(jobs) * kRecBytes, kWorkspaceAlign); }
+size_t costs_bytes(long long jobs) { return align_up(static_cast<size_t>(jobs), kWorkspaceAlign); }
 size_t chain_ws_bytes(const ChainPlan& pl) {
-    return counters_bytes(pl.ncta) + handoff_bytes(pl.ncta) + masks_bytes(pl.ntiles) + tables_bytes(pl.total);
+    return counters_bytes(pl.ncta) + handoff_bytes(pl.ncta) + masks_bytes(pl.ntiles) + tables_bytes(pl.total) +
+           costs_bytes(pl.total);
 }
 
 ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
@@ -1004,32 +1124,38 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
         reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + counters + handoff_bytes(pl.ncta));
     uint8_t* tables =
         static_cast<uint8_t*>(ws) + counters + handoff_bytes(pl.ncta) + masks_bytes(pl.ntiles);
+    uint8_t* costs = tables + tables_bytes(pl.total);
     CUtensorMap tx, tb, tc, tl, ty;
     if (!make_map_bf16(&tx, a.x, d.headdim, d.nheads, d.seqlen, d.batch) ||
         !make_map_bf16(&tb, a.B, d.dstate, d.ngroups, d.seqlen, d.batch) ||
         !make_map_bf16(&tc, a.C, d.dstate, d.ngroups, d.seqlen, d.batch) ||
         !make_map_bf16(&tl, masks, kT, 1, kT, static_cast<uint64_t>(pl.ntiles)) ||
-        !make_map_bf16(&ty, a.y, d.headdim, d.nheads, d.seqlen, d.batch, kYRows))
+        !make_map_bf16(&ty, a.y, d.headdim, d.nheads, d.seqlen, d.batch))
         return SSD_ERR_CUDA;
     if (cudaMemsetAsync(ws, 0, counters, a.stream) != cudaSuccess) return SSD_ERR_CUDA;
     if (cudaFuncSetAttribute(chain_masks, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kMaskSmem)) != cudaSuccess)
         return SSD_ERR_CUDA;
-    chain_masks<<<static_cast<unsigned>(pl.ntiles), 128, kMaskSmem, a.stream>>>(
-        tb, tc, masks, static_cast<int>(pl.nblk), static_cast<int>(d.ngroups), a.status_word);
     TableParams tp;
     tp.dt = a.dt;
     tp.dt_bias = a.dt_bias;
     tp.A = a.A;
     tp.D = a.D;
     tp.out = tables;
+    tp.cost = costs;
     tp.L = d.seqlen;
     tp.H = static_cast<int>(d.nheads);
     tp.nblk = static_cast<int>(pl.nblk);
     tp.chains_per_b = static_cast<int>(d.nheads / kHG);
     tp.dt_min = a.dt_min;
     tp.dt_max = a.dt_max;
-    chain_tables<<<static_cast<unsigned>(pl.total), 128, 0, a.stream>>>(tp);
+    tp.total = static_cast<int>(pl.total);
+    chain_tables<<<static_cast<unsigned>((pl.total + 3) / 4), 128, 0, a.stream>>>(tp);
+    chain_masks<<<static_cast<unsigned>(pl.ntiles), 128, kMaskSmem, a.stream>>>(
+        tb, tc, masks, static_cast<int>(pl.nblk), static_cast<int>(d.ngroups), a.status_word);
+    uint32_t* ctr = static_cast<uint32_t*>(ws);  // ticket, flags [ncta]
+    // with fewer than kBalanceMin jobs per CTA the jobs are split evenly by count
+    const bool balance = pl.total >= static_cast<long long>(kBalanceMin) * pl.ncta;
     ChainParams p;
     p.dt = a.dt;
     p.dt_bias = a.dt_bias;
@@ -1041,8 +1167,9 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     p.y = static_cast<__nv_bfloat16*>(a.y);
     p.masks = masks;
     p.tables = tables;
-    p.ticket = static_cast<uint32_t*>(ws);
-    p.flags = p.ticket + 1;
+    p.ticket = ctr;
+    p.flags = ctr + 1;
+    p.cost = balance ? costs : nullptr;
     p.handoff = handoff;
     p.status = a.status_word;
     p.batch = static_cast<int>(d.batch);

@@ -65,6 +65,27 @@ def test_chain_path_strong_and_weak_decay(dt_shift, A_scale):
     assert rel_err(fs.cpu().numpy(), f_ref) < 2e-2
 
 
+def test_chain_path_vanishing_dt():
+    """Heads whose dt underflows (dt_bias -100, mixed with ordinary heads inside
+    head pairs): their W factor falls below the bf16 range, so D x comes from x
+    itself; with dt = 0 the state stays the initial one and y = C s_in + D x."""
+    import oracle
+    inp = make_inputs(2, 700, 8, 64, 2, 128, io_dtype="bf16", init="normal", seed=23)
+    inp["dt_bias"] = inp["dt_bias"].copy()
+    inp["dt_bias"][[1, 4, 6]] = -100.0
+    t = to_device(inp, "bf16")
+    y, fs = run_gpu(t, 256, "chain")
+    y_ref, f_ref = oracle_full(inp)
+    yg = y.float().cpu().numpy()
+    for sel in ([1, 4, 6], [0, 2, 3, 5, 7]):
+        assert rel_err(yg[:, :, sel], y_ref[:, :, sel]) < TOL["bf16"], sel
+    assert rel_err(fs.cpu().numpy(), f_ref) < TOL["bf16"]
+    # the D term is a large part of y on those heads: dropping it would fail
+    y_nod, _ = oracle.recurrence(inp["x"], inp["dt"], inp["dt_bias"], inp["A"], inp["B"], inp["C"],
+                                 np.zeros_like(inp["D"]), inp["init_state"])
+    assert rel_err(y_nod[:, :, [1, 4, 6]], y_ref[:, :, [1, 4, 6]]) > 0.1
+
+
 def test_chain_path_mixed_modes_within_a_pair():
     """Heads of one pair decay at very different rates, and a head's blocks
     switch between whole, split and extreme along the chain (dt bursts)."""
