@@ -66,7 +66,7 @@ typedef enum {
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
 /* Which kernels compute the forward.
- *   SSD_PATH_AUTO:  SSD_PATH_TC when supported, else SSD_PATH_CHAIN when
+ *   SSD_PATH_AUTO:  SSD_PATH_CHAIN when supported, else SSD_PATH_TC when
  *                   supported, else the SIMT path.
  *   SSD_PATH_SIMT:  fp32 CUDA-core kernels, any supported shape, the five
  *                   stages at exactly chunk_len (chunk states in workspace).

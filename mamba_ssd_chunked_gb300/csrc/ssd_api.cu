@@ -88,8 +88,8 @@ ssd_status check_pointers(const void* x, const float* dt, const float* dt_bias, 
 
 ssd_path resolve_path(const ssd_dims& d, ssd_dtype io, int chunk_len, ssd_path want) {
     if (want != SSD_PATH_AUTO) return want;
-    if (tc_supported(d, io, chunk_len)) return SSD_PATH_TC;
     if (chain_supported(d, io, chunk_len)) return SSD_PATH_CHAIN;
+    if (tc_supported(d, io, chunk_len)) return SSD_PATH_TC;
     return SSD_PATH_SIMT;
 }
 

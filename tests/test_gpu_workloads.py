@@ -34,7 +34,12 @@ def test_full_size_workload_matches_oracle(name):
     y, fs = pkg.ssd_fwd(t["x"], t["dt"], t["dt_bias"], t["A"], t["B"], t["C"], t["D"], t["init_state"],
                         chunk_len=w.chunk_len)
     assert pkg.ssd_device_status() == 0
-    expect_path = "simt" if w.io_dtype == "f32" else "tc"
+    if w.io_dtype == "f32":
+        expect_path = "simt"
+    elif w.dstate == 128 and (w.nheads // w.ngroups) % 2 == 0:
+        expect_path = "chain"
+    else:
+        expect_path = "tc"
     assert pkg.ssd_select_path(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.io_dtype,
                                w.chunk_len) == expect_path
     if SAMPLE[name] is None:

@@ -115,9 +115,10 @@ def test_workspace_too_small(lib):
 
 
 def test_path_selection(lib):
-    assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 256) == "tc"
-    assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 128) == "tc"
-    assert pkg.ssd_select_path(1, 131072, 64, 64, 1, 256, "bf16", 256) == "tc"
+    assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 256) == "chain"
+    assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 128) == "chain"
+    assert pkg.ssd_select_path(1, 131072, 64, 64, 1, 256, "bf16", 256) == "tc"  # dstate 256
+    assert pkg.ssd_select_path(1, 4096, 6, 64, 2, 128, "bf16", 256) == "tc"  # odd heads per group
     assert pkg.ssd_select_path(1, 256, 4, 16, 1, 16, "f32", 64) == "simt"
     assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "f32", 256) == "simt"
     assert pkg.ssd_select_path(4, 4096, 80, 32, 1, 128, "bf16", 256) == "simt"
