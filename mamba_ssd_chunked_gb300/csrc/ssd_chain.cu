@@ -314,7 +314,7 @@ __device__ __noinline__ void fixup_tokens(uint32_t ycol, uint32_t extreme, int q
 // starts after the job i whose cost interval (before, after] holds
 // T_c = ceil(c total / ncta), c in [1, ncta); T_c increases with c, so every
 // such c lands on exactly one job. With at least kBalanceMin jobs per CTA,
-// T_{c+1} - T_c >= 5 kBalanceMin - 1 exceeds any one job's cost (at most 46),
+// T_{c+1} - T_c >= 10 kBalanceMin - 1 exceeds any one job's cost (at most 108),
 // so no range is empty. Thread t sums the costs of a contiguous run of the
 // byte array, a block scan places each thread's run on the cost line, and the
 // thread whose run holds T_cta or T_cta+1 finds the job.
@@ -420,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = misc[0];
     const int cta = static_cast<int>(misc[1]);
     volatile uint32_t* abort_flag = misc + 3;
+    ptx::griddep_wait();  // L tiles, tables and costs from the two kernels before
     auto WB = [&](int bar, uint32_t parity) { wait_bar(&bars[bar], parity, prm.status, abort_flag); };
     int first = static_cast<int>(prm.total * cta / prm.ncta), last = static_cast<int>(prm.total * (cta + 1) / prm.ncta);
     if (prm.cost) {
@@ -852,11 +853,14 @@ struct TableParams {
     float dt_min, dt_max;
 };
 
-// Estimated cost of a job in the chain kernel: every sub-block beyond the first
-// adds a pass of the state path, an extreme one the CUDA-core intra-block sum,
-// tokens with a tiny W factor a fix-up pass. At most 5 + 7 + 32 + 2.
+// Estimated cost of a job in the chain kernel, in units of a tenth of a
+// whole-block job: measured per-job times on the 2.7B shape put a job split in
+// two sub-blocks at 1.1 and one split in four at 2.1 whole-block jobs; eight
+// sub-blocks, extreme sub-blocks (CUDA-core intra-block sum) and the tiny-W
+// fix-up pass are weighted by their extra work. At most 10 + 30 + 64 + 4 = 108.
 __device__ __forceinline__ uint32_t job_cost(int nq, uint32_t extreme, int tiny) {
-    return 5u + static_cast<uint32_t>(nq - 1) + 4u * static_cast<uint32_t>(__popc(extreme)) + (tiny ? 2u : 0u);
+    const uint32_t split = nq == 2 ? 1u : nq == 4 ? 11u : nq == 8 ? 30u : 0u;
+    return 10u + split + 8u * static_cast<uint32_t>(__popc(extreme)) + (tiny ? 4u : 0u);
 }
 
 constexpr int kBalanceMin = 20;  // cost balancing from this many jobs per chain CTA up (see cta_range)
@@ -869,6 +873,7 @@ constexpr int kBalanceMin = 20;  // cost balancing from this many jobs per chain
 // W factor, the epilogue factors u and D / wf, the sub-block-relative cumsum
 // and dt, and per sub-block the state scales e^{c}, the H scale and 1 / sigma.
 __global__ void __launch_bounds__(128) chain_tables(const TableParams prm) {
+    ptx::griddep_launch_dependents();  // chain_masks does not read the tables until its end
     const int wl = threadIdx.x & 31;
     const long long job = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);  // one warp per job
     if (job < prm.total) {
@@ -1076,6 +1081,11 @@ __global__ void __launch_bounds__(128)
     __syncthreads();
     ptx::tc_fence_after();
     if (warp == 0) ptx::tmem_dealloc(tmem, 128);
+    // this grid may overlap chain_tables, but completes only after it, so the
+    // chain kernel's wait on this grid covers both; the chain kernel may launch
+    // once every CTA here is past this point (no table CTA is left to schedule)
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
 }
 
 // ---------------------------------------------------------------- host side
@@ -1151,8 +1161,21 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     tp.dt_max = a.dt_max;
     tp.total = static_cast<int>(pl.total);
     chain_tables<<<static_cast<unsigned>((pl.total + 3) / 4), 128, 0, a.stream>>>(tp);
-    chain_masks<<<static_cast<unsigned>(pl.ntiles), 128, kMaskSmem, a.stream>>>(
-        tb, tc, masks, static_cast<int>(pl.nblk), static_cast<int>(d.ngroups), a.status_word);
+    // chain_masks and the chain kernel start early (programmatic stream
+    // serialization) and wait on the device for what they read
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t mcfg = {};
+    mcfg.gridDim = dim3(static_cast<unsigned>(pl.ntiles));
+    mcfg.blockDim = dim3(128);
+    mcfg.dynamicSmemBytes = kMaskSmem;
+    mcfg.stream = a.stream;
+    mcfg.attrs = pdl;
+    mcfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&mcfg, chain_masks, tb, tc, masks, static_cast<int>(pl.nblk), static_cast<int>(d.ngroups),
+                           a.status_word) != cudaSuccess)
+        return SSD_ERR_CUDA;
     uint32_t* ctr = static_cast<uint32_t*>(ws);  // ticket, flags [ncta]
     // with fewer than kBalanceMin jobs per CTA the jobs are split evenly by count
     const bool balance = pl.total >= static_cast<long long>(kBalanceMin) * pl.ncta;
@@ -1186,7 +1209,14 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     if (cudaFuncSetAttribute(ssd_chain_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Cfg::SMEM_BYTES)) != cudaSuccess)
         return SSD_ERR_CUDA;
-    ssd_chain_fused<<<static_cast<unsigned>(pl.ncta), kThreads, Cfg::SMEM_BYTES, a.stream>>>(tx, tb, tc, tl, ty, p);
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3(static_cast<unsigned>(pl.ncta));
+    ccfg.blockDim = dim3(kThreads);
+    ccfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    ccfg.stream = a.stream;
+    ccfg.attrs = pdl;
+    ccfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&ccfg, ssd_chain_fused, tx, tb, tc, tl, ty, p) != cudaSuccess) return SSD_ERR_CUDA;
     note_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
