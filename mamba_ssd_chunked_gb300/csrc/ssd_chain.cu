@@ -559,6 +559,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
                 ptx::tma_load_4d(dst, &tm_x, fb, 0, jp.h0, jp.blk * kT, jp.b);
                 ptx::tma_load_4d(dst + kTile, &tm_x, fb, 0, jp.h0 + 1, jp.blk * kT, jp.b);
+                if (jx + 2 < njobs) {
+                    // the X of job jx + 2 into L2: its load, once the slot is free, then hits L2
+                    const JobPos jn = job_pos(jobs, jx + 2, chains_per_b, HperG);
+                    ptx::tma_prefetch_4d(&tm_x, 0, jn.h0, jn.blk * kT, jn.b);
+                    ptx::tma_prefetch_4d(&tm_x, 0, jn.h0 + 1, jn.blk * kT, jn.b);
+                }
             }
             for (int i = 0; i < 2 && i < jx; ++i) {
                 const int J = jx - 1 - i;
@@ -755,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2* g2 = reinterpret_cast<const float2*>(T(ts, j, TAB_UG));
             const uint32_t extreme = JW(ts)[1];
             const bool rare = (extreme | JW(ts)[2]) != 0u;
+            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG);
             WB(B_Y_FULL0 + yb, (J >> 1) & 1);
             WB(B_XW_FREE0 + xs, (J >> 1) & 1);  // k3 and k5a no longer read W
             ptx::tc_fence_after();
@@ -798,7 +805,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::fence_proxy_async_smem();
             ptx::named_sync(3, 128);
-            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG);
             if (et == 0) {
                 for (int jj = 0; jj < kHG; ++jj)
                     ptx::tma_store_4d(&tm_y, smem + K::OFF_XW + (xs * kHG + jj) * kTile, 0, jp.h0 + jj,
