@@ -18,14 +18,20 @@ __device__ unsigned g_status_word;
 
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s per device-side wait
 constexpr int kMaxDevices = 64;
+constexpr int kHostSlices = 4;  // ssd_fwd_host: batch slices in flight on their own streams
 
 struct DeviceState {
     unsigned* status = nullptr;     // device address of g_status_word
     void* ws = nullptr;             // library-owned workspace
     size_t ws_bytes = 0;
-    // staging for ssd_fwd_host
+    // staging for ssd_fwd_host: device copies of the inputs and outputs, one
+    // stream and one workspace per batch slice, events that order them
     void* dev_io = nullptr;
     size_t dev_io_bytes = 0;
+    cudaStream_t slice_stream[kHostSlices] = {};
+    cudaEvent_t slice_event[kHostSlices + 1] = {};
+    void* slice_ws = nullptr;
+    size_t slice_ws_bytes = 0;  // per slice
 };
 
 std::mutex g_mu;
@@ -274,54 +280,127 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
     if (!x || !dt || !dt_bias || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
     const ssd_dims& d = *dims;
     const size_t eb = elem_bytes(io_dtype);
-    const size_t sz_x = eb * d.batch * d.seqlen * d.nheads * d.headdim;
-    const size_t sz_dt = 4 * d.batch * d.seqlen * d.nheads;
+    // bytes per batch row of each batched tensor (batch is the outermost dimension of all of them)
+    const size_t row_x = eb * d.seqlen * d.nheads * d.headdim;
+    const size_t row_dt = 4 * d.seqlen * d.nheads;
+    const size_t row_bc = eb * d.seqlen * d.ngroups * d.dstate;
+    const size_t row_state = 4 * d.nheads * d.headdim * d.dstate;
     const size_t sz_h = 4 * d.nheads;
-    const size_t sz_bc = eb * d.batch * d.seqlen * d.ngroups * d.dstate;
-    const size_t sz_state = 4 * d.batch * d.nheads * d.headdim * d.dstate;
     // device layout: x, y, dt, B, C, dt_bias, A, D, init, final
-    const size_t sizes[10] = {sz_x, sz_x, sz_dt, sz_bc, sz_bc, sz_h, sz_h, sz_h, sz_state, sz_state};
+    const size_t sizes[10] = {row_x * d.batch, row_x * d.batch, row_dt * d.batch, row_bc * d.batch, row_bc * d.batch,
+                              sz_h, sz_h, sz_h, row_state * d.batch, row_state * d.batch};
     size_t offs[10], total = 0;
     for (int i = 0; i < 10; ++i) {
         offs[i] = total;
         total += align_up(sizes[i], kWorkspaceAlign);
     }
+    // The batch rows are independent problems: slice them so that the upload of
+    // one slice, the forward of another and the download of a third overlap.
+    const int nsl = static_cast<int>(std::min<int64_t>(d.batch, kHostSlices));
+    auto slice_rows = [&](int i, int64_t* b0, int64_t* nb) {
+        *b0 = d.batch * i / nsl;
+        *nb = d.batch * (i + 1) / nsl - *b0;
+    };
+    size_t ws_need = 0;
+    for (int i = 0; i < nsl; ++i) {
+        int64_t b0, nb;
+        slice_rows(i, &b0, &nb);
+        ssd_dims ds = d;
+        ds.batch = nb;
+        const ssd_path p = resolve_path(ds, io_dtype, chunk_len, SSD_PATH_AUTO);
+        if (!path_supported(ds, io_dtype, chunk_len, p)) return SSD_ERR_UNSUPPORTED;
+        ws_need = std::max(ws_need, align_up(workspace_for(ds, chunk_len, p), kWorkspaceAlign));
+    }
     int dev = 0;
     st = current_device(&dev);
     if (st != SSD_OK) return st;
     char* base = nullptr;
+    char* wsb = nullptr;
+    cudaStream_t ss[kHostSlices];
+    cudaEvent_t ev[kHostSlices + 1];
     {
         std::lock_guard<std::mutex> lock(g_mu);
         DeviceState& s = g_dev[dev];
-        if (s.dev_io_bytes < total) {
-            if (s.dev_io) {
-                if (cudaDeviceSynchronize() != cudaSuccess) return SSD_ERR_CUDA;
-                cudaFree(s.dev_io);
+        if (s.dev_io_bytes < total || s.slice_ws_bytes < ws_need) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return SSD_ERR_CUDA;  // the old buffers may be in use
+            if (s.dev_io_bytes < total) {
+                if (s.dev_io) cudaFree(s.dev_io);
                 s.dev_io = nullptr;
                 s.dev_io_bytes = 0;
+                if (cudaMalloc(&s.dev_io, total) != cudaSuccess) return SSD_ERR_CUDA;
+                s.dev_io_bytes = total;
             }
-            if (cudaMalloc(&s.dev_io, total) != cudaSuccess) return SSD_ERR_CUDA;
-            s.dev_io_bytes = total;
+            if (s.slice_ws_bytes < ws_need) {
+                if (s.slice_ws) cudaFree(s.slice_ws);
+                s.slice_ws = nullptr;
+                s.slice_ws_bytes = 0;
+                if (cudaMalloc(&s.slice_ws, ws_need * kHostSlices) != cudaSuccess) return SSD_ERR_CUDA;
+                // the tensor-core path's state slots must start zero-filled (see ssd_fwd_ws)
+                if (cudaMemset(s.slice_ws, 0, ws_need * kHostSlices) != cudaSuccess) return SSD_ERR_CUDA;
+                s.slice_ws_bytes = ws_need;
+            }
         }
+        for (int i = 0; i < kHostSlices; ++i)
+            if (!s.slice_stream[i] && cudaStreamCreateWithFlags(&s.slice_stream[i], cudaStreamNonBlocking) != cudaSuccess)
+                return SSD_ERR_CUDA;
+        for (int i = 0; i <= kHostSlices; ++i)
+            if (!s.slice_event[i] && cudaEventCreateWithFlags(&s.slice_event[i], cudaEventDisableTiming) != cudaSuccess)
+                return SSD_ERR_CUDA;
         base = static_cast<char*>(s.dev_io);
+        wsb = static_cast<char*>(s.slice_ws);
+        for (int i = 0; i < kHostSlices; ++i) ss[i] = s.slice_stream[i];
+        for (int i = 0; i <= kHostSlices; ++i) ev[i] = s.slice_event[i];
+        ws_need = s.slice_ws_bytes;
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const void* src[10] = {x, nullptr, dt, B, C, dt_bias, A, D, init_state, nullptr};
-    for (int i = 0; i < 10; ++i) {
-        if (!src[i]) continue;
-        if (cudaMemcpyAsync(base + offs[i], src[i], sizes[i], cudaMemcpyHostToDevice, s) != cudaSuccess)
+    cudaStream_t user = static_cast<cudaStream_t>(stream);
+    auto cp = [](void* dst, const void* src, size_t n, cudaMemcpyKind k, cudaStream_t st_) {
+        return n == 0 || cudaMemcpyAsync(dst, src, n, k, st_) == cudaSuccess;
+    };
+    // the per-head parameters go first on the caller's stream; every slice waits for them
+    if (!cp(base + offs[5], dt_bias, sz_h, cudaMemcpyHostToDevice, user) ||
+        !cp(base + offs[6], A, sz_h, cudaMemcpyHostToDevice, user) ||
+        (D && !cp(base + offs[7], D, sz_h, cudaMemcpyHostToDevice, user)))
+        return SSD_ERR_CUDA;
+    if (cudaEventRecord(ev[kHostSlices], user) != cudaSuccess) return SSD_ERR_CUDA;
+    const char* hx = static_cast<const char*>(x);
+    const char* hdt = reinterpret_cast<const char*>(dt);
+    const char* hB = static_cast<const char*>(B);
+    const char* hC = static_cast<const char*>(C);
+    const char* hinit = reinterpret_cast<const char*>(init_state);
+    char* hy = static_cast<char*>(y);
+    char* hfs = reinterpret_cast<char*>(final_state);
+    for (int i = 0; i < nsl; ++i) {
+        int64_t b0, nb;
+        slice_rows(i, &b0, &nb);
+        cudaStream_t si = ss[i];
+        if (cudaStreamWaitEvent(si, ev[kHostSlices], 0) != cudaSuccess) return SSD_ERR_CUDA;
+        char* dx = base + offs[0] + b0 * row_x;
+        char* dy = base + offs[1] + b0 * row_x;
+        char* ddt = base + offs[2] + b0 * row_dt;
+        char* dB = base + offs[3] + b0 * row_bc;
+        char* dC = base + offs[4] + b0 * row_bc;
+        char* dinit = base + offs[8] + b0 * row_state;
+        char* dfs = base + offs[9] + b0 * row_state;
+        if (!cp(dx, hx + b0 * row_x, nb * row_x, cudaMemcpyHostToDevice, si) ||
+            !cp(ddt, hdt + b0 * row_dt, nb * row_dt, cudaMemcpyHostToDevice, si) ||
+            !cp(dB, hB + b0 * row_bc, nb * row_bc, cudaMemcpyHostToDevice, si) ||
+            !cp(dC, hC + b0 * row_bc, nb * row_bc, cudaMemcpyHostToDevice, si) ||
+            (hinit && !cp(dinit, hinit + b0 * row_state, nb * row_state, cudaMemcpyHostToDevice, si)))
+            return SSD_ERR_CUDA;
+        ssd_dims ds = d;
+        ds.batch = nb;
+        st = run(&ds, io_dtype, dx, reinterpret_cast<const float*>(ddt),
+                 reinterpret_cast<const float*>(base + offs[5]), reinterpret_cast<const float*>(base + offs[6]), dB,
+                 dC, D ? reinterpret_cast<const float*>(base + offs[7]) : nullptr,
+                 hinit ? reinterpret_cast<const float*>(dinit) : nullptr, chunk_len, ngroups, dy,
+                 hfs ? reinterpret_cast<float*>(dfs) : nullptr, SSD_PATH_AUTO, wsb + i * ws_need, ws_need, false, si);
+        if (st != SSD_OK) return st;
+        if (!cp(hy + b0 * row_x, dy, nb * row_x, cudaMemcpyDeviceToHost, si) ||
+            (hfs && !cp(hfs + b0 * row_state, dfs, nb * row_state, cudaMemcpyDeviceToHost, si)))
+            return SSD_ERR_CUDA;
+        if (cudaEventRecord(ev[i], si) != cudaSuccess || cudaStreamWaitEvent(user, ev[i], 0) != cudaSuccess)
             return SSD_ERR_CUDA;
     }
-    st = ssd_fwd(dims, io_dtype, base + offs[0], reinterpret_cast<const float*>(base + offs[2]),
-                 reinterpret_cast<const float*>(base + offs[5]), reinterpret_cast<const float*>(base + offs[6]),
-                 base + offs[3], base + offs[4], D ? reinterpret_cast<const float*>(base + offs[7]) : nullptr,
-                 init_state ? reinterpret_cast<const float*>(base + offs[8]) : nullptr, chunk_len, ngroups,
-                 base + offs[1], final_state ? reinterpret_cast<float*>(base + offs[9]) : nullptr, stream);
-    if (st != SSD_OK) return st;
-    if (cudaMemcpyAsync(y, base + offs[1], sizes[1], cudaMemcpyDeviceToHost, s) != cudaSuccess) return SSD_ERR_CUDA;
-    if (final_state &&
-        cudaMemcpyAsync(final_state, base + offs[9], sizes[9], cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return SSD_ERR_CUDA;
     return ssd_device_status(stream);
 }
 
@@ -363,15 +442,17 @@ void ssd_release(void) {
     const bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
     for (int d = 0; d < kMaxDevices; ++d) {
         DeviceState& s = g_dev[d];
-        if (!s.ws && !s.dev_io) continue;
+        if (!s.ws && !s.dev_io && !s.slice_ws && !s.slice_stream[0]) continue;
         if (cudaSetDevice(d) != cudaSuccess) continue;
         cudaDeviceSynchronize();
         if (s.ws) cudaFree(s.ws);
         if (s.dev_io) cudaFree(s.dev_io);
-        s.ws = nullptr;
-        s.ws_bytes = 0;
-        s.dev_io = nullptr;
-        s.dev_io_bytes = 0;
+        if (s.slice_ws) cudaFree(s.slice_ws);
+        for (int i = 0; i < kHostSlices; ++i)
+            if (s.slice_stream[i]) cudaStreamDestroy(s.slice_stream[i]);
+        for (int i = 0; i <= kHostSlices; ++i)
+            if (s.slice_event[i]) cudaEventDestroy(s.slice_event[i]);
+        s = DeviceState{};
     }
     if (have_prev) cudaSetDevice(prev);
 }
