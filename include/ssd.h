@@ -183,6 +183,20 @@ SSD_API const char* ssd_status_string(ssd_status status);
 /* Kernels this library has launched in this process (all devices, all calls). */
 SSD_API uint64_t ssd_kernel_launches(void);
 
+/*
+ * Device time of each forward's fused kernel, for measurement. While enabled
+ * (enable != 0), every ssd_fwd* call records a CUDA event pair on its stream
+ * right before and after the launch of its main kernel (the fused kernel of
+ * the tensor-core paths, the three kernels of the SIMT path). An event record
+ * between launches keeps consecutive kernels from overlapping, so enable it
+ * only for a measurement pass. ssd_kernel_timing_read waits for the recorded
+ * pairs (all of the current device), writes their summed elapsed time in
+ * milliseconds and their number, and forgets them. Returns SSD_ERR_INVALID_ARG
+ * for NULL outputs and SSD_ERR_CUDA if a CUDA event call failed.
+ */
+SSD_API void ssd_kernel_timing(int enable);
+SSD_API ssd_status ssd_kernel_timing_read(double* total_ms, uint64_t* count);
+
 /* Frees the library-owned device and pinned buffers of every device. Not safe
  * while calls that use them are in flight. */
 SSD_API void ssd_release(void);

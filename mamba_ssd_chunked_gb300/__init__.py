@@ -20,7 +20,7 @@ from typing import Optional, Tuple
 
 __all__ = [
     "SsdError", "library", "ssd_fwd", "ssd_fwd_host", "ssd_device_status", "ssd_fwd_workspace_bytes",
-    "ssd_select_path", "ssd_kernel_launches", "ssd_release", "ssd_step", "ssd_conv1d_silu", "ssd_conv1d_step",
+    "ssd_select_path", "ssd_kernel_launches", "ssd_kernel_timing", "ssd_kernel_timing_read", "ssd_release", "ssd_step", "ssd_conv1d_silu", "ssd_conv1d_step",
     "ssd_gated_rmsnorm", "Dims", "ConvDims", "DtLimit", "PATHS", "STATUS",
 ]
 
@@ -80,6 +80,10 @@ def library() -> ctypes.CDLL:
     lib.ssd_status_string.argtypes = [i]
     lib.ssd_kernel_launches.restype = ctypes.c_uint64
     lib.ssd_kernel_launches.argtypes = []
+    lib.ssd_kernel_timing.restype = None
+    lib.ssd_kernel_timing.argtypes = [ctypes.c_int]
+    lib.ssd_kernel_timing_read.restype = ctypes.c_int
+    lib.ssd_kernel_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]
     lib.ssd_release.restype = None
     lib.ssd_release.argtypes = []
     lib.ssd_step.restype = i
@@ -417,6 +421,20 @@ def ssd_select_path(batch, seqlen, nheads, headdim, ngroups, dstate, io="bf16", 
 
 def ssd_kernel_launches() -> int:
     return int(library().ssd_kernel_launches())
+
+
+def ssd_kernel_timing(enable: bool) -> None:
+    """Record CUDA events around each forward's main kernel (ssd_kernel_timing)."""
+    library().ssd_kernel_timing(1 if enable else 0)
+
+
+def ssd_kernel_timing_read() -> Tuple[float, int]:
+    """(summed milliseconds, count) of the recorded main-kernel launches; clears them."""
+    ms, n = ctypes.c_double(0.0), ctypes.c_uint64(0)
+    rc = library().ssd_kernel_timing_read(ctypes.byref(ms), ctypes.byref(n))
+    if rc != 0:
+        raise SsdError(rc, "ssd_kernel_timing_read")
+    return float(ms.value), int(n.value)
 
 
 def ssd_release() -> None:

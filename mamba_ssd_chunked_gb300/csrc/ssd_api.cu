@@ -225,6 +225,41 @@ ssd_status noalloc_scratch(int dev, void** out) {
 
 void note_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+// ---- ssd_kernel_timing
+std::atomic<int> g_timing{0};
+std::mutex g_timing_mu;
+std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_timed;  // recorded pairs, not yet read
+std::vector<cudaEvent_t> g_spare_events;
+thread_local cudaEvent_t t_begin = nullptr;  // begin event of the launch this host thread is timing
+
+cudaEvent_t timing_event() {
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    if (!g_spare_events.empty()) {
+        cudaEvent_t e = g_spare_events.back();
+        g_spare_events.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+void timing_begin(cudaStream_t s) {
+    if (!g_timing.load(std::memory_order_relaxed)) return;
+    t_begin = timing_event();
+    if (t_begin && cudaEventRecord(t_begin, s) != cudaSuccess) t_begin = nullptr;
+}
+
+void timing_end(cudaStream_t s) {
+    if (!t_begin) return;
+    cudaEvent_t e = timing_event();
+    if (e && cudaEventRecord(e, s) == cudaSuccess) {
+        std::lock_guard<std::mutex> lock(g_timing_mu);
+        g_timed.emplace_back(t_begin, e);
+    }
+    t_begin = nullptr;
+}
+
 }  // namespace ssd
 
 using namespace ssd;
@@ -435,6 +470,27 @@ const char* ssd_status_string(ssd_status status) {
 }
 
 uint64_t ssd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void ssd_kernel_timing(int enable) { g_timing.store(enable ? 1 : 0, std::memory_order_relaxed); }
+
+ssd_status ssd_kernel_timing_read(double* total_ms, uint64_t* count) {
+    if (!total_ms || !count) return SSD_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    double sum = 0.0;
+    ssd_status st = SSD_OK;
+    for (auto& pr : g_timed) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(pr.second) != cudaSuccess || cudaEventElapsedTime(&ms, pr.first, pr.second) != cudaSuccess)
+            st = SSD_ERR_CUDA;
+        sum += ms;
+        g_spare_events.push_back(pr.first);
+        g_spare_events.push_back(pr.second);
+    }
+    *total_ms = sum;
+    *count = g_timed.size();
+    g_timed.clear();
+    return st;
+}
 
 void ssd_release(void) {
     std::lock_guard<std::mutex> lock(g_mu);

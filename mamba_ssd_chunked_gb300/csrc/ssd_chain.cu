@@ -1222,7 +1222,9 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     ccfg.stream = a.stream;
     ccfg.attrs = pdl;
     ccfg.numAttrs = 1;
+    timing_begin(a.stream);
     if (cudaLaunchKernelEx(&ccfg, ssd_chain_fused, tx, tb, tc, tl, ty, p) != cudaSuccess) return SSD_ERR_CUDA;
+    timing_end(a.stream);
     note_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

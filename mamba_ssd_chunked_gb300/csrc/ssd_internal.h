@@ -76,6 +76,11 @@ ssd_status step_forward(const StepArgs& a);
 // Launch bookkeeping (every kernel launch of the library goes through it).
 void note_launches(uint64_t n);
 
+// ssd_kernel_timing: event pair around a forward's main kernel on its stream
+// (no-ops while timing is off)
+void timing_begin(cudaStream_t s);
+void timing_end(cudaStream_t s);
+
 constexpr size_t kWorkspaceAlign = 256;
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -259,6 +259,7 @@ ssd_status launch_all(const FwdArgs& a, float* states, float* logdecay) {
                              static_cast<int>(smem3)) != cudaSuccess)
         return SSD_ERR_CUDA;
 
+    timing_begin(a.stream);
     simt_chunk_state<T><<<dim3(nc, H, static_cast<unsigned>(d.batch)), block, smem1, a.stream>>>(
         x, a.dt, a.dt_bias, a.A, Bm, d.seqlen, H, G, P, N, Q, nc, states, logdecay, make_float2(a.dt_min, a.dt_max));
     const int PN = P * N;
@@ -268,6 +269,7 @@ ssd_status launch_all(const FwdArgs& a, float* states, float* logdecay) {
     simt_chunk_scan<T><<<dim3(nc * tiles, H, static_cast<unsigned>(d.batch)), block, smem3, a.stream>>>(
         x, a.dt, a.dt_bias, a.A, Bm, Cm, a.D, states, d.seqlen, H, G, P, N, Q, nc, tiles,
         static_cast<T*>(a.y), make_float2(a.dt_min, a.dt_max));
+    timing_end(a.stream);
     note_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

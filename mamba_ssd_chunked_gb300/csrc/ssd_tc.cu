@@ -749,7 +749,9 @@ ssd_status launch(const FwdArgs& a, void* ws) {
                              static_cast<int>(K::SMEM_BYTES)) != cudaSuccess)
         return SSD_ERR_CUDA;
     const long long units = static_cast<long long>(p.nblk) * d.batch * p.ngrp;
+    timing_begin(a.stream);
     ssd_tc_fused<NST><<<static_cast<unsigned>(units), K::THREADS, K::SMEM_BYTES, a.stream>>>(tx, tb, tc, ty, p);
+    timing_end(a.stream);
     note_launches(1);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

@@ -190,6 +190,25 @@ def test_host_buffer_entry_point(shape, io, init, with_D, final):
         assert fs is None
 
 
+@pytest.mark.parametrize("path", ["chain", "tc", "simt"])
+def test_kernel_timing_records_one_pair_per_forward(path):
+    import mamba_ssd_chunked_gb300 as pkg
+    inp = make_inputs(2, 300, 4, 64, 2, 128, io_dtype="bf16", init="normal", seed=3)
+    t = to_device(inp, "bf16")
+    pkg.ssd_kernel_timing_read()  # forget anything recorded before
+    run_gpu(t, 256, path)
+    assert pkg.ssd_kernel_timing_read() == (0.0, 0)  # off by default
+    pkg.ssd_kernel_timing(True)
+    try:
+        for _ in range(3):
+            run_gpu(t, 256, path)
+    finally:
+        pkg.ssd_kernel_timing(False)
+    ms, n = pkg.ssd_kernel_timing_read()
+    assert n == 3 and ms > 0.0
+    assert pkg.ssd_kernel_timing_read() == (0.0, 0)
+
+
 def test_launch_counter_counts_kernels():
     import mamba_ssd_chunked_gb300 as pkg
     inp = make_inputs(1, 256, 2, 64, 1, 128, io_dtype="bf16", init="zero", seed=1)
