@@ -391,12 +391,18 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
     auto cp = [](void* dst, const void* src, size_t n, cudaMemcpyKind k, cudaStream_t st_) {
         return n == 0 || cudaMemcpyAsync(dst, src, n, k, st_) == cudaSuccess;
     };
+    // on a failure after work was queued, nothing may still use the staging buffers on return
+    auto fail = [&](ssd_status e) {
+        for (int i = 0; i < kHostSlices; ++i) cudaStreamSynchronize(ss[i]);
+        cudaStreamSynchronize(user);
+        return e;
+    };
     // the per-head parameters go first on the caller's stream; every slice waits for them
     if (!cp(base + offs[5], dt_bias, sz_h, cudaMemcpyHostToDevice, user) ||
         !cp(base + offs[6], A, sz_h, cudaMemcpyHostToDevice, user) ||
         (D && !cp(base + offs[7], D, sz_h, cudaMemcpyHostToDevice, user)))
-        return SSD_ERR_CUDA;
-    if (cudaEventRecord(ev[kHostSlices], user) != cudaSuccess) return SSD_ERR_CUDA;
+        return fail(SSD_ERR_CUDA);
+    if (cudaEventRecord(ev[kHostSlices], user) != cudaSuccess) return fail(SSD_ERR_CUDA);
     const char* hx = static_cast<const char*>(x);
     const char* hdt = reinterpret_cast<const char*>(dt);
     const char* hB = static_cast<const char*>(B);
@@ -408,7 +414,7 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
         int64_t b0, nb;
         slice_rows(i, &b0, &nb);
         cudaStream_t si = ss[i];
-        if (cudaStreamWaitEvent(si, ev[kHostSlices], 0) != cudaSuccess) return SSD_ERR_CUDA;
+        if (cudaStreamWaitEvent(si, ev[kHostSlices], 0) != cudaSuccess) return fail(SSD_ERR_CUDA);
         char* dx = base + offs[0] + b0 * row_x;
         char* dy = base + offs[1] + b0 * row_x;
         char* ddt = base + offs[2] + b0 * row_dt;
@@ -421,7 +427,7 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
             !cp(dB, hB + b0 * row_bc, nb * row_bc, cudaMemcpyHostToDevice, si) ||
             !cp(dC, hC + b0 * row_bc, nb * row_bc, cudaMemcpyHostToDevice, si) ||
             (hinit && !cp(dinit, hinit + b0 * row_state, nb * row_state, cudaMemcpyHostToDevice, si)))
-            return SSD_ERR_CUDA;
+            return fail(SSD_ERR_CUDA);
         ssd_dims ds = d;
         ds.batch = nb;
         st = run(&ds, io_dtype, dx, reinterpret_cast<const float*>(ddt),
@@ -429,12 +435,12 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
                  dC, D ? reinterpret_cast<const float*>(base + offs[7]) : nullptr,
                  hinit ? reinterpret_cast<const float*>(dinit) : nullptr, chunk_len, ngroups, dy,
                  hfs ? reinterpret_cast<float*>(dfs) : nullptr, SSD_PATH_AUTO, wsb + i * ws_need, ws_need, false, si);
-        if (st != SSD_OK) return st;
+        if (st != SSD_OK) return fail(st);
         if (!cp(hy + b0 * row_x, dy, nb * row_x, cudaMemcpyDeviceToHost, si) ||
             (hfs && !cp(hfs + b0 * row_state, dfs, nb * row_state, cudaMemcpyDeviceToHost, si)))
-            return SSD_ERR_CUDA;
+            return fail(SSD_ERR_CUDA);
         if (cudaEventRecord(ev[i], si) != cudaSuccess || cudaStreamWaitEvent(user, ev[i], 0) != cudaSuccess)
-            return SSD_ERR_CUDA;
+            return fail(SSD_ERR_CUDA);
     }
     return ssd_device_status(stream);
 }
