@@ -559,6 +559,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
                 ptx::tma_load_4d(dst, &tm_x, fb, 0, jp.h0, jp.blk * kT, jp.b);
                 ptx::tma_load_4d(dst + kTile, &tm_x, fb, 0, jp.h0 + 1, jp.blk * kT, jp.b);
+                if (jp.blk == 0 && prm.init)  // a chain start: its initial state into L2 for the state warps
+                    ptx::bulk_prefetch_l2(prm.init + (static_cast<size_t>(jp.b) * prm.H + jp.h0) * kP * kN,
+                                          kHG * kP * kN * sizeof(float));
                 if (jx + 2 < njobs) {
                     // the X of job jx + 2 into L2: its load, once the slot is free, then hits L2
                     const JobPos jn = job_pos(jobs, jx + 2, chains_per_b, HperG);
