@@ -974,23 +974,22 @@ __global__ void __launch_bounds__(128) chain_tables(const TableParams prm) {
             }
             const float cse = endv - base;
             const float c = (-cse <= kMaxSubDecay) ? 0.5f * cse : cse + kExtremeRef;
-            float wf4[4], u4[4], g4[4], c4[4];
+            float wf4[4], u4[4], g4[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float csl = cs[j][i] - base;
-                const float wfv = dtv[j][i] * __expf(c - csl);
+                const float e = __expf(c - csl);  // within e^{+-75} outside extreme sub-blocks
+                const float wfv = dtv[j][i] * e;
                 const bool tiny = !ext && wfv < kTinyWF;  // D x from x itself (fixup_tokens)
                 any_tiny |= tiny && (tg0 + i < prm.L);
                 wf4[i] = wfv;
-                u4[i] = ext ? __expf(csl) : __expf(csl - c);
-                g4[i] = (ext || tiny) ? 0.f : Dh / wfv;
-                c4[i] = csl;
+                u4[i] = ext ? __expf(csl) : __frcp_rn(e);
+                g4[i] = (ext || tiny) ? 0.f : __fdividef(Dh, wfv);
+                cs[j][i] = csl;  // kept for the rare-token arrays below
             }
             *T(j, TAB_WF) = make_float4(wf4[0], wf4[1], wf4[2], wf4[3]);
             *T(j, TAB_U) = make_float4(u4[0], u4[1], u4[2], u4[3]);
             *T(j, TAB_UG) = make_float4(g4[0], g4[1], g4[2], g4[3]);
-            *TX(j, TABX_CS) = make_float4(c4[0], c4[1], c4[2], c4[3]);
-            *TX(j, TABX_DT) = make_float4(dtv[j][0], dtv[j][1], dtv[j][2], dtv[j][3]);
             if (wl < nq) {
                 // the sub-block scalars: lane wl serves sub-block wl
                 float lo_ = 0.f, hi_ = 0.f;
@@ -1009,6 +1008,14 @@ __global__ void __launch_bounds__(128) chain_tables(const TableParams prm) {
             if (wl == 0) S(j)[SC_D] = Dh;
         }
         any_tiny = __any_sync(0xffffffffu, any_tiny);
+        if (extreme != 0u || any_tiny) {
+            // sub-block cumsum and dt: read only by fixup_tokens, for jobs with rare tokens
+#pragma unroll
+            for (int j = 0; j < kHG; ++j) {
+                *TX(j, TABX_CS) = make_float4(cs[j][0], cs[j][1], cs[j][2], cs[j][3]);
+                *TX(j, TABX_DT) = make_float4(dtv[j][0], dtv[j][1], dtv[j][2], dtv[j][3]);
+            }
+        }
         if (wl == 0) {
             jw[0] = static_cast<uint32_t>(nq);
             jw[1] = extreme;
