@@ -881,7 +881,8 @@ constexpr int kBalanceMin = 20;  // cost balancing from this many jobs per chain
 // kMaxSubDecay; 16-token sub-blocks beyond it are extreme), then per token the
 // W factor, the epilogue factors u and D / wf, the sub-block-relative cumsum
 // and dt, and per sub-block the state scales e^{c}, the H scale and 1 / sigma.
-__global__ void __launch_bounds__(128) chain_tables(const TableParams prm) {
+// At most 56 registers so that 9 CTAs fit an SM: 1280 CTAs of the 2.7B shape in one wave.
+__global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
     ptx::griddep_launch_dependents();  // chain_masks does not read the tables until its end
     const int wl = threadIdx.x & 31;
     const long long job = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);  // one warp per job
@@ -897,25 +898,31 @@ __global__ void __launch_bounds__(128) chain_tables(const TableParams prm) {
         auto T = [&](int j, int arr) { return reinterpret_cast<float4*>(tabs + (j * kNumTab + arr) * kT) + wl; };
         auto TX = [&](int j, int arr) { return reinterpret_cast<float4*>(tabx + (j * kNumTabX + arr) * kT) + wl; };
         auto S = [&](int j) { return scal + j * kScal; };
-        // lane wl owns tokens 4 wl .. 4 wl + 3 of the block (one 16-token unit)
+        // lane wl owns tokens 4 wl .. 4 wl + 3 of the block (one 16-token unit); every
+        // global load is issued here, before the first store
         const long long tg0 = static_cast<long long>(blk) * kT + 4 * wl;
+        const float2 bias = __ldg(reinterpret_cast<const float2*>(prm.dt_bias + h0));
+        const float2 a2 = __ldg(reinterpret_cast<const float2*>(prm.A + h0));
+        const float2 d2 = prm.D ? __ldg(reinterpret_cast<const float2*>(prm.D + h0)) : make_float2(0.f, 0.f);
+        float2 raw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            raw[i] = tg0 + i < prm.L ? __ldg(reinterpret_cast<const float2*>(
+                                           prm.dt + (static_cast<long long>(b) * prm.L + tg0 + i) * prm.H + h0))
+                                     : make_float2(0.f, 0.f);
         float dtv[kHG][4], cs[kHG][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const long long tg = tg0 + i;
-            const float2 raw = tg < prm.L ? *reinterpret_cast<const float2*>(
-                                                prm.dt + (static_cast<long long>(b) * prm.L + tg) * prm.H + h0)
-                                          : make_float2(0.f, 0.f);
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < kHG; ++j)
-                dtv[j][i] = tg < prm.L ? fminf(fmaxf(softplus_f((j ? raw.y : raw.x) + prm.dt_bias[h0 + j]), prm.dt_min),
-                                               prm.dt_max)
-                                       : 0.f;
-        }
+                dtv[j][i] = tg0 + i < prm.L
+                                ? fminf(fmaxf(softplus_f((j ? raw[i].y : raw[i].x) + (j ? bias.y : bias.x)), prm.dt_min),
+                                        prm.dt_max)
+                                : 0.f;
         float bnd[kHG][8];  // cumsum at token 16k + 15
 #pragma unroll
         for (int j = 0; j < kHG; ++j) {
-            const float a = prm.A[h0 + j];
+            const float a = j ? a2.y : a2.x;
             float run = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -964,7 +971,7 @@ __global__ void __launch_bounds__(128) chain_tables(const TableParams prm) {
         bool any_tiny = false;
 #pragma unroll
         for (int j = 0; j < kHG; ++j) {
-            const float Dh = prm.D ? prm.D[h0 + j] : 0.f;
+            const float Dh = j ? d2.y : d2.x;
             // cumsum relative to the sub-block start, and the sub-block's end value
             float base = 0.f, endv = 0.f;
 #pragma unroll
