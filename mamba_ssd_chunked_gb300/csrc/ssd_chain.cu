@@ -885,12 +885,13 @@ constexpr int kBalanceMin = 20;  // cost balancing from this many jobs per chain
 __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
     ptx::griddep_launch_dependents();  // chain_masks does not read the tables until its end
     const int wl = threadIdx.x & 31;
-    const long long job = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);  // one warp per job
+    // one warp per job (job indices fit 31 bits: the host launches only then)
+    const int job = static_cast<int>(blockIdx.x) * 4 + static_cast<int>(threadIdx.x >> 5);
     if (job < prm.total) {
-        const int blk = static_cast<int>(job % prm.nblk);
-        const int chain = static_cast<int>(job / prm.nblk);
+        const int blk = job % prm.nblk;
+        const int chain = job / prm.nblk;
         const int b = chain / prm.chains_per_b, h0 = (chain % prm.chains_per_b) * kHG;
-        uint8_t* rec = prm.out + job * kRecBytes;
+        uint8_t* rec = prm.out + static_cast<size_t>(job) * kRecBytes;
         float* tabs = reinterpret_cast<float*>(rec);
         float* scal = reinterpret_cast<float*>(rec + kRecTab);
         uint32_t* jw = reinterpret_cast<uint32_t*>(rec + kRecTab + kRecScal);
@@ -900,7 +901,7 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
         auto S = [&](int j) { return scal + j * kScal; };
         // lane wl owns tokens 4 wl .. 4 wl + 3 of the block (one 16-token unit); every
         // global load is issued here, before the first store
-        const long long tg0 = static_cast<long long>(blk) * kT + 4 * wl;
+        const int tg0 = blk * kT + 4 * wl;
         const float2 bias = __ldg(reinterpret_cast<const float2*>(prm.dt_bias + h0));
         const float2 a2 = __ldg(reinterpret_cast<const float2*>(prm.A + h0));
         const float2 d2 = prm.D ? __ldg(reinterpret_cast<const float2*>(prm.D + h0)) : make_float2(0.f, 0.f);
@@ -908,7 +909,7 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             raw[i] = tg0 + i < prm.L ? __ldg(reinterpret_cast<const float2*>(
-                                           prm.dt + (static_cast<long long>(b) * prm.L + tg0 + i) * prm.H + h0))
+                                           prm.dt + (static_cast<long long>(b) * prm.L + (tg0 + i)) * prm.H + h0))
                                      : make_float2(0.f, 0.f);
         float dtv[kHG][4], cs[kHG][4];
 #pragma unroll
@@ -920,6 +921,7 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
                                         prm.dt_max)
                                 : 0.f;
         float bnd[kHG][8];  // cumsum at token 16k + 15
+        float vtot[kHG];     // cumsum at token 4 wl + 3 (this lane's last token)
 #pragma unroll
         for (int j = 0; j < kHG; ++j) {
             const float a = j ? a2.y : a2.x;
@@ -938,6 +940,7 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
             const float pre = v - run;
 #pragma unroll
             for (int i = 0; i < 4; ++i) cs[j][i] += pre;
+            vtot[j] = v;
 #pragma unroll
             for (int k = 0; k < 8; ++k) bnd[j][k] = __shfl_sync(0xffffffffu, v, 4 * k + 3);
         }
@@ -965,20 +968,22 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
                     if (lo_ - bnd[j][r] > kMaxSubDecay) extreme |= 1u << r;
                 }
         }
-        const int qs = kT / nq, m = qs / 16;
+        const int qs = kT / nq;
         const int q = 4 * wl / qs;  // the lane's sub-block
         const bool ext = (extreme >> q) & 1u;
         bool any_tiny = false;
 #pragma unroll
         for (int j = 0; j < kHG; ++j) {
             const float Dh = j ? d2.y : d2.x;
-            // cumsum relative to the sub-block start, and the sub-block's end value
-            float base = 0.f, endv = 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (q > 0 && k == q * m - 1) base = bnd[j][k];
-                if (k == (q + 1) * m - 1) endv = bnd[j][k];
-            }
+            // cumsum relative to the sub-block start, and the sub-block's end value: the
+            // cumsums at tokens q qs - 1 and (q + 1) qs - 1 sit in lanes q qs / 4 - 1 and
+            // (q + 1) qs / 4 - 1; the same shuffles give lane wl the bounds of sub-block wl
+            const int ql = q * qs / 4, wlo = wl * qs / 4;
+            const float sb = __shfl_sync(0xffffffffu, vtot[j], max(ql - 1, 0));
+            const float se_ = __shfl_sync(0xffffffffu, vtot[j], min(ql + qs / 4, 32) - 1);
+            const float lo_w = __shfl_sync(0xffffffffu, vtot[j], min(max(wlo - 1, 0), 31));
+            const float hi_w = __shfl_sync(0xffffffffu, vtot[j], min(wlo + qs / 4, 32) - 1);
+            const float base = q > 0 ? sb : 0.f, endv = se_;
             const float cse = endv - base;
             const float c = (-cse <= kMaxSubDecay) ? 0.5f * cse : cse + kExtremeRef;
             float wf4[4], u4[4], g4[4];
@@ -990,7 +995,7 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
                 const bool tiny = !ext && wfv < kTinyWF;  // D x from x itself (fixup_tokens)
                 any_tiny |= tiny && (tg0 + i < prm.L);
                 wf4[i] = wfv;
-                u4[i] = ext ? __expf(csl) : __frcp_rn(e);
+                u4[i] = __expf(ext ? csl : csl - c);
                 g4[i] = (ext || tiny) ? 0.f : __fdividef(Dh, wfv);
                 cs[j][i] = csl;  // kept for the rare-token arrays below
             }
@@ -999,13 +1004,7 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
             *T(j, TAB_UG) = make_float4(g4[0], g4[1], g4[2], g4[3]);
             if (wl < nq) {
                 // the sub-block scalars: lane wl serves sub-block wl
-                float lo_ = 0.f, hi_ = 0.f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    if (wl > 0 && k == wl * m - 1) lo_ = bnd[j][k];
-                    if (k == (wl + 1) * m - 1) hi_ = bnd[j][k];
-                }
-                const float se = hi_ - lo_;
+                const float se = hi_w - (wl > 0 ? lo_w : 0.f);
                 const bool sext = (extreme >> wl) & 1u;
                 const float sc_ = (-se <= kMaxSubDecay) ? 0.5f * se : se + kExtremeRef;
                 S(j)[SC_EC + wl] = __expf(sc_);
