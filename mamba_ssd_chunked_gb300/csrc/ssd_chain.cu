@@ -856,7 +856,9 @@ struct TableParams {
     const float* A;
     const float* D;
     uint8_t* out;      // [chain * nblk + block] table records
-    uint8_t* cost;     // [jobs, padded to kSplitRound] estimated job costs
+    uint8_t* cost;       // [jobs] estimated job costs (cta_range)
+    uint32_t* counters;  // the chain kernel's ticket and flags, zeroed here
+    int ncounters;
     long long L;
     int H, nblk, chains_per_b, total;
     float dt_min, dt_max;
@@ -883,7 +885,12 @@ constexpr int kBalanceMin = 20;  // cost balancing from this many jobs per chain
 // and dt, and per sub-block the state scales e^{c}, the H scale and 1 / sigma.
 // At most 56 registers so that 9 CTAs fit an SM: 1280 CTAs of the 2.7B shape in one wave.
 __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
+    // launched early behind the previous kernel of the stream (which may still use the
+    // workspace or write the inputs): nothing is touched before it completes
+    ptx::griddep_wait();
     ptx::griddep_launch_dependents();  // chain_masks does not read the tables until its end
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < prm.ncounters; i += blockDim.x) prm.counters[i] = 0u;
     const int wl = threadIdx.x & 31;
     // one warp per job (job indices fit 31 bits: the host launches only then)
     const int job = static_cast<int>(blockIdx.x) * 4 + static_cast<int>(threadIdx.x >> 5);
@@ -1164,7 +1171,6 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
         !make_map_bf16(&tl, masks, kT, 1, kT, static_cast<uint64_t>(pl.ntiles)) ||
         !make_map_bf16(&ty, a.y, d.headdim, d.nheads, d.seqlen, d.batch))
         return SSD_ERR_CUDA;
-    if (cudaMemsetAsync(ws, 0, counters, a.stream) != cudaSuccess) return SSD_ERR_CUDA;
     if (cudaFuncSetAttribute(chain_masks, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kMaskSmem)) != cudaSuccess)
         return SSD_ERR_CUDA;
@@ -1182,12 +1188,20 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     tp.dt_min = a.dt_min;
     tp.dt_max = a.dt_max;
     tp.total = static_cast<int>(pl.total);
-    chain_tables<<<static_cast<unsigned>((pl.total + 3) / 4), 128, 0, a.stream>>>(tp);
-    // chain_masks and the chain kernel start early (programmatic stream
-    // serialization) and wait on the device for what they read
+    tp.counters = static_cast<uint32_t*>(ws);
+    tp.ncounters = 1 + pl.ncta;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t tcfg = {};
+    tcfg.gridDim = dim3(static_cast<unsigned>((pl.total + 3) / 4));
+    tcfg.blockDim = dim3(128);
+    tcfg.stream = a.stream;
+    tcfg.attrs = pdl;
+    tcfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&tcfg, chain_tables, tp) != cudaSuccess) return SSD_ERR_CUDA;
+    // chain_masks and the chain kernel start early as well (programmatic stream
+    // serialization) and wait on the device for what they read
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(static_cast<unsigned>(pl.ntiles));
     mcfg.blockDim = dim3(128);
