@@ -38,6 +38,15 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"libssd.so does not export {name}"
 
 
+def test_kernel_timing_arguments(lib):
+    import ctypes
+    lib.ssd_kernel_timing(0)
+    assert lib.ssd_kernel_timing_read(None, None) == 1  # SSD_ERR_INVALID_ARG
+    ms, n = ctypes.c_double(-1.0), ctypes.c_uint64(7)
+    assert lib.ssd_kernel_timing_read(ctypes.byref(ms), ctypes.byref(n)) == 0  # nothing recorded: no CUDA call
+    assert ms.value == 0.0 and n.value == 0
+
+
 def test_status_strings(lib):
     for code in range(6):
         assert lib.ssd_status_string(code)
