@@ -161,12 +161,6 @@ __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-// Waits until at most N of this thread's committed bulk groups still read their source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
 __device__ __forceinline__ void bulk_wait_group_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
@@ -330,53 +324,6 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
 // bar.sync on barrier `id` (1..15) for `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// ---------------------------------------------------------------- global loads
-// 16-byte load cached in L2 only; volatile so that it is issued where it is
-// written (early, to overlap its latency) rather than next to its first use.
-__device__ __forceinline__ float4 ld_cg_v4(const float* p) {
-    float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-// 64-bit relaxed (morally strong, gpu scope) accesses: single-copy atomic, so
-// a 32-bit value and a 32-bit tag stored together are always seen together.
-__device__ __forceinline__ uint64_t ld_relaxed_b64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_relaxed_b64(uint64_t* p, uint64_t v) {
-    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Two 64-bit relaxed words per access (16-byte aligned); each word is its own
-// single-copy-atomic element.
-__device__ __forceinline__ void ld_relaxed_2xb64(const uint64_t* p, uint64_t& a, uint64_t& b) {
-    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
-
-__device__ __forceinline__ void st_relaxed_2xb64(uint64_t* p, uint64_t a, uint64_t b) {
-    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
-}
-
-// bar.red.and on named barrier `id`: true iff `pred` holds in every participating thread.
-__device__ __forceinline__ bool named_sync_and(uint32_t id, uint32_t nthreads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.and.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
 }
 
 // ---------------------------------------------------------------- global flags
