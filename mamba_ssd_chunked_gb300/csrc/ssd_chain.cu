@@ -35,17 +35,19 @@
 //
 // L for every (batch, block, group) is computed once by a small kernel
 // (chain_masks) into the workspace, and so is every job's table record (dt,
-// sub-block split, per-token factors; chain_tables); the chain kernel streams
-// both like inputs. The last table CTA also splits the jobs into one contiguous
-// range per chain CTA with equal estimated cost (a job costs more the more
-// sub-blocks it has), so that CTAs holding fast-decaying heads finish with the
-// rest.
+// sub-block split, per-token factors; chain_tables) with its estimated cost;
+// the chain kernel streams both like inputs. Each chain CTA takes the
+// contiguous job range that carries its share of the total cost (cta_range; a
+// job costs more the more sub-blocks it has), so that CTAs holding
+// fast-decaying heads finish with the rest. The three kernels are launched
+// with programmatic stream serialization.
 //
 // Roles (16 warps):
 //   warp 0       TMA producer: L, B and C through a ring of four slots
 //   warp 1       MMA issuer, state path: k3
 //   warp 2       MMA issuer, output path: k5a, k5b
-//   warp 3       TMA producer: X (2 job slots of two heads) and each job's table record
+//   warp 3       TMA producer: X (2 job slots of two heads) and each job's table
+//                record; L2 prefetch of the X two jobs ahead and of chain-start states
 //   warps 4..7   W from X in place
 //   warps 8..11  state: rescale Z, write H; load / store states at segment ends
 //   warps 12..15 epilogue: y from Y (TMEM) and W (shared memory), written over W
