@@ -1,11 +1,19 @@
 """Benchmark of the Mamba-2 SSD chunked-scan forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--path auto|tc|chain|simt] [--step | --conv | --norm]
 
 One step = one full forward (all five stages) over one batch of the
 workload's synthetic inputs, already resident in HBM. Prints one JSON line
 (rank 0). Under torchrun every rank runs the whole workload on its own GPU
 (independent replicas: the path has no exchange step), so scaling is weak.
+
+The roofline's achieved figure divides the algorithmic bytes by the main
+kernel's own mean launch time, which the library records with CUDA events
+in a separate pass (ssd_kernel_timing); path_achieved divides by the whole
+call. e2e goes through ssd_fwd_host with pinned host buffers. --step,
+--conv and --norm time the decode step, the conv1d + SiLU and the gated
+RMSNorm instead.
 
 --impl reference times the fp64 CPU oracle (the only reference arm: the
 pages ship no runnable implementation) on the host cores, on a bounded
