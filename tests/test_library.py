@@ -59,7 +59,13 @@ def _dims(**kw):
     return pkg.Dims(*[base[k] for k in ("batch", "seqlen", "nheads", "headdim", "ngroups", "dstate")])
 
 
-FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+# Every pointer handed to the library below is a real, writable buffer of at
+# least the size the call declares (host memory: this file runs without a
+# GPU). Validation rejects each call before any CUDA work; if that ever
+# changed, the damage would be a wrong return code or output, not a fault.
+_BUF = ctypes.create_string_buffer(8 << 20)
+FAKE = (ctypes.addressof(_BUF) + 15) // 16 * 16  # 16-byte aligned
+assert FAKE + 4 * 1024 * 1024 <= ctypes.addressof(_BUF) + len(_BUF)
 
 
 @pytest.mark.parametrize("bad", [
@@ -107,14 +113,14 @@ def test_unsupported_chunk_len(lib):
     rc = lib.ssd_fwd(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 512, 2, FAKE, None, None)
     assert rc == 2
     rc = lib.ssd_fwd_ws(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 64, 2, FAKE, None, 2,
-                        FAKE, 1 << 30, None)
+                        FAKE, 4 << 20, None)
     assert rc == 2  # the tensor-core path takes chunk_len 128 or 256 only
 
 
 def test_workspace_too_small(lib):
     d = _dims()
     need = lib.ssd_fwd_workspace_bytes(ctypes.byref(d), 1, 256, 2)
-    assert need > 0
+    assert 0 < need and need + 64 <= 4 << 20
     rc = lib.ssd_fwd_ws(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 2, FAKE, None, 2,
                         FAKE, need - 1, None)
     assert rc == 5

@@ -2,9 +2,9 @@
 memory (a memory manager owns the device, or cudaMalloc's possible device
 synchronisation is not allowed on their path). It runs the fused kernel on a
 fixed scratch array inside the library. Checked through the C ABI against
-ssd_fwd on two calls in a row (the second one finds the array as the first
-left it). This file sorts last so that a failure here comes after every
-other test has run."""
+ssd_fwd and against the fp64 oracle on two calls in a row (the second one
+finds the array as the first left it). This file sorts last so that a failure
+here comes after every other test has run."""
 import ctypes
 
 import numpy as np
@@ -13,6 +13,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 from forms import rel_err
+from gpu_util import TOL, oracle_full
 from mamba_ssd_chunked_gb300.inputs import make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -68,8 +69,12 @@ def test_noalloc_matches_ssd_fwd_on_two_calls(lib):
         fs = torch.full((b, h, p, n), float("nan"), dtype=torch.float32, device="cuda")
         assert _call(lib.ssd_fwd_noalloc, dims, t, y, fs, 256, stream) == 0
         assert lib.ssd_device_status(stream) == 0
-        assert rel_err(y.float().cpu().numpy(), y_ref.float().cpu().numpy()) < 2e-2
-        assert rel_err(fs.cpu().numpy(), f_ref.cpu().numpy()) < 2e-2
+        assert rel_err(y.float().cpu().numpy(), y_ref.float().cpu().numpy()) < TOL["bf16"]
+        assert rel_err(fs.cpu().numpy(), f_ref.cpu().numpy()) < TOL["bf16"]
+        # and against the fp64 oracle, so that a bias both GPU paths share would show
+        y_o, f_o = oracle_full(inp)
+        assert rel_err(y.float().cpu().numpy(), y_o) < TOL["bf16"]
+        assert rel_err(fs.cpu().numpy(), f_o) < TOL["bf16"]
 
 
 def test_noalloc_rejects_work_beyond_its_scratch(lib):
@@ -77,9 +82,19 @@ def test_noalloc_rejects_work_beyond_its_scratch(lib):
     # 4 x 80 chains at dstate 128 need 20 MiB of scratch, more than the 16 MiB array
     dims = pkg.Dims(4, 256, 80, 64, 1, 128)
     assert pkg.ssd_fwd_workspace_bytes(4, 256, 80, 64, 1, 128, "bf16", 256, "tc") > SCRATCH_BYTES
-    fake = 1 << 16
+    # real device buffers of the declared shapes: if the size check ever moved behind
+    # the launch, this would show as a wrong return code or output, not as a fault
+    b, L, h, p, g, n = 4, 256, 80, 64, 1, 128
+    x = torch.zeros((b, L, h, p), dtype=torch.bfloat16, device="cuda")
+    dt = torch.zeros((b, L, h), dtype=torch.float32, device="cuda")
+    hv = torch.zeros((h,), dtype=torch.float32, device="cuda")
+    A = -torch.ones((h,), dtype=torch.float32, device="cuda")
+    B = torch.zeros((b, L, g, n), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((b, L, g, n), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros_like(x)
+    torch.cuda.synchronize()
     c0 = pkg.ssd_kernel_launches()
-    rc = lib.ssd_fwd_noalloc(ctypes.byref(dims), 1, fake, fake, fake, fake, fake, fake, None, None, 256, 1, fake,
-                             None, None)
+    rc = lib.ssd_fwd_noalloc(ctypes.byref(dims), 1, x.data_ptr(), dt.data_ptr(), hv.data_ptr(), A.data_ptr(),
+                             B.data_ptr(), C.data_ptr(), None, None, 256, 1, y.data_ptr(), None, None)
     assert rc == 5  # SSD_ERR_WORKSPACE, before any launch
     assert pkg.ssd_kernel_launches() == c0
