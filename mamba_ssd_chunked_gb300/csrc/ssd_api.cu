@@ -49,6 +49,15 @@ unsigned long long wait_limit_ns() {
     return kDefaultWaitNs;
 }
 
+// Chain path warm-up mode (FwdArgs::chain_warmup). The environment variable
+// SSD_CHAIN_WARMUP (read at every call: 0, 1 or 2) overrides the default 1;
+// tests use 0 to force the hand-off path and 2 to force warm-ups.
+int chain_warmup_mode() {
+    const char* e = std::getenv("SSD_CHAIN_WARMUP");
+    if (e && (e[0] == '0' || e[0] == '1' || e[0] == '2') && e[1] == '\0') return e[0] - '0';
+    return 1;
+}
+
 ssd_status current_device(int* dev) {
     if (cudaGetDevice(dev) != cudaSuccess) return SSD_ERR_CUDA;
     if (*dev < 0 || *dev >= kMaxDevices) return SSD_ERR_UNSUPPORTED;
@@ -175,6 +184,7 @@ ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* d
     a.wait_limit_ns = wait_limit_ns();
     a.dt_min = dt_min;
     a.dt_max = dt_max;
+    a.chain_warmup = chain_warmup_mode();
     if (p == SSD_PATH_TC) return tc_forward(a, ws, ws_bytes);
     if (p == SSD_PATH_CHAIN) return chain_forward(a, ws, ws_bytes);
     return simt_forward(a, ws, ws_bytes);

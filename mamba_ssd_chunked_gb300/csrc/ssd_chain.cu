@@ -81,6 +81,14 @@ constexpr int kNumTabX = 2;             // per-token tables per (job, head) read
 enum TabX { TABX_CS = 0, TABX_DT = 1 }; // sub-block cumsum and dt (extreme sub-blocks)
 constexpr int kScal = 32;               // scalars per (job, head): ec[8], hs[8], is[8], D
 enum Scal { SC_EC = 0, SC_HS = 8, SC_IS = 16, SC_D = 24 };
+// A continuation segment may start from a zero state this many nats of decay
+// (both heads) before its first block instead of waiting for the previous CTA's
+// hand-off: what the zero start leaves out is scaled by e^{-44} < 2^-63.
+constexpr float kWarmupNats = 44.f;
+// Decay-sorted head pairs: the pair table is sorted when nheads and the
+// per-group sort stay this small (every table CTA sorts its own copy).
+constexpr int kSortMaxHeads = 1024;
+constexpr long long kSortMaxWork = 65536;  // nheads x heads per group
 constexpr int kThreads = 512;
 constexpr int kRing = 4;                // slots of the L / B / C ring
 // Per-job table record in the workspace: [2 heads][kNumTab][128] floats,
@@ -137,6 +145,10 @@ struct ChainParams {
     const __nv_bfloat16* masks;  // [b][nblk][G][t][s] bf16 L tiles (read again by the extreme path)
     const uint8_t* tables;       // [chain * nblk + block] table records
     const uint8_t* cost;         // [jobs] estimated job costs (cta_range); null: even split by count
+    const uint8_t* job_cost;     // [jobs] the same costs, always set (warm-up decision)
+    const float2* decay;         // [jobs] (head 0, head 1) decay of the whole block, in nats
+    const int* order;            // [H] heads in pair order: chain cb of a row is heads order[2 cb], order[2 cb + 1]
+    int warmup;                  // 0: never warm up, 1: when the hand-off would come late, 2: whenever possible
     float* handoff;              // [nCTA][2][P][N] fp32 states handed from CTA i to CTA i + 1
     uint32_t* ticket;            // CTA order counter
     uint32_t* flags;             // [nCTA]: 1 once CTA i's hand-off state is in place
@@ -149,16 +161,21 @@ struct ChainParams {
 
 // A job is one block of one chain. The CTA's jobs, in processing order (all
 // indices fit 31 bits: the host only launches when chains * blocks < 2^31).
+// The segment of chain cF (the head of the range, processed last) starts at
+// block a; with wu > 0 it is preceded by wu warm-up blocks that only advance
+// the state (no y), starting from a zero state (or from the initial state when
+// they reach back to block 0) instead of from the previous CTA's hand-off.
 struct JobList {
     int first, last;   // flat range [first, last) = chain * nblk + block
     int nblk;
     int cF, cL;        // first and last chain touched
     int nE, nM;        // lengths of the tail part (processed first) and of the full chains
-    __device__ int count() const { return last - first; }
+    int a, wu;         // first output block of chain cF's segment, warm-up blocks before it
+    __device__ int count() const { return last - first + wu; }
     __device__ __forceinline__ void at(int J, int& chain, int& blk, int& seg_lo, int& seg_hi) const {
         if (cF == cL) {
             chain = cF;
-            seg_lo = first - cF * nblk;
+            seg_lo = a - wu;
             blk = seg_lo + J;
             seg_hi = last - cF * nblk;
         } else if (J < nE) {
@@ -174,7 +191,7 @@ struct JobList {
             seg_hi = nblk;
         } else {
             chain = cF;
-            seg_lo = first - cF * nblk;
+            seg_lo = a - wu;
             blk = seg_lo + (J - nE - nM);
             seg_hi = nblk;
         }
@@ -190,21 +207,32 @@ __device__ __forceinline__ JobList make_jobs(const ChainParams& p, int first, in
     jl.cL = (jl.last - 1) / p.nblk;
     jl.nE = jl.last - jl.cL * p.nblk;
     jl.nM = (jl.cF == jl.cL) ? 0 : (jl.cL - jl.cF - 1) * p.nblk;
+    jl.a = jl.first - jl.cF * p.nblk;
+    jl.wu = 0;
     return jl;
 }
 
 struct JobPos {
     int blk, lo, hi;  // block, and the block range of the job's segment
-    int b, h0, g;     // batch row, first head, B/C group
+    int b, cb, g;     // batch row, chain (head pair) within the row, B/C group
+    int h[kHG];       // the pair's heads
+    bool warm;        // warm-up block: advances the state, writes no y
+    bool wait;        // the segment starts from the previous CTA's hand-off
 };
 
-__device__ __noinline__ JobPos job_pos(const JobList& jobs, int J, int chains_per_b, int HperG) {
+__device__ __forceinline__ JobPos job_pos(const JobList& jobs, int J, int chains_per_b, int HperG,
+                                       const int* __restrict__ order) {
     JobPos jp;
     int chain;
     jobs.at(J, chain, jp.blk, jp.lo, jp.hi);
     jp.b = chain / chains_per_b;
-    jp.h0 = (chain - jp.b * chains_per_b) * kHG;
-    jp.g = jp.h0 / HperG;
+    jp.cb = chain - jp.b * chains_per_b;
+    jp.g = (jp.cb * kHG) / HperG;  // pairs never straddle a group
+    jp.h[0] = __ldg(order + kHG * jp.cb);
+    jp.h[1] = __ldg(order + kHG * jp.cb + 1);
+    const bool seg_f = (chain == jobs.cF);
+    jp.warm = seg_f && jp.blk < jobs.a;
+    jp.wait = seg_f && jp.lo > 0 && jobs.wu == 0;
     return jp;
 }
 
@@ -316,7 +344,7 @@ __device__ __noinline__ void fixup_tokens(uint32_t ycol, uint32_t extreme, int q
 // starts after the job i whose cost interval (before, after] holds
 // T_c = ceil(c total / ncta), c in [1, ncta); T_c increases with c, so every
 // such c lands on exactly one job. With at least kBalanceMin jobs per CTA,
-// T_{c+1} - T_c >= 10 kBalanceMin - 1 exceeds any one job's cost (at most 108),
+// T_{c+1} - T_c >= 10 kBalanceMin - 1 exceeds any one job's cost (at most 110),
 // so no range is empty. Thread t sums the costs of a contiguous run of the
 // byte array, a block scan places each thread's run on the cost line, and the
 // thread whose run holds T_cta or T_cta+1 finds the job.
@@ -370,6 +398,79 @@ __device__ __noinline__ void cta_range(const uint8_t* cost, long long njob, long
         }
     }
     __syncthreads();
+}
+
+// Warm-up blocks before the segment of chain cF that starts at block a > 0 (one
+// warp; 0 = take the previous CTA's hand-off). The horizon m is the number of
+// blocks before a over which both heads decay by kWarmupNats (all of [0, a) if
+// they never do: then the warm-up starts from the chain's initial state and is
+// exact). Costs are in the job-cost units of cta_range. The hand-off is ready
+// no earlier than the chain's blocks [0, a) take when run one after another
+// (t_ready); this CTA needs it once the rest of its range is done (t_need, the
+// segment runs last). Waiting ends the range at t_ready + t_seg, warming up at
+// t_range + cost(warm-up): warm up when that is earlier (warmup = 1), or
+// always (warmup = 2). Every load of a pass over the bytes is issued before
+// the first sum, so the decision costs about one memory round trip per 128
+// jobs of the chain.
+__device__ __noinline__ int warmup_blocks(const ChainParams& prm, const JobList& jobs, int lane) {
+    const int a = jobs.a;
+    const long long base = static_cast<long long>(jobs.cF) * jobs.nblk;
+    // horizon: walk back from block a - 1, 32 blocks per step
+    int m = a;
+    float d0 = 0.f, d1 = 0.f;
+    for (int k0 = a - 1; k0 >= 0; k0 -= 32) {
+        const int k = k0 - lane;
+        float e0 = 0.f, e1 = 0.f;
+        if (k >= 0) {
+            const float2 e = __ldg(prm.decay + base + k);
+            e0 = e.x;
+            e1 = e.y;
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {  // inclusive scan: lane l sums blocks k0 - l .. k0
+            const float t0 = __shfl_up_sync(0xffffffffu, e0, o), t1 = __shfl_up_sync(0xffffffffu, e1, o);
+            if (lane >= o) {
+                e0 += t0;
+                e1 += t1;
+            }
+        }
+        const bool ok = k >= 0 && d0 + e0 >= kWarmupNats && d1 + e1 >= kWarmupNats;
+        const uint32_t hit = __ballot_sync(0xffffffffu, ok);
+        if (hit) {
+            m = a - (k0 - (__ffs(hit) - 1));
+            break;
+        }
+        d0 += __shfl_sync(0xffffffffu, e0, 31);
+        d1 += __shfl_sync(0xffffffffu, e1, 31);
+    }
+    if (prm.warmup == 2) return m;
+    // one pass over the cost bytes of [base, max(last, segment end)): every job
+    // byte falls into the sums it belongs to
+    const long long seg_end = jobs.cF == jobs.cL ? jobs.last : base + jobs.nblk;
+    const long long hi = max(static_cast<long long>(jobs.last), seg_end);
+    const long long wu0 = base + a - m;
+    uint32_t t_ready = 0, t_range = 0, t_seg = 0, t_wu = 0;
+    for (long long j0 = base & ~3ll; j0 < hi; j0 += 128) {
+        const long long j = j0 + 4 * lane;
+        const uint32_t v = j < hi ? __ldg(reinterpret_cast<const uint32_t*>(prm.job_cost + j)) : 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const long long q = j + e;
+            const uint32_t c = (v >> (8 * e)) & 0xffu;
+            if (q >= base && q < base + a) t_ready += c;
+            if (q >= wu0 && q < base + a) t_wu += c;
+            if (q >= jobs.first && q < jobs.last) t_range += c;
+            if (q >= jobs.first && q < seg_end) t_seg += c;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        t_ready += __shfl_xor_sync(0xffffffffu, t_ready, o);
+        t_wu += __shfl_xor_sync(0xffffffffu, t_wu, o);
+        t_range += __shfl_xor_sync(0xffffffffu, t_range, o);
+        t_seg += __shfl_xor_sync(0xffffffffu, t_seg, o);
+    }
+    return (t_range + t_wu < t_ready + t_seg) ? m : 0;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -431,10 +532,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         first = cta == 0 ? 0 : static_cast<int>(out[0]);
         last = cta == prm.ncta - 1 ? static_cast<int>(prm.total) : static_cast<int>(out[1]);
     }
-    const JobList jobs = make_jobs(prm, first, last);
+    JobList jobs = make_jobs(prm, first, last);
+    if (jobs.a > 0 && prm.warmup != 0) {
+        if (warp == 0) {
+            const int wu = warmup_blocks(prm, jobs, lane);
+            if (lane == 0) misc[6] = static_cast<uint32_t>(wu);
+        }
+        __syncthreads();
+        jobs.wu = static_cast<int>(misc[6]);
+    }
     const int njobs = jobs.count();
     const int HperG = prm.H / prm.G;
     const int chains_per_b = prm.H / kHG;
+    const int* order = prm.order;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer: L, B, C ring
@@ -446,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ru > 0) WB(B_R_EMPTY0 + rs, (ru - 1) & 1);
                 if (*abort_flag) break;
                 const int J = pr / 3, kind = pr - 3 * J;
-                const JobPos jp = job_pos(jobs, J, chains_per_b, HperG);
+                const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order);
                 uint64_t* fb = &bars[B_R_FULL0 + rs];
                 uint8_t* dst = smem + K::OFF_RING + rs * 2 * kTile;
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
@@ -509,13 +619,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int qs = kT / nq, ksub = 8 / nq;
                 const uint32_t yc = tmem + K::COL_Y + 128 * yb;
                 const int pl = 3 * J + RK_L, pc = 3 * J + RK_C;
+                const bool warm = job_pos(jobs, J, chains_per_b, HperG, order).warm;  // no output: no k5a / k5b
                 if (J >= 2) WB(B_Y_EMPTY0 + yb, ((J >> 1) - 1) & 1);  // the epilogue has read job J - 2
                 WB(B_W_FULL0 + xs, (J >> 1) & 1);
                 WB(B_R_FULL0 + pl % kRing, (pl / kRing) & 1);
                 ptx::tc_fence_after();
                 const uint64_t a_w = ptx::desc_sw128(sbase + K::OFF_XW + xs * 2 * kTile, kTile, 1024);
                 const uint32_t id_a = idesc_n(qs, true, false), id_b = idesc_n(qs, false, false);
-                for (int q = 0; q < nq; ++q) {
+                for (int q = 0; q < nq && !warm; ++q) {
                     if ((extreme >> q) & 1u) continue;
                     const uint64_t b_l =
                         ptx::desc_sw128(sbase + K::OFF_RING + (pl % kRing) * 2 * kTile + q * qs * 128, 16, 1024);
@@ -530,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     const uint64_t b_c =
                         ptx::desc_sw128(sbase + K::OFF_RING + (pc % kRing) * 2 * kTile + q * qs * 128, 16, 1024);
-                    mma_k5b(yc + q * qs, tmem + K::COL_H + 64 * hb, b_c, id_b, (~extreme >> q) & 1u);
+                    if (!warm) mma_k5b(yc + q * qs, tmem + K::COL_H + 64 * hb, b_c, id_b, (~extreme >> q) & 1u);
                     ptx::mma_commit(&bars[B_H_EMPTY0 + hb]);
                 }
                 ptx::mma_commit(&bars[B_R_EMPTY0 + pc % kRing]);
@@ -548,8 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ts = jx & (kTabSlots - 1);
                 if (jx >= kTabSlots) WB(B_TAB_EMPTY0 + ts, ((jx / kTabSlots) - 1) & 1);
                 if (*abort_flag) break;
-                const JobPos jp = job_pos(jobs, jx, chains_per_b, HperG);
-                const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.h0 / kHG) * prm.nblk + jp.blk;
+                const JobPos jp = job_pos(jobs, jx, chains_per_b, HperG, order);
+                const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.cb) * prm.nblk + jp.blk;
                 ptx::mbar_arrive_expect_tx(&bars[B_TAB_FULL0 + ts], kRecSmem);
                 ptx::bulk_load(smem + K::OFF_TAB + ts * kRecSmem, prm.tables + rec * kRecBytes, kRecSmem,
                                &bars[B_TAB_FULL0 + ts]);
@@ -559,16 +670,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint64_t* fb = &bars[B_X_FULL0 + (jx & 1)];
                 uint8_t* dst = smem + K::OFF_XW + (jx & 1) * 2 * kTile;
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
-                ptx::tma_load_4d(dst, &tm_x, fb, 0, jp.h0, jp.blk * kT, jp.b);
-                ptx::tma_load_4d(dst + kTile, &tm_x, fb, 0, jp.h0 + 1, jp.blk * kT, jp.b);
-                if (jp.blk == 0 && prm.init)  // a chain start: its initial state into L2 for the state warps
-                    ptx::bulk_prefetch_l2(prm.init + (static_cast<size_t>(jp.b) * prm.H + jp.h0) * kP * kN,
-                                          kHG * kP * kN * sizeof(float));
+                ptx::tma_load_4d(dst, &tm_x, fb, 0, jp.h[0], jp.blk * kT, jp.b);
+                ptx::tma_load_4d(dst + kTile, &tm_x, fb, 0, jp.h[1], jp.blk * kT, jp.b);
+                if (jp.blk == 0 && prm.init)  // a chain start: its initial states into L2 for the state warps
+                    for (int j = 0; j < kHG; ++j)
+                        ptx::bulk_prefetch_l2(prm.init + (static_cast<size_t>(jp.b) * prm.H + jp.h[j]) * kP * kN,
+                                              kP * kN * sizeof(float));
                 if (jx + 2 < njobs) {
                     // the X of job jx + 2 into L2: its load, once the slot is free, then hits L2
-                    const JobPos jn = job_pos(jobs, jx + 2, chains_per_b, HperG);
-                    ptx::tma_prefetch_4d(&tm_x, 0, jn.h0, jn.blk * kT, jn.b);
-                    ptx::tma_prefetch_4d(&tm_x, 0, jn.h0 + 1, jn.blk * kT, jn.b);
+                    const JobPos jn = job_pos(jobs, jx + 2, chains_per_b, HperG, order);
+                    ptx::tma_prefetch_4d(&tm_x, 0, jn.h[0], jn.blk * kT, jn.b);
+                    ptx::tma_prefetch_4d(&tm_x, 0, jn.h[1], jn.blk * kT, jn.b);
                 }
             }
             for (int i = 0; i < 2 && i < jx; ++i) {
@@ -627,10 +739,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sdone = 0, u = 0;
         for (int J = 0; J < njobs; ++J) {
             const int ts = J & (kTabSlots - 1);
-            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG);
+            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order);
             const bool seg_start = (jp.blk == jp.lo), seg_end = (jp.blk == jp.hi - 1);
-            const int h = jp.h0 + j;
-            if (seg_start && jp.lo > 0) {
+            const int h = jp.h[j];
+            if (seg_start && jp.wait) {
                 // wait for the previous CTA's hand-off of this chain's state
                 if (st == 0) {
                     const uint32_t* f = prm.flags + (cta - 1);
@@ -652,8 +764,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* sc = S(ts, j);
             const float* src = nullptr;  // segment start: the incoming state row [n]
             if (seg_start) {
-                if (jp.lo > 0)
+                if (jp.wait)
                     src = misc[2] ? nullptr : prm.handoff + ((static_cast<size_t>(cta - 1) * kHG + j) * kP + p) * kN;
+                else if (jp.lo > 0)
+                    src = nullptr;  // warm-up from a zero state
                 else if (prm.init)
                     src = prm.init + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * kN;
                 inv_prev = 1.f;
@@ -766,10 +880,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2* g2 = reinterpret_cast<const float2*>(T(ts, j, TAB_UG));
             const uint32_t extreme = JW(ts)[1];
             const bool rare = (extreme | JW(ts)[2]) != 0u;
-            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG);
+            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order);
             WB(B_Y_FULL0 + yb, (J >> 1) & 1);
             WB(B_XW_FREE0 + xs, (J >> 1) & 1);  // k3 and k5a no longer read W
             ptx::tc_fence_after();
+            if (jp.warm) {
+                // a warm-up block has no output: hand the accumulator, the slot and the
+                // table record straight back
+                warp_arrive(&bars[B_Y_EMPTY0 + yb], lane);
+                if (et == 0) ptx::mbar_arrive(&bars[B_XW_EMPTY0 + xs]);
+                warp_arrive(&bars[B_TAB_EMPTY0 + ts], lane);
+                continue;
+            }
             const uint32_t tile = sbase + K::OFF_XW + (xs * kHG + j) * kTile;
 #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
@@ -812,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::named_sync(3, 128);
             if (et == 0) {
                 for (int jj = 0; jj < kHG; ++jj)
-                    ptx::tma_store_4d(&tm_y, smem + K::OFF_XW + (xs * kHG + jj) * kTile, 0, jp.h0 + jj,
+                    ptx::tma_store_4d(&tm_y, smem + K::OFF_XW + (xs * kHG + jj) * kTile, 0, jp.h[jj],
                                       jp.blk * kT, jp.b);
                 ptx::bulk_commit_group();
                 ptx::bulk_wait_group_read0();
@@ -829,8 +951,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int p = et & 63;
                 const long long t0 = static_cast<long long>(jp.blk) * kT;
                 const int tn = static_cast<int>(min(static_cast<long long>(kT), prm.L - t0));  // valid tokens
-                const long long off = ((static_cast<long long>(jp.b) * prm.L + t0) * prm.H + jp.h0 + j) * kP + p;
-                const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.h0 / kHG) * prm.nblk + jp.blk;
+                const long long off = ((static_cast<long long>(jp.b) * prm.L + t0) * prm.H + jp.h[j]) * kP + p;
+                const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.cb) * prm.nblk + jp.blk;
                 const float* xt = reinterpret_cast<const float*>(prm.tables + rec * kRecBytes + kRecSmem) +
                                   j * kNumTabX * kT;
                 const __nv_bfloat16* lg =
@@ -859,20 +981,23 @@ struct TableParams {
     const float* D;
     uint8_t* out;      // [chain * nblk + block] table records
     uint8_t* cost;       // [jobs] estimated job costs (cta_range)
+    float2* decay;       // [jobs] decay of the whole block per head (warm-up horizon)
     uint32_t* counters;  // the chain kernel's ticket and flags, zeroed here
     int ncounters;
+    int* order;          // [H] heads in pair order (written by CTA 0)
+    int sort_pairs;      // pair the heads of each group by decay rate (else 2 cb, 2 cb + 1)
     long long L;
-    int H, nblk, chains_per_b, total;
+    int H, G, nblk, chains_per_b, total;
     float dt_min, dt_max;
 };
 
 // Estimated cost of a job in the chain kernel, in units of a tenth of a
-// whole-block job: measured per-job times on the 2.7B shape put a job split in
-// two sub-blocks at 1.1 and one split in four at 2.1 whole-block jobs; eight
-// sub-blocks, extreme sub-blocks (CUDA-core intra-block sum) and the tiny-W
-// fix-up pass are weighted by their extra work. At most 10 + 30 + 64 + 4 = 108.
+// whole-block job: measured per-job periods on the 2.7B shape put a job split
+// in two sub-blocks at 1.3 whole-block jobs; four and eight sub-blocks,
+// extreme sub-blocks (CUDA-core intra-block sum) and the tiny-W fix-up pass are
+// weighted by their extra state round trips and work. At most 10 + 32 + 64 + 4 = 110.
 __device__ __forceinline__ uint32_t job_cost(int nq, uint32_t extreme, int tiny) {
-    const uint32_t split = nq == 2 ? 1u : nq == 4 ? 11u : nq == 8 ? 30u : 0u;
+    const uint32_t split = nq == 2 ? 3u : nq == 4 ? 13u : nq == 8 ? 32u : 0u;
     return 10u + split + 8u * static_cast<uint32_t>(__popc(extreme)) + (tiny ? 4u : 0u);
 }
 
@@ -884,22 +1009,56 @@ constexpr int kBalanceMin = 20;  // cost balancing from this many jobs per chain
 // split (the largest of 128, 64, 32, 16 tokens whose decays all stay within
 // kMaxSubDecay; 16-token sub-blocks beyond it are extreme), then per token the
 // W factor, the epilogue factors u and D / wf, the sub-block-relative cumsum
-// and dt, and per sub-block the state scales e^{c}, the H scale and 1 / sigma.
+// and dt, and per sub-block the state scales e^{c}, the H scale and 1 / sigma;
+// besides the record, the job's cost and its block decay per head (the warm-up horizon).
+//
+// Head pairs: within each B/C group the heads are ranked by their decay rate
+// clamp(softplus(dt_bias)) * (-A) and paired rank 2i with rank 2i + 1, so that
+// fast-decaying heads (whose blocks split into sub-blocks) share chains and a
+// slowly decaying head is not tied to them. Every CTA ranks the heads itself
+// (nheads x heads-per-group comparisons); CTA 0 also stores the order for the
+// chain kernel. The pairing only schedules: each head's result is its own.
 // At most 56 registers so that 9 CTAs fit an SM: 1280 CTAs of the 2.7B shape in one wave.
 __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
+    __shared__ float s_key[kSortMaxHeads];
+    __shared__ int s_order[kSortMaxHeads];
     // launched early behind the previous kernel of the stream (which may still use the
     // workspace or write the inputs): nothing is touched before it completes
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();  // chain_masks does not read the tables until its end
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < prm.ncounters; i += blockDim.x) prm.counters[i] = 0u;
+    if (prm.sort_pairs) {
+        const int r = prm.H / prm.G;
+        for (int h = threadIdx.x; h < prm.H; h += blockDim.x) {
+            const float sp = fminf(fmaxf(softplus_f(__ldg(prm.dt_bias + h)), prm.dt_min), prm.dt_max);
+            const float k = sp * -__ldg(prm.A + h);
+            s_key[h] = (k == k) ? k : __int_as_float(0x7f800000);  // NaN ranks as +inf
+        }
+        __syncthreads();
+        for (int h = threadIdx.x; h < prm.H; h += blockDim.x) {
+            const int g0 = (h / r) * r;
+            const float kh = s_key[h];
+            int rank = 0;
+            for (int i = g0; i < g0 + r; ++i) {
+                const float ki = s_key[i];
+                rank += (ki < kh || (ki == kh && i < h)) ? 1 : 0;  // (key, head) is a strict total order
+            }
+            s_order[g0 + rank] = h;
+        }
+        __syncthreads();
+    }
+    if (blockIdx.x == 0)
+        for (int h = threadIdx.x; h < prm.H; h += blockDim.x) prm.order[h] = prm.sort_pairs ? s_order[h] : h;
     const int wl = threadIdx.x & 31;
     // one warp per job (job indices fit 31 bits: the host launches only then)
     const int job = static_cast<int>(blockIdx.x) * 4 + static_cast<int>(threadIdx.x >> 5);
     if (job < prm.total) {
         const int blk = job % prm.nblk;
         const int chain = job / prm.nblk;
-        const int b = chain / prm.chains_per_b, h0 = (chain % prm.chains_per_b) * kHG;
+        const int b = chain / prm.chains_per_b, cb = chain % prm.chains_per_b;
+        const int hh[kHG] = {prm.sort_pairs ? s_order[kHG * cb] : kHG * cb,
+                             prm.sort_pairs ? s_order[kHG * cb + 1] : kHG * cb + 1};
         uint8_t* rec = prm.out + static_cast<size_t>(job) * kRecBytes;
         float* tabs = reinterpret_cast<float*>(rec);
         float* scal = reinterpret_cast<float*>(rec + kRecTab);
@@ -911,15 +1070,15 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
         // lane wl owns tokens 4 wl .. 4 wl + 3 of the block (one 16-token unit); every
         // global load is issued here, before the first store
         const int tg0 = blk * kT + 4 * wl;
-        const float2 bias = __ldg(reinterpret_cast<const float2*>(prm.dt_bias + h0));
-        const float2 a2 = __ldg(reinterpret_cast<const float2*>(prm.A + h0));
-        const float2 d2 = prm.D ? __ldg(reinterpret_cast<const float2*>(prm.D + h0)) : make_float2(0.f, 0.f);
+        const float2 bias = make_float2(__ldg(prm.dt_bias + hh[0]), __ldg(prm.dt_bias + hh[1]));
+        const float2 a2 = make_float2(__ldg(prm.A + hh[0]), __ldg(prm.A + hh[1]));
+        const float2 d2 = prm.D ? make_float2(__ldg(prm.D + hh[0]), __ldg(prm.D + hh[1])) : make_float2(0.f, 0.f);
         float2 raw[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            raw[i] = tg0 + i < prm.L ? __ldg(reinterpret_cast<const float2*>(
-                                           prm.dt + (static_cast<long long>(b) * prm.L + (tg0 + i)) * prm.H + h0))
-                                     : make_float2(0.f, 0.f);
+        for (int i = 0; i < 4; ++i) {
+            const float* row = prm.dt + (static_cast<long long>(b) * prm.L + (tg0 + i)) * prm.H;
+            raw[i] = tg0 + i < prm.L ? make_float2(__ldg(row + hh[0]), __ldg(row + hh[1])) : make_float2(0.f, 0.f);
+        }
         float dtv[kHG][4], cs[kHG][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -1037,6 +1196,7 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
             jw[2] = any_tiny ? 1u : 0u;  // some valid token has wf < kTinyWF
             jw[3] = 0u;
             prm.cost[job] = static_cast<uint8_t>(job_cost(nq, extreme, any_tiny));
+            prm.decay[job] = make_float2(-bnd[0][7], -bnd[1][7]);  // cumsum at the block's last token
         }
     }
 }
@@ -1129,7 +1289,7 @@ int sm_count() {
 
 struct ChainPlan {
     int ncta;
-    long long nchains, nblk, total, ntiles;
+    long long nchains, nblk, total, ntiles, nheads;
 };
 
 ChainPlan plan(const ssd_dims& d, int nsm) {
@@ -1139,6 +1299,7 @@ ChainPlan plan(const ssd_dims& d, int nsm) {
     p.total = p.nchains * p.nblk;
     p.ncta = static_cast<int>(std::min<long long>(nsm, p.total));
     p.ntiles = d.batch * p.nblk * d.ngroups;
+    p.nheads = d.nheads;
     return p;
 }
 
@@ -1152,9 +1313,11 @@ size_t handoff_bytes(int ncta) {
 size_t masks_bytes(long long ntiles) { return align_up(static_cast<size_t>(ntiles) * kT * kT * 2, kWorkspaceAlign); }
 size_t tables_bytes(long long jobs) { return align_up(static_cast<size_t>(jobs) * kRecBytes, kWorkspaceAlign); }
 size_t costs_bytes(long long jobs) { return align_up(static_cast<size_t>(jobs), kWorkspaceAlign); }
+size_t order_bytes(long long heads) { return align_up(static_cast<size_t>(heads) * sizeof(int), kWorkspaceAlign); }
+size_t decay_bytes(long long jobs) { return align_up(static_cast<size_t>(jobs) * sizeof(float2), kWorkspaceAlign); }
 size_t chain_ws_bytes(const ChainPlan& pl) {
     return counters_bytes(pl.ncta) + handoff_bytes(pl.ncta) + masks_bytes(pl.ntiles) + tables_bytes(pl.total) +
-           costs_bytes(pl.total);
+           costs_bytes(pl.total) + order_bytes(pl.nheads) + decay_bytes(pl.total);
 }
 
 ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
@@ -1166,6 +1329,8 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     uint8_t* tables =
         static_cast<uint8_t*>(ws) + counters + handoff_bytes(pl.ncta) + masks_bytes(pl.ntiles);
     uint8_t* costs = tables + tables_bytes(pl.total);
+    int* order = reinterpret_cast<int*>(costs + costs_bytes(pl.total));
+    float2* decay = reinterpret_cast<float2*>(reinterpret_cast<char*>(order) + order_bytes(pl.nheads));
     CUtensorMap tx, tb, tc, tl, ty;
     if (!make_map_bf16(&tx, a.x, d.headdim, d.nheads, d.seqlen, d.batch) ||
         !make_map_bf16(&tb, a.B, d.dstate, d.ngroups, d.seqlen, d.batch) ||
@@ -1183,6 +1348,7 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     tp.D = a.D;
     tp.out = tables;
     tp.cost = costs;
+    tp.decay = decay;
     tp.L = d.seqlen;
     tp.H = static_cast<int>(d.nheads);
     tp.nblk = static_cast<int>(pl.nblk);
@@ -1192,6 +1358,9 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     tp.total = static_cast<int>(pl.total);
     tp.counters = static_cast<uint32_t*>(ws);
     tp.ncounters = 1 + pl.ncta;
+    tp.order = order;
+    tp.G = static_cast<int>(d.ngroups);
+    tp.sort_pairs = (d.nheads <= kSortMaxHeads && d.nheads * (d.nheads / d.ngroups) <= kSortMaxWork) ? 1 : 0;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1231,6 +1400,10 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     p.ticket = ctr;
     p.flags = ctr + 1;
     p.cost = balance ? costs : nullptr;
+    p.job_cost = costs;
+    p.decay = decay;
+    p.order = order;
+    p.warmup = a.chain_warmup;
     p.handoff = handoff;
     p.status = a.status_word;
     p.batch = static_cast<int>(d.batch);

@@ -31,6 +31,10 @@ struct FwdArgs {
     unsigned long long wait_limit_ns;  // per-wait wall-clock limit on the device
     float dt_min = 0.f;                // softplus(dt + dt_bias) is clamped to [dt_min, dt_max]
     float dt_max = __builtin_inff();
+    // chain path: where a chain crosses into this CTA, recompute its state over the
+    // blocks it takes to decay away instead of waiting for the previous CTA's hand-off:
+    // 0 never, 1 when the hand-off would come late, 2 whenever possible
+    int chain_warmup = 1;
 };
 
 // CUDA-core path: the five stages at exactly chunk_len, chunk states in workspace.
