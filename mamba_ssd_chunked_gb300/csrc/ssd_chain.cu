@@ -992,12 +992,13 @@ struct TableParams {
 };
 
 // Estimated cost of a job in the chain kernel, in units of a tenth of a
-// whole-block job: measured per-job periods on the 2.7B shape put a job split
-// in two sub-blocks at 1.3 whole-block jobs; four and eight sub-blocks,
-// extreme sub-blocks (CUDA-core intra-block sum) and the tiny-W fix-up pass are
-// weighted by their extra state round trips and work. At most 10 + 32 + 64 + 4 = 110.
+// whole-block job: a regression of measured per-job periods on the 2.7B shape
+// on the job mix puts a job split in two sub-blocks at 1.3 and one split in four
+// at 1.9 whole-block jobs; eight sub-blocks, extreme sub-blocks (CUDA-core
+// intra-block sum) and the tiny-W fix-up pass are weighted by their extra state
+// round trips and work. At most 10 + 32 + 64 + 4 = 110.
 __device__ __forceinline__ uint32_t job_cost(int nq, uint32_t extreme, int tiny) {
-    const uint32_t split = nq == 2 ? 3u : nq == 4 ? 13u : nq == 8 ? 32u : 0u;
+    const uint32_t split = nq == 2 ? 3u : nq == 4 ? 9u : nq == 8 ? 32u : 0u;
     return 10u + split + 8u * static_cast<uint32_t>(__popc(extreme)) + (tiny ? 4u : 0u);
 }
 
