@@ -45,7 +45,7 @@ def _load(path: str) -> ctypes.CDLL:
     f = lib.ssd_oracle_recurrence
     f.restype = ctypes.c_int
     i64, fp = ctypes.c_int64, ctypes.c_void_p
-    f.argtypes = [i64] * 6 + [fp] * 8 + [i64, fp, fp, fp, fp, ctypes.c_int, ctypes.c_double, ctypes.c_double]
+    f.argtypes = [i64] * 6 + [fp] * 8 + [i64, fp, fp, fp, fp, ctypes.c_int, ctypes.c_double, ctypes.c_double, fp]
     return lib
 
 
@@ -83,11 +83,17 @@ def recurrence(
     want_y: bool = True,
     lib: Optional[ctypes.CDLL] = None,
     dt_limit: Tuple[float, float] = (0.0, float("inf")),
+    seq_idx: Optional[np.ndarray] = None,
 ) -> Tuple[Optional[np.ndarray], np.ndarray]:
     """Run the fp64 recurrence.
 
     ``dt_limit`` = (lo, hi) clamps softplus(dt + dt_bias) like torch.clamp
     (fla "mamba2.py", the time_step_limit clamp; (0, inf) is no clamp).
+
+    ``seq_idx`` [b, L] (int32) packs several sequences into a row: the state
+    restarts from zero wherever seq_idx changes between consecutive tokens
+    (fla "mamba2.py" passes seq_idx to the fused chunked scan; reading of the
+    packed-sequence case).
 
     Shapes: x [b,L,h,p], dt [b,L,h] (raw), dt_bias [h], A [h], B/C [b,L,g,n],
     D [h] or None, init_state [b,h,p,n] or None.
@@ -99,6 +105,10 @@ def recurrence(
     x, dt, dt_bias, A, B, C = (_f32(v) for v in (x, dt, dt_bias, A, B, C))
     D, init_state = _f32(D), _f32(init_state)
     b, L, h, p = x.shape
+    if seq_idx is not None:
+        seq_idx = np.ascontiguousarray(seq_idx, dtype=np.int32)
+        if seq_idx.shape != (b, L):
+            raise ValueError(f"seq_idx must be [{b}, {L}], got {seq_idx.shape}")
     g, n = B.shape[2], B.shape[3]
     full = chains is None
     if full:
@@ -114,7 +124,7 @@ def recurrence(
         b, L, h, p, g, n,
         _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
         k, _ptr(sel_b), _ptr(sel_h), _ptr(y_sel), _ptr(final_sel), int(nthreads),
-        float(dt_limit[0]), float(dt_limit[1]))
+        float(dt_limit[0]), float(dt_limit[1]), _ptr(seq_idx))
     if rc != 0:
         raise RuntimeError(f"ssd_oracle_recurrence failed with code {rc}")
     if not full:

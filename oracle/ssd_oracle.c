@@ -10,6 +10,7 @@
  *
  *   s_{-1}  = init_state[b,h]                 (zeros when init_state is NULL)
  *   for t = 0 .. L-1:
+ *     if seq_idx given and t > 0 and seq_idx[b,t] != seq_idx[b,t-1]: s_{t-1} = 0
  *     delta_t = clamp(softplus(dt[b,t,h] + dt_bias[h]), dt_min, dt_max)
  *     s_t     = exp(delta_t * A[h]) * s_{t-1} + delta_t * x[b,t,h,:] (outer) B[b,t,g,:]
  *     y[b,t,h,:] = s_t . C[b,t,g,:] + D[h] * x[b,t,h,:]
@@ -28,6 +29,13 @@
  *     passes on as dt_limit.
  *   - Group map head -> group = head / (nheads/ngroups): burn-mamba
  *     "mamba2/ssd/serial.rs", ssd_serial (heads_per_group).
+ *   - seq_idx (packed sequences): flash-linear-attention "fla/layers/mamba2.py"
+ *     passes seq_idx to the fused chunked scan, the one place it appears; the
+ *     pages never spell out what it does. Reading taken: tokens of one row
+ *     whose seq_idx differ belong to different sequences, so no state crosses
+ *     a change of seq_idx between consecutive tokens: the state restarts from
+ *     zero there. init_state is the state before the row's first token (its
+ *     first sequence); final_state is the state after the row's last token.
  *
  * Precision: inputs are fp32 arrays (bf16 inputs arrive widened, exactly);
  * every operation is done in fp64. softplus(v) = log1p(exp(v)), evaluated as
@@ -42,6 +50,7 @@
 typedef struct {
     int64_t batch, seqlen, nheads, headdim, ngroups, dstate;
     const float *x, *dt, *dt_bias, *A, *B, *C, *D, *init_state;
+    const int32_t *seq_idx; /* [batch, seqlen] or NULL */
     double dt_min, dt_max;
     int64_t nsel;
     const int64_t *sel_b, *sel_h;
@@ -72,7 +81,10 @@ static void run_chain(const oracle_job *j, int64_t k, double *s) {
     }
 
     double *y = j->y_sel ? j->y_sel + k * L * P : NULL;
+    const int32_t *seq = j->seq_idx ? j->seq_idx + b * L : NULL;
     for (int64_t t = 0; t < L; ++t) {
+        if (seq && t > 0 && seq[t] != seq[t - 1])
+            memset(s, 0, sizeof(double) * (size_t)(P * N)); /* a new sequence starts from zero */
         double delta = softplus((double)j->dt[(b * L + t) * H + h] + bias_h);
         if (delta < j->dt_min) delta = j->dt_min;
         if (delta > j->dt_max) delta = j->dt_max;
@@ -112,7 +124,9 @@ static void *worker(void *arg) {
 
 /*
  * Runs the recurrence for the selected (b, h) chains (every token of each),
- * with softplus(dt + dt_bias) clamped to [dt_min, dt_max] (0, INFINITY: none).
+ * with softplus(dt + dt_bias) clamped to [dt_min, dt_max] (0, INFINITY: none)
+ * and, when seq_idx [batch, seqlen] is given, the state reset to zero wherever
+ * seq_idx changes between consecutive tokens of a row.
  * Returns 0 on success, -1 on invalid arguments, -2 on allocation/thread failure.
  * y_sel or final_sel may be NULL to skip that output.
  */
@@ -123,7 +137,7 @@ int ssd_oracle_recurrence(int64_t batch, int64_t seqlen, int64_t nheads, int64_t
                           const float *init_state,
                           int64_t nsel, const int64_t *sel_b, const int64_t *sel_h,
                           double *y_sel, double *final_sel, int nthreads,
-                          double dt_min, double dt_max) {
+                          double dt_min, double dt_max, const int32_t *seq_idx) {
     if (batch < 1 || seqlen < 1 || nheads < 1 || headdim < 1 || ngroups < 1 || dstate < 1)
         return -1;
     if (nheads % ngroups != 0) return -1;
@@ -137,6 +151,7 @@ int ssd_oracle_recurrence(int64_t batch, int64_t seqlen, int64_t nheads, int64_t
     j.ngroups = ngroups; j.dstate = dstate;
     j.x = x; j.dt = dt; j.dt_bias = dt_bias; j.A = A; j.B = B; j.C = C; j.D = D;
     j.init_state = init_state;
+    j.seq_idx = seq_idx;
     j.dt_min = dt_min; j.dt_max = dt_max;
     j.nsel = nsel; j.sel_b = sel_b; j.sel_h = sel_h;
     j.y_sel = y_sel; j.final_sel = final_sel;

@@ -41,9 +41,13 @@ def _expand_groups(M: np.ndarray, nheads: int) -> np.ndarray:
     return np.repeat(M, r, axis=2)
 
 
-def quadratic(x, dt, dt_bias, A, B, C, D=None, init_state=None, dt_limit=None) -> Tuple[np.ndarray, np.ndarray]:
+def quadratic(x, dt, dt_bias, A, B, C, D=None, init_state=None, dt_limit=None,
+              seq_idx=None) -> Tuple[np.ndarray, np.ndarray]:
     """Brute-force semiseparable form in fp64 (O(L^2) per chain: tiny inputs only).
-    dt_limit = (lo, hi) bounds the softplus output with np.clip."""
+    dt_limit = (lo, hi) bounds the softplus output with np.clip. seq_idx [b, L]
+    packs sequences into a row: token s reaches token t only if seq_idx does
+    not change anywhere between them (no k in s+1..t with seq[k] != seq[k-1]),
+    and the initial state only reaches tokens before the row's first change."""
     x = np.asarray(x, np.float64)
     b, L, h, p = x.shape
     n = B.shape[3]
@@ -56,12 +60,19 @@ def quadratic(x, dt, dt_bias, A, B, C, D=None, init_state=None, dt_limit=None) -
     y = np.zeros((b, L, h, p))
     final = np.zeros((b, h, p, n))
     for bi in range(b):
+        seq = None if seq_idx is None else np.asarray(seq_idx[bi])
+
+        def cut(lo, hi_):  # a sequence boundary at some k in lo..hi_ (inclusive)
+            return seq is not None and any(seq[k] != seq[k - 1] for k in range(max(lo, 1), hi_ + 1))
+
         for hi in range(h):
             dA = delta[bi, :, hi] * A[hi]
             s0 = np.zeros((p, n)) if init_state is None else np.asarray(init_state[bi, hi], np.float64)
             for t in range(L):
                 acc = np.zeros(p)
                 for s in range(t + 1):
+                    if cut(s + 1, t):
+                        continue
                     expo = 0.0
                     for k in range(s + 1, t + 1):
                         expo += dA[k]
@@ -70,13 +81,16 @@ def quadratic(x, dt, dt_bias, A, B, C, D=None, init_state=None, dt_limit=None) -
                 expo0 = 0.0
                 for k in range(0, t + 1):
                     expo0 += dA[k]
-                acc += np.exp(expo0) * (s0 @ Ch[bi, t, hi])
+                if not cut(1, t):
+                    acc += np.exp(expo0) * (s0 @ Ch[bi, t, hi])
                 if D is not None:
                     acc += float(D[hi]) * x[bi, t, hi]
                 y[bi, t, hi] = acc
             # final state: the same weights with t = L - 1, without the C readout
             fs = np.zeros((p, n))
             for s in range(L):
+                if cut(s + 1, L - 1):
+                    continue
                 expo = 0.0
                 for k in range(s + 1, L):
                     expo += dA[k]
@@ -84,7 +98,7 @@ def quadratic(x, dt, dt_bias, A, B, C, D=None, init_state=None, dt_limit=None) -
             expo0 = 0.0
             for k in range(L):
                 expo0 += dA[k]
-            final[bi, hi] = fs + np.exp(expo0) * s0
+            final[bi, hi] = fs + (0.0 if cut(1, L - 1) else np.exp(expo0)) * s0
     return y, final
 
 
