@@ -6,6 +6,7 @@
  *
  *   delta[b,t,h] = softplus(dt[b,t,h] + dt_bias[h])   (ssd_fwd_ex / ssd_step_ex: clamped, ssd_dt_limit)
  *   s_{-1}       = init_state[b,h]        (zeros when init_state == NULL)
+ *   s_{t-1}      = 0 where seq_idx[b,t] != seq_idx[b,t-1], t > 0   (ssd_fwd_ex with seq_idx only)
  *   s_t          = exp(delta[b,t,h] A[h]) s_{t-1} + delta[b,t,h] x[b,t,h,:] (outer) B[b,t,g(h),:]
  *   y[b,t,h,:]   = s_t C[b,t,g(h),:] + D[h] x[b,t,h,:]           (D == NULL: no skip)
  *   final_state[b,h] = s_{L-1}
@@ -137,17 +138,29 @@ SSD_API ssd_status ssd_fwd_ws(const ssd_dims* dims, ssd_dtype io_dtype,
                       ssd_path path, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * ssd_fwd_ex -- ssd_fwd with a dt limit and an optional explicit path and
- * workspace: dt_limit NULL means no clamp (SSD_ERR_INVALID_ARG when
- * dt_min < 0, dt_max < dt_min or either is NaN); workspace NULL means the
- * library-owned workspace (as ssd_fwd, path honoured), else a caller
- * workspace under the rules of ssd_fwd_ws. Everything else as ssd_fwd.
+ * ssd_fwd_ex -- ssd_fwd with a dt limit, packed sequences, and an optional
+ * explicit path and workspace (fla "fla/layers/mamba2.py": the dt_limit and
+ * seq_idx arguments of the fused chunked-scan call).
+ *
+ * dt_limit        NULL: no clamp; else delta = min(max(softplus(..), dt_min), dt_max)
+ *                 (SSD_ERR_INVALID_ARG when dt_min < 0, dt_max < dt_min or either is NaN).
+ * seq_idx         NULL, or device [batch, seqlen] int32 (4-byte aligned; else
+ *                 SSD_ERR_UNSUPPORTED): several sequences packed into each row.
+ *                 Wherever seq_idx changes between consecutive tokens of a row
+ *                 the state restarts from zero (no state crosses; any int32
+ *                 values, increasing or not). init_state is the state before
+ *                 the row's first token and final_state the state after its
+ *                 last. The pages pass seq_idx but do not define it further;
+ *                 this is the reading taken.
+ * workspace       NULL: the library-owned workspace (as ssd_fwd, path
+ *                 honoured); else a caller workspace under the rules of ssd_fwd_ws.
+ * Everything else as ssd_fwd.
  */
 SSD_API ssd_status ssd_fwd_ex(const ssd_dims* dims, ssd_dtype io_dtype,
                               const void* x, const float* dt, const float* dt_bias, const float* A,
                               const void* B, const void* C, const float* D, const float* init_state,
                               int chunk_len, int ngroups, void* y, float* final_state,
-                              const ssd_dt_limit* dt_limit, ssd_path path,
+                              const ssd_dt_limit* dt_limit, const int32_t* seq_idx, ssd_path path,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes ssd_fwd_ws needs for these arguments (0 if they are invalid). */

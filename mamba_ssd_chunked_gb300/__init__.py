@@ -90,7 +90,7 @@ def library() -> ctypes.CDLL:
     lib.ssd_step.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, vp, vp]
     plim = ctypes.POINTER(DtLimit)
     lib.ssd_fwd_ex.restype = i
-    lib.ssd_fwd_ex.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, i, vp, fp, plim, i, vp, ctypes.c_size_t,
+    lib.ssd_fwd_ex.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, i, vp, fp, plim, vp, i, vp, ctypes.c_size_t,
                                vp]
     lib.ssd_step_ex.restype = i
     lib.ssd_step_ex.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, vp, plim, vp]
@@ -165,9 +165,11 @@ def _check_all(x, dt, dt_bias, A, B, C, D, init_state, device_type):
 def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: int = 256,
             ngroups: Optional[int] = None, y=None, final_state=None, return_final_state: bool = True,
             path: str = "auto", workspace=None, stream=None,
-            dt_limit: Optional[Tuple[float, float]] = None) -> Tuple[object, Optional[object]]:
+            dt_limit: Optional[Tuple[float, float]] = None, seq_idx=None) -> Tuple[object, Optional[object]]:
     """Run the SSD forward on the GPU through ssd_fwd / ssd_fwd_ws (ssd_fwd_ex
-    when a dt_limit = (lo, hi) clamp of softplus(dt + dt_bias) is given).
+    when a dt_limit = (lo, hi) clamp of softplus(dt + dt_bias) or packed
+    sequences seq_idx [b, L] int32 are given: the state restarts from zero
+    wherever seq_idx changes between consecutive tokens of a row).
 
     Returns (y, final_state); final_state is None when return_final_state is
     False. With path != "auto" or an explicit workspace (a uint8 CUDA tensor)
@@ -195,13 +197,16 @@ def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: int = 2
     if stream is None:
         stream = torch.cuda.current_stream(x.device).cuda_stream
     io = _io_code(x)
-    if dt_limit is not None:
-        lim = DtLimit(float(dt_limit[0]), float(dt_limit[1]))
+    if seq_idx is not None:
+        _check(seq_idx, "seq_idx", (dims.batch, dims.seqlen), torch.int32, "cuda")
+    if dt_limit is not None or seq_idx is not None:
+        lim = DtLimit(float(dt_limit[0]), float(dt_limit[1])) if dt_limit is not None else None
         ws_ptr = workspace.data_ptr() if workspace is not None else None
         ws_len = workspace.numel() if workspace is not None else 0
         rc = lib.ssd_fwd_ex(ctypes.byref(dims), io, _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
                             _ptr(D), _ptr(init_state), int(chunk_len), int(ngroups), _ptr(y), _ptr(final_state),
-                            ctypes.byref(lim), PATHS[path], ws_ptr, ws_len, stream)
+                            ctypes.byref(lim) if lim is not None else None, _ptr(seq_idx), PATHS[path], ws_ptr,
+                            ws_len, stream)
     elif path == "auto" and workspace is None:
         rc = lib.ssd_fwd(ctypes.byref(dims), io, _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
                          _ptr(D), _ptr(init_state), int(chunk_len), int(ngroups), _ptr(y), _ptr(final_state),

@@ -124,13 +124,15 @@ size_t workspace_for(const ssd_dims& d, int chunk_len, ssd_path path) {
 ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* dt, const float* dt_bias,
                const float* A, const void* B, const void* C, const float* D, const float* init, int chunk_len,
                int ngroups, void* y, float* fs, ssd_path path, void* ws, size_t ws_bytes, bool own_ws,
-               void* stream, float dt_min = 0.f, float dt_max = __builtin_inff()) {
+               void* stream, float dt_min = 0.f, float dt_max = __builtin_inff(),
+               const int32_t* seq_idx = nullptr) {
     ssd_status st = check_dims(dims, io, chunk_len, ngroups);
     if (st != SSD_OK) return st;
     if (path != SSD_PATH_AUTO && path != SSD_PATH_SIMT && path != SSD_PATH_TC && path != SSD_PATH_CHAIN)
         return SSD_ERR_INVALID_ARG;
     st = check_pointers(x, dt, dt_bias, A, B, C, D, init, y, fs);
     if (st != SSD_OK) return st;
+    if (seq_idx && (reinterpret_cast<uintptr_t>(seq_idx) & 3u) != 0) return SSD_ERR_UNSUPPORTED;
     const ssd_path p = resolve_path(*dims, io, chunk_len, path);
     if (!path_supported(*dims, io, chunk_len, p)) return SSD_ERR_UNSUPPORTED;
     const size_t need = workspace_for(*dims, chunk_len, p);
@@ -185,6 +187,7 @@ ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* d
     a.dt_min = dt_min;
     a.dt_max = dt_max;
     a.chain_warmup = chain_warmup_mode();
+    a.seq_idx = seq_idx;
     if (p == SSD_PATH_TC) return tc_forward(a, ws, ws_bytes);
     if (p == SSD_PATH_CHAIN) return chain_forward(a, ws, ws_bytes);
     return simt_forward(a, ws, ws_bytes);
@@ -294,13 +297,13 @@ ssd_status ssd_fwd_ws(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, c
 ssd_status ssd_fwd_ex(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, const float* dt,
                       const float* dt_bias, const float* A, const void* B, const void* C, const float* D,
                       const float* init_state, int chunk_len, int ngroups, void* y, float* final_state,
-                      const ssd_dt_limit* dt_limit, ssd_path path, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+                      const ssd_dt_limit* dt_limit, const int32_t* seq_idx, ssd_path path, void* workspace,
+                      size_t workspace_bytes, void* stream) {
     float lo, hi;
     if (!dt_limit_ok(dt_limit, &lo, &hi)) return SSD_ERR_INVALID_ARG;
     const bool own = workspace == nullptr;
     return run(dims, io_dtype, x, dt, dt_bias, A, B, C, D, init_state, chunk_len, ngroups, y, final_state, path,
-               workspace, workspace_bytes, own, stream, lo, hi);
+               workspace, workspace_bytes, own, stream, lo, hi, seq_idx);
 }
 
 size_t ssd_fwd_workspace_bytes(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len, ssd_path path) {

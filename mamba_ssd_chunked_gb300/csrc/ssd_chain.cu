@@ -985,6 +985,7 @@ struct TableParams {
     uint32_t* counters;  // the chain kernel's ticket and flags, zeroed here
     int ncounters;
     int* order;          // [H] heads in pair order (written by CTA 0)
+    const int32_t* seq;  // [batch, L] packed-sequence ids, or null
     int sort_pairs;      // pair the heads of each group by decay rate (else 2 cb, 2 cb + 1)
     long long L;
     int H, G, nblk, chains_per_b, total;
@@ -1081,6 +1082,16 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
             raw[i] = tg0 + i < prm.L ? make_float2(__ldg(row + hh[0]), __ldg(row + hh[1])) : make_float2(0.f, 0.f);
         }
         float dtv[kHG][4], cs[kHG][4];
+        float cut[4];  // a new packed sequence starts at the token: no state crosses (kSeqCutNats)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const long long t = tg0 + i;
+            cut[i] = (prm.seq && t > 0 && t < prm.L &&
+                      __ldg(prm.seq + static_cast<long long>(b) * prm.L + t) !=
+                          __ldg(prm.seq + static_cast<long long>(b) * prm.L + t - 1))
+                         ? -kSeqCutNats
+                         : 0.f;
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -1097,7 +1108,7 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
             float run = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                run += dtv[j][i] * a;
+                run += fmaf(dtv[j][i], a, cut[i]);
                 cs[j][i] = run;
             }
             float v = run;  // inclusive scan of the lane totals
@@ -1356,6 +1367,7 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     tp.chains_per_b = static_cast<int>(d.nheads / kHG);
     tp.dt_min = a.dt_min;
     tp.dt_max = a.dt_max;
+    tp.seq = a.seq_idx;
     tp.total = static_cast<int>(pl.total);
     tp.counters = static_cast<uint32_t*>(ws);
     tp.ncounters = 1 + pl.ncta;

@@ -35,7 +35,17 @@ struct FwdArgs {
     // blocks it takes to decay away instead of waiting for the previous CTA's hand-off:
     // 0 never, 1 when the hand-off would come late, 2 whenever possible
     int chain_warmup = 1;
+    // [batch, seqlen] packed-sequence ids (nullable): the state restarts from
+    // zero wherever the id changes between consecutive tokens of a row
+    const int32_t* seq_idx = nullptr;
 };
+
+// A change of seq_idx before token t adds -kSeqCutNats to that token's
+// log-decay dt*A in every path's cumulative sum. The state carried across is
+// then scaled by e^{-256 + at most 75} (the largest positive exponent of any
+// path's factored form), exactly 0 in fp32: the restart is exact, and the
+// paths' large-decay handling (split blocks, per-entry masks) takes it as is.
+constexpr float kSeqCutNats = 256.f;
 
 // CUDA-core path: the five stages at exactly chunk_len, chunk states in workspace.
 bool simt_supported(const ssd_dims& d, int chunk_len);

@@ -53,15 +53,18 @@ __device__ __forceinline__ float softplus_f(float v) {
 
 // k1 for chunk c of chain (b, h): s_dt[t] = softplus(dt + dt_bias) clamped to
 // [lim.x, lim.y] (0 past the sequence end: padding comes after discretisation), s_cs[t] = inclusive
-// cumulative sum of dt*A within the chunk. Needs blockDim.x == 256, Q <= 256.
+// cumulative sum of dt*A within the chunk, with -kSeqCutNats at each token
+// where seq_idx (if given) changes. Needs blockDim.x == 256, Q <= 256.
 __device__ void chunk_dt_cumsum(const float* __restrict__ dt, const float* __restrict__ dt_bias,
-                                const float* __restrict__ A, int64_t b, int h, int c, int Q, int64_t L, int H,
-                                float2 lim, float* s_dt, float* s_cs, float* s_warp) {
+                                const float* __restrict__ A, const int32_t* __restrict__ seq, int64_t b, int h,
+                                int c, int Q, int64_t L, int H, float2 lim, float* s_dt, float* s_cs,
+                                float* s_warp) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t t = static_cast<int64_t>(c) * Q + tid;
     float dtv = 0.f;
     if (tid < Q && t < L) dtv = fminf(fmaxf(softplus_f(dt[(b * L + t) * H + h] + dt_bias[h]), lim.x), lim.y);
     float v = dtv * A[h];
+    if (seq && tid < Q && t > 0 && t < L && seq[b * L + t] != seq[b * L + t - 1]) v -= kSeqCutNats;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const float o = __shfl_up_sync(0xffffffffu, v, off);
@@ -86,7 +89,8 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_state(const T* __restrict
                                                              const float* __restrict__ A, const T* __restrict__ Bm,
                                                              int64_t L, int H, int G, int P, int N, int Q, int nc,
                                                              float* __restrict__ states,
-                                                             float* __restrict__ chunk_logdecay, float2 lim) {
+                                                             float* __restrict__ chunk_logdecay, float2 lim,
+                                                             const int32_t* __restrict__ seq) {
     extern __shared__ float sm[];
     float* s_dt = sm;
     float* s_cs = s_dt + kMaxChunk;
@@ -99,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_state(const T* __restrict
     const int64_t b = blockIdx.z;
     const int g = h / (H / G);
     const int tid = threadIdx.x;
-    chunk_dt_cumsum(dt, dt_bias, A, b, h, c, Q, L, H, lim, s_dt, s_cs, s_warp);
+    chunk_dt_cumsum(dt, dt_bias, A, seq, b, h, c, Q, L, H, lim, s_dt, s_cs, s_warp);
     const float cs_end = s_cs[Q - 1];
     for (int t = tid; t < Q; t += kThreads) s_w[t] = s_dt[t] * expf(cs_end - s_cs[t]);
     if (tid == 0) chunk_logdecay[(b * H + h) * nc + c] = cs_end;
@@ -177,7 +181,8 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_scan(const T* __restrict_
                                                             const T* __restrict__ Cm, const float* __restrict__ D,
                                                             const float* __restrict__ states, int64_t L, int H,
                                                             int G, int P, int N, int Q, int nc, int tiles,
-                                                            T* __restrict__ y, float2 lim) {
+                                                            T* __restrict__ y, float2 lim,
+                                                            const int32_t* __restrict__ seq) {
     extern __shared__ float sm[];
     float* s_dt = sm;
     float* s_cs = s_dt + kMaxChunk;
@@ -190,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_scan(const T* __restrict_
     const int64_t b = blockIdx.z;
     const int g = h / (H / G);
     const int tid = threadIdx.x;
-    chunk_dt_cumsum(dt, dt_bias, A, b, h, c, Q, L, H, lim, s_dt, s_cs, s_warp);
+    chunk_dt_cumsum(dt, dt_bias, A, seq, b, h, c, Q, L, H, lim, s_dt, s_cs, s_warp);
 
     const int rows = min(kRows, Q - r0);
     for (int i = tid; i < kRows * N; i += kThreads) {
@@ -261,14 +266,15 @@ ssd_status launch_all(const FwdArgs& a, float* states, float* logdecay) {
 
     timing_begin(a.stream);
     simt_chunk_state<T><<<dim3(nc, H, static_cast<unsigned>(d.batch)), block, smem1, a.stream>>>(
-        x, a.dt, a.dt_bias, a.A, Bm, d.seqlen, H, G, P, N, Q, nc, states, logdecay, make_float2(a.dt_min, a.dt_max));
+        x, a.dt, a.dt_bias, a.A, Bm, d.seqlen, H, G, P, N, Q, nc, states, logdecay, make_float2(a.dt_min, a.dt_max),
+        a.seq_idx);
     const int PN = P * N;
     simt_state_pass<<<dim3((PN + kThreads - 1) / kThreads, H, static_cast<unsigned>(d.batch)), block, 0,
                       a.stream>>>(states, logdecay, a.init, a.final_state, H, PN, nc);
     const int tiles = (Q + kRows - 1) / kRows;
     simt_chunk_scan<T><<<dim3(nc * tiles, H, static_cast<unsigned>(d.batch)), block, smem3, a.stream>>>(
         x, a.dt, a.dt_bias, a.A, Bm, Cm, a.D, states, d.seqlen, H, G, P, N, Q, nc, tiles,
-        static_cast<T*>(a.y), make_float2(a.dt_min, a.dt_max));
+        static_cast<T*>(a.y), make_float2(a.dt_min, a.dt_max), a.seq_idx);
     timing_end(a.stream);
     note_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;

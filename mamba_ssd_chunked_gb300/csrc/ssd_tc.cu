@@ -125,6 +125,7 @@ struct TcParams {
     long long L;
     unsigned long long chain_wait_ns;  // limit on waiting for the previous block's state
     float dt_min, dt_max;              // clamp of softplus(dt + dt_bias)
+    const int32_t* seq;                // [batch, L] packed-sequence ids, or null
 };
 
 __device__ __forceinline__ float softplus_f(float v) {
@@ -238,6 +239,9 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
                               prm.dt_min),
                         prm.dt_max);
         float v = dtv * prm.A[h];
+        // a new packed sequence starts at t: no state crosses (kSeqCutNats)
+        if (prm.seq && t > 0 && t < L && prm.seq[static_cast<long long>(b) * L + t] != prm.seq[static_cast<long long>(b) * L + t - 1])
+            v -= kSeqCutNats;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const float o = __shfl_up_sync(0xffffffffu, v, off);
@@ -745,6 +749,7 @@ ssd_status launch(const FwdArgs& a, void* ws) {
     p.chain_wait_ns = a.wait_limit_ns;
     p.dt_min = a.dt_min;
     p.dt_max = a.dt_max;
+    p.seq = a.seq_idx;
     if (cudaFuncSetAttribute(ssd_tc_fused<NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(K::SMEM_BYTES)) != cudaSuccess)
         return SSD_ERR_CUDA;

@@ -202,7 +202,13 @@ def test_bad_dt_limit_rejected_on_host(lib, lo, hi):
     d = pkg.Dims(1, 8, 2, 64, 1, 128)
     lim = pkg.DtLimit(lo, hi)
     assert lib.ssd_fwd_ex(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 1, FAKE, None,
-                          ctypes.byref(lim), 0, None, 0, None) == 1
+                          ctypes.byref(lim), None, 0, None, 0, None) == 1
     d1 = pkg.Dims(1, 1, 2, 64, 1, 128)
     assert lib.ssd_step_ex(ctypes.byref(d1), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, FAKE,
                            ctypes.byref(lim), None) == 1
+
+
+def test_misaligned_seq_idx_is_unsupported(lib):
+    d = pkg.Dims(1, 8, 2, 64, 1, 128)
+    assert lib.ssd_fwd_ex(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 1, FAKE, None,
+                          None, FAKE + 2, 0, None, 0, None) == 2
