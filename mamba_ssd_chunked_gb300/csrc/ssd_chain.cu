@@ -65,7 +65,6 @@ namespace {
 
 constexpr int kT = 128;                 // tokens per block
 constexpr int kP = 64;                  // headdim
-constexpr int kN = 128;                 // dstate
 constexpr int kHG = 2;                  // heads per chain
 constexpr uint32_t kTile = 16384;       // 128 rows x 128 bytes, 128-byte swizzle
 constexpr float kMaxSubDecay = 150.f;   // a sub-block decaying at most this keeps factors within e^{+-75}
@@ -99,11 +98,32 @@ constexpr uint32_t kRecScal = kHG * kScal * 4;
 constexpr uint32_t kRecSmem = kRecTab + kRecScal + 16;
 constexpr uint32_t kRecBytes = kRecSmem + kHG * kNumTabX * kT * 4;
 static_assert(kRecSmem % 16 == 0 && kRecBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
-enum RingKind { RK_L = 0, RK_B = 1, RK_C = 2 };
+
+// Per-dstate layout (NS = 128 or 256). The ring carries, per job, L and then
+// B and C in 128-column halves of n: kKinds ring entries of 32 KB at
+// positions kKinds J + kind (kind 0: L, 1 .. kNB: B halves, then C halves).
+// TMEM (512 columns): the fp32 state Z (NS columns), kHBuf bf16 copies H of
+// the scaled state (NS / 2 columns each, the A operand of k5b) and kYBuf
+// output accumulators Y (128 columns each). At NS = 256 the state takes half
+// of TMEM, so H and Y are single-buffered.
+template <int NS>
+struct Lay {
+    static_assert(NS == 128 || NS == 256, "dstate 128 or 256");
+    static constexpr int kNB = NS / 128;
+    static constexpr int kKinds = 1 + 2 * kNB;
+    static constexpr int kHBuf = NS == 128 ? 2 : 1;
+    static constexpr int kYBuf = NS == 128 ? 2 : 1;
+    static constexpr uint32_t COL_Z = 0;
+    static constexpr uint32_t COL_H = NS;
+    static constexpr uint32_t COL_Y = NS + kHBuf * (NS / 2);
+    static_assert(COL_Y + kYBuf * 128 == 512, "TMEM budget");
+    __host__ __device__ static constexpr int kindB(int half) { return 1 + half; }
+    __host__ __device__ static constexpr int kindC(int half) { return 1 + kNB + half; }
+};
 
 struct Cfg {
     // ring of kRing 32 KB slots ([t][128] as two 64-column tiles) holding, in
-    // consumption order, L, B and C of each job: ring position 3J + kind
+    // consumption order, L and the B and C halves of each job (Lay<NS>)
     static constexpr uint32_t OFF_RING = 0;
     static constexpr uint32_t OFF_XW = 8 * kTile;        // 2 job slots x 2 heads, X then W then y
     static constexpr uint32_t OFF_TAB = 12 * kTile;      // [slots] table records
@@ -113,9 +133,6 @@ struct Cfg {
     static constexpr uint32_t OFF_SCAN = OFF_MISC + 64;  // [kThreads / 32] u64, cta_range
     static constexpr uint32_t SMEM_BYTES = OFF_SCAN + 128 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    static constexpr uint32_t COL_Z = 0;     // state, fp32, 128 columns (n)
-    static constexpr uint32_t COL_H = 128;   // 2 x 64 columns, bf16 pairs
-    static constexpr uint32_t COL_Y = 256;   // 2 x 128 columns (t)
 };
 
 enum Bar {
@@ -473,11 +490,13 @@ __device__ __noinline__ int warmup_blocks(const ChainParams& prm, const JobList&
     return (t_range + t_wu < t_ready + t_seg) ? m : 0;
 }
 
+template <int NS>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chain_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_l,
                     const __grid_constant__ CUtensorMap tm_y, const ChainParams prm) {
     using K = Cfg;
+    using Y = Lay<NS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
@@ -549,25 +568,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer: L, B, C ring
         if (lane == 0) {
-            const int npos = 3 * njobs;
+            const int npos = Y::kKinds * njobs;
             int pr = 0;
             for (; pr < npos; ++pr) {
                 const int rs = pr % kRing, ru = pr / kRing;
                 if (ru > 0) WB(B_R_EMPTY0 + rs, (ru - 1) & 1);
                 if (*abort_flag) break;
-                const int J = pr / 3, kind = pr - 3 * J;
+                const int J = pr / Y::kKinds, kind = pr - Y::kKinds * J;
                 const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order);
                 uint64_t* fb = &bars[B_R_FULL0 + rs];
                 uint8_t* dst = smem + K::OFF_RING + rs * 2 * kTile;
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
-                if (kind == RK_L) {
+                if (kind == 0) {
                     const int tile = (jp.b * prm.nblk + jp.blk) * prm.G + jp.g;
                     ptx::tma_load_4d(dst, &tm_l, fb, 0, 0, 0, tile);
                     ptx::tma_load_4d(dst + kTile, &tm_l, fb, 64, 0, 0, tile);
                 } else {
-                    const CUtensorMap* m = kind == RK_B ? &tm_b : &tm_c;
-                    ptx::tma_load_4d(dst, m, fb, 0, jp.g, jp.blk * kT, jp.b);
-                    ptx::tma_load_4d(dst + kTile, m, fb, 64, jp.g, jp.blk * kT, jp.b);
+                    // a 128-column half of B or C: n in [128 half, 128 half + 128)
+                    const bool is_b = kind <= Y::kNB;
+                    const int n0 = 128 * (is_b ? kind - 1 : kind - 1 - Y::kNB);
+                    const CUtensorMap* m = is_b ? &tm_b : &tm_c;
+                    ptx::tma_load_4d(dst, m, fb, n0, jp.g, jp.blk * kT, jp.b);
+                    ptx::tma_load_4d(dst + kTile, m, fb, n0 + 64, jp.g, jp.blk * kT, jp.b);
                 }
             }
             // no copy into shared memory may be left in flight at exit: wait for the
@@ -589,18 +611,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nq = static_cast<int>(JW(ts)[0]);
                 const int ksub = 8 / nq;  // K steps per sub-block
                 ptx::mbar_arrive(&bars[B_TAB_EMPTY0 + ts]);  // this issuer is done with the record
-                const int pb = 3 * J + RK_B;
                 WB(B_W_FULL0 + xs, (J >> 1) & 1);
-                WB(B_R_FULL0 + pb % kRing, (pb / kRing) & 1);
                 const uint64_t a_w = ptx::desc_sw128(sbase + K::OFF_XW + xs * 2 * kTile, kTile, 1024);
-                const uint64_t b_b = ptx::desc_sw128(sbase + K::OFF_RING + (pb % kRing) * 2 * kTile, kTile, 1024);
+                uint64_t b_b[Y::kNB];
+#pragma unroll
+                for (int hh = 0; hh < Y::kNB; ++hh) {
+                    const int pb = Y::kKinds * J + Y::kindB(hh);
+                    WB(B_R_FULL0 + pb % kRing, (pb / kRing) & 1);
+                    b_b[hh] = ptx::desc_sw128(sbase + K::OFF_RING + (pb % kRing) * 2 * kTile, kTile, 1024);
+                }
                 for (int q = 0; q < nq; ++q, ++u) {
                     WB(B_SCALED, u & 1);
                     ptx::tc_fence_after();
-                    mma_k3(tmem + K::COL_Z, a_w, b_b, idesc, q * ksub, ksub);
+#pragma unroll
+                    for (int hh = 0; hh < Y::kNB; ++hh)  // Z columns [128 hh, 128 hh + 128) are n of that half
+                        mma_k3(tmem + Y::COL_Z + 128 * hh, a_w, b_b[hh], idesc, q * ksub, ksub);
                     ptx::mma_commit(&bars[B_S_DONE]);
                 }
-                ptx::mma_commit(&bars[B_R_EMPTY0 + pb % kRing]);
+#pragma unroll
+                for (int hh = 0; hh < Y::kNB; ++hh)
+                    ptx::mma_commit(&bars[B_R_EMPTY0 + (Y::kKinds * J + Y::kindB(hh)) % kRing]);
                 ptx::mma_commit(&bars[B_XW_FREE0 + xs]);
             }
             ptx::mma_commit(&bars[B_DRAIN_K3]);
@@ -612,15 +642,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t u = 0;
             for (int J = 0; J < njobs; ++J) {
-                const int ts = J & (kTabSlots - 1), xs = J & 1, yb = J & 1;
+                const int ts = J & (kTabSlots - 1), xs = J & 1, yb = J % Y::kYBuf;
                 WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
                 const int nq = static_cast<int>(JW(ts)[0]);
                 const uint32_t extreme = JW(ts)[1];
                 const int qs = kT / nq, ksub = 8 / nq;
-                const uint32_t yc = tmem + K::COL_Y + 128 * yb;
-                const int pl = 3 * J + RK_L, pc = 3 * J + RK_C;
+                const uint32_t yc = tmem + Y::COL_Y + 128 * yb;
+                const int pl = Y::kKinds * J;
                 const bool warm = job_pos(jobs, J, chains_per_b, HperG, order).warm;  // no output: no k5a / k5b
-                if (J >= 2) WB(B_Y_EMPTY0 + yb, ((J >> 1) - 1) & 1);  // the epilogue has read job J - 2
+                if (J >= Y::kYBuf)  // the epilogue has read job J - kYBuf
+                    WB(B_Y_EMPTY0 + yb, ((J / Y::kYBuf) - 1) & 1);
                 WB(B_W_FULL0 + xs, (J >> 1) & 1);
                 WB(B_R_FULL0 + pl % kRing, (pl / kRing) & 1);
                 ptx::tc_fence_after();
@@ -634,17 +665,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::mma_commit(&bars[B_R_EMPTY0 + pl % kRing]);
                 ptx::mma_commit(&bars[B_XW_FREE0 + xs]);
-                WB(B_R_FULL0 + pc % kRing, (pc / kRing) & 1);
+                uint32_t c_slot[Y::kNB];
+#pragma unroll
+                for (int hh = 0; hh < Y::kNB; ++hh) {
+                    const int pc = Y::kKinds * J + Y::kindC(hh);
+                    WB(B_R_FULL0 + pc % kRing, (pc / kRing) & 1);
+                    c_slot[hh] = sbase + K::OFF_RING + (pc % kRing) * 2 * kTile;
+                }
                 for (int q = 0; q < nq; ++q, ++u) {
-                    const int hb = u & 1;
-                    WB(B_H_FULL0 + hb, (u >> 1) & 1);
+                    const int hb = u % Y::kHBuf;
+                    WB(B_H_FULL0 + hb, (u / Y::kHBuf) & 1);
                     ptx::tc_fence_after();
-                    const uint64_t b_c =
-                        ptx::desc_sw128(sbase + K::OFF_RING + (pc % kRing) * 2 * kTile + q * qs * 128, 16, 1024);
-                    if (!warm) mma_k5b(yc + q * qs, tmem + K::COL_H + 64 * hb, b_c, id_b, (~extreme >> q) & 1u);
+                    if (!warm) {
+#pragma unroll
+                        for (int hh = 0; hh < Y::kNB; ++hh) {  // K = n in halves: H columns 64 hh.., C half hh
+                            const uint64_t b_c = ptx::desc_sw128(c_slot[hh] + q * qs * 128, 16, 1024);
+                            mma_k5b(yc + q * qs, tmem + Y::COL_H + (NS / 2) * hb + 64 * hh, b_c, id_b,
+                                    hh > 0 ? 1u : ((~extreme >> q) & 1u));
+                        }
+                    }
                     ptx::mma_commit(&bars[B_H_EMPTY0 + hb]);
                 }
-                ptx::mma_commit(&bars[B_R_EMPTY0 + pc % kRing]);
+#pragma unroll
+                for (int hh = 0; hh < Y::kNB; ++hh)
+                    ptx::mma_commit(&bars[B_R_EMPTY0 + (Y::kKinds * J + Y::kindC(hh)) % kRing]);
                 ptx::mma_commit(&bars[B_Y_FULL0 + yb]);
             }
             ptx::mma_commit(&bars[B_DRAIN_Y]);
@@ -674,8 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_4d(dst + kTile, &tm_x, fb, 0, jp.h[1], jp.blk * kT, jp.b);
                 if (jp.blk == 0 && prm.init)  // a chain start: its initial states into L2 for the state warps
                     for (int j = 0; j < kHG; ++j)
-                        ptx::bulk_prefetch_l2(prm.init + (static_cast<size_t>(jp.b) * prm.H + jp.h[j]) * kP * kN,
-                                              kP * kN * sizeof(float));
+                        ptx::bulk_prefetch_l2(prm.init + (static_cast<size_t>(jp.b) * prm.H + jp.h[j]) * kP * NS,
+                                              kP * NS * sizeof(float));
                 if (jx + 2 < njobs) {
                     // the X of job jx + 2 into L2: its load, once the slot is free, then hits L2
                     const JobPos jn = job_pos(jobs, jx + 2, chains_per_b, HperG, order);
@@ -765,11 +809,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* src = nullptr;  // segment start: the incoming state row [n]
             if (seg_start) {
                 if (jp.wait)
-                    src = misc[2] ? nullptr : prm.handoff + ((static_cast<size_t>(cta - 1) * kHG + j) * kP + p) * kN;
+                    src = misc[2] ? nullptr : prm.handoff + ((static_cast<size_t>(cta - 1) * kHG + j) * kP + p) * NS;
                 else if (jp.lo > 0)
                     src = nullptr;  // warm-up from a zero state
                 else if (prm.init)
-                    src = prm.init + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * kN;
+                    src = prm.init + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * NS;
                 inv_prev = 1.f;
             }
             for (int q = 0; q < nq; ++q, ++u) {
@@ -778,14 +822,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     WB(B_S_DONE, sdone & 1);
                     ++sdone;
                 }
-                const int hb = u & 1;
-                if (u >= 2) WB(B_H_EMPTY0 + hb, ((u >> 1) - 1) & 1);
+                const int hb = u % Y::kHBuf;
+                if (u >= static_cast<uint32_t>(Y::kHBuf)) WB(B_H_EMPTY0 + hb, ((u / Y::kHBuf) - 1) & 1);
                 ptx::tc_fence_after();
                 const float ec = sc[SC_EC + q], hs = sc[SC_HS + q];
-                const uint32_t zcol = tmem + lane_base + K::COL_Z;
-                const uint32_t hcol = tmem + lane_base + K::COL_H + 64 * hb;
+                const uint32_t zcol = tmem + lane_base + Y::COL_Z;
+                const uint32_t hcol = tmem + lane_base + Y::COL_H + (NS / 2) * hb;
 #pragma unroll 1
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < NS / 32; ++k) {
                     uint32_t r[32];
                     if (from_src) {
                         if (src) {
@@ -833,13 +877,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++sdone;
                 ptx::tc_fence_after();
                 float* dst = to_final ? (prm.final_state
-                                             ? prm.final_state + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * kN
+                                             ? prm.final_state + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * NS
                                              : nullptr)
-                                      : prm.handoff + ((static_cast<size_t>(cta) * kHG + j) * kP + p) * kN;
+                                      : prm.handoff + ((static_cast<size_t>(cta) * kHG + j) * kP + p) * NS;
 #pragma unroll 1
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < NS / 32; ++k) {
                     uint32_t r[32];
-                    ptx::tmem_ld32(tmem + lane_base + K::COL_Z + 32 * k, r);
+                    ptx::tmem_ld32(tmem + lane_base + Y::COL_Z + 32 * k, r);
                     ptx::tmem_wait_ld(r);
                     if (dst) {
 #pragma unroll
@@ -874,14 +918,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mrow = lane & 7, mm = lane >> 3;
         const long long x_tstride = static_cast<long long>(prm.H) * kP;
         for (int J = 0; J < njobs; ++J) {
-            const int ts = J & (kTabSlots - 1), yb = J & 1, xs = J & 1;
+            const int ts = J & (kTabSlots - 1), yb = J % Y::kYBuf, xs = J & 1;
             WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
             const float2* u2 = reinterpret_cast<const float2*>(T(ts, j, TAB_U));
             const float2* g2 = reinterpret_cast<const float2*>(T(ts, j, TAB_UG));
             const uint32_t extreme = JW(ts)[1];
             const bool rare = (extreme | JW(ts)[2]) != 0u;
             const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order);
-            WB(B_Y_FULL0 + yb, (J >> 1) & 1);
+            WB(B_Y_FULL0 + yb, (J / Y::kYBuf) & 1);
             WB(B_XW_FREE0 + xs, (J >> 1) & 1);  // k3 and k5a no longer read W
             ptx::tc_fence_after();
             if (jp.warm) {
@@ -895,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tile = sbase + K::OFF_XW + (xs * kHG + j) * kTile;
 #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
-                const uint32_t ylane = tmem + (static_cast<uint32_t>(32 * q4 + 16 * hf) << 16) + K::COL_Y + 128 * yb;
+                const uint32_t ylane = tmem + (static_cast<uint32_t>(32 * q4 + 16 * hf) << 16) + Y::COL_Y + 128 * yb;
                 const uint32_t pc = 4 * (q4 & 1) + 2 * hf + (mm & 1);  // 16-byte chunk of p in the row
 #pragma unroll 1
                 for (int k = 0; k < 4; ++k) {
@@ -957,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   j * kNumTabX * kT;
                 const __nv_bfloat16* lg =
                     prm.masks + static_cast<size_t>((jp.b * prm.nblk + jp.blk) * prm.G + jp.g) * kT * kT;
-                fixup_tokens(tmem + lane_base + K::COL_Y + 128 * yb, extreme, kT / static_cast<int>(JW(ts)[0]), tn,
+                fixup_tokens(tmem + lane_base + Y::COL_Y + 128 * yb, extreme, kT / static_cast<int>(JW(ts)[0]), tn,
                              T(ts, j, TAB_U), T(ts, j, TAB_WF), xt + TABX_CS * kT, xt + TABX_DT * kT, S(ts, j)[SC_D],
                              prm.x + off, prm.y + off, x_tstride, lg);
                 ptx::tc_fence_before();
@@ -1214,17 +1258,23 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
 }
 
 // L = C.B^T masked to s <= t, in bf16, for one (batch, block, group): the matrix
-// every head of the group shares (burn-mamba k2_ssd_bmm plus the causal mask).
-// One CTA of 128 threads per tile; thread t writes row t.
-constexpr uint32_t kMaskSmem = 4 * kTile + 64 + 1024;
+// every head of the group shares (burn-mamba k2_ssd_bmm plus the causal mask),
+// the contraction over all NS columns of n. One CTA of 128 threads per tile;
+// thread t writes row t.
+template <int NS>
+constexpr uint32_t mask_smem() {
+    return 2 * (NS / 64) * kTile + 64 + 1024;
+}
 
+template <int NS>
 __global__ void __launch_bounds__(128)
     chain_masks(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
                 __nv_bfloat16* __restrict__ out, int nblk, int G, uint32_t* status) {
+    constexpr int kNT = NS / 64;  // 64-column tiles of C (and of B)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 4 * kTile);
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + 4 * kTile + 16);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kNT * kTile);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + 2 * kNT * kTile + 16);
     const int tile = blockIdx.x;
     const int g = tile % G, blk = (tile / G) % nblk, b = tile / (G * nblk);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -1243,16 +1293,17 @@ __global__ void __launch_bounds__(128)
     const uint32_t tmem = misc[0];
     const uint32_t sbase = ptx::smem_u32(smem);
     if (tid == 0) {
-        ptx::mbar_arrive_expect_tx(&bars[0], 4 * kTile);
-        ptx::tma_load_4d(smem, &tm_c, &bars[0], 0, g, blk * kT, b);
-        ptx::tma_load_4d(smem + kTile, &tm_c, &bars[0], 64, g, blk * kT, b);
-        ptx::tma_load_4d(smem + 2 * kTile, &tm_b, &bars[0], 0, g, blk * kT, b);
-        ptx::tma_load_4d(smem + 3 * kTile, &tm_b, &bars[0], 64, g, blk * kT, b);
+        ptx::mbar_arrive_expect_tx(&bars[0], 2 * kNT * kTile);
+        for (int i = 0; i < kNT; ++i) {
+            ptx::tma_load_4d(smem + i * kTile, &tm_c, &bars[0], 64 * i, g, blk * kT, b);
+            ptx::tma_load_4d(smem + (kNT + i) * kTile, &tm_b, &bars[0], 64 * i, g, blk * kT, b);
+        }
         if (ptx::mbar_wait(&bars[0], 0, kLocalWaitNs)) {
             ptx::tc_fence_after();
-            const uint64_t a = ptx::desc_sw128(sbase, 16, 1024), bb = ptx::desc_sw128(sbase + 2 * kTile, 16, 1024);
+            const uint64_t a = ptx::desc_sw128(sbase, 16, 1024),
+                           bb = ptx::desc_sw128(sbase + kNT * kTile, 16, 1024);
             const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
-            for (int k = 0; k < 8; ++k) ptx::mma_bf16(tmem, a + kmaj(k), bb + kmaj(k), idesc, k > 0 ? 1u : 0u);
+            for (int k = 0; k < NS / 16; ++k) ptx::mma_bf16(tmem, a + kmaj(k), bb + kmaj(k), idesc, k > 0 ? 1u : 0u);
         } else {
             atomicOr(status, 2u);
         }
@@ -1301,7 +1352,7 @@ int sm_count() {
 
 struct ChainPlan {
     int ncta;
-    long long nchains, nblk, total, ntiles, nheads;
+    long long nchains, nblk, total, ntiles, nheads, ns;
 };
 
 ChainPlan plan(const ssd_dims& d, int nsm) {
@@ -1312,6 +1363,7 @@ ChainPlan plan(const ssd_dims& d, int nsm) {
     p.ncta = static_cast<int>(std::min<long long>(nsm, p.total));
     p.ntiles = d.batch * p.nblk * d.ngroups;
     p.nheads = d.nheads;
+    p.ns = d.dstate;
     return p;
 }
 
@@ -1319,8 +1371,8 @@ ChainPlan plan(const ssd_dims& d, int nsm) {
 size_t counters_bytes(int ncta) {
     return align_up(sizeof(uint32_t) * (1 + static_cast<size_t>(ncta)), kWorkspaceAlign);
 }
-size_t handoff_bytes(int ncta) {
-    return align_up(static_cast<size_t>(ncta) * kHG * kP * kN * sizeof(float), kWorkspaceAlign);
+size_t handoff_bytes(int ncta, long long ns) {
+    return align_up(static_cast<size_t>(ncta) * kHG * kP * ns * sizeof(float), kWorkspaceAlign);
 }
 size_t masks_bytes(long long ntiles) { return align_up(static_cast<size_t>(ntiles) * kT * kT * 2, kWorkspaceAlign); }
 size_t tables_bytes(long long jobs) { return align_up(static_cast<size_t>(jobs) * kRecBytes, kWorkspaceAlign); }
@@ -1328,18 +1380,19 @@ size_t costs_bytes(long long jobs) { return align_up(static_cast<size_t>(jobs), 
 size_t order_bytes(long long heads) { return align_up(static_cast<size_t>(heads) * sizeof(int), kWorkspaceAlign); }
 size_t decay_bytes(long long jobs) { return align_up(static_cast<size_t>(jobs) * sizeof(float2), kWorkspaceAlign); }
 size_t chain_ws_bytes(const ChainPlan& pl) {
-    return counters_bytes(pl.ncta) + handoff_bytes(pl.ncta) + masks_bytes(pl.ntiles) + tables_bytes(pl.total) +
+    return counters_bytes(pl.ncta) + handoff_bytes(pl.ncta, pl.ns) + masks_bytes(pl.ntiles) + tables_bytes(pl.total) +
            costs_bytes(pl.total) + order_bytes(pl.nheads) + decay_bytes(pl.total);
 }
 
+template <int NS>
 ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     const ssd_dims& d = a.d;
     const size_t counters = counters_bytes(pl.ncta);
     float* handoff = reinterpret_cast<float*>(static_cast<char*>(ws) + counters);
     __nv_bfloat16* masks =
-        reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + counters + handoff_bytes(pl.ncta));
+        reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + counters + handoff_bytes(pl.ncta, pl.ns));
     uint8_t* tables =
-        static_cast<uint8_t*>(ws) + counters + handoff_bytes(pl.ncta) + masks_bytes(pl.ntiles);
+        static_cast<uint8_t*>(ws) + counters + handoff_bytes(pl.ncta, pl.ns) + masks_bytes(pl.ntiles);
     uint8_t* costs = tables + tables_bytes(pl.total);
     int* order = reinterpret_cast<int*>(costs + costs_bytes(pl.total));
     float2* decay = reinterpret_cast<float2*>(reinterpret_cast<char*>(order) + order_bytes(pl.nheads));
@@ -1350,8 +1403,8 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
         !make_map_bf16(&tl, masks, kT, 1, kT, static_cast<uint64_t>(pl.ntiles)) ||
         !make_map_bf16(&ty, a.y, d.headdim, d.nheads, d.seqlen, d.batch))
         return SSD_ERR_CUDA;
-    if (cudaFuncSetAttribute(chain_masks, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kMaskSmem)) != cudaSuccess)
+    if (cudaFuncSetAttribute(chain_masks<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(mask_smem<NS>())) != cudaSuccess)
         return SSD_ERR_CUDA;
     TableParams tp;
     tp.dt = a.dt;
@@ -1389,11 +1442,11 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(static_cast<unsigned>(pl.ntiles));
     mcfg.blockDim = dim3(128);
-    mcfg.dynamicSmemBytes = kMaskSmem;
+    mcfg.dynamicSmemBytes = mask_smem<NS>();
     mcfg.stream = a.stream;
     mcfg.attrs = pdl;
     mcfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&mcfg, chain_masks, tb, tc, masks, static_cast<int>(pl.nblk), static_cast<int>(d.ngroups),
+    if (cudaLaunchKernelEx(&mcfg, chain_masks<NS>, tb, tc, masks, static_cast<int>(pl.nblk), static_cast<int>(d.ngroups),
                            a.status_word) != cudaSuccess)
         return SSD_ERR_CUDA;
     uint32_t* ctr = static_cast<uint32_t*>(ws);  // ticket, flags [ncta]
@@ -1430,7 +1483,7 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     p.chain_wait_ns = a.wait_limit_ns;
     p.dt_min = a.dt_min;
     p.dt_max = a.dt_max;
-    if (cudaFuncSetAttribute(ssd_chain_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(ssd_chain_fused<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Cfg::SMEM_BYTES)) != cudaSuccess)
         return SSD_ERR_CUDA;
     cudaLaunchConfig_t ccfg = {};
@@ -1441,7 +1494,7 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     ccfg.attrs = pdl;
     ccfg.numAttrs = 1;
     timing_begin(a.stream);
-    if (cudaLaunchKernelEx(&ccfg, ssd_chain_fused, tx, tb, tc, tl, ty, p) != cudaSuccess) return SSD_ERR_CUDA;
+    if (cudaLaunchKernelEx(&ccfg, ssd_chain_fused<NS>, tx, tb, tc, tl, ty, p) != cudaSuccess) return SSD_ERR_CUDA;
     timing_end(a.stream);
     note_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
@@ -1451,7 +1504,7 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
 
 bool chain_supported(const ssd_dims& d, ssd_dtype io, int chunk_len) {
     if (io != SSD_BF16) return false;
-    if (d.headdim != kP || d.dstate != kN) return false;
+    if (d.headdim != kP || (d.dstate != 128 && d.dstate != 256)) return false;
     if (chunk_len != 128 && chunk_len != 256) return false;
     if ((d.nheads / d.ngroups) % kHG != 0) return false;  // a chain's two heads share a B/C group
     if (d.seqlen >= (1ll << 31) || d.batch >= (1ll << 20) || d.nheads >= (1 << 20)) return false;
@@ -1476,7 +1529,7 @@ ssd_status chain_forward(const FwdArgs& a, void* ws, size_t ws_bytes) {
     for (const void* p : {a.x, static_cast<const void*>(a.B), static_cast<const void*>(a.C),
                           static_cast<const void*>(a.y)})
         if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return SSD_ERR_UNSUPPORTED;
-    return launch_chain(a, ws, pl);
+    return a.d.dstate == 256 ? launch_chain<256>(a, ws, pl) : launch_chain<128>(a, ws, pl);
 }
 
 }  // namespace ssd

@@ -42,6 +42,12 @@ CHAIN_SHAPES = [
     (3, 513, 8, 64, 2, 128),
     (1, 2000, 2, 64, 1, 128),     # one chain spread over many CTAs: a hand-off at every block
     (2, 4100, 6, 64, 1, 128),     # long chains split across CTAs mid-chain
+    # dstate 256: the state fills half of tensor memory (single-buffered H and Y)
+    (1, 128, 2, 64, 1, 256),
+    (2, 300, 4, 64, 2, 256),
+    (1, 1000, 6, 64, 3, 256),
+    (1, 2000, 2, 64, 1, 256),     # a hand-off at every block
+    (2, 4100, 6, 64, 1, 256),
 ]
 
 
@@ -51,11 +57,12 @@ def test_chain_path_matches_oracle(shape, chunk_len):
     check_against_oracle(shape, "bf16", chunk_len, "chain", seed=sum(shape) + chunk_len + 1)
 
 
+@pytest.mark.parametrize("n", [128, 256])
 @pytest.mark.parametrize("dt_shift,A_scale", [(3.0, 4.0), (1.0, 2.0), (-2.0, 0.25), (0.0, 1.0)])
-def test_chain_path_strong_and_weak_decay(dt_shift, A_scale):
+def test_chain_path_strong_and_weak_decay(dt_shift, A_scale, n):
     """Uniformly strong decay (most 16-token sub-blocks extreme), moderate
     (blocks split into sub-blocks), weak (whole blocks)."""
-    inp = make_inputs(2, 1100, 8, 64, 2, 128, io_dtype="bf16", init="normal", seed=43)
+    inp = make_inputs(2, 1100, 8, 64, 2, n, io_dtype="bf16", init="normal", seed=43)
     inp["dt"] = (inp["dt"] + dt_shift).astype(np.float32)
     inp["A"] = (inp["A"] * A_scale).astype(np.float32)
     t = to_device(inp, "bf16")

@@ -81,7 +81,7 @@ def test_full_size_workload_matches_oracle(name):
     assert pkg.ssd_device_status() == 0
     if w.io_dtype == "f32":
         expect_path = "simt"
-    elif w.dstate == 128 and (w.nheads // w.ngroups) % 2 == 0:
+    elif w.dstate in (128, 256) and (w.nheads // w.ngroups) % 2 == 0:
         expect_path = "chain"
     else:
         expect_path = "tc"

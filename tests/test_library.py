@@ -132,8 +132,10 @@ def test_workspace_too_small(lib):
 def test_path_selection(lib):
     assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 256) == "chain"
     assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 128) == "chain"
-    assert pkg.ssd_select_path(1, 131072, 64, 64, 1, 256, "bf16", 256) == "tc"  # dstate 256
+    assert pkg.ssd_select_path(1, 131072, 64, 64, 1, 256, "bf16", 256) == "chain"  # dstate 256
     assert pkg.ssd_select_path(1, 4096, 6, 64, 2, 128, "bf16", 256) == "tc"  # odd heads per group
+    assert pkg.ssd_select_path(1, 4096, 6, 64, 2, 256, "bf16", 256) == "tc"
+    assert pkg.ssd_select_path(1, 4096, 4, 64, 1, 192, "bf16", 256) == "simt"  # dstate neither 128 nor 256
     assert pkg.ssd_select_path(1, 256, 4, 16, 1, 16, "f32", 64) == "simt"
     assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "f32", 256) == "simt"
     assert pkg.ssd_select_path(4, 4096, 80, 32, 1, 128, "bf16", 256) == "simt"
@@ -156,7 +158,9 @@ def test_workspace_sizes(lib):
     # device to ask for its SM count it sizes for 1024 CTAs of two heads
     need = pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, n, "bf16", 256, "chain")
     assert need >= 1024 * 2 * p * n * 4
-    assert pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, 256, "bf16", 256, "chain") == 0
+    need256 = pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, 256, "bf16", 256, "chain")
+    assert need256 >= 1024 * 2 * p * 256 * 4  # the hand-off states are twice as wide
+    assert pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, 192, "bf16", 256, "chain") == 0
 
 
 def test_kernel_counter_starts_without_launches(lib):
