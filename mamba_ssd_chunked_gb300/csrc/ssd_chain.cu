@@ -82,8 +82,9 @@ constexpr int kScal = 32;               // scalars per (job, head): ec[8], hs[8]
 enum Scal { SC_EC = 0, SC_HS = 8, SC_IS = 16, SC_D = 24 };
 // A continuation segment may start from a zero state this many nats of decay
 // (both heads) before its first block instead of waiting for the previous CTA's
-// hand-off: what the zero start leaves out is scaled by e^{-44} < 2^-63.
-constexpr float kWarmupNats = 44.f;
+// hand-off: what the zero start leaves out is scaled by e^{-32} < 2^-46, some
+// 2^-22 of one fp32 unit in the last place of the state it is added to.
+constexpr float kWarmupNats = 32.f;
 // Decay-sorted head pairs: the pair table is sorted when nheads and the
 // per-group sort stay this small (every table CTA sorts its own copy).
 constexpr int kSortMaxHeads = 1024;
@@ -99,9 +100,14 @@ constexpr uint32_t kRecSmem = kRecTab + kRecScal + 16;
 constexpr uint32_t kRecBytes = kRecSmem + kHG * kNumTabX * kT * 4;
 static_assert(kRecSmem % 16 == 0 && kRecBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 
-// Per-dstate layout (NS = 128 or 256). The ring carries, per job, L and then
-// B and C in 128-column halves of n: kKinds ring entries of 32 KB at
-// positions kKinds J + kind (kind 0: L, 1 .. kNB: B halves, then C halves).
+// Per-dstate layout (NS = 128 or 256). The ring carries, per job, L and B and C
+// in 128-column halves of n: kKinds ring entries of 32 KB at positions
+// kKinds J + kind, in the order L, B halves, C halves. A ring entry reuses the
+// slot of the entry four positions earlier, so at 256 (five entries for four
+// slots) a job's last C half waits for its own L, which k5a frees. It must not
+// wait for a B half: k3 frees B only after its last sub-block, whose state
+// rescale waits (H being single-buffered) for k5b of the sub-block before,
+// which needs that C half.
 // TMEM (512 columns): the fp32 state Z (NS columns), kHBuf bf16 copies H of
 // the scaled state (NS / 2 columns each, the A operand of k5b) and kYBuf
 // output accumulators Y (128 columns each). At NS = 256 the state takes half
@@ -117,6 +123,7 @@ struct Lay {
     static constexpr uint32_t COL_H = NS;
     static constexpr uint32_t COL_Y = NS + kHBuf * (NS / 2);
     static_assert(COL_Y + kYBuf * 128 == 512, "TMEM budget");
+    __host__ __device__ static constexpr int kindL() { return 0; }
     __host__ __device__ static constexpr int kindB(int half) { return 1 + half; }
     __host__ __device__ static constexpr int kindC(int half) { return 1 + kNB + half; }
 };
@@ -358,15 +365,25 @@ __device__ __noinline__ void fixup_tokens(uint32_t ycol, uint32_t extreme, int q
 
 // This CTA's job range [first, last) when the jobs are split by estimated cost
 // (all kThreads threads; out[0..1] and sh[0..15] in shared memory). CTA c
-// starts after the job i whose cost interval (before, after] holds
-// T_c = ceil(c total / ncta), c in [1, ncta); T_c increases with c, so every
-// such c lands on exactly one job. With at least kBalanceMin jobs per CTA,
-// T_{c+1} - T_c >= 10 kBalanceMin - 1 exceeds any one job's cost (at most 110),
-// so no range is empty. Thread t sums the costs of a contiguous run of the
-// byte array, a block scan places each thread's run on the cost line, and the
-// thread whose run holds T_cta or T_cta+1 finds the job.
+// starts after the job i whose cost interval (before, after] holds the target
+// T_c, c in [1, ncta); T_c increases with c, so every such c lands on exactly
+// one job. Plain split: T_c = ceil(c total / ncta). With at least kBalanceMin
+// jobs per CTA, T_{c+1} - T_c >= 10 kBalanceMin - 1 exceeds any one job's cost
+// (at most 110), so no range is empty. Thread t sums the costs of a contiguous
+// run of the byte array, a block scan places each thread's run on the cost
+// line, and the thread whose run holds a target finds its job.
+//
+// Long chains (horizon != null, pen[ncta] in shared memory): a CTA whose range
+// starts at block a > 0 of a chain first warms up over min(a, horizon[chain])
+// blocks, so the split charges each boundary that warm-up: a first pass places
+// the plain boundaries and records pen[c] (10 per warm-up block) at each, and
+// the second sets T_c = ceil(c (total + sum pen) / ncta) - sum_{c' < c} pen[c'],
+// so that range cost plus warm-up is the same for every CTA. A charge is
+// capped at half a plain share, which keeps the boundaries increasing and, with
+// kBalanceMin jobs per CTA, every range non-empty.
 __device__ __noinline__ void cta_range(const uint8_t* cost, long long njob, long long ncta, int cta,
-                                       unsigned long long* sh, uint32_t* out) {
+                                       unsigned long long* sh, uint32_t* out, const int* horizon, int nblk,
+                                       uint32_t* pen) {
     const int t = threadIdx.x, l = t & 31, wp = t >> 5;
     const long long nw = (njob + 3) / 4;  // 4-byte words (the array is padded to them)
     const long long k = (nw + kThreads - 1) / kThreads;
@@ -394,25 +411,97 @@ __device__ __noinline__ void cta_range(const uint8_t* cost, long long njob, long
         if (i < wp) before += sh[i];
         total += sh[i];
     }
+    // the job after the one whose cost interval holds tc, or -1 when tc is not in this thread's run
+    auto find = [&](unsigned long long tc) -> long long {
+        if (!(before < tc && tc <= before + sum)) return -1;
+        unsigned long long run = before;
+        for (long long i = w0; i < w1; ++i) {
+            const uint32_t v = word(i);
+            for (int b = 0; b < 4; ++b) {
+                run += (v >> (8 * b)) & 0xffu;
+                if (run >= tc) return 4 * i + b + 1;
+            }
+        }
+        return -1;
+    };
+    unsigned long long tgt[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) tgt[e] = ((cta + e) * total + ncta - 1) / ncta;
+    if (horizon) {
+        // pass 1: the warm-up charge at every plain boundary, recorded by the thread that finds it
+        if (t == 0) pen[0] = 0u;
+        if (sum > 0) {
+            long long c = static_cast<long long>((before * ncta) / total);  // the first c with T_c > before is c or c + 1
+            for (; c < ncta; ++c) {
+                const unsigned long long tc = (c * total + ncta - 1) / ncta;
+                if (c == 0 || tc <= before) continue;
+                if (tc > before + sum) break;
+                const long long j = find(tc);
+                const long long ch = j / nblk, a = j - ch * nblk;
+                const long long wu = a > 0 ? 10 * min(a, static_cast<long long>(horizon[ch])) : 0;
+                pen[c] = static_cast<uint32_t>(min(wu, static_cast<long long>(total / ncta / 2)));
+            }
+        }
+        __syncthreads();
+        unsigned long long p_all = 0, p_before[2] = {0, 0};
+        for (long long c = 1; c < ncta; ++c) {
+            p_all += pen[c];
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                if (c < cta + e) p_before[e] += pen[c];
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const long long tc = static_cast<long long>(((cta + e) * (total + p_all) + ncta - 1) / ncta) -
+                                 static_cast<long long>(p_before[e]);
+            tgt[e] = static_cast<unsigned long long>(max(1ll, min(tc, static_cast<long long>(total))));
+        }
+    }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const long long c = cta + e;
         if (c == 0 || c == ncta) continue;
-        const unsigned long long tc = (c * total + ncta - 1) / ncta;
-        if (before < tc && tc <= before + sum) {
-            unsigned long long run = before;
-            for (long long i = w0; i < w1; ++i) {
-                const uint32_t v = word(i);
-                for (int b = 0; b < 4; ++b) {
-                    run += (v >> (8 * b)) & 0xffu;
-                    if (run >= tc) {
-                        out[e] = static_cast<uint32_t>(4 * i + b + 1);
-                        i = w1;
-                        break;
-                    }
-                }
+        const long long j = find(tgt[e]);
+        if (j >= 0) out[e] = static_cast<uint32_t>(j);
+    }
+    __syncthreads();
+}
+
+// Per-chain warm-up horizon for the long-chain split (all kThreads threads):
+// the mean block decay of each head over the chain, from the per-job decays;
+// horizon[chain] = min(nblk, ceil(kWarmupNats / the smaller mean)) blocks.
+// dsum[2 nchains] is shared-memory scratch.
+__device__ __noinline__ void chain_horizons(const float2* __restrict__ decay, long long njob, int nblk, int nchains,
+                                            float* dsum, int* horizon) {
+    const int t = threadIdx.x;
+    for (int i = t; i < 2 * nchains; i += kThreads) dsum[i] = 0.f;
+    __syncthreads();
+    const long long k = (njob + kThreads - 1) / kThreads;
+    const long long j0 = min(njob, t * k), j1 = min(njob, j0 + k);
+    long long cur = -1;
+    float a0 = 0.f, a1 = 0.f;
+    for (long long j = j0; j < j1; ++j) {
+        const long long c = j / nblk;
+        if (c != cur) {
+            if (cur >= 0) {
+                atomicAdd(dsum + 2 * cur, a0);
+                atomicAdd(dsum + 2 * cur + 1, a1);
             }
+            cur = c;
+            a0 = a1 = 0.f;
         }
+        const float2 d = __ldg(decay + j);
+        a0 += d.x;
+        a1 += d.y;
+    }
+    if (cur >= 0) {
+        atomicAdd(dsum + 2 * cur, a0);
+        atomicAdd(dsum + 2 * cur + 1, a1);
+    }
+    __syncthreads();
+    for (int c = t; c < nchains; c += kThreads) {
+        const float m = fminf(dsum[2 * c], dsum[2 * c + 1]) / static_cast<float>(nblk);
+        horizon[c] = m > 0.f ? static_cast<int>(fminf(ceilf(kWarmupNats / m), static_cast<float>(nblk))) : nblk;
     }
     __syncthreads();
 }
@@ -426,10 +515,10 @@ __device__ __noinline__ void cta_range(const uint8_t* cost, long long njob, long
 // (t_ready); this CTA needs it once the rest of its range is done (t_need, the
 // segment runs last). Waiting ends the range at t_ready + t_seg, warming up at
 // t_range + cost(warm-up): warm up when that is earlier (warmup = 1), or
-// always (warmup = 2). Every load of a pass over the bytes is issued before
+// always (warmup = 2, or long chains, whose split already charges it). Every load of a pass over the bytes is issued before
 // the first sum, so the decision costs about one memory round trip per 128
 // jobs of the chain.
-__device__ __noinline__ int warmup_blocks(const ChainParams& prm, const JobList& jobs, int lane) {
+__device__ __noinline__ int warmup_blocks(const ChainParams& prm, const JobList& jobs, int lane, bool force) {
     const int a = jobs.a;
     const long long base = static_cast<long long>(jobs.cF) * jobs.nblk;
     // horizon: walk back from block a - 1, 32 blocks per step
@@ -460,7 +549,7 @@ __device__ __noinline__ int warmup_blocks(const ChainParams& prm, const JobList&
         d0 += __shfl_sync(0xffffffffu, e0, 31);
         d1 += __shfl_sync(0xffffffffu, e1, 31);
     }
-    if (prm.warmup == 2) return m;
+    if (prm.warmup == 2 || force) return m;
     // one pass over the cost bytes of [base, max(last, segment end)): every job
     // byte falls into the sums it belongs to
     const long long seg_end = jobs.cF == jobs.cL ? jobs.last : base + jobs.nblk;
@@ -545,16 +634,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::griddep_wait();  // L tiles, tables and costs from the two kernels before
     auto WB = [&](int bar, uint32_t parity) { wait_bar(&bars[bar], parity, prm.status, abort_flag); };
     int first = static_cast<int>(prm.total * cta / prm.ncta), last = static_cast<int>(prm.total * (cta + 1) / prm.ncta);
+    // Long chains (more than two CTA shares of jobs): most CTAs lie inside one
+    // chain, their hand-offs would come one after another, so every CTA
+    // boundary inside a chain warms up, and
+    // the split charges each boundary its warm-up. The ring and X/W areas of
+    // shared memory serve as scratch until the pipeline starts.
+    const bool long_chains = prm.cost && prm.warmup != 0 && static_cast<long long>(prm.nblk) * prm.ncta > 2 * prm.total &&
+                             static_cast<long long>(prm.nchains) * 12 + 4 * prm.ncta <= 12 * kTile;
     if (prm.cost) {
         uint32_t* out = misc + 4;
-        cta_range(prm.cost, prm.total, prm.ncta, cta, reinterpret_cast<unsigned long long*>(smem + K::OFF_SCAN), out);
+        int* horizon = nullptr;
+        uint32_t* pen = nullptr;
+        if (long_chains) {
+            float* dsum = reinterpret_cast<float*>(smem + K::OFF_RING);
+            horizon = reinterpret_cast<int*>(dsum + 2 * prm.nchains);
+            pen = reinterpret_cast<uint32_t*>(horizon + prm.nchains);
+            chain_horizons(prm.decay, prm.total, prm.nblk, prm.nchains, dsum, horizon);
+        }
+        cta_range(prm.cost, prm.total, prm.ncta, cta, reinterpret_cast<unsigned long long*>(smem + K::OFF_SCAN), out,
+                  horizon, prm.nblk, pen);
+        if (long_chains) {  // the scratch is overwritten by TMA copies next
+            ptx::fence_proxy_async_smem();
+            __syncthreads();
+        }
         first = cta == 0 ? 0 : static_cast<int>(out[0]);
         last = cta == prm.ncta - 1 ? static_cast<int>(prm.total) : static_cast<int>(out[1]);
     }
     JobList jobs = make_jobs(prm, first, last);
     if (jobs.a > 0 && prm.warmup != 0) {
         if (warp == 0) {
-            const int wu = warmup_blocks(prm, jobs, lane);
+            const int wu = warmup_blocks(prm, jobs, lane, long_chains);
             if (lane == 0) misc[6] = static_cast<uint32_t>(wu);
         }
         __syncthreads();
@@ -579,14 +688,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint64_t* fb = &bars[B_R_FULL0 + rs];
                 uint8_t* dst = smem + K::OFF_RING + rs * 2 * kTile;
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
-                if (kind == 0) {
+                if (kind == Y::kindL()) {
                     const int tile = (jp.b * prm.nblk + jp.blk) * prm.G + jp.g;
                     ptx::tma_load_4d(dst, &tm_l, fb, 0, 0, 0, tile);
                     ptx::tma_load_4d(dst + kTile, &tm_l, fb, 64, 0, 0, tile);
                 } else {
                     // a 128-column half of B or C: n in [128 half, 128 half + 128)
-                    const bool is_b = kind <= Y::kNB;
-                    const int n0 = 128 * (is_b ? kind - 1 : kind - 1 - Y::kNB);
+                    const bool is_b = kind < Y::kindC(0);
+                    const int n0 = 128 * (is_b ? kind - Y::kindB(0) : kind - Y::kindC(0));
                     const CUtensorMap* m = is_b ? &tm_b : &tm_c;
                     ptx::tma_load_4d(dst, m, fb, n0, jp.g, jp.blk * kT, jp.b);
                     ptx::tma_load_4d(dst + kTile, m, fb, n0 + 64, jp.g, jp.blk * kT, jp.b);
@@ -648,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t extreme = JW(ts)[1];
                 const int qs = kT / nq, ksub = 8 / nq;
                 const uint32_t yc = tmem + Y::COL_Y + 128 * yb;
-                const int pl = Y::kKinds * J;
+                const int pl = Y::kKinds * J + Y::kindL();
                 const bool warm = job_pos(jobs, J, chains_per_b, HperG, order).warm;  // no output: no k5a / k5b
                 if (J >= Y::kYBuf)  // the epilogue has read job J - kYBuf
                     WB(B_Y_EMPTY0 + yb, ((J / Y::kYBuf) - 1) & 1);
