@@ -61,7 +61,8 @@ typedef enum {
     SSD_ERR_UNSUPPORTED = 2,     /* valid but outside what the chosen path implements */
     SSD_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed */
     SSD_ERR_DEVICE_TIMEOUT = 4,  /* a bounded device-side wait gave up */
-    SSD_ERR_WORKSPACE = 5        /* caller workspace too small or misaligned */
+    SSD_ERR_WORKSPACE = 5,       /* caller workspace too small or misaligned */
+    SSD_ERR_DEBUG_CHECK = 6      /* debug build only: a kernel's index or bounds check failed */
 } ssd_status;
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
@@ -187,8 +188,24 @@ SSD_API ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype,
                         int chunk_len, int ngroups, void* y, float* final_state, void* stream);
 
 /* Synchronizes `stream`, then returns and clears the current device's status
- * word: SSD_OK, SSD_ERR_DEVICE_TIMEOUT, or SSD_ERR_CUDA if the sync failed. */
+ * word: SSD_OK, SSD_ERR_DEVICE_TIMEOUT, SSD_ERR_DEBUG_CHECK (debug build only,
+ * see ssd_debug_build), or SSD_ERR_CUDA if the sync failed. */
 SSD_API ssd_status ssd_device_status(void* stream);
+
+/*
+ * Debug build (libssd_debug.so, compiled with SSD_DEBUG; the stand-in for a
+ * memory checker): every index the tensor-core kernels compute by hand (ring,
+ * X/W and table slots, tensor-memory columns, TMA coordinates, global state
+ * rows, job positions) is checked before use. A failed check skips that
+ * access (a skipped copy then ends in a bounded-wait timeout, never in a
+ * fault), and ssd_device_status reports SSD_ERR_DEBUG_CHECK.
+ * ssd_debug_build: 1 in that build, 0 in the release build.
+ * ssd_debug_failed_line: source line of the first failed check since the last
+ * ssd_device_status call that saw it (0: none; always 0 in the release build);
+ * call it before ssd_device_status, which clears it. Synchronizes `stream`.
+ */
+SSD_API int ssd_debug_build(void);
+SSD_API unsigned ssd_debug_failed_line(void* stream);
 
 /* Static, human-readable name of a status code. */
 SSD_API const char* ssd_status_string(ssd_status status);

@@ -26,9 +26,10 @@ __all__ = [
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(_HERE, "libssd.so")
+LIBRARY_DEBUG = os.path.join(_HERE, "libssd_debug.so")  # the index-checked build (SSD_DEBUG)
 
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_CUDA",
-          4: "SSD_ERR_DEVICE_TIMEOUT", 5: "SSD_ERR_WORKSPACE"}
+          4: "SSD_ERR_DEVICE_TIMEOUT", 5: "SSD_ERR_WORKSPACE", 6: "SSD_ERR_DEBUG_CHECK"}
 PATHS = {"auto": 0, "simt": 1, "tc": 2, "chain": 3}
 DTYPES = {"f32": 0, "bf16": 1}
 
@@ -52,6 +53,16 @@ class SsdError(RuntimeError):
 
 
 _lib: Optional[ctypes.CDLL] = None
+
+
+def use_library(path: str) -> str:
+    """Make every later call go through the libssd build at `path` (for
+    example LIBRARY_DEBUG); returns the path used until now."""
+    global _lib, LIBRARY
+    old = LIBRARY
+    LIBRARY = path
+    _lib = None
+    return old
 
 
 def library() -> ctypes.CDLL:
@@ -86,6 +97,10 @@ def library() -> ctypes.CDLL:
     lib.ssd_kernel_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]
     lib.ssd_release.restype = None
     lib.ssd_release.argtypes = []
+    lib.ssd_debug_build.restype = i
+    lib.ssd_debug_build.argtypes = []
+    lib.ssd_debug_failed_line.restype = ctypes.c_uint
+    lib.ssd_debug_failed_line.argtypes = [vp]
     lib.ssd_step.restype = i
     lib.ssd_step.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, i, vp, vp]
     plim = ctypes.POINTER(DtLimit)

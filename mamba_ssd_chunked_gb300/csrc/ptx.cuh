@@ -26,6 +26,20 @@
 #include <cstdint>
 #include <cuda.h>
 
+// SSD_CHECK(status, cond): in a build with SSD_DEBUG defined, a false cond sets
+// bit 3 of the device status word `status` (an unsigned[2]; word 1 keeps the
+// source line of the first failed check) and yields false, so that the caller
+// skips the access it guards; in other builds it is `true` and costs nothing.
+// The debug build checks the indices the kernels compute by hand (ring, X/W and
+// table slots, tensor-memory columns, TMA coordinates, global state rows, job
+// positions); a skipped copy ends in a bounded-wait timeout, never in a fault.
+#ifdef SSD_DEBUG
+#define SSD_CHECK(status, cond) \
+    ((cond) ? true : (atomicCAS((status) + 1, 0u, static_cast<unsigned>(__LINE__)), atomicOr((status), 8u), false))
+#else
+#define SSD_CHECK(status, cond) true
+#endif
+
 namespace ssd {
 namespace ptx {
 

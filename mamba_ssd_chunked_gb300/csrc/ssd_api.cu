@@ -13,8 +13,10 @@ namespace {
 
 std::atomic<uint64_t> g_launches{0};
 
-// Bit 0: a bounded device-side wait gave up (see the kernels).
-__device__ unsigned g_status_word;
+// Word 0: bit 0 / 1: a bounded device-side wait gave up (see the kernels);
+// bit 3: a debug-build index check failed (SSD_CHECK). Word 1: source line of
+// the first failed debug check.
+__device__ unsigned g_status_word[2];
 
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s per device-side wait
 constexpr int kMaxDevices = 64;
@@ -469,9 +471,9 @@ ssd_status ssd_device_status(void* stream) {
     unsigned v = 0;
     if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SSD_ERR_CUDA;
     if (v != 0) {
-        const unsigned zero = 0;
-        if (cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SSD_ERR_CUDA;
-        return SSD_ERR_DEVICE_TIMEOUT;
+        const unsigned zero[2] = {0, 0};
+        if (cudaMemcpy(word, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SSD_ERR_CUDA;
+        return (v & 8u) ? SSD_ERR_DEBUG_CHECK : SSD_ERR_DEVICE_TIMEOUT;
     }
     return SSD_OK;
 }
@@ -484,11 +486,31 @@ const char* ssd_status_string(ssd_status status) {
         case SSD_ERR_CUDA: return "CUDA error";
         case SSD_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         case SSD_ERR_WORKSPACE: return "workspace too small or misaligned";
+        case SSD_ERR_DEBUG_CHECK: return "a debug-build index or bounds check failed in a kernel";
     }
     return "unknown status";
 }
 
 uint64_t ssd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int ssd_debug_build(void) {
+#ifdef SSD_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+unsigned ssd_debug_failed_line(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return 0;
+    int dev = 0;
+    if (current_device(&dev) != SSD_OK) return 0;
+    unsigned* word = nullptr;
+    if (status_word(dev, &word) != SSD_OK) return 0;
+    unsigned v[2] = {0, 0};
+    if (cudaMemcpy(v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return 0;
+    return v[1];
+}
 
 void ssd_kernel_timing(int enable) { g_timing.store(enable ? 1 : 0, std::memory_order_relaxed); }
 

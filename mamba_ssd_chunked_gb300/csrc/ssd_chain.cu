@@ -245,7 +245,7 @@ struct JobPos {
 };
 
 __device__ __forceinline__ JobPos job_pos(const JobList& jobs, int J, int chains_per_b, int HperG,
-                                       const int* __restrict__ order) {
+                                       const int* __restrict__ order, uint32_t* status) {
     JobPos jp;
     int chain;
     jobs.at(J, chain, jp.blk, jp.lo, jp.hi);
@@ -254,6 +254,11 @@ __device__ __forceinline__ JobPos job_pos(const JobList& jobs, int J, int chains
     jp.g = (jp.cb * kHG) / HperG;  // pairs never straddle a group
     jp.h[0] = __ldg(order + kHG * jp.cb);
     jp.h[1] = __ldg(order + kHG * jp.cb + 1);
+    // a job inside its segment and the block range; both heads real heads of the pair's group
+    SSD_CHECK(status, J >= 0 && J < jobs.count() && 0 <= jp.lo && jp.lo <= jp.blk && jp.blk < jp.hi &&
+                          jp.hi <= jobs.nblk && chain >= 0);
+    SSD_CHECK(status, jp.h[0] >= 0 && jp.h[1] >= 0 && jp.h[0] < kHG * chains_per_b && jp.h[1] < kHG * chains_per_b &&
+                          jp.h[0] != jp.h[1] && jp.h[0] / HperG == jp.g && jp.h[1] / HperG == jp.g);
     const bool seg_f = (chain == jobs.cF);
     jp.warm = seg_f && jp.blk < jobs.a;
     jp.wait = seg_f && jp.lo > 0 && jobs.wu == 0;
@@ -660,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         first = cta == 0 ? 0 : static_cast<int>(out[0]);
         last = cta == prm.ncta - 1 ? static_cast<int>(prm.total) : static_cast<int>(out[1]);
     }
+    SSD_CHECK(prm.status, 0 <= first && first < last && last <= prm.total);
     JobList jobs = make_jobs(prm, first, last);
     if (jobs.a > 0 && prm.warmup != 0) {
         if (warp == 0) {
@@ -684,12 +690,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ru > 0) WB(B_R_EMPTY0 + rs, (ru - 1) & 1);
                 if (*abort_flag) break;
                 const int J = pr / Y::kKinds, kind = pr - Y::kKinds * J;
-                const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order);
+                const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
                 uint64_t* fb = &bars[B_R_FULL0 + rs];
                 uint8_t* dst = smem + K::OFF_RING + rs * 2 * kTile;
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
+                SSD_CHECK(prm.status, rs < kRing && jp.b < prm.batch && jp.g < prm.G);
                 if (kind == Y::kindL()) {
                     const int tile = (jp.b * prm.nblk + jp.blk) * prm.G + jp.g;
+                    SSD_CHECK(prm.status, tile >= 0 && tile < prm.batch * prm.nblk * prm.G);
                     ptx::tma_load_4d(dst, &tm_l, fb, 0, 0, 0, tile);
                     ptx::tma_load_4d(dst + kTile, &tm_l, fb, 64, 0, 0, tile);
                 } else {
@@ -697,6 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool is_b = kind < Y::kindC(0);
                     const int n0 = 128 * (is_b ? kind - Y::kindB(0) : kind - Y::kindC(0));
                     const CUtensorMap* m = is_b ? &tm_b : &tm_c;
+                    // a TMA copy's innermost coordinate must stay 16-byte aligned (8 bf16)
+                    SSD_CHECK(prm.status, n0 % 8 == 0 && n0 >= 0 && n0 + 128 <= NS);
                     ptx::tma_load_4d(dst, m, fb, n0, jp.g, jp.blk * kT, jp.b);
                     ptx::tma_load_4d(dst + kTile, m, fb, n0 + 64, jp.g, jp.blk * kT, jp.b);
                 }
@@ -734,7 +744,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
 #pragma unroll
                     for (int hh = 0; hh < Y::kNB; ++hh)  // Z columns [128 hh, 128 hh + 128) are n of that half
-                        mma_k3(tmem + Y::COL_Z + 128 * hh, a_w, b_b[hh], idesc, q * ksub, ksub);
+                        if (SSD_CHECK(prm.status, Y::COL_Z + 128 * hh + 128 <= Y::COL_H && (q + 1) * ksub <= 8))
+                            mma_k3(tmem + Y::COL_Z + 128 * hh, a_w, b_b[hh], idesc, q * ksub, ksub);
                     ptx::mma_commit(&bars[B_S_DONE]);
                 }
 #pragma unroll
@@ -758,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int qs = kT / nq, ksub = 8 / nq;
                 const uint32_t yc = tmem + Y::COL_Y + 128 * yb;
                 const int pl = Y::kKinds * J + Y::kindL();
-                const bool warm = job_pos(jobs, J, chains_per_b, HperG, order).warm;  // no output: no k5a / k5b
+                const bool warm = job_pos(jobs, J, chains_per_b, HperG, order, prm.status).warm;  // no output: no k5a / k5b
                 if (J >= Y::kYBuf)  // the epilogue has read job J - kYBuf
                     WB(B_Y_EMPTY0 + yb, ((J / Y::kYBuf) - 1) & 1);
                 WB(B_W_FULL0 + xs, (J >> 1) & 1);
@@ -770,7 +781,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if ((extreme >> q) & 1u) continue;
                     const uint64_t b_l =
                         ptx::desc_sw128(sbase + K::OFF_RING + (pl % kRing) * 2 * kTile + q * qs * 128, 16, 1024);
-                    mma_k5a(yc + q * qs, a_w, b_l, id_a, q * ksub, ksub);
+                    if (SSD_CHECK(prm.status, yb < Y::kYBuf && (q + 1) * qs <= kT && (q + 1) * ksub <= 8 &&
+                                                  Y::COL_Y + 128 * yb + 128 <= 512))
+                        mma_k5a(yc + q * qs, a_w, b_l, id_a, q * ksub, ksub);
                 }
                 ptx::mma_commit(&bars[B_R_EMPTY0 + pl % kRing]);
                 ptx::mma_commit(&bars[B_XW_FREE0 + xs]);
@@ -789,8 +802,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int hh = 0; hh < Y::kNB; ++hh) {  // K = n in halves: H columns 64 hh.., C half hh
                             const uint64_t b_c = ptx::desc_sw128(c_slot[hh] + q * qs * 128, 16, 1024);
-                            mma_k5b(yc + q * qs, tmem + Y::COL_H + (NS / 2) * hb + 64 * hh, b_c, id_b,
-                                    hh > 0 ? 1u : ((~extreme >> q) & 1u));
+                            if (SSD_CHECK(prm.status, hb < Y::kHBuf && Y::COL_H + (NS / 2) * hb + 64 * hh + 64 <= Y::COL_Y &&
+                                                          (q + 1) * qs <= kT))
+                                mma_k5b(yc + q * qs, tmem + Y::COL_H + (NS / 2) * hb + 64 * hh, b_c, id_b,
+                                        hh > 0 ? 1u : ((~extreme >> q) & 1u));
                         }
                     }
                     ptx::mma_commit(&bars[B_H_EMPTY0 + hb]);
@@ -812,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ts = jx & (kTabSlots - 1);
                 if (jx >= kTabSlots) WB(B_TAB_EMPTY0 + ts, ((jx / kTabSlots) - 1) & 1);
                 if (*abort_flag) break;
-                const JobPos jp = job_pos(jobs, jx, chains_per_b, HperG, order);
+                const JobPos jp = job_pos(jobs, jx, chains_per_b, HperG, order, prm.status);
                 const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.cb) * prm.nblk + jp.blk;
                 ptx::mbar_arrive_expect_tx(&bars[B_TAB_FULL0 + ts], kRecSmem);
                 ptx::bulk_load(smem + K::OFF_TAB + ts * kRecSmem, prm.tables + rec * kRecBytes, kRecSmem,
@@ -822,6 +837,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*abort_flag) break;
                 uint64_t* fb = &bars[B_X_FULL0 + (jx & 1)];
                 uint8_t* dst = smem + K::OFF_XW + (jx & 1) * 2 * kTile;
+                SSD_CHECK(prm.status, K::OFF_XW + ((jx & 1) + 1) * 2 * kTile <= K::OFF_TAB &&
+                                          static_cast<long long>(jp.blk) * kT < prm.L && jp.b < prm.batch);
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
                 ptx::tma_load_4d(dst, &tm_x, fb, 0, jp.h[0], jp.blk * kT, jp.b);
                 ptx::tma_load_4d(dst + kTile, &tm_x, fb, 0, jp.h[1], jp.blk * kT, jp.b);
@@ -831,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               kP * NS * sizeof(float));
                 if (jx + 2 < njobs) {
                     // the X of job jx + 2 into L2: its load, once the slot is free, then hits L2
-                    const JobPos jn = job_pos(jobs, jx + 2, chains_per_b, HperG, order);
+                    const JobPos jn = job_pos(jobs, jx + 2, chains_per_b, HperG, order, prm.status);
                     ptx::tma_prefetch_4d(&tm_x, 0, jn.h[0], jn.blk * kT, jn.b);
                     ptx::tma_prefetch_4d(&tm_x, 0, jn.h[1], jn.blk * kT, jn.b);
                 }
@@ -892,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sdone = 0, u = 0;
         for (int J = 0; J < njobs; ++J) {
             const int ts = J & (kTabSlots - 1);
-            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order);
+            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
             const bool seg_start = (jp.blk == jp.lo), seg_end = (jp.blk == jp.hi - 1);
             const int h = jp.h[j];
             if (seg_start && jp.wait) {
@@ -923,6 +940,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     src = nullptr;  // warm-up from a zero state
                 else if (prm.init)
                     src = prm.init + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * NS;
+                // a hand-off row of the previous CTA or an initial-state row of a real (batch, head)
+                if (!SSD_CHECK(prm.status, (jp.wait ? (cta >= 1 && cta <= prm.ncta - 1)
+                                                    : (jp.b < prm.batch && h >= 0 && h < prm.H)) && p < kP))
+                    src = nullptr;
                 inv_prev = 1.f;
             }
             for (int q = 0; q < nq; ++q, ++u) {
@@ -937,6 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float ec = sc[SC_EC + q], hs = sc[SC_HS + q];
                 const uint32_t zcol = tmem + lane_base + Y::COL_Z;
                 const uint32_t hcol = tmem + lane_base + Y::COL_H + (NS / 2) * hb;
+                SSD_CHECK(prm.status, hb < Y::kHBuf && Y::COL_H + (NS / 2) * (hb + 1) <= Y::COL_Y && q < 8 && ts < kTabSlots);
 #pragma unroll 1
                 for (int k = 0; k < NS / 32; ++k) {
                     uint32_t r[32];
@@ -989,6 +1011,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ? prm.final_state + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * NS
                                              : nullptr)
                                       : prm.handoff + ((static_cast<size_t>(cta) * kHG + j) * kP + p) * NS;
+                // the final state of a real (batch, head), or this CTA's own hand-off slot
+                if (!SSD_CHECK(prm.status, to_final ? (jp.b < prm.batch && h >= 0 && h < prm.H) : (cta < prm.ncta - 1)))
+                    dst = nullptr;
 #pragma unroll 1
                 for (int k = 0; k < NS / 32; ++k) {
                     uint32_t r[32];
@@ -1033,7 +1058,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2* g2 = reinterpret_cast<const float2*>(T(ts, j, TAB_UG));
             const uint32_t extreme = JW(ts)[1];
             const bool rare = (extreme | JW(ts)[2]) != 0u;
-            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order);
+            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
             WB(B_Y_FULL0 + yb, (J / Y::kYBuf) & 1);
             WB(B_XW_FREE0 + xs, (J >> 1) & 1);  // k3 and k5a no longer read W
             ptx::tc_fence_after();
@@ -1049,6 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
                 const uint32_t ylane = tmem + (static_cast<uint32_t>(32 * q4 + 16 * hf) << 16) + Y::COL_Y + 128 * yb;
+                SSD_CHECK(prm.status, yb < Y::kYBuf && Y::COL_Y + 128 * (yb + 1) <= 512 && xs < 2);
                 const uint32_t pc = 4 * (q4 & 1) + 2 * hf + (mm & 1);  // 16-byte chunk of p in the row
 #pragma unroll 1
                 for (int k = 0; k < 4; ++k) {
@@ -1064,6 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int tb = 32 * k + 16 * c;
                         const int trow = tb + 8 * (mm >> 1) + mrow;
                         const uint32_t addr = tile + trow * 128 + ((pc ^ (trow & 7)) << 4);
+                        SSD_CHECK(prm.status, trow < kT && pc < 8);
                         uint32_t w[4];
                         ptx::ldmatrix_x4_trans(addr, w);
                         uint32_t o[4];
@@ -1085,6 +1112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::fence_proxy_async_smem();
             ptx::named_sync(3, 128);
+            // a store starts at non-negative coordinates inside the tensor (rows past L are dropped)
+            SSD_CHECK(prm.status, jp.h[0] < prm.H && jp.h[1] < prm.H && jp.b < prm.batch &&
+                                      static_cast<long long>(jp.blk) * kT < prm.L);
             if (et == 0) {
                 for (int jj = 0; jj < kHG; ++jj)
                     ptx::tma_store_4d(&tm_y, smem + K::OFF_XW + (xs * kHG + jj) * kTile, 0, jp.h[jj],
@@ -1104,6 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int p = et & 63;
                 const long long t0 = static_cast<long long>(jp.blk) * kT;
                 const int tn = static_cast<int>(min(static_cast<long long>(kT), prm.L - t0));  // valid tokens
+                SSD_CHECK(prm.status, tn >= 1 && tn <= kT && p < kP && ts < kTabSlots);
                 const long long off = ((static_cast<long long>(jp.b) * prm.L + t0) * prm.H + jp.h[j]) * kP + p;
                 const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.cb) * prm.nblk + jp.blk;
                 const float* xt = reinterpret_cast<const float*>(prm.tables + rec * kRecBytes + kRecSmem) +
@@ -1137,6 +1168,7 @@ struct TableParams {
     float2* decay;       // [jobs] decay of the whole block per head (warm-up horizon)
     uint32_t* counters;  // the chain kernel's ticket and flags, zeroed here
     int ncounters;
+    uint32_t* status;    // device status word (debug-build checks)
     int* order;          // [H] heads in pair order (written by CTA 0)
     const int32_t* seq;  // [batch, L] packed-sequence ids, or null
     int sort_pairs;      // pair the heads of each group by decay rate (else 2 cb, 2 cb + 1)
@@ -1214,6 +1246,7 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
         const int b = chain / prm.chains_per_b, cb = chain % prm.chains_per_b;
         const int hh[kHG] = {prm.sort_pairs ? s_order[kHG * cb] : kHG * cb,
                              prm.sort_pairs ? s_order[kHG * cb + 1] : kHG * cb + 1};
+        SSD_CHECK(prm.status, hh[0] >= 0 && hh[1] >= 0 && hh[0] < prm.H && hh[1] < prm.H && hh[0] != hh[1]);
         uint8_t* rec = prm.out + static_cast<size_t>(job) * kRecBytes;
         float* tabs = reinterpret_cast<float*>(rec);
         float* scal = reinterpret_cast<float*>(rec + kRecTab);
@@ -1532,6 +1565,7 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     tp.seq = a.seq_idx;
     tp.total = static_cast<int>(pl.total);
     tp.counters = static_cast<uint32_t*>(ws);
+    tp.status = a.status_word;
     tp.ncounters = 1 + pl.ncta;
     tp.order = order;
     tp.G = static_cast<int>(d.ngroups);

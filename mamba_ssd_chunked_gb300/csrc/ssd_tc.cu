@@ -213,6 +213,9 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
     uint64_t* bar_st = bar_of(slot, 7);
     uint64_t* bar_pub = bar_of(slot, 8);
     const bool leader = is_math && stid == 0;
+    // the unit is a real (block, batch row, head group) and its heads share one B/C group
+    SSD_CHECK(prm.status, b < prm.batch && blk < prm.nblk && h0 + hpu <= prm.H && hpu <= kMaxHeads && g < prm.G &&
+                              (h0 + hpu - 1) / (prm.H / prm.G) == g && slot < K::SLOTS);
 
     // ---- TMA: B and C for the unit; X for each slot's first head
     if (tid == 0) {
@@ -370,6 +373,7 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
             for (int q = 0; q < nh; ++q) {
                 const int h = h0 + sl + q * K::SLOTS;
                 const int chain = b * prm.H + h;
+                SSD_CHECK(prm.status, h < h0 + hpu && chain < prm.batch * prm.H && sl < K::SLOTS);
                 bool fail = false;
                 if (blk > 0) {
                     const uint32_t* pf = prm.flags + chain * 2 + ((blk - 1) & 1);
@@ -672,7 +676,7 @@ __global__ void __launch_bounds__(Cfg<NST>::THREADS, 1)
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         ptx::named_sync(1 + slot, 256);
-        if (leader && chain_ok) {
+        if (leader && chain_ok && SSD_CHECK(prm.status, h < prm.H && h >= h0 && h < h0 + hpu)) {
             ptx::tma_store_4d(&tm_y, slot_base + K::SY, 0, h, t0, b);
             ptx::bulk_commit_group();
         }

@@ -29,7 +29,8 @@ def test_header_declares_the_documented_entry_points():
     names = declared_functions()
     for n in ("ssd_fwd", "ssd_fwd_ws", "ssd_fwd_host", "ssd_fwd_workspace_bytes", "ssd_device_status",
               "ssd_status_string", "ssd_kernel_launches", "ssd_release", "ssd_select_path", "ssd_step",
-              "ssd_conv1d_silu", "ssd_conv1d_step", "ssd_gated_rmsnorm", "ssd_fwd_ex", "ssd_step_ex"):
+              "ssd_conv1d_silu", "ssd_conv1d_step", "ssd_gated_rmsnorm", "ssd_fwd_ex", "ssd_step_ex",
+              "ssd_debug_build", "ssd_debug_failed_line"):
         assert n in names
 
 
@@ -47,8 +48,19 @@ def test_kernel_timing_arguments(lib):
     assert ms.value == 0.0 and n.value == 0
 
 
+def test_release_and_debug_builds_say_which_they_are(lib):
+    import ctypes as ct
+    from mamba_ssd_chunked_gb300 import build
+    assert lib.ssd_debug_build() == 0
+    dbg = ct.CDLL(build.build(debug=True))
+    assert dbg.ssd_debug_build() == 1
+    names = declared_functions()
+    for name in names:
+        assert hasattr(dbg, name), f"libssd_debug.so does not export {name}"
+
+
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         assert lib.ssd_status_string(code)
     assert lib.ssd_status_string(99) == b"unknown status"
 
