@@ -90,7 +90,8 @@ constexpr float kWarmupNats = 32.f;
 constexpr int kSortMaxHeads = 1024;
 constexpr long long kSortMaxWork = 65536;  // nheads x heads per group
 constexpr int kThreads = 512;
-constexpr int kRing = 4;                // slots of the L / B / C ring
+constexpr int kRingMax = 4;             // slots of the L / B / C ring, at most (Lay::kRing)
+constexpr int kXWMax = 3;               // X / W / y job slots, at most (Lay::kXW)
 // Per-job table record in the workspace: [2 heads][kNumTab][128] floats,
 // [2 heads][kScal] floats, {nq, extreme, 0, 0} (the part a shared-memory slot
 // holds), then [2 heads][kNumTabX][128] floats.
@@ -119,6 +120,14 @@ struct Lay {
     static constexpr int kKinds = 1 + 2 * kNB;
     static constexpr int kHBuf = NS == 128 ? 2 : 1;
     static constexpr int kYBuf = NS == 128 ? 2 : 1;
+    // Shared memory: kRing ring slots and kXW X/W/y job slots of 32 KB each, six
+    // in all. At 128 a job's L, B and C each own a ring slot and three jobs are
+    // in flight; at 256 a job takes five ring entries, and four ring slots (two
+    // jobs in flight) keep its last C half from waiting for its own B.
+    static constexpr int kRing = NS == 128 ? 3 : 4;
+    static constexpr int kXW = NS == 128 ? 3 : 2;
+    static_assert(kRing <= kRingMax && kXW <= kXWMax && kRing + kXW == 6, "six 32 KB slots");
+    static constexpr uint32_t OFF_XW = 2 * kRing * kTile;
     static constexpr uint32_t COL_Z = 0;
     static constexpr uint32_t COL_H = NS;
     static constexpr uint32_t COL_Y = NS + kHBuf * (NS / 2);
@@ -131,23 +140,22 @@ struct Lay {
 struct Cfg {
     // ring of kRing 32 KB slots ([t][128] as two 64-column tiles) holding, in
     // consumption order, L and the B and C halves of each job (Lay<NS>)
-    static constexpr uint32_t OFF_RING = 0;
-    static constexpr uint32_t OFF_XW = 8 * kTile;        // 2 job slots x 2 heads, X then W then y
+    static constexpr uint32_t OFF_RING = 0;               // then the X/W slots at Lay::OFF_XW
     static constexpr uint32_t OFF_TAB = 12 * kTile;      // [slots] table records
     static constexpr uint32_t OFF_BAR = (OFF_TAB + kTabSlots * kRecSmem + 7) & ~7u;
     static constexpr int NBAR = 40;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_SCAN = OFF_MISC + 64;  // [kThreads / 32] u64, cta_range
-    static constexpr uint32_t SMEM_BYTES = OFF_SCAN + 128 + 1024;
+    static constexpr uint32_t OFF_ORDER = OFF_SCAN + 128;  // [kSortMaxHeads] the pair order (job_pos)
+    static constexpr uint32_t SMEM_BYTES = OFF_ORDER + kSortMaxHeads * 4 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 enum Bar {
-    B_R_FULL0 = 0, B_R_FULL1, B_R_FULL2, B_R_FULL3, B_R_EMPTY0, B_R_EMPTY1, B_R_EMPTY2, B_R_EMPTY3,
-    B_X_FULL0, B_X_FULL1, B_XW_FREE0, B_XW_FREE1, B_XW_EMPTY0, B_XW_EMPTY1,
-    B_TAB_FULL0, B_TAB_FULL3 = B_TAB_FULL0 + 3, B_TAB_EMPTY0, B_TAB_EMPTY3 = B_TAB_EMPTY0 + 3,
-    B_W_FULL0, B_W_FULL1,
-    B_SCALED, B_S_DONE, B_H_FULL0, B_H_FULL1, B_H_EMPTY0, B_H_EMPTY1,
+    B_R_FULL0 = 0, B_R_EMPTY0 = B_R_FULL0 + kRingMax,
+    B_X_FULL0 = B_R_EMPTY0 + kRingMax, B_XW_FREE0 = B_X_FULL0 + kXWMax, B_XW_EMPTY0 = B_XW_FREE0 + kXWMax,
+    B_TAB_FULL0 = B_XW_EMPTY0 + kXWMax, B_TAB_FULL3 = B_TAB_FULL0 + 3, B_TAB_EMPTY0, B_TAB_EMPTY3 = B_TAB_EMPTY0 + 3,
+    B_W_FULL0, B_SCALED = B_W_FULL0 + kXWMax, B_S_DONE, B_H_FULL0, B_H_FULL1, B_H_EMPTY0, B_H_EMPTY1,
     B_Y_FULL0, B_Y_FULL1, B_Y_EMPTY0, B_Y_EMPTY1,
     B_DRAIN_K3, B_DRAIN_Y,
     B_COUNT
@@ -196,6 +204,10 @@ struct JobList {
     int nE, nM;        // lengths of the tail part (processed first) and of the full chains
     int a, wu;         // first output block of chain cF's segment, warm-up blocks before it
     __device__ int count() const { return last - first + wu; }
+    // job J is a warm-up block (the first wu jobs of chain cF's segment, which runs last)
+    __device__ __forceinline__ bool warm(int J) const {
+        return wu > 0 && (cF == cL ? J < wu : (J >= nE + nM && J < nE + nM + wu));
+    }
     __device__ __forceinline__ void at(int J, int& chain, int& blk, int& seg_lo, int& seg_hi) const {
         if (cF == cL) {
             chain = cF;
@@ -252,8 +264,9 @@ __device__ __forceinline__ JobPos job_pos(const JobList& jobs, int J, int chains
     jp.b = chain / chains_per_b;
     jp.cb = chain - jp.b * chains_per_b;
     jp.g = (jp.cb * kHG) / HperG;  // pairs never straddle a group
-    jp.h[0] = __ldg(order + kHG * jp.cb);
-    jp.h[1] = __ldg(order + kHG * jp.cb + 1);
+    // the pair order, from this CTA's shared-memory copy (null: the natural order 2 cb, 2 cb + 1)
+    jp.h[0] = order ? order[kHG * jp.cb] : kHG * jp.cb;
+    jp.h[1] = order ? order[kHG * jp.cb + 1] : kHG * jp.cb + 1;
     // a job inside its segment and the block range; both heads real heads of the pair's group
     SSD_CHECK(status, J >= 0 && J < jobs.count() && 0 <= jp.lo && jp.lo <= jp.blk && jp.blk < jp.hi &&
                           jp.hi <= jobs.nblk && chain >= 0);
@@ -616,11 +629,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t counts[B_COUNT];
         for (int i = 0; i < B_COUNT; ++i) counts[i] = 1;
         for (int i = 0; i < kTabSlots; ++i) counts[B_TAB_EMPTY0 + i] = 5;  // epilogue warps, k3 issuer
-        counts[B_W_FULL0] = counts[B_W_FULL1] = 4;                          // W warps
+        for (int i = 0; i < kXWMax; ++i) {
+            counts[B_W_FULL0 + i] = 4;                                      // W warps
+            counts[B_XW_FREE0 + i] = 2;                                     // k3 and k5a commits
+        }
         counts[B_SCALED] = 4;                                               // state warps
         counts[B_H_FULL0] = counts[B_H_FULL1] = 4;                          // state warps
         counts[B_Y_EMPTY0] = counts[B_Y_EMPTY1] = 4;                        // epilogue warps
-        counts[B_XW_FREE0] = counts[B_XW_FREE1] = 2;                        // k3 and k5a commits
         // B_XW_EMPTY: one epilogue thread, once the y store has read the slot
         for (int i = 0; i < B_COUNT; ++i) ptx::mbar_init(&bars[i], counts[i]);
         misc[3] = 0u;
@@ -678,7 +693,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int njobs = jobs.count();
     const int HperG = prm.H / prm.G;
     const int chains_per_b = prm.H / kHG;
-    const int* order = prm.order;
+    // the pair order into shared memory: every role looks heads up per job; with
+    // more heads than the prep kernel sorts, the order is the natural one
+    int* order = nullptr;
+    if (prm.H <= kSortMaxHeads) {
+        order = reinterpret_cast<int*>(smem + K::OFF_ORDER);
+        for (int i = tid; i < prm.H; i += kThreads) order[i] = __ldg(prm.order + i);
+        __syncthreads();
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer: L, B, C ring
@@ -686,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int npos = Y::kKinds * njobs;
             int pr = 0;
             for (; pr < npos; ++pr) {
-                const int rs = pr % kRing, ru = pr / kRing;
+                const int rs = pr % Y::kRing, ru = pr / Y::kRing;
                 if (ru > 0) WB(B_R_EMPTY0 + rs, (ru - 1) & 1);
                 if (*abort_flag) break;
                 const int J = pr / Y::kKinds, kind = pr - Y::kKinds * J;
@@ -694,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint64_t* fb = &bars[B_R_FULL0 + rs];
                 uint8_t* dst = smem + K::OFF_RING + rs * 2 * kTile;
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
-                SSD_CHECK(prm.status, rs < kRing && jp.b < prm.batch && jp.g < prm.G);
+                SSD_CHECK(prm.status, rs < Y::kRing && jp.b < prm.batch && jp.g < prm.G);
                 if (kind == Y::kindL()) {
                     const int tile = (jp.b * prm.nblk + jp.blk) * prm.G + jp.g;
                     SSD_CHECK(prm.status, tile >= 0 && tile < prm.batch * prm.nblk * prm.G);
@@ -713,9 +735,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // no copy into shared memory may be left in flight at exit: wait for the
             // last load of each slot (earlier ones completed before their reuse)
-            for (int i = 0; i < kRing && i < pr; ++i) {
+            for (int i = 0; i < Y::kRing && i < pr; ++i) {
                 const int P = pr - 1 - i;
-                ptx::mbar_wait(&bars[B_R_FULL0 + P % kRing], (P / kRing) & 1, kLocalWaitNs);
+                ptx::mbar_wait(&bars[B_R_FULL0 + P % Y::kRing], (P / Y::kRing) & 1, kLocalWaitNs);
             }
         }
         __syncwarp();
@@ -725,19 +747,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = idesc_n(128, true, true);
             uint32_t u = 0;  // sub-blocks so far
             for (int J = 0; J < njobs; ++J) {
-                const int ts = J & (kTabSlots - 1), xs = J & 1;
+                const int ts = J & (kTabSlots - 1), xs = J % Y::kXW;
                 WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
                 const int nq = static_cast<int>(JW(ts)[0]);
                 const int ksub = 8 / nq;  // K steps per sub-block
                 ptx::mbar_arrive(&bars[B_TAB_EMPTY0 + ts]);  // this issuer is done with the record
-                WB(B_W_FULL0 + xs, (J >> 1) & 1);
-                const uint64_t a_w = ptx::desc_sw128(sbase + K::OFF_XW + xs * 2 * kTile, kTile, 1024);
+                WB(B_W_FULL0 + xs, (J / Y::kXW) & 1);
+                const uint64_t a_w = ptx::desc_sw128(sbase + Y::OFF_XW + xs * 2 * kTile, kTile, 1024);
                 uint64_t b_b[Y::kNB];
 #pragma unroll
                 for (int hh = 0; hh < Y::kNB; ++hh) {
                     const int pb = Y::kKinds * J + Y::kindB(hh);
-                    WB(B_R_FULL0 + pb % kRing, (pb / kRing) & 1);
-                    b_b[hh] = ptx::desc_sw128(sbase + K::OFF_RING + (pb % kRing) * 2 * kTile, kTile, 1024);
+                    WB(B_R_FULL0 + pb % Y::kRing, (pb / Y::kRing) & 1);
+                    b_b[hh] = ptx::desc_sw128(sbase + K::OFF_RING + (pb % Y::kRing) * 2 * kTile, kTile, 1024);
                 }
                 for (int q = 0; q < nq; ++q, ++u) {
                     WB(B_SCALED, u & 1);
@@ -750,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int hh = 0; hh < Y::kNB; ++hh)
-                    ptx::mma_commit(&bars[B_R_EMPTY0 + (Y::kKinds * J + Y::kindB(hh)) % kRing]);
+                    ptx::mma_commit(&bars[B_R_EMPTY0 + (Y::kKinds * J + Y::kindB(hh)) % Y::kRing]);
                 ptx::mma_commit(&bars[B_XW_FREE0 + xs]);
             }
             ptx::mma_commit(&bars[B_DRAIN_K3]);
@@ -762,37 +784,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t u = 0;
             for (int J = 0; J < njobs; ++J) {
-                const int ts = J & (kTabSlots - 1), xs = J & 1, yb = J % Y::kYBuf;
+                const int ts = J & (kTabSlots - 1), xs = J % Y::kXW, yb = J % Y::kYBuf;
                 WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
                 const int nq = static_cast<int>(JW(ts)[0]);
                 const uint32_t extreme = JW(ts)[1];
                 const int qs = kT / nq, ksub = 8 / nq;
                 const uint32_t yc = tmem + Y::COL_Y + 128 * yb;
                 const int pl = Y::kKinds * J + Y::kindL();
-                const bool warm = job_pos(jobs, J, chains_per_b, HperG, order, prm.status).warm;  // no output: no k5a / k5b
+                const bool warm = jobs.warm(J);  // no output: no k5a / k5b
                 if (J >= Y::kYBuf)  // the epilogue has read job J - kYBuf
                     WB(B_Y_EMPTY0 + yb, ((J / Y::kYBuf) - 1) & 1);
-                WB(B_W_FULL0 + xs, (J >> 1) & 1);
-                WB(B_R_FULL0 + pl % kRing, (pl / kRing) & 1);
+                WB(B_W_FULL0 + xs, (J / Y::kXW) & 1);
+                WB(B_R_FULL0 + pl % Y::kRing, (pl / Y::kRing) & 1);
                 ptx::tc_fence_after();
-                const uint64_t a_w = ptx::desc_sw128(sbase + K::OFF_XW + xs * 2 * kTile, kTile, 1024);
+                const uint64_t a_w = ptx::desc_sw128(sbase + Y::OFF_XW + xs * 2 * kTile, kTile, 1024);
                 const uint32_t id_a = idesc_n(qs, true, false), id_b = idesc_n(qs, false, false);
                 for (int q = 0; q < nq && !warm; ++q) {
                     if ((extreme >> q) & 1u) continue;
                     const uint64_t b_l =
-                        ptx::desc_sw128(sbase + K::OFF_RING + (pl % kRing) * 2 * kTile + q * qs * 128, 16, 1024);
+                        ptx::desc_sw128(sbase + K::OFF_RING + (pl % Y::kRing) * 2 * kTile + q * qs * 128, 16, 1024);
                     if (SSD_CHECK(prm.status, yb < Y::kYBuf && (q + 1) * qs <= kT && (q + 1) * ksub <= 8 &&
                                                   Y::COL_Y + 128 * yb + 128 <= 512))
                         mma_k5a(yc + q * qs, a_w, b_l, id_a, q * ksub, ksub);
                 }
-                ptx::mma_commit(&bars[B_R_EMPTY0 + pl % kRing]);
+                ptx::mma_commit(&bars[B_R_EMPTY0 + pl % Y::kRing]);
                 ptx::mma_commit(&bars[B_XW_FREE0 + xs]);
                 uint32_t c_slot[Y::kNB];
 #pragma unroll
                 for (int hh = 0; hh < Y::kNB; ++hh) {
                     const int pc = Y::kKinds * J + Y::kindC(hh);
-                    WB(B_R_FULL0 + pc % kRing, (pc / kRing) & 1);
-                    c_slot[hh] = sbase + K::OFF_RING + (pc % kRing) * 2 * kTile;
+                    WB(B_R_FULL0 + pc % Y::kRing, (pc / Y::kRing) & 1);
+                    c_slot[hh] = sbase + K::OFF_RING + (pc % Y::kRing) * 2 * kTile;
                 }
                 for (int q = 0; q < nq; ++q, ++u) {
                     const int hb = u % Y::kHBuf;
@@ -812,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int hh = 0; hh < Y::kNB; ++hh)
-                    ptx::mma_commit(&bars[B_R_EMPTY0 + (Y::kKinds * J + Y::kindC(hh)) % kRing]);
+                    ptx::mma_commit(&bars[B_R_EMPTY0 + (Y::kKinds * J + Y::kindC(hh)) % Y::kRing]);
                 ptx::mma_commit(&bars[B_Y_FULL0 + yb]);
             }
             ptx::mma_commit(&bars[B_DRAIN_Y]);
@@ -833,11 +855,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::bulk_load(smem + K::OFF_TAB + ts * kRecSmem, prm.tables + rec * kRecBytes, kRecSmem,
                                &bars[B_TAB_FULL0 + ts]);
                 ++ntab;
-                if (jx >= 2) WB(B_XW_EMPTY0 + (jx & 1), ((jx >> 1) - 1) & 1);  // y of job jx - 2 has left
+                const int xs = jx % Y::kXW;
+                if (jx >= Y::kXW) WB(B_XW_EMPTY0 + xs, ((jx / Y::kXW) - 1) & 1);  // y of job jx - kXW has left
                 if (*abort_flag) break;
-                uint64_t* fb = &bars[B_X_FULL0 + (jx & 1)];
-                uint8_t* dst = smem + K::OFF_XW + (jx & 1) * 2 * kTile;
-                SSD_CHECK(prm.status, K::OFF_XW + ((jx & 1) + 1) * 2 * kTile <= K::OFF_TAB &&
+                uint64_t* fb = &bars[B_X_FULL0 + xs];
+                uint8_t* dst = smem + Y::OFF_XW + xs * 2 * kTile;
+                SSD_CHECK(prm.status, Y::OFF_XW + (xs + 1) * 2 * kTile <= K::OFF_TAB &&
                                           static_cast<long long>(jp.blk) * kT < prm.L && jp.b < prm.batch);
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
                 ptx::tma_load_4d(dst, &tm_x, fb, 0, jp.h[0], jp.blk * kT, jp.b);
@@ -846,16 +869,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < kHG; ++j)
                         ptx::bulk_prefetch_l2(prm.init + (static_cast<size_t>(jp.b) * prm.H + jp.h[j]) * kP * NS,
                                               kP * NS * sizeof(float));
-                if (jx + 2 < njobs) {
-                    // the X of job jx + 2 into L2: its load, once the slot is free, then hits L2
-                    const JobPos jn = job_pos(jobs, jx + 2, chains_per_b, HperG, order, prm.status);
+                if (jx + Y::kXW < njobs) {
+                    // the X of job jx + kXW into L2: its load, once the slot is free, then hits L2
+                    const JobPos jn = job_pos(jobs, jx + Y::kXW, chains_per_b, HperG, order, prm.status);
                     ptx::tma_prefetch_4d(&tm_x, 0, jn.h[0], jn.blk * kT, jn.b);
                     ptx::tma_prefetch_4d(&tm_x, 0, jn.h[1], jn.blk * kT, jn.b);
                 }
             }
-            for (int i = 0; i < 2 && i < jx; ++i) {
+            for (int i = 0; i < Y::kXW && i < jx; ++i) {
                 const int J = jx - 1 - i;
-                ptx::mbar_wait(&bars[B_X_FULL0 + (J & 1)], (J >> 1) & 1, kLocalWaitNs);
+                ptx::mbar_wait(&bars[B_X_FULL0 + J % Y::kXW], (J / Y::kXW) & 1, kLocalWaitNs);
             }
 
             // table copies: the last one per slot
@@ -869,13 +892,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ W from X, in place
         const int wt = tid - 128;  // 0..127
         for (int J = 0; J < njobs; ++J) {
-            const int ts = J & (kTabSlots - 1), xs = J & 1;
+            const int ts = J & (kTabSlots - 1), xs = J % Y::kXW;
             WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
-            WB(B_X_FULL0 + xs, (J >> 1) & 1);
+            WB(B_X_FULL0 + xs, (J / Y::kXW) & 1);
 #pragma unroll 1
             for (int j = 0; j < kHG; ++j) {
                 const float* wf = T(ts, j, TAB_WF);
-                uint8_t* tile = smem + K::OFF_XW + (xs * kHG + j) * kTile;
+                uint8_t* tile = smem + Y::OFF_XW + (xs * kHG + j) * kTile;
                 // all loads first, then the stores: the compiler cannot move a load past
                 // a shared-memory store it may alias
                 uint4 v[8];
@@ -1052,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mrow = lane & 7, mm = lane >> 3;
         const long long x_tstride = static_cast<long long>(prm.H) * kP;
         for (int J = 0; J < njobs; ++J) {
-            const int ts = J & (kTabSlots - 1), yb = J % Y::kYBuf, xs = J & 1;
+            const int ts = J & (kTabSlots - 1), yb = J % Y::kYBuf, xs = J % Y::kXW;
             WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
             const float2* u2 = reinterpret_cast<const float2*>(T(ts, j, TAB_U));
             const float2* g2 = reinterpret_cast<const float2*>(T(ts, j, TAB_UG));
@@ -1060,7 +1083,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool rare = (extreme | JW(ts)[2]) != 0u;
             const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
             WB(B_Y_FULL0 + yb, (J / Y::kYBuf) & 1);
-            WB(B_XW_FREE0 + xs, (J >> 1) & 1);  // k3 and k5a no longer read W
+            WB(B_XW_FREE0 + xs, (J / Y::kXW) & 1);  // k3 and k5a no longer read W
             ptx::tc_fence_after();
             if (jp.warm) {
                 // a warm-up block has no output: hand the accumulator, the slot and the
@@ -1070,11 +1093,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 warp_arrive(&bars[B_TAB_EMPTY0 + ts], lane);
                 continue;
             }
-            const uint32_t tile = sbase + K::OFF_XW + (xs * kHG + j) * kTile;
+            const uint32_t tile = sbase + Y::OFF_XW + (xs * kHG + j) * kTile;
 #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
                 const uint32_t ylane = tmem + (static_cast<uint32_t>(32 * q4 + 16 * hf) << 16) + Y::COL_Y + 128 * yb;
-                SSD_CHECK(prm.status, yb < Y::kYBuf && Y::COL_Y + 128 * (yb + 1) <= 512 && xs < 2);
+                SSD_CHECK(prm.status, yb < Y::kYBuf && Y::COL_Y + 128 * (yb + 1) <= 512 && xs < Y::kXW);
                 const uint32_t pc = 4 * (q4 & 1) + 2 * hf + (mm & 1);  // 16-byte chunk of p in the row
 #pragma unroll 1
                 for (int k = 0; k < 4; ++k) {
@@ -1117,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       static_cast<long long>(jp.blk) * kT < prm.L);
             if (et == 0) {
                 for (int jj = 0; jj < kHG; ++jj)
-                    ptx::tma_store_4d(&tm_y, smem + K::OFF_XW + (xs * kHG + jj) * kTile, 0, jp.h[jj],
+                    ptx::tma_store_4d(&tm_y, smem + Y::OFF_XW + (xs * kHG + jj) * kTile, 0, jp.h[jj],
                                       jp.blk * kT, jp.b);
                 ptx::bulk_commit_group();
                 ptx::bulk_wait_group_read0();

@@ -57,7 +57,7 @@ bool tc_supported(const ssd_dims& d, ssd_dtype io, int chunk_len);
 size_t tc_workspace_bytes(const ssd_dims& d, int chunk_len);
 ssd_status tc_forward(const FwdArgs& a, void* ws, size_t ws_bytes);
 
-// Chain-local fused tcgen05/TMA path (dstate 128): persistent CTAs, state kept on chip.
+// Chain-local fused tcgen05/TMA path (dstate 128 or 256): persistent CTAs, state kept on chip.
 bool chain_supported(const ssd_dims& d, ssd_dtype io, int chunk_len);
 size_t chain_workspace_bytes(const ssd_dims& d);
 ssd_status chain_forward(const FwdArgs& a, void* ws, size_t ws_bytes);

@@ -4,7 +4,7 @@ pairing of heads by decay rate, against the fp64 oracle.
 Where a CTA's range begins inside a chain, the CTA either waits for the
 previous CTA's hand-off of the state or recomputes that state itself from the
 blocks before its segment (a warm-up): from a zero state where both heads of
-the pair decay by more than 44 nats over the warm-up, else from the chain's
+the pair decay by more than 32 nats over the warm-up, else from the chain's
 initial state at block 0. SSD_CHAIN_WARMUP selects 0 (always the hand-off),
 1 (the default: warm up where the hand-off would come late) or 2 (warm up
 wherever possible). Every mode must give the oracle's result.
