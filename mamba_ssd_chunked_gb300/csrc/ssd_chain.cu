@@ -103,12 +103,15 @@ static_assert(kRecSmem % 16 == 0 && kRecBytes % 16 == 0, "bulk copies move multi
 
 // Per-dstate layout (NS = 128 or 256). The ring carries, per job, L and B and C
 // in 128-column halves of n: kKinds ring entries of 32 KB at positions
-// kKinds J + kind, in the order L, B halves, C halves. A ring entry reuses the
-// slot of the entry four positions earlier, so at 256 (five entries for four
-// slots) a job's last C half waits for its own L, which k5a frees. It must not
-// wait for a B half: k3 frees B only after its last sub-block, whose state
-// rescale waits (H being single-buffered) for k5b of the sub-block before,
-// which needs that C half.
+// kKinds J + kind. At 128 there is one slot per kind and the order is B, L, C:
+// the producer issues a job's B as soon as k3 of the job before has freed its
+// slot, ahead of L and C, whose slots k5a and k5b free later; B is what the
+// state path (k3) waits for. At 256 the order is L, B halves, C halves, and a
+// ring entry reuses the slot of the entry four positions earlier, so (five
+// entries for four slots) a job's last C half waits for its own L, which k5a
+// frees. It must not wait for a B half: k3 frees B only after its last
+// sub-block, whose state rescale waits (H being single-buffered) for k5b of
+// the sub-block before, which needs that C half.
 // TMEM (512 columns): the fp32 state Z (NS columns), kHBuf bf16 copies H of
 // the scaled state (NS / 2 columns each, the A operand of k5b) and kYBuf
 // output accumulators Y (128 columns each). At NS = 256 the state takes half
@@ -132,8 +135,8 @@ struct Lay {
     static constexpr uint32_t COL_H = NS;
     static constexpr uint32_t COL_Y = NS + kHBuf * (NS / 2);
     static_assert(COL_Y + kYBuf * 128 == 512, "TMEM budget");
-    __host__ __device__ static constexpr int kindL() { return 0; }
-    __host__ __device__ static constexpr int kindB(int half) { return 1 + half; }
+    __host__ __device__ static constexpr int kindL() { return NS == 128 ? 1 : 0; }
+    __host__ __device__ static constexpr int kindB(int half) { return NS == 128 ? 0 : 1 + half; }
     __host__ __device__ static constexpr int kindC(int half) { return 1 + kNB + half; }
 };
 
@@ -724,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tma_load_4d(dst + kTile, &tm_l, fb, 64, 0, 0, tile);
                 } else {
                     // a 128-column half of B or C: n in [128 half, 128 half + 128)
-                    const bool is_b = kind < Y::kindC(0);
+                    const bool is_b = kind >= Y::kindB(0) && kind < Y::kindB(0) + Y::kNB;
                     const int n0 = 128 * (is_b ? kind - Y::kindB(0) : kind - Y::kindC(0));
                     const CUtensorMap* m = is_b ? &tm_b : &tm_c;
                     // a TMA copy's innermost coordinate must stay 16-byte aligned (8 bf16)
