@@ -142,6 +142,11 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, 
 }
 
 // Fetches `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+// Prefetch of the line holding addr into L2 (no data returned to the thread).
+__device__ __forceinline__ void prefetch_l2(const void* addr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(addr)));
+}
+
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                  : "memory");

@@ -281,8 +281,15 @@ __device__ __forceinline__ JobPos job_pos(const JobList& jobs, int J, int chains
     return jp;
 }
 
+// softplus(v) = max(v, 0) + log1p(z), z = e^{-|v|} in (0, 1]. log1p(z) is the
+// Taylor series z - z^2/2 + z^3/3 - z^4/4 for z < 1/32 (truncation under
+// z^5/5: a relative 2e-7) and log(1 + z) above, where the rounding of 1 + z
+// (2^-24) is at most 2e-6 of the result (>= 0.03); the exponential and the
+// logarithm are the fast hardware approximations (a few ulp).
 __device__ __forceinline__ float softplus_f(float v) {
-    return v > 0.f ? v + log1pf(expf(-v)) : log1pf(expf(v));
+    const float z = __expf(-fabsf(v));
+    const float l = z < 0.03125f ? z * (1.f - z * (0.5f - z * (0.33333334f - 0.25f * z))) : __logf(1.f + z);
+    return fmaxf(v, 0.f) + l;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -970,6 +977,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!SSD_CHECK(prm.status, (jp.wait ? (cta >= 1 && cta <= prm.ncta - 1)
                                                     : (jp.b < prm.batch && h >= 0 && h < prm.H)) && p < kP))
                     src = nullptr;
+                // every line of the row on its way to L2 before the first load waits
+                if (src)
+#pragma unroll
+                    for (int k = 0; k < NS / 32; ++k) ptx::prefetch_l2(src + 32 * k);
                 inv_prev = 1.f;
             }
             for (int q = 0; q < nq; ++q, ++u) {
@@ -1215,6 +1226,7 @@ __device__ __forceinline__ uint32_t job_cost(int nq, uint32_t extreme, int tiny)
 }
 
 constexpr int kBalanceMin = 20;  // cost balancing from this many jobs per chain CTA up (see cta_range)
+constexpr int kTableWarps = 4;   // chain_tables: jobs (warps) per CTA
 
 // The table record of one job (one block of one head pair), one warp per job:
 // lane l owns tokens 4l .. 4l + 3 of the block for both heads. dt =
@@ -1232,8 +1244,8 @@ constexpr int kBalanceMin = 20;  // cost balancing from this many jobs per chain
 // (nheads x heads-per-group comparisons); CTA 0 also stores the order for the
 // chain kernel. The pairing only schedules: each head's result is its own.
 // At most 56 registers so that 9 CTAs fit an SM: 1280 CTAs of the 2.7B shape in one wave.
-__global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
-    __shared__ float s_key[kSortMaxHeads];
+__global__ void __launch_bounds__(kTableWarps * 32, 9) chain_tables(const TableParams prm) {
+    __shared__ __align__(16) uint32_t s_key[kSortMaxHeads];
     __shared__ int s_order[kSortMaxHeads];
     // launched early behind the previous kernel of the stream (which may still use the
     // workspace or write the inputs): nothing is touched before it completes
@@ -1245,18 +1257,21 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
         const int r = prm.H / prm.G;
         for (int h = threadIdx.x; h < prm.H; h += blockDim.x) {
             const float sp = fminf(fmaxf(softplus_f(__ldg(prm.dt_bias + h)), prm.dt_min), prm.dt_max);
-            const float k = sp * -__ldg(prm.A + h);
-            s_key[h] = (k == k) ? k : __int_as_float(0x7f800000);  // NaN ranks as +inf
+            float k = sp * -__ldg(prm.A + h);
+            k = (k == k) ? k + 0.f : __int_as_float(0x7f800000);  // NaN ranks as +inf, -0 as +0
+            // the float order as an unsigned order: flip all bits of negatives, the sign of the rest
+            const uint32_t u = __float_as_uint(k);
+            s_key[h] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
         }
         __syncthreads();
+        // rank of head h in its group by (key, head), a strict total order: heads
+        // before h count when their key is not above h's, heads after h when below
         for (int h = threadIdx.x; h < prm.H; h += blockDim.x) {
             const int g0 = (h / r) * r;
-            const float kh = s_key[h];
+            const uint32_t kh = s_key[h];
             int rank = 0;
-            for (int i = g0; i < g0 + r; ++i) {
-                const float ki = s_key[i];
-                rank += (ki < kh || (ki == kh && i < h)) ? 1 : 0;  // (key, head) is a strict total order
-            }
+            for (int i = g0; i < h; ++i) rank += s_key[i] <= kh ? 1 : 0;
+            for (int i = h + 1; i < g0 + r; ++i) rank += s_key[i] < kh ? 1 : 0;
             s_order[g0 + rank] = h;
         }
         __syncthreads();
@@ -1265,7 +1280,7 @@ __global__ void __launch_bounds__(128, 9) chain_tables(const TableParams prm) {
         for (int h = threadIdx.x; h < prm.H; h += blockDim.x) prm.order[h] = prm.sort_pairs ? s_order[h] : h;
     const int wl = threadIdx.x & 31;
     // one warp per job (job indices fit 31 bits: the host launches only then)
-    const int job = static_cast<int>(blockIdx.x) * 4 + static_cast<int>(threadIdx.x >> 5);
+    const int job = static_cast<int>(blockIdx.x) * kTableWarps + static_cast<int>(threadIdx.x >> 5);
     if (job < prm.total) {
         const int blk = job % prm.nblk;
         const int chain = job / prm.nblk;
@@ -1600,8 +1615,8 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t tcfg = {};
-    tcfg.gridDim = dim3(static_cast<unsigned>((pl.total + 3) / 4));
-    tcfg.blockDim = dim3(128);
+    tcfg.gridDim = dim3(static_cast<unsigned>((pl.total + kTableWarps - 1) / kTableWarps));
+    tcfg.blockDim = dim3(kTableWarps * 32);
     tcfg.stream = a.stream;
     tcfg.attrs = pdl;
     tcfg.numAttrs = 1;
