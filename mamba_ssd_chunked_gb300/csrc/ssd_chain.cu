@@ -101,17 +101,17 @@ constexpr uint32_t kRecSmem = kRecTab + kRecScal + 16;
 constexpr uint32_t kRecBytes = kRecSmem + kHG * kNumTabX * kT * 4;
 static_assert(kRecSmem % 16 == 0 && kRecBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 
-// Per-dstate layout (NS = 128 or 256). The ring carries, per job, L and B and C
-// in 128-column halves of n: kKinds ring entries of 32 KB at positions
-// kKinds J + kind. At 128 there is one slot per kind and the order is B, L, C:
-// the producer issues a job's B as soon as k3 of the job before has freed its
-// slot, ahead of L and C, whose slots k5a and k5b free later; B is what the
-// state path (k3) waits for. At 256 the order is L, B halves, C halves, and a
-// ring entry reuses the slot of the entry four positions earlier, so (five
-// entries for four slots) a job's last C half waits for its own L, which k5a
-// frees. It must not wait for a B half: k3 frees B only after its last
-// sub-block, whose state rescale waits (H being single-buffered) for k5b of
-// the sub-block before, which needs that C half.
+// Per-dstate layout (NS = 128 or 256).
+// At 128 the ring carries, per job, B, L and C, one 32 KB slot each, at
+// positions kKinds J + kind in the order B, L, C: the producer issues a job's
+// B as soon as k3 of the job before has freed its slot, ahead of L and C,
+// whose slots k5a and k5b free later; B is what the state path (k3) waits for.
+// At 256, B (both 128-column halves of n, 64 KB) has a buffer of its own,
+// which the k3 issuer refills with the next job's B as soon as k3 of the job
+// has read it; k3 then runs at N = 256 over the contiguous halves. The ring
+// carries L and the two C halves in two slots: an entry reuses the slot of
+// the entry two positions earlier, so a job's second C half waits for its own
+// L, which k5a frees (k5a waits for nothing of that C half).
 // TMEM (512 columns): the fp32 state Z (NS columns), kHBuf bf16 copies H of
 // the scaled state (NS / 2 columns each, the A operand of k5b) and kYBuf
 // output accumulators Y (128 columns each). At NS = 256 the state takes half
@@ -120,24 +120,24 @@ template <int NS>
 struct Lay {
     static_assert(NS == 128 || NS == 256, "dstate 128 or 256");
     static constexpr int kNB = NS / 128;
-    static constexpr int kKinds = 1 + 2 * kNB;
+    static constexpr bool kOwnB = NS == 256;  // B in a buffer of its own, loaded by the k3 issuer
+    static constexpr int kKinds = kOwnB ? 1 + kNB : 1 + 2 * kNB;
     static constexpr int kHBuf = NS == 128 ? 2 : 1;
     static constexpr int kYBuf = NS == 128 ? 2 : 1;
-    // Shared memory: kRing ring slots and kXW X/W/y job slots of 32 KB each, six
-    // in all. At 128 a job's L, B and C each own a ring slot and three jobs are
-    // in flight; at 256 a job takes five ring entries, and four ring slots (two
-    // jobs in flight) keep its last C half from waiting for its own B.
-    static constexpr int kRing = NS == 128 ? 3 : 4;
+    // Shared memory: kRing ring slots, the B buffer (kOwnB) and kXW X/W/y job
+    // slots, six 32 KB slots in all; three jobs in flight at 128, two at 256.
+    static constexpr int kRing = NS == 128 ? 3 : 2;
     static constexpr int kXW = NS == 128 ? 3 : 2;
-    static_assert(kRing <= kRingMax && kXW <= kXWMax && kRing + kXW == 6, "six 32 KB slots");
-    static constexpr uint32_t OFF_XW = 2 * kRing * kTile;
+    static_assert(kRing <= kRingMax && kXW <= kXWMax && kRing + (kOwnB ? kNB : 0) + kXW == 6, "six 32 KB slots");
+    static constexpr uint32_t OFF_B = 2 * kRing * kTile;  // kOwnB: B as 2 kNB tiles of 64 columns of n
+    static constexpr uint32_t OFF_XW = OFF_B + (kOwnB ? 2 * kNB * kTile : 0);
     static constexpr uint32_t COL_Z = 0;
     static constexpr uint32_t COL_H = NS;
     static constexpr uint32_t COL_Y = NS + kHBuf * (NS / 2);
     static_assert(COL_Y + kYBuf * 128 == 512, "TMEM budget");
-    __host__ __device__ static constexpr int kindL() { return NS == 128 ? 1 : 0; }
-    __host__ __device__ static constexpr int kindB(int half) { return NS == 128 ? 0 : 1 + half; }
-    __host__ __device__ static constexpr int kindC(int half) { return 1 + kNB + half; }
+    __host__ __device__ static constexpr int kindB(int half) { return kOwnB ? -1 : half; }  // ring kinds at 128 only
+    __host__ __device__ static constexpr int kindL() { return kOwnB ? 0 : kNB; }
+    __host__ __device__ static constexpr int kindC(int half) { return kOwnB ? 1 + half : 1 + kNB + half; }
 };
 
 struct Cfg {
@@ -146,7 +146,7 @@ struct Cfg {
     static constexpr uint32_t OFF_RING = 0;               // then the X/W slots at Lay::OFF_XW
     static constexpr uint32_t OFF_TAB = 12 * kTile;      // [slots] table records
     static constexpr uint32_t OFF_BAR = (OFF_TAB + kTabSlots * kRecSmem + 7) & ~7u;
-    static constexpr int NBAR = 40;
+    static constexpr int NBAR = 44;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_SCAN = OFF_MISC + 64;  // [kThreads / 32] u64, cta_range
     static constexpr uint32_t OFF_ORDER = OFF_SCAN + 128;  // [kSortMaxHeads] the pair order (job_pos)
@@ -160,7 +160,7 @@ enum Bar {
     B_TAB_FULL0 = B_XW_EMPTY0 + kXWMax, B_TAB_FULL3 = B_TAB_FULL0 + 3, B_TAB_EMPTY0, B_TAB_EMPTY3 = B_TAB_EMPTY0 + 3,
     B_W_FULL0, B_SCALED = B_W_FULL0 + kXWMax, B_S_DONE, B_H_FULL0, B_H_FULL1, B_H_EMPTY0, B_H_EMPTY1,
     B_Y_FULL0, B_Y_FULL1, B_Y_EMPTY0, B_Y_EMPTY1,
-    B_DRAIN_K3, B_DRAIN_Y,
+    B_DRAIN_K3, B_DRAIN_Y, B_B_FULL, B_B_EMPTY,
     B_COUNT
 };
 static_assert(B_COUNT <= Cfg::NBAR, "barrier budget");
@@ -734,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tma_load_4d(dst + kTile, &tm_l, fb, 64, 0, 0, tile);
                 } else {
                     // a 128-column half of B or C: n in [128 half, 128 half + 128)
-                    const bool is_b = kind >= Y::kindB(0) && kind < Y::kindB(0) + Y::kNB;
+                    const bool is_b = !Y::kOwnB && kind >= Y::kindB(0) && kind < Y::kindB(0) + Y::kNB;
                     const int n0 = 128 * (is_b ? kind - Y::kindB(0) : kind - Y::kindC(0));
                     const CUtensorMap* m = is_b ? &tm_b : &tm_c;
                     // a TMA copy's innermost coordinate must stay 16-byte aligned (8 bf16)
@@ -754,8 +754,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer: k3
         if (lane == 0) {
-            const uint32_t idesc = idesc_n(128, true, true);
             uint32_t u = 0;  // sub-blocks so far
+            // kOwnB: B of job J into its buffer (phase J of B_B_FULL), all 2 kNB tiles
+            int nb = 0;  // B loads issued
+            auto load_b = [&](int J) {
+                const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
+                SSD_CHECK(prm.status, jp.b < prm.batch && jp.g < prm.G);
+                ptx::mbar_arrive_expect_tx(&bars[B_B_FULL], 2 * Y::kNB * kTile);
+                for (int i = 0; i < 2 * Y::kNB; ++i)
+                    ptx::tma_load_4d(smem + Y::OFF_B + i * kTile, &tm_b, &bars[B_B_FULL], 64 * i, jp.g, jp.blk * kT,
+                                     jp.b);
+                ++nb;
+            };
+            if (Y::kOwnB && njobs > 0) load_b(0);
             for (int J = 0; J < njobs; ++J) {
                 const int ts = J & (kTabSlots - 1), xs = J % Y::kXW;
                 WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
@@ -765,26 +776,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 WB(B_W_FULL0 + xs, (J / Y::kXW) & 1);
                 const uint64_t a_w = ptx::desc_sw128(sbase + Y::OFF_XW + xs * 2 * kTile, kTile, 1024);
                 uint64_t b_b[Y::kNB];
+                if (Y::kOwnB) {
+                    WB(B_B_FULL, J & 1);
+                    b_b[0] = ptx::desc_sw128(sbase + Y::OFF_B, kTile, 1024);  // N = NS over 2 kNB tiles
+                } else {
 #pragma unroll
-                for (int hh = 0; hh < Y::kNB; ++hh) {
-                    const int pb = Y::kKinds * J + Y::kindB(hh);
-                    WB(B_R_FULL0 + pb % Y::kRing, (pb / Y::kRing) & 1);
-                    b_b[hh] = ptx::desc_sw128(sbase + K::OFF_RING + (pb % Y::kRing) * 2 * kTile, kTile, 1024);
+                    for (int hh = 0; hh < Y::kNB; ++hh) {
+                        const int pb = Y::kKinds * J + Y::kindB(hh);
+                        WB(B_R_FULL0 + pb % Y::kRing, (pb / Y::kRing) & 1);
+                        b_b[hh] = ptx::desc_sw128(sbase + K::OFF_RING + (pb % Y::kRing) * 2 * kTile, kTile, 1024);
+                    }
                 }
                 for (int q = 0; q < nq; ++q, ++u) {
                     WB(B_SCALED, u & 1);
                     ptx::tc_fence_after();
+                    if (Y::kOwnB) {
+                        if (SSD_CHECK(prm.status, Y::COL_Z + NS <= Y::COL_H && (q + 1) * ksub <= 8))
+                            mma_k3(tmem + Y::COL_Z, a_w, b_b[0], idesc_n(NS, true, true), q * ksub, ksub);
+                    } else {
 #pragma unroll
-                    for (int hh = 0; hh < Y::kNB; ++hh)  // Z columns [128 hh, 128 hh + 128) are n of that half
-                        if (SSD_CHECK(prm.status, Y::COL_Z + 128 * hh + 128 <= Y::COL_H && (q + 1) * ksub <= 8))
-                            mma_k3(tmem + Y::COL_Z + 128 * hh, a_w, b_b[hh], idesc, q * ksub, ksub);
+                        for (int hh = 0; hh < Y::kNB; ++hh)  // Z columns [128 hh, 128 hh + 128) are n of that half
+                            if (SSD_CHECK(prm.status, Y::COL_Z + 128 * hh + 128 <= Y::COL_H && (q + 1) * ksub <= 8))
+                                mma_k3(tmem + Y::COL_Z + 128 * hh, a_w, b_b[hh], idesc_n(128, true, true), q * ksub,
+                                       ksub);
+                    }
                     ptx::mma_commit(&bars[B_S_DONE]);
                 }
+                if (Y::kOwnB) {
+                    ptx::mma_commit(&bars[B_B_EMPTY]);
+                } else {
 #pragma unroll
-                for (int hh = 0; hh < Y::kNB; ++hh)
-                    ptx::mma_commit(&bars[B_R_EMPTY0 + (Y::kKinds * J + Y::kindB(hh)) % Y::kRing]);
+                    for (int hh = 0; hh < Y::kNB; ++hh)
+                        ptx::mma_commit(&bars[B_R_EMPTY0 + (Y::kKinds * J + Y::kindB(hh)) % Y::kRing]);
+                }
                 ptx::mma_commit(&bars[B_XW_FREE0 + xs]);
+                if (Y::kOwnB && J + 1 < njobs) {
+                    WB(B_B_EMPTY, J & 1);  // k3 of job J has read B
+                    if (*abort_flag) break;
+                    load_b(J + 1);
+                }
             }
+            // no copy into shared memory may be left in flight at exit
+            if (nb > 0) ptx::mbar_wait(&bars[B_B_FULL], (nb - 1) & 1, kLocalWaitNs);
             ptx::mma_commit(&bars[B_DRAIN_K3]);
             ptx::mbar_wait(&bars[B_DRAIN_K3], 0, kLocalWaitNs);
         }
