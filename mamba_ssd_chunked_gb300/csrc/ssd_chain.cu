@@ -725,6 +725,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
                 uint64_t* fb = &bars[B_R_FULL0 + rs];
                 uint8_t* dst = smem + K::OFF_RING + rs * 2 * kTile;
+                const bool is_b = !Y::kOwnB && kind >= Y::kindB(0) && kind < Y::kindB(0) + Y::kNB;
+                if (jp.warm && !is_b) {
+                    // a warm-up block writes no y: no L or C, the entry's phase completes empty
+                    ptx::mbar_arrive(fb);
+                    continue;
+                }
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
                 SSD_CHECK(prm.status, rs < Y::kRing && jp.b < prm.batch && jp.g < prm.G);
                 if (kind == Y::kindL()) {
@@ -734,7 +740,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tma_load_4d(dst + kTile, &tm_l, fb, 64, 0, 0, tile);
                 } else {
                     // a 128-column half of B or C: n in [128 half, 128 half + 128)
-                    const bool is_b = !Y::kOwnB && kind >= Y::kindB(0) && kind < Y::kindB(0) + Y::kNB;
                     const int n0 = 128 * (is_b ? kind - Y::kindB(0) : kind - Y::kindC(0));
                     const CUtensorMap* m = is_b ? &tm_b : &tm_c;
                     // a TMA copy's innermost coordinate must stay 16-byte aligned (8 bf16)
