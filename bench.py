@@ -22,6 +22,7 @@ sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -422,7 +423,7 @@ def run_ours(args, w: Workload, world, rank, local, pg):
     else:
         achieved, peak, unit = aflops / kernel_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
         path_achieved = aflops / mean_step / 1e12
-    traffic = profiled_traffic(w.name, path)
+    traffic = profiled_traffic(w.name, path) if w == WORKLOADS[w.name] else None
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -642,6 +643,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="a shorter (or longer) case of the workload: its shapes and recipe with this sequence "
+                         "length (for profiler captures of a smaller case; the line's config carries the length)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "tc", "chain", "simt"],
                     help="kernel path of the timed step (auto: the library's choice)")
@@ -662,6 +666,10 @@ def main(argv=None):
         print(json.dumps(run_layer_op(args, "conv" if args.conv else "norm")), flush=True)
         return
     w = WORKLOADS[args.workload]
+    if args.seqlen is not None:
+        if args.seqlen < 1:
+            ap.error("--seqlen must be >= 1")
+        w = dataclasses.replace(w, seqlen=args.seqlen)
     world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
         out = run_reference(args, w, world, rank)
