@@ -715,6 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer: L, B, C ring
         if (lane == 0) {
+            // L, B and C are read again by every head pair of the group: last out of L2
+            const uint64_t keep = ptx::policy_evict_last();
             const int npos = Y::kKinds * njobs;
             int pr = 0;
             for (; pr < npos; ++pr) {
@@ -736,16 +738,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kind == Y::kindL()) {
                     const int tile = (jp.b * prm.nblk + jp.blk) * prm.G + jp.g;
                     SSD_CHECK(prm.status, tile >= 0 && tile < prm.batch * prm.nblk * prm.G);
-                    ptx::tma_load_4d(dst, &tm_l, fb, 0, 0, 0, tile);
-                    ptx::tma_load_4d(dst + kTile, &tm_l, fb, 64, 0, 0, tile);
+                    ptx::tma_load_4d(dst, &tm_l, fb, 0, 0, 0, tile, keep);
+                    ptx::tma_load_4d(dst + kTile, &tm_l, fb, 64, 0, 0, tile, keep);
                 } else {
                     // a 128-column half of B or C: n in [128 half, 128 half + 128)
                     const int n0 = 128 * (is_b ? kind - Y::kindB(0) : kind - Y::kindC(0));
                     const CUtensorMap* m = is_b ? &tm_b : &tm_c;
                     // a TMA copy's innermost coordinate must stay 16-byte aligned (8 bf16)
                     SSD_CHECK(prm.status, n0 % 8 == 0 && n0 >= 0 && n0 + 128 <= NS);
-                    ptx::tma_load_4d(dst, m, fb, n0, jp.g, jp.blk * kT, jp.b);
-                    ptx::tma_load_4d(dst + kTile, m, fb, n0 + 64, jp.g, jp.blk * kT, jp.b);
+                    ptx::tma_load_4d(dst, m, fb, n0, jp.g, jp.blk * kT, jp.b, keep);
+                    ptx::tma_load_4d(dst + kTile, m, fb, n0 + 64, jp.g, jp.blk * kT, jp.b, keep);
                 }
             }
             // no copy into shared memory may be left in flight at exit: wait for the
@@ -762,13 +764,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t u = 0;  // sub-blocks so far
             // kOwnB: B of job J into its buffer (phase J of B_B_FULL), all 2 kNB tiles
             int nb = 0;  // B loads issued
+            const uint64_t keep = ptx::policy_evict_last();  // B is read again by the group's other pairs
             auto load_b = [&](int J) {
                 const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
                 SSD_CHECK(prm.status, jp.b < prm.batch && jp.g < prm.G);
                 ptx::mbar_arrive_expect_tx(&bars[B_B_FULL], 2 * Y::kNB * kTile);
                 for (int i = 0; i < 2 * Y::kNB; ++i)
                     ptx::tma_load_4d(smem + Y::OFF_B + i * kTile, &tm_b, &bars[B_B_FULL], 64 * i, jp.g, jp.blk * kT,
-                                     jp.b);
+                                     jp.b, keep);
                 ++nb;
             };
             if (Y::kOwnB && njobs > 0) load_b(0);
@@ -892,6 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 3) {
         // ------------------------------------------------------------ TMA producer: X
         if (lane == 0) {
+            const uint64_t once = ptx::policy_evict_first();  // X and the table records are read once
             int jx = 0, ntab = 0;
             for (; jx < njobs; ++jx) {
                 const int ts = jx & (kTabSlots - 1);
@@ -901,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.cb) * prm.nblk + jp.blk;
                 ptx::mbar_arrive_expect_tx(&bars[B_TAB_FULL0 + ts], kRecSmem);
                 ptx::bulk_load(smem + K::OFF_TAB + ts * kRecSmem, prm.tables + rec * kRecBytes, kRecSmem,
-                               &bars[B_TAB_FULL0 + ts]);
+                               &bars[B_TAB_FULL0 + ts], once);
                 ++ntab;
                 const int xs = jx % Y::kXW;
                 if (jx >= Y::kXW) WB(B_XW_EMPTY0 + xs, ((jx / Y::kXW) - 1) & 1);  // y of job jx - kXW has left
@@ -911,8 +915,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 SSD_CHECK(prm.status, Y::OFF_XW + (xs + 1) * 2 * kTile <= K::OFF_TAB &&
                                           static_cast<long long>(jp.blk) * kT < prm.L && jp.b < prm.batch);
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
-                ptx::tma_load_4d(dst, &tm_x, fb, 0, jp.h[0], jp.blk * kT, jp.b);
-                ptx::tma_load_4d(dst + kTile, &tm_x, fb, 0, jp.h[1], jp.blk * kT, jp.b);
+                ptx::tma_load_4d(dst, &tm_x, fb, 0, jp.h[0], jp.blk * kT, jp.b, once);
+                ptx::tma_load_4d(dst + kTile, &tm_x, fb, 0, jp.h[1], jp.blk * kT, jp.b, once);
                 if (jp.blk == 0 && prm.init)  // a chain start: its initial states into L2 for the state warps
                     for (int j = 0; j < kHG; ++j)
                         ptx::bulk_prefetch_l2(prm.init + (static_cast<size_t>(jp.b) * prm.H + jp.h[j]) * kP * NS,
@@ -1191,9 +1195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             SSD_CHECK(prm.status, jp.h[0] < prm.H && jp.h[1] < prm.H && jp.b < prm.batch &&
                                       static_cast<long long>(jp.blk) * kT < prm.L);
             if (et == 0) {
+                const uint64_t once = ptx::policy_evict_first();  // y is written once
                 for (int jj = 0; jj < kHG; ++jj)
                     ptx::tma_store_4d(&tm_y, smem + Y::OFF_XW + (xs * kHG + jj) * kTile, 0, jp.h[jj],
-                                      jp.blk * kT, jp.b);
+                                      jp.blk * kT, jp.b, once);
                 ptx::bulk_commit_group();
                 ptx::bulk_wait_group_read0();
                 ptx::mbar_arrive(&bars[B_XW_EMPTY0 + xs]);  // the slot may take the next X
