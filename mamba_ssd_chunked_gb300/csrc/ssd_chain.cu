@@ -1,14 +1,16 @@
 // Chain-local fused forward, head-pair-major form (tcgen05/TMA, bf16 io,
-// dstate 128, headdim 64).
+// dstate 128 or 256, headdim 64).
 //
 // A persistent CTA per SM walks a contiguous range of the flattened
 // (chain, block) index space. A chain is a pair of heads of one batch row that
-// read the same B/C group; a block is 128 tokens. Along a chain the blocks are
-// processed in order by the same CTA, so the chunk state stays in tensor memory
-// from block to block; only where a CTA's range starts or ends inside a chain
-// is a state handed to the neighbouring CTA through global memory. A CTA
-// processes the tail of its range (a chain start) first and the head of its
-// range (the continuation that consumes the previous CTA's hand-off) last.
+// read the same B/C group (paired by decay rate, chain_tables); a block is 128
+// tokens. Along a chain the blocks are processed in order by the same CTA, so
+// the chunk state stays in tensor memory from block to block; only where a
+// CTA's range starts or ends inside a chain does a state cross to the
+// neighbouring CTA: through global memory behind a flag (the hand-off), or the
+// later CTA recomputes it from a zero state over the blocks in which it decays
+// by kWarmupNats (the warm-up, warmup_blocks). A CTA processes the tail of its
+// range (a chain start) first and the head of its range (the continuation) last.
 //
 // Per block the chunked SSD (burn-mamba "mamba2/ssd/serial.rs" k1..k5; fla
 // "mamba2.py" naive chunked SSD) is computed with every MMA's M dimension
@@ -43,11 +45,12 @@
 // with programmatic stream serialization.
 //
 // Roles (16 warps):
-//   warp 0       TMA producer: L, B and C through a ring of four slots
-//   warp 1       MMA issuer, state path: k3
+//   warp 0       TMA producer: the L / B / C ring (Lay<NS>)
+//   warp 1       MMA issuer, state path: k3 (at dstate 256 also the B loads)
 //   warp 2       MMA issuer, output path: k5a, k5b
-//   warp 3       TMA producer: X (2 job slots of two heads) and each job's table
-//                record; L2 prefetch of the X two jobs ahead and of chain-start states
+//   warp 3       TMA producer: X (three or two job slots of two heads) and each
+//                job's table record; L2 prefetch of chain-start states and (two
+//                slots) of the X a slot round ahead
 //   warps 4..7   W from X in place
 //   warps 8..11  state: rescale Z, write H; load / store states at segment ends
 //   warps 12..15 epilogue: y from Y (TMEM) and W (shared memory), written over W
@@ -128,6 +131,10 @@ struct Lay {
     // slots, six 32 KB slots in all; three jobs in flight at 128, two at 256.
     static constexpr int kRing = NS == 128 ? 3 : 2;
     static constexpr int kXW = NS == 128 ? 3 : 2;
+    // L2 prefetch of the X a slot round ahead (from the second round on: the first
+    // round's copies already crowd the start). It pays with two X/W slots; with three,
+    // the slot frees late enough for the load itself and the prefetch only adds traffic.
+    static constexpr bool kPrefetchX = kXW == 2;
     static_assert(kRing <= kRingMax && kXW <= kXWMax && kRing + (kOwnB ? kNB : 0) + kXW == 6, "six 32 KB slots");
     static constexpr uint32_t OFF_B = 2 * kRing * kTile;  // kOwnB: B as 2 kNB tiles of 64 columns of n
     static constexpr uint32_t OFF_XW = OFF_B + (kOwnB ? 2 * kNB * kTile : 0);
@@ -921,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < kHG; ++j)
                         ptx::bulk_prefetch_l2(prm.init + (static_cast<size_t>(jp.b) * prm.H + jp.h[j]) * kP * NS,
                                               kP * NS * sizeof(float));
-                if (jx + Y::kXW < njobs) {
+                if (Y::kPrefetchX && jx >= Y::kXW && jx + Y::kXW < njobs) {
                     // the X of job jx + kXW into L2: its load, once the slot is free, then hits L2
                     const JobPos jn = job_pos(jobs, jx + Y::kXW, chains_per_b, HperG, order, prm.status);
                     ptx::tma_prefetch_4d(&tm_x, 0, jn.h[0], jn.blk * kT, jn.b);
