@@ -1166,33 +1166,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 4; ++k) {
                     uint32_t r[16];
                     ptx::tmem_ld16x256_x4(ylane + 32 * k, r);
+                    // the W fragments and the factors of these 32 tokens while the TMEM load runs
+                    uint32_t w[2][4], addr[2];
+                    float2 uf[4], gf[4];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {  // 16 tokens: groups g = 2c, 2c + 1
+                        const int tb = 32 * k + 16 * c;
+                        const int trow = tb + 8 * (mm >> 1) + mrow;
+                        addr[c] = tile + trow * 128 + ((pc ^ (trow & 7)) << 4);
+                        SSD_CHECK(prm.status, trow < kT && pc < 8);
+                        ptx::ldmatrix_x4_trans(addr[c], w[c]);
+#pragma unroll
+                        for (int gg = 0; gg < 2; ++gg) {
+                            const int tp = (tb + 8 * gg) / 2 + lq;  // token pair (t, t + 1) / 2
+                            uf[2 * c + gg] = u2[tp];
+                            gf[2 * c + gg] = g2[tp];
+                        }
+                    }
                     ptx::tmem_wait_ld(r);
                     if (hf == 1 && k == 3 && !rare) {
                         ptx::tc_fence_before();
                         warp_arrive(&bars[B_Y_EMPTY0 + yb], lane);  // the accumulator has been read
                     }
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {  // 16 tokens: groups g = 2c, 2c + 1
-                        const int tb = 32 * k + 16 * c;
-                        const int trow = tb + 8 * (mm >> 1) + mrow;
-                        const uint32_t addr = tile + trow * 128 + ((pc ^ (trow & 7)) << 4);
-                        SSD_CHECK(prm.status, trow < kT && pc < 8);
-                        uint32_t w[4];
-                        ptx::ldmatrix_x4_trans(addr, w);
+                    for (int c = 0; c < 2; ++c) {
                         uint32_t o[4];
 #pragma unroll
                         for (int gg = 0; gg < 2; ++gg) {
                             const int g = 2 * c + gg;
-                            const int tp = (tb + 8 * gg) / 2 + lq;  // token pair (t, t + 1) / 2
-                            const float2 u = u2[tp], gw = g2[tp];
+                            const float2 u = uf[g], gw = gf[g];
 #pragma unroll
                             for (int hp = 0; hp < 2; ++hp) {  // p = lr, p = 8 + lr
-                                const float2 wv = unpack_bf16x2(w[2 * gg + hp]);
+                                const float2 wv = unpack_bf16x2(w[c][2 * gg + hp]);
                                 o[2 * gg + hp] = pack_bf16x2(fmaf(u.x, __uint_as_float(r[4 * g + 2 * hp]), gw.x * wv.x),
                                                              fmaf(u.y, __uint_as_float(r[4 * g + 2 * hp + 1]), gw.y * wv.y));
                             }
                         }
-                        ptx::stmatrix_x4_trans(addr, o);
+                        ptx::stmatrix_x4_trans(addr[c], o);
                     }
                 }
             }
