@@ -1269,6 +1269,7 @@ struct TableParams {
     int* order;          // [H] heads in pair order (written by CTA 0)
     const int32_t* seq;  // [batch, L] packed-sequence ids, or null
     int sort_pairs;      // pair the heads of each group by decay rate (else 2 cb, 2 cb + 1)
+    int jobs_per_warp;   // consecutive jobs per warp (1 or 2)
     long long L;
     int H, G, nblk, chains_per_b, total;
     float dt_min, dt_max;
@@ -1286,9 +1287,171 @@ __device__ __forceinline__ uint32_t job_cost(int nq, uint32_t extreme, int tiny)
 }
 
 constexpr int kBalanceMin = 20;  // cost balancing from this many jobs per chain CTA up (see cta_range)
-constexpr int kTableWarps = 4;   // chain_tables: jobs (warps) per CTA
+constexpr int kTableWarps = 4;   // chain_tables: warps per CTA
+constexpr int kTableCtasPerSm = 9;  // chain_tables: resident CTAs per SM (56 registers)
 
-// The table record of one job (one block of one head pair), one warp per job:
+// The table record of one job: the work of one warp (see chain_tables).
+__device__ __forceinline__ void table_job(const TableParams& prm, int job, int wl, const int* s_order) {
+    const int blk = job % prm.nblk;
+    const int chain = job / prm.nblk;
+    const int b = chain / prm.chains_per_b, cb = chain % prm.chains_per_b;
+    const int hh[kHG] = {prm.sort_pairs ? s_order[kHG * cb] : kHG * cb,
+                         prm.sort_pairs ? s_order[kHG * cb + 1] : kHG * cb + 1};
+    SSD_CHECK(prm.status, hh[0] >= 0 && hh[1] >= 0 && hh[0] < prm.H && hh[1] < prm.H && hh[0] != hh[1]);
+    uint8_t* rec = prm.out + static_cast<size_t>(job) * kRecBytes;
+    float* tabs = reinterpret_cast<float*>(rec);
+    float* scal = reinterpret_cast<float*>(rec + kRecTab);
+    uint32_t* jw = reinterpret_cast<uint32_t*>(rec + kRecTab + kRecScal);
+    float* tabx = reinterpret_cast<float*>(rec + kRecSmem);
+    auto T = [&](int j, int arr) { return reinterpret_cast<float4*>(tabs + (j * kNumTab + arr) * kT) + wl; };
+    auto TX = [&](int j, int arr) { return reinterpret_cast<float4*>(tabx + (j * kNumTabX + arr) * kT) + wl; };
+    auto S = [&](int j) { return scal + j * kScal; };
+    // lane wl owns tokens 4 wl .. 4 wl + 3 of the block (one 16-token unit); every
+    // global load is issued here, before the first store
+    const int tg0 = blk * kT + 4 * wl;
+    const float2 bias = make_float2(__ldg(prm.dt_bias + hh[0]), __ldg(prm.dt_bias + hh[1]));
+    const float2 a2 = make_float2(__ldg(prm.A + hh[0]), __ldg(prm.A + hh[1]));
+    const float2 d2 = prm.D ? make_float2(__ldg(prm.D + hh[0]), __ldg(prm.D + hh[1])) : make_float2(0.f, 0.f);
+    float2 raw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float* row = prm.dt + (static_cast<long long>(b) * prm.L + (tg0 + i)) * prm.H;
+        raw[i] = tg0 + i < prm.L ? make_float2(__ldg(row + hh[0]), __ldg(row + hh[1])) : make_float2(0.f, 0.f);
+    }
+    float dtv[kHG][4], cs[kHG][4];
+    float cut[4];  // a new packed sequence starts at the token: no state crosses (kSeqCutNats)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const long long t = tg0 + i;
+        cut[i] = (prm.seq && t > 0 && t < prm.L &&
+                  __ldg(prm.seq + static_cast<long long>(b) * prm.L + t) !=
+                      __ldg(prm.seq + static_cast<long long>(b) * prm.L + t - 1))
+                     ? -kSeqCutNats
+                     : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < kHG; ++j)
+            dtv[j][i] = tg0 + i < prm.L
+                            ? fminf(fmaxf(softplus_f((j ? raw[i].y : raw[i].x) + (j ? bias.y : bias.x)), prm.dt_min),
+                                    prm.dt_max)
+                            : 0.f;
+    float bnd[kHG][8];  // cumsum at token 16k + 15
+    float vtot[kHG];     // cumsum at token 4 wl + 3 (this lane's last token)
+#pragma unroll
+    for (int j = 0; j < kHG; ++j) {
+        const float a = j ? a2.y : a2.x;
+        float run = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            run += fmaf(dtv[j][i], a, cut[i]);
+            cs[j][i] = run;
+        }
+        float v = run;  // inclusive scan of the lane totals
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, v, off);
+            if (wl >= off) v += o;
+        }
+        const float pre = v - run;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cs[j][i] += pre;
+        vtot[j] = v;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) bnd[j][k] = __shfl_sync(0xffffffffu, v, 4 * k + 3);
+    }
+    int nq = 8;
+#pragma unroll
+    for (int cand = 1; cand < 8; cand <<= 1) {
+        const int m = 8 / cand;  // 16-token units per sub-block
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < kHG; ++j)
+#pragma unroll
+            for (int r = 0; r < cand; ++r) {
+                const float lo_ = r > 0 ? bnd[j][r * m - 1] : 0.f;
+                ok = ok && (lo_ - bnd[j][(r + 1) * m - 1] <= kMaxSubDecay);
+            }
+        if (ok && nq == 8) nq = cand;
+    }
+    uint32_t extreme = 0u;
+    if (nq == 8) {
+#pragma unroll
+        for (int j = 0; j < kHG; ++j)
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float lo_ = r > 0 ? bnd[j][r - 1] : 0.f;
+                if (lo_ - bnd[j][r] > kMaxSubDecay) extreme |= 1u << r;
+            }
+    }
+    const int qs = kT / nq;
+    const int q = 4 * wl / qs;  // the lane's sub-block
+    const bool ext = (extreme >> q) & 1u;
+    bool any_tiny = false;
+#pragma unroll
+    for (int j = 0; j < kHG; ++j) {
+        const float Dh = j ? d2.y : d2.x;
+        // cumsum relative to the sub-block start, and the sub-block's end value: the
+        // cumsums at tokens q qs - 1 and (q + 1) qs - 1 sit in lanes q qs / 4 - 1 and
+        // (q + 1) qs / 4 - 1; the same shuffles give lane wl the bounds of sub-block wl
+        const int ql = q * qs / 4, wlo = wl * qs / 4;
+        const float sb = __shfl_sync(0xffffffffu, vtot[j], max(ql - 1, 0));
+        const float se_ = __shfl_sync(0xffffffffu, vtot[j], min(ql + qs / 4, 32) - 1);
+        const float lo_w = __shfl_sync(0xffffffffu, vtot[j], min(max(wlo - 1, 0), 31));
+        const float hi_w = __shfl_sync(0xffffffffu, vtot[j], min(wlo + qs / 4, 32) - 1);
+        const float base = q > 0 ? sb : 0.f, endv = se_;
+        const float cse = endv - base;
+        const float c = (-cse <= kMaxSubDecay) ? 0.5f * cse : cse + kExtremeRef;
+        float wf4[4], u4[4], g4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float csl = cs[j][i] - base;
+            const float e = __expf(c - csl);  // within e^{+-75} outside extreme sub-blocks
+            const float wfv = dtv[j][i] * e;
+            const bool tiny = !ext && wfv < kTinyWF;  // D x from x itself (fixup_tokens)
+            any_tiny |= tiny && (tg0 + i < prm.L);
+            wf4[i] = wfv;
+            u4[i] = __expf(ext ? csl : csl - c);
+            g4[i] = (ext || tiny) ? 0.f : __fdividef(Dh, wfv);
+            cs[j][i] = csl;  // kept for the rare-token arrays below
+        }
+        *T(j, TAB_WF) = make_float4(wf4[0], wf4[1], wf4[2], wf4[3]);
+        *T(j, TAB_U) = make_float4(u4[0], u4[1], u4[2], u4[3]);
+        *T(j, TAB_UG) = make_float4(g4[0], g4[1], g4[2], g4[3]);
+        if (wl < nq) {
+            // the sub-block scalars: lane wl serves sub-block wl
+            const float se = hi_w - (wl > 0 ? lo_w : 0.f);
+            const bool sext = (extreme >> wl) & 1u;
+            const float sc_ = (-se <= kMaxSubDecay) ? 0.5f * se : se + kExtremeRef;
+            S(j)[SC_EC + wl] = __expf(sc_);
+            S(j)[SC_HS + wl] = sext ? 1.f : __expf(sc_);
+            S(j)[SC_IS + wl] = __expf(se - sc_);
+        }
+        if (wl == 0) S(j)[SC_D] = Dh;
+    }
+    any_tiny = __any_sync(0xffffffffu, any_tiny);
+    if (extreme != 0u || any_tiny) {
+        // sub-block cumsum and dt: read only by fixup_tokens, for jobs with rare tokens
+#pragma unroll
+        for (int j = 0; j < kHG; ++j) {
+            *TX(j, TABX_CS) = make_float4(cs[j][0], cs[j][1], cs[j][2], cs[j][3]);
+            *TX(j, TABX_DT) = make_float4(dtv[j][0], dtv[j][1], dtv[j][2], dtv[j][3]);
+        }
+    }
+    if (wl == 0) {
+        jw[0] = static_cast<uint32_t>(nq);
+        jw[1] = extreme;
+        jw[2] = any_tiny ? 1u : 0u;  // some valid token has wf < kTinyWF
+        jw[3] = 0u;
+        prm.cost[job] = static_cast<uint8_t>(job_cost(nq, extreme, any_tiny));
+        prm.decay[job] = make_float2(-bnd[0][7], -bnd[1][7]);  // cumsum at the block's last token
+    }
+}
+
+// The table record of one job (one block of one head pair), one warp per job
+// (two consecutive jobs per warp where one per warp would take more than one
+// wave of CTAs: every CTA ranks the heads, once for all of its jobs):
 // lane l owns tokens 4l .. 4l + 3 of the block for both heads. dt =
 // clamp(softplus(dt_raw + dt_bias)), the block cumsum of dt*A, the sub-block
 // split (the largest of 128, 64, 32, 16 tokens whose decays all stay within
@@ -1303,8 +1466,8 @@ constexpr int kTableWarps = 4;   // chain_tables: jobs (warps) per CTA
 // slowly decaying head is not tied to them. Every CTA ranks the heads itself
 // (nheads x heads-per-group comparisons); CTA 0 also stores the order for the
 // chain kernel. The pairing only schedules: each head's result is its own.
-// At most 56 registers so that 9 CTAs fit an SM: 1280 CTAs of the 2.7B shape in one wave.
-__global__ void __launch_bounds__(kTableWarps * 32, 9) chain_tables(const TableParams prm) {
+// At most 56 registers so that 9 CTAs fit an SM: the 1280 CTAs of the 2.7B shape in one wave.
+__global__ void __launch_bounds__(kTableWarps * 32, kTableCtasPerSm) chain_tables(const TableParams prm) {
     __shared__ __align__(16) uint32_t s_key[kSortMaxHeads];
     __shared__ int s_order[kSortMaxHeads];
     // launched early behind the previous kernel of the stream (which may still use the
@@ -1339,165 +1502,11 @@ __global__ void __launch_bounds__(kTableWarps * 32, 9) chain_tables(const TableP
     if (blockIdx.x == 0)
         for (int h = threadIdx.x; h < prm.H; h += blockDim.x) prm.order[h] = prm.sort_pairs ? s_order[h] : h;
     const int wl = threadIdx.x & 31;
-    // one warp per job (job indices fit 31 bits: the host launches only then)
-    const int job = static_cast<int>(blockIdx.x) * kTableWarps + static_cast<int>(threadIdx.x >> 5);
-    if (job < prm.total) {
-        const int blk = job % prm.nblk;
-        const int chain = job / prm.nblk;
-        const int b = chain / prm.chains_per_b, cb = chain % prm.chains_per_b;
-        const int hh[kHG] = {prm.sort_pairs ? s_order[kHG * cb] : kHG * cb,
-                             prm.sort_pairs ? s_order[kHG * cb + 1] : kHG * cb + 1};
-        SSD_CHECK(prm.status, hh[0] >= 0 && hh[1] >= 0 && hh[0] < prm.H && hh[1] < prm.H && hh[0] != hh[1]);
-        uint8_t* rec = prm.out + static_cast<size_t>(job) * kRecBytes;
-        float* tabs = reinterpret_cast<float*>(rec);
-        float* scal = reinterpret_cast<float*>(rec + kRecTab);
-        uint32_t* jw = reinterpret_cast<uint32_t*>(rec + kRecTab + kRecScal);
-        float* tabx = reinterpret_cast<float*>(rec + kRecSmem);
-        auto T = [&](int j, int arr) { return reinterpret_cast<float4*>(tabs + (j * kNumTab + arr) * kT) + wl; };
-        auto TX = [&](int j, int arr) { return reinterpret_cast<float4*>(tabx + (j * kNumTabX + arr) * kT) + wl; };
-        auto S = [&](int j) { return scal + j * kScal; };
-        // lane wl owns tokens 4 wl .. 4 wl + 3 of the block (one 16-token unit); every
-        // global load is issued here, before the first store
-        const int tg0 = blk * kT + 4 * wl;
-        const float2 bias = make_float2(__ldg(prm.dt_bias + hh[0]), __ldg(prm.dt_bias + hh[1]));
-        const float2 a2 = make_float2(__ldg(prm.A + hh[0]), __ldg(prm.A + hh[1]));
-        const float2 d2 = prm.D ? make_float2(__ldg(prm.D + hh[0]), __ldg(prm.D + hh[1])) : make_float2(0.f, 0.f);
-        float2 raw[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float* row = prm.dt + (static_cast<long long>(b) * prm.L + (tg0 + i)) * prm.H;
-            raw[i] = tg0 + i < prm.L ? make_float2(__ldg(row + hh[0]), __ldg(row + hh[1])) : make_float2(0.f, 0.f);
-        }
-        float dtv[kHG][4], cs[kHG][4];
-        float cut[4];  // a new packed sequence starts at the token: no state crosses (kSeqCutNats)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const long long t = tg0 + i;
-            cut[i] = (prm.seq && t > 0 && t < prm.L &&
-                      __ldg(prm.seq + static_cast<long long>(b) * prm.L + t) !=
-                          __ldg(prm.seq + static_cast<long long>(b) * prm.L + t - 1))
-                         ? -kSeqCutNats
-                         : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < kHG; ++j)
-                dtv[j][i] = tg0 + i < prm.L
-                                ? fminf(fmaxf(softplus_f((j ? raw[i].y : raw[i].x) + (j ? bias.y : bias.x)), prm.dt_min),
-                                        prm.dt_max)
-                                : 0.f;
-        float bnd[kHG][8];  // cumsum at token 16k + 15
-        float vtot[kHG];     // cumsum at token 4 wl + 3 (this lane's last token)
-#pragma unroll
-        for (int j = 0; j < kHG; ++j) {
-            const float a = j ? a2.y : a2.x;
-            float run = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                run += fmaf(dtv[j][i], a, cut[i]);
-                cs[j][i] = run;
-            }
-            float v = run;  // inclusive scan of the lane totals
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, v, off);
-                if (wl >= off) v += o;
-            }
-            const float pre = v - run;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) cs[j][i] += pre;
-            vtot[j] = v;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) bnd[j][k] = __shfl_sync(0xffffffffu, v, 4 * k + 3);
-        }
-        int nq = 8;
-#pragma unroll
-        for (int cand = 1; cand < 8; cand <<= 1) {
-            const int m = 8 / cand;  // 16-token units per sub-block
-            bool ok = true;
-#pragma unroll
-            for (int j = 0; j < kHG; ++j)
-#pragma unroll
-                for (int r = 0; r < cand; ++r) {
-                    const float lo_ = r > 0 ? bnd[j][r * m - 1] : 0.f;
-                    ok = ok && (lo_ - bnd[j][(r + 1) * m - 1] <= kMaxSubDecay);
-                }
-            if (ok && nq == 8) nq = cand;
-        }
-        uint32_t extreme = 0u;
-        if (nq == 8) {
-#pragma unroll
-            for (int j = 0; j < kHG; ++j)
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const float lo_ = r > 0 ? bnd[j][r - 1] : 0.f;
-                    if (lo_ - bnd[j][r] > kMaxSubDecay) extreme |= 1u << r;
-                }
-        }
-        const int qs = kT / nq;
-        const int q = 4 * wl / qs;  // the lane's sub-block
-        const bool ext = (extreme >> q) & 1u;
-        bool any_tiny = false;
-#pragma unroll
-        for (int j = 0; j < kHG; ++j) {
-            const float Dh = j ? d2.y : d2.x;
-            // cumsum relative to the sub-block start, and the sub-block's end value: the
-            // cumsums at tokens q qs - 1 and (q + 1) qs - 1 sit in lanes q qs / 4 - 1 and
-            // (q + 1) qs / 4 - 1; the same shuffles give lane wl the bounds of sub-block wl
-            const int ql = q * qs / 4, wlo = wl * qs / 4;
-            const float sb = __shfl_sync(0xffffffffu, vtot[j], max(ql - 1, 0));
-            const float se_ = __shfl_sync(0xffffffffu, vtot[j], min(ql + qs / 4, 32) - 1);
-            const float lo_w = __shfl_sync(0xffffffffu, vtot[j], min(max(wlo - 1, 0), 31));
-            const float hi_w = __shfl_sync(0xffffffffu, vtot[j], min(wlo + qs / 4, 32) - 1);
-            const float base = q > 0 ? sb : 0.f, endv = se_;
-            const float cse = endv - base;
-            const float c = (-cse <= kMaxSubDecay) ? 0.5f * cse : cse + kExtremeRef;
-            float wf4[4], u4[4], g4[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float csl = cs[j][i] - base;
-                const float e = __expf(c - csl);  // within e^{+-75} outside extreme sub-blocks
-                const float wfv = dtv[j][i] * e;
-                const bool tiny = !ext && wfv < kTinyWF;  // D x from x itself (fixup_tokens)
-                any_tiny |= tiny && (tg0 + i < prm.L);
-                wf4[i] = wfv;
-                u4[i] = __expf(ext ? csl : csl - c);
-                g4[i] = (ext || tiny) ? 0.f : __fdividef(Dh, wfv);
-                cs[j][i] = csl;  // kept for the rare-token arrays below
-            }
-            *T(j, TAB_WF) = make_float4(wf4[0], wf4[1], wf4[2], wf4[3]);
-            *T(j, TAB_U) = make_float4(u4[0], u4[1], u4[2], u4[3]);
-            *T(j, TAB_UG) = make_float4(g4[0], g4[1], g4[2], g4[3]);
-            if (wl < nq) {
-                // the sub-block scalars: lane wl serves sub-block wl
-                const float se = hi_w - (wl > 0 ? lo_w : 0.f);
-                const bool sext = (extreme >> wl) & 1u;
-                const float sc_ = (-se <= kMaxSubDecay) ? 0.5f * se : se + kExtremeRef;
-                S(j)[SC_EC + wl] = __expf(sc_);
-                S(j)[SC_HS + wl] = sext ? 1.f : __expf(sc_);
-                S(j)[SC_IS + wl] = __expf(se - sc_);
-            }
-            if (wl == 0) S(j)[SC_D] = Dh;
-        }
-        any_tiny = __any_sync(0xffffffffu, any_tiny);
-        if (extreme != 0u || any_tiny) {
-            // sub-block cumsum and dt: read only by fixup_tokens, for jobs with rare tokens
-#pragma unroll
-            for (int j = 0; j < kHG; ++j) {
-                *TX(j, TABX_CS) = make_float4(cs[j][0], cs[j][1], cs[j][2], cs[j][3]);
-                *TX(j, TABX_DT) = make_float4(dtv[j][0], dtv[j][1], dtv[j][2], dtv[j][3]);
-            }
-        }
-        if (wl == 0) {
-            jw[0] = static_cast<uint32_t>(nq);
-            jw[1] = extreme;
-            jw[2] = any_tiny ? 1u : 0u;  // some valid token has wf < kTinyWF
-            jw[3] = 0u;
-            prm.cost[job] = static_cast<uint8_t>(job_cost(nq, extreme, any_tiny));
-            prm.decay[job] = make_float2(-bnd[0][7], -bnd[1][7]);  // cumsum at the block's last token
-        }
-    }
+    // jobs_per_warp consecutive jobs per warp, one after another (job indices fit
+    // 31 bits: the host launches only then)
+    const int job0 = (static_cast<int>(blockIdx.x) * kTableWarps + static_cast<int>(threadIdx.x >> 5)) * prm.jobs_per_warp;
+#pragma unroll 1
+    for (int job = job0; job < job0 + prm.jobs_per_warp && job < prm.total; ++job) table_job(prm, job, wl, s_order);
 }
 
 // L = C.B^T masked to s <= t, in bf16, for one (batch, block, group): the matrix
@@ -1675,7 +1684,10 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t tcfg = {};
-    tcfg.gridDim = dim3(static_cast<unsigned>((pl.total + kTableWarps - 1) / kTableWarps));
+    // two jobs per warp once one per warp would take more than a wave of CTAs (fewer CTAs rank the heads)
+    tp.jobs_per_warp = pl.total > static_cast<long long>(kTableWarps) * kTableCtasPerSm * pl.ncta ? 2 : 1;
+    const long long per_cta = static_cast<long long>(kTableWarps) * tp.jobs_per_warp;
+    tcfg.gridDim = dim3(static_cast<unsigned>((pl.total + per_cta - 1) / per_cta));
     tcfg.blockDim = dim3(kTableWarps * 32);
     tcfg.stream = a.stream;
     tcfg.attrs = pdl;
