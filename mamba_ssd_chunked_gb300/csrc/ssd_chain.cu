@@ -88,6 +88,9 @@ enum Scal { SC_EC = 0, SC_HS = 8, SC_IS = 16, SC_D = 24 };
 // hand-off: what the zero start leaves out is scaled by e^{-32} < 2^-46, some
 // 2^-22 of one fp32 unit in the last place of the state it is added to.
 constexpr float kWarmupNats = 32.f;
+// A warm-up block's time as a share of its job cost, in percent (the warm-up
+// decision; on the 130M and 2.7B layer shapes 60 to 70 balance best).
+constexpr uint32_t kWarmupCostPct = 70;
 // Decay-sorted head pairs: the pair table is sorted when nheads and the
 // per-group sort stay this small (every table CTA sorts its own copy).
 constexpr int kSortMaxHeads = 1024;
@@ -549,8 +552,10 @@ __device__ __noinline__ void chain_horizons(const float2* __restrict__ decay, lo
 // no earlier than the chain's blocks [0, a) take when run one after another
 // (t_ready); this CTA needs it once the rest of its range is done (t_need, the
 // segment runs last). Waiting ends the range at t_ready + t_seg, warming up at
-// t_range + cost(warm-up): warm up when that is earlier (warmup = 1), or
-// always (warmup = 2, or long chains, whose split already charges it). Every load of a pass over the bytes is issued before
+// t_range + cost(warm-up), a warm-up block taking kWarmupCostPct percent of its
+// job cost (it loads no L or C and has no k5 or epilogue): warm up when that is
+// earlier (warmup = 1), or always (warmup = 2, or long chains, whose split
+// already charges it). Every load of a pass over the bytes is issued before
 // the first sum, so the decision costs about one memory round trip per 128
 // jobs of the chain.
 __device__ __noinline__ int warmup_blocks(const ChainParams& prm, const JobList& jobs, int lane, bool force) {
@@ -611,7 +616,7 @@ __device__ __noinline__ int warmup_blocks(const ChainParams& prm, const JobList&
         t_range += __shfl_xor_sync(0xffffffffu, t_range, o);
         t_seg += __shfl_xor_sync(0xffffffffu, t_seg, o);
     }
-    return (t_range + t_wu < t_ready + t_seg) ? m : 0;
+    return (t_range + (t_wu * kWarmupCostPct) / 100 < t_ready + t_seg) ? m : 0;
 }
 
 template <int NS>
