@@ -872,13 +872,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::mma_commit(&bars[B_R_EMPTY0 + pl % Y::kRing]);
                 ptx::mma_commit(&bars[B_XW_FREE0 + xs]);
+                // the second C half (dstate 256) is waited for only before its first k5b
+                // MMAs: it loads once k5a has freed L's slot, and the first half's MMAs
+                // run meanwhile
                 uint32_t c_slot[Y::kNB];
-#pragma unroll
-                for (int hh = 0; hh < Y::kNB; ++hh) {
+                uint32_t c_have = 0u;
+                auto wait_c = [&](int hh) {
+                    if ((c_have >> hh) & 1u) return;
                     const int pc = Y::kKinds * J + Y::kindC(hh);
                     WB(B_R_FULL0 + pc % Y::kRing, (pc / Y::kRing) & 1);
                     c_slot[hh] = sbase + K::OFF_RING + (pc % Y::kRing) * 2 * kTile;
-                }
+                    c_have |= 1u << hh;
+                };
+                wait_c(0);
                 for (int q = 0; q < nq; ++q, ++u) {
                     const int hb = u % Y::kHBuf;
                     WB(B_H_FULL0 + hb, (u / Y::kHBuf) & 1);
@@ -886,6 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!warm) {
 #pragma unroll
                         for (int hh = 0; hh < Y::kNB; ++hh) {  // K = n in halves: H columns 64 hh.., C half hh
+                            wait_c(hh);
                             const uint64_t b_c = ptx::desc_sw128(c_slot[hh] + q * qs * 128, 16, 1024);
                             if (SSD_CHECK(prm.status, hb < Y::kHBuf && Y::COL_H + (NS / 2) * hb + 64 * hh + 64 <= Y::COL_Y &&
                                                           (q + 1) * qs <= kT))
@@ -895,6 +902,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::mma_commit(&bars[B_H_EMPTY0 + hb]);
                 }
+#pragma unroll
+                for (int hh = 0; hh < Y::kNB; ++hh) wait_c(hh);  // warm-up jobs: the entries complete empty
 #pragma unroll
                 for (int hh = 0; hh < Y::kNB; ++hh)
                     ptx::mma_commit(&bars[B_R_EMPTY0 + (Y::kKinds * J + Y::kindC(hh)) % Y::kRing]);
