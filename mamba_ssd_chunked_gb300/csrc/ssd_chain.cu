@@ -752,6 +752,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     SSD_CHECK(prm.status, tile >= 0 && tile < prm.batch * prm.nblk * prm.G);
                     ptx::tma_load_4d(dst, &tm_l, fb, 0, 0, 0, tile, keep);
                     ptx::tma_load_4d(dst + kTile, &tm_l, fb, 64, 0, 0, tile, keep);
+                    if (Y::kNB == 2) {
+                        // the second C half loads only once k5a has freed this slot: into L2 now
+                        ptx::tma_prefetch_4d(&tm_c, 128, jp.g, jp.blk * kT, jp.b);
+                        ptx::tma_prefetch_4d(&tm_c, 192, jp.g, jp.blk * kT, jp.b);
+                    }
                 } else {
                     // a 128-column half of B or C: n in [128 half, 128 half + 128)
                     const int n0 = 128 * (is_b ? kind - Y::kindB(0) : kind - Y::kindC(0));
