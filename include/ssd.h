@@ -78,8 +78,9 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
  *                   or 256).
  *   SSD_PATH_CHAIN: fused tcgen05/TMA kernel, one persistent CTA per SM that
  *                   walks whole chains block by block with the chunk state
- *                   kept in tensor memory (bf16 io, headdim 64, dstate 128,
- *                   chunk_len 128 or 256). Its workspace depends on the
+ *                   kept in tensor memory (bf16 io, headdim 64 with an even
+ *                   number of heads per group, or headdim 128; dstate 128 or
+ *                   256; chunk_len 128 or 256). Its workspace depends on the
  *                   current device's SM count. */
 typedef enum { SSD_PATH_AUTO = 0, SSD_PATH_SIMT = 1, SSD_PATH_TC = 2, SSD_PATH_CHAIN = 3 } ssd_path;
 

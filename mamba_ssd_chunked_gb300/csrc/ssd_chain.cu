@@ -67,7 +67,7 @@ namespace ssd {
 namespace {
 
 constexpr int kT = 128;                 // tokens per block
-constexpr int kP = 64;                  // headdim
+constexpr int kP = 64;                  // rows per chain half: a head at headdim 64, half a head at 128
 constexpr int kHG = 2;                  // heads per chain
 constexpr uint32_t kTile = 16384;       // 128 rows x 128 bytes, 128-byte swizzle
 constexpr float kMaxSubDecay = 150.f;   // a sub-block decaying at most this keeps factors within e^{+-75}
@@ -264,27 +264,36 @@ __device__ __forceinline__ JobList make_jobs(const ChainParams& p, int first, in
 struct JobPos {
     int blk, lo, hi;  // block, and the block range of the job's segment
     int b, cb, g;     // batch row, chain (head pair) within the row, B/C group
-    int h[kHG];       // the pair's heads
+    int h[kHG];       // the heads of the chain's two 64-row halves (one head twice at headdim 128)
+    int p0[kHG];      // the first p of each half within its head (0, or 0 and 64 at headdim 128)
     bool warm;        // warm-up block: advances the state, writes no y
     bool wait;        // the segment starts from the previous CTA's hand-off
 };
 
 __device__ __forceinline__ JobPos job_pos(const JobList& jobs, int J, int chains_per_b, int HperG,
-                                       const int* __restrict__ order, uint32_t* status) {
+                                       const int* __restrict__ order, uint32_t* status, int hpc = kHG) {
     JobPos jp;
     int chain;
     jobs.at(J, chain, jp.blk, jp.lo, jp.hi);
     jp.b = chain / chains_per_b;
     jp.cb = chain - jp.b * chains_per_b;
-    jp.g = (jp.cb * kHG) / HperG;  // pairs never straddle a group
-    // the pair order, from this CTA's shared-memory copy (null: the natural order 2 cb, 2 cb + 1)
-    jp.h[0] = order ? order[kHG * jp.cb] : kHG * jp.cb;
-    jp.h[1] = order ? order[kHG * jp.cb + 1] : kHG * jp.cb + 1;
+    jp.g = (jp.cb * hpc) / HperG;  // pairs never straddle a group
+    if (hpc == kHG) {
+        // the pair order, from this CTA's shared-memory copy (null: the natural order 2 cb, 2 cb + 1)
+        jp.h[0] = order ? order[kHG * jp.cb] : kHG * jp.cb;
+        jp.h[1] = order ? order[kHG * jp.cb + 1] : kHG * jp.cb + 1;
+        jp.p0[0] = jp.p0[1] = 0;
+    } else {  // headdim 128: chain cb is head cb, its halves p < 64 and p >= 64
+        jp.h[0] = jp.h[1] = jp.cb;
+        jp.p0[0] = 0;
+        jp.p0[1] = kP;
+    }
     // a job inside its segment and the block range; both heads real heads of the pair's group
     SSD_CHECK(status, J >= 0 && J < jobs.count() && 0 <= jp.lo && jp.lo <= jp.blk && jp.blk < jp.hi &&
                           jp.hi <= jobs.nblk && chain >= 0);
-    SSD_CHECK(status, jp.h[0] >= 0 && jp.h[1] >= 0 && jp.h[0] < kHG * chains_per_b && jp.h[1] < kHG * chains_per_b &&
-                          jp.h[0] != jp.h[1] && jp.h[0] / HperG == jp.g && jp.h[1] / HperG == jp.g);
+    SSD_CHECK(status, jp.h[0] >= 0 && jp.h[1] >= 0 && jp.h[0] < hpc * chains_per_b && jp.h[1] < hpc * chains_per_b &&
+                          (hpc == kHG ? jp.h[0] != jp.h[1] : jp.h[0] == jp.h[1]) && jp.h[0] / HperG == jp.g &&
+                          jp.h[1] / HperG == jp.g);
     const bool seg_f = (chain == jobs.cF);
     jp.warm = seg_f && jp.blk < jobs.a;
     jp.wait = seg_f && jp.lo > 0 && jobs.wu == 0;
@@ -619,13 +628,15 @@ __device__ __noinline__ int warmup_blocks(const ChainParams& prm, const JobList&
     return (t_range + (t_wu * kWarmupCostPct) / 100 < t_ready + t_seg) ? m : 0;
 }
 
-template <int NS>
+template <int NS, int PD>  // dstate, headdim
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chain_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_l,
                     const __grid_constant__ CUtensorMap tm_y, const ChainParams prm) {
     using K = Cfg;
     using Y = Lay<NS>;
+    static_assert(PD == kP || PD == 2 * kP, "headdim 64 or 128");
+    constexpr int kHpc = PD == kP ? kHG : 1;  // heads per chain
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
@@ -714,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int njobs = jobs.count();
     const int HperG = prm.H / prm.G;
-    const int chains_per_b = prm.H / kHG;
+    const int chains_per_b = prm.H / kHpc;
     // the pair order into shared memory: every role looks heads up per job; with
     // more heads than the prep kernel sorts, the order is the natural one
     int* order = nullptr;
@@ -736,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ru > 0) WB(B_R_EMPTY0 + rs, (ru - 1) & 1);
                 if (*abort_flag) break;
                 const int J = pr / Y::kKinds, kind = pr - Y::kKinds * J;
-                const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
+                const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status, kHpc);
                 uint64_t* fb = &bars[B_R_FULL0 + rs];
                 uint8_t* dst = smem + K::OFF_RING + rs * 2 * kTile;
                 const bool is_b = !Y::kOwnB && kind >= Y::kindB(0) && kind < Y::kindB(0) + Y::kNB;
@@ -783,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int nb = 0;  // B loads issued
             const uint64_t keep = ptx::policy_evict_last();  // B is read again by the group's other pairs
             auto load_b = [&](int J) {
-                const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
+                const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status, kHpc);
                 SSD_CHECK(prm.status, jp.b < prm.batch && jp.g < prm.G);
                 ptx::mbar_arrive_expect_tx(&bars[B_B_FULL], 2 * Y::kNB * kTile);
                 for (int i = 0; i < 2 * Y::kNB; ++i)
@@ -927,7 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ts = jx & (kTabSlots - 1);
                 if (jx >= kTabSlots) WB(B_TAB_EMPTY0 + ts, ((jx / kTabSlots) - 1) & 1);
                 if (*abort_flag) break;
-                const JobPos jp = job_pos(jobs, jx, chains_per_b, HperG, order, prm.status);
+                const JobPos jp = job_pos(jobs, jx, chains_per_b, HperG, order, prm.status, kHpc);
                 const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.cb) * prm.nblk + jp.blk;
                 ptx::mbar_arrive_expect_tx(&bars[B_TAB_FULL0 + ts], kRecSmem);
                 ptx::bulk_load(smem + K::OFF_TAB + ts * kRecSmem, prm.tables + rec * kRecBytes, kRecSmem,
@@ -941,17 +952,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 SSD_CHECK(prm.status, Y::OFF_XW + (xs + 1) * 2 * kTile <= K::OFF_TAB &&
                                           static_cast<long long>(jp.blk) * kT < prm.L && jp.b < prm.batch);
                 ptx::mbar_arrive_expect_tx(fb, 2 * kTile);
-                ptx::tma_load_4d(dst, &tm_x, fb, 0, jp.h[0], jp.blk * kT, jp.b, once);
-                ptx::tma_load_4d(dst + kTile, &tm_x, fb, 0, jp.h[1], jp.blk * kT, jp.b, once);
+                ptx::tma_load_4d(dst, &tm_x, fb, jp.p0[0], jp.h[0], jp.blk * kT, jp.b, once);
+                ptx::tma_load_4d(dst + kTile, &tm_x, fb, jp.p0[1], jp.h[1], jp.blk * kT, jp.b, once);
                 if (jp.blk == 0 && prm.init)  // a chain start: its initial states into L2 for the state warps
                     for (int j = 0; j < kHG; ++j)
-                        ptx::bulk_prefetch_l2(prm.init + (static_cast<size_t>(jp.b) * prm.H + jp.h[j]) * kP * NS,
-                                              kP * NS * sizeof(float));
+                        ptx::bulk_prefetch_l2(
+                            prm.init + ((static_cast<size_t>(jp.b) * prm.H + jp.h[j]) * PD + jp.p0[j]) * NS,
+                            kP * NS * sizeof(float));
                 if (Y::kPrefetchX && jx >= Y::kXW && jx + Y::kXW < njobs) {
                     // the X of job jx + kXW into L2: its load, once the slot is free, then hits L2
-                    const JobPos jn = job_pos(jobs, jx + Y::kXW, chains_per_b, HperG, order, prm.status);
-                    ptx::tma_prefetch_4d(&tm_x, 0, jn.h[0], jn.blk * kT, jn.b);
-                    ptx::tma_prefetch_4d(&tm_x, 0, jn.h[1], jn.blk * kT, jn.b);
+                    const JobPos jn = job_pos(jobs, jx + Y::kXW, chains_per_b, HperG, order, prm.status, kHpc);
+                    ptx::tma_prefetch_4d(&tm_x, jn.p0[0], jn.h[0], jn.blk * kT, jn.b);
+                    ptx::tma_prefetch_4d(&tm_x, jn.p0[1], jn.h[1], jn.blk * kT, jn.b);
                 }
             }
             for (int i = 0; i < Y::kXW && i < jx; ++i) {
@@ -1010,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sdone = 0, u = 0;
         for (int J = 0; J < njobs; ++J) {
             const int ts = J & (kTabSlots - 1);
-            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
+            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status, kHpc);
             const bool seg_start = (jp.blk == jp.lo), seg_end = (jp.blk == jp.hi - 1);
             const int h = jp.h[j];
             if (seg_start && jp.wait) {
@@ -1040,7 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else if (jp.lo > 0)
                     src = nullptr;  // warm-up from a zero state
                 else if (prm.init)
-                    src = prm.init + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * NS;
+                    src = prm.init + ((static_cast<size_t>(jp.b) * prm.H + h) * PD + jp.p0[j] + p) * NS;
                 // a hand-off row of the previous CTA or an initial-state row of a real (batch, head)
                 if (!SSD_CHECK(prm.status, (jp.wait ? (cta >= 1 && cta <= prm.ncta - 1)
                                                     : (jp.b < prm.batch && h >= 0 && h < prm.H)) && p < kP))
@@ -1113,7 +1125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++sdone;
                 ptx::tc_fence_after();
                 float* dst = to_final ? (prm.final_state
-                                             ? prm.final_state + ((static_cast<size_t>(jp.b) * prm.H + h) * kP + p) * NS
+                                             ? prm.final_state + ((static_cast<size_t>(jp.b) * prm.H + h) * PD + jp.p0[j] + p) * NS
                                              : nullptr)
                                       : prm.handoff + ((static_cast<size_t>(cta) * kHG + j) * kP + p) * NS;
                 // the final state of a real (batch, head), or this CTA's own hand-off slot
@@ -1155,7 +1167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ldmatrix / stmatrix row addresses: lane l serves row l % 8 of matrix l / 8
         // (matrix m: tokens + 8 (m >> 1), p chunk + (m & 1))
         const int mrow = lane & 7, mm = lane >> 3;
-        const long long x_tstride = static_cast<long long>(prm.H) * kP;
+        const long long x_tstride = static_cast<long long>(prm.H) * PD;
         for (int J = 0; J < njobs; ++J) {
             const int ts = J & (kTabSlots - 1), yb = J % Y::kYBuf, xs = J % Y::kXW;
             WB(B_TAB_FULL0 + ts, (J / kTabSlots) & 1);
@@ -1163,7 +1175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2* g2 = reinterpret_cast<const float2*>(T(ts, j, TAB_UG));
             const uint32_t extreme = JW(ts)[1];
             const bool rare = (extreme | JW(ts)[2]) != 0u;
-            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status);
+            const JobPos jp = job_pos(jobs, J, chains_per_b, HperG, order, prm.status, kHpc);
             WB(B_Y_FULL0 + yb, (J / Y::kYBuf) & 1);
             WB(B_XW_FREE0 + xs, (J / Y::kXW) & 1);  // k3 and k5a no longer read W
             ptx::tc_fence_after();
@@ -1233,7 +1245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (et == 0) {
                 const uint64_t once = ptx::policy_evict_first();  // y is written once
                 for (int jj = 0; jj < kHG; ++jj)
-                    ptx::tma_store_4d(&tm_y, smem + Y::OFF_XW + (xs * kHG + jj) * kTile, 0, jp.h[jj],
+                    ptx::tma_store_4d(&tm_y, smem + Y::OFF_XW + (xs * kHG + jj) * kTile, jp.p0[jj], jp.h[jj],
                                       jp.blk * kT, jp.b, once);
                 ptx::bulk_commit_group();
                 ptx::bulk_wait_group_read0();
@@ -1251,7 +1263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const long long t0 = static_cast<long long>(jp.blk) * kT;
                 const int tn = static_cast<int>(min(static_cast<long long>(kT), prm.L - t0));  // valid tokens
                 SSD_CHECK(prm.status, tn >= 1 && tn <= kT && p < kP && ts < kTabSlots);
-                const long long off = ((static_cast<long long>(jp.b) * prm.L + t0) * prm.H + jp.h[j]) * kP + p;
+                const long long off = ((static_cast<long long>(jp.b) * prm.L + t0) * prm.H + jp.h[j]) * PD + jp.p0[j] + p;
                 const long long rec = (static_cast<long long>(jp.b) * chains_per_b + jp.cb) * prm.nblk + jp.blk;
                 const float* xt = reinterpret_cast<const float*>(prm.tables + rec * kRecBytes + kRecSmem) +
                                   j * kNumTabX * kT;
@@ -1288,6 +1300,7 @@ struct TableParams {
     int* order;          // [H] heads in pair order (written by CTA 0)
     const int32_t* seq;  // [batch, L] packed-sequence ids, or null
     int sort_pairs;      // pair the heads of each group by decay rate (else 2 cb, 2 cb + 1)
+    int hpc;             // heads per chain: 2, or 1 at headdim 128 (both halves of chain cb are head cb)
     int jobs_per_warp;   // consecutive jobs per warp (1 or 2)
     long long L;
     int H, G, nblk, chains_per_b, total;
@@ -1314,9 +1327,12 @@ __device__ __forceinline__ void table_job(const TableParams& prm, int job, int w
     const int blk = job % prm.nblk;
     const int chain = job / prm.nblk;
     const int b = chain / prm.chains_per_b, cb = chain % prm.chains_per_b;
-    const int hh[kHG] = {prm.sort_pairs ? s_order[kHG * cb] : kHG * cb,
-                         prm.sort_pairs ? s_order[kHG * cb + 1] : kHG * cb + 1};
-    SSD_CHECK(prm.status, hh[0] >= 0 && hh[1] >= 0 && hh[0] < prm.H && hh[1] < prm.H && hh[0] != hh[1]);
+    // heads per chain hpc = 2: ranks 2 cb, 2 cb + 1 of the pair order (or heads 2 cb, 2 cb + 1);
+    // hpc = 1 (headdim 128): head cb for both 64-row halves
+    const int c0 = prm.hpc * cb;
+    const int hh[kHG] = {prm.sort_pairs ? s_order[c0] : c0, prm.sort_pairs ? s_order[c0 + 1] : c0 + prm.hpc - 1};
+    SSD_CHECK(prm.status, hh[0] >= 0 && hh[1] >= 0 && hh[0] < prm.H && hh[1] < prm.H &&
+                              (prm.hpc == kHG) == (hh[0] != hh[1]));
     uint8_t* rec = prm.out + static_cast<size_t>(job) * kRecBytes;
     float* tabs = reinterpret_cast<float*>(rec);
     float* scal = reinterpret_cast<float*>(rec + kRecTab);
@@ -1629,7 +1645,7 @@ struct ChainPlan {
 ChainPlan plan(const ssd_dims& d, int nsm) {
     ChainPlan p;
     p.nblk = (d.seqlen + kT - 1) / kT;
-    p.nchains = d.batch * d.nheads / kHG;
+    p.nchains = d.batch * d.nheads / (d.headdim == 2 * kP ? 1 : kHG);
     p.total = p.nchains * p.nblk;
     p.ncta = static_cast<int>(std::min<long long>(nsm, p.total));
     p.ntiles = d.batch * p.nblk * d.ngroups;
@@ -1688,7 +1704,8 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     tp.L = d.seqlen;
     tp.H = static_cast<int>(d.nheads);
     tp.nblk = static_cast<int>(pl.nblk);
-    tp.chains_per_b = static_cast<int>(d.nheads / kHG);
+    tp.hpc = d.headdim == 2 * kP ? 1 : kHG;
+    tp.chains_per_b = static_cast<int>(d.nheads / tp.hpc);
     tp.dt_min = a.dt_min;
     tp.dt_max = a.dt_max;
     tp.seq = a.seq_idx;
@@ -1698,7 +1715,8 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     tp.ncounters = 1 + pl.ncta;
     tp.order = order;
     tp.G = static_cast<int>(d.ngroups);
-    tp.sort_pairs = (d.nheads <= kSortMaxHeads && d.nheads * (d.nheads / d.ngroups) <= kSortMaxWork) ? 1 : 0;
+    tp.sort_pairs = (tp.hpc == kHG && d.nheads <= kSortMaxHeads && d.nheads * (d.nheads / d.ngroups) <= kSortMaxWork)
+                        ? 1 : 0;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1758,7 +1776,8 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     p.chain_wait_ns = a.wait_limit_ns;
     p.dt_min = a.dt_min;
     p.dt_max = a.dt_max;
-    if (cudaFuncSetAttribute(ssd_chain_fused<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto* kernel = d.headdim == 2 * kP ? ssd_chain_fused<NS, 2 * kP> : ssd_chain_fused<NS, kP>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Cfg::SMEM_BYTES)) != cudaSuccess)
         return SSD_ERR_CUDA;
     cudaLaunchConfig_t ccfg = {};
@@ -1769,7 +1788,7 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
     ccfg.attrs = pdl;
     ccfg.numAttrs = 1;
     timing_begin(a.stream);
-    if (cudaLaunchKernelEx(&ccfg, ssd_chain_fused<NS>, tx, tb, tc, tl, ty, p) != cudaSuccess) return SSD_ERR_CUDA;
+    if (cudaLaunchKernelEx(&ccfg, kernel, tx, tb, tc, tl, ty, p) != cudaSuccess) return SSD_ERR_CUDA;
     timing_end(a.stream);
     note_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
@@ -1779,9 +1798,10 @@ ssd_status launch_chain(const FwdArgs& a, void* ws, const ChainPlan& pl) {
 
 bool chain_supported(const ssd_dims& d, ssd_dtype io, int chunk_len) {
     if (io != SSD_BF16) return false;
-    if (d.headdim != kP || (d.dstate != 128 && d.dstate != 256)) return false;
+    if ((d.headdim != kP && d.headdim != 2 * kP) || (d.dstate != 128 && d.dstate != 256)) return false;
     if (chunk_len != 128 && chunk_len != 256) return false;
-    if ((d.nheads / d.ngroups) % kHG != 0) return false;  // a chain's two heads share a B/C group
+    // a chain's two heads share a B/C group (at headdim 128 a chain is one head)
+    if (d.headdim == kP && (d.nheads / d.ngroups) % kHG != 0) return false;
     if (d.seqlen >= (1ll << 31) || d.batch >= (1ll << 20) || d.nheads >= (1 << 20)) return false;
     const long long nblk = (d.seqlen + kT - 1) / kT;
     if (nblk * d.batch * d.nheads >= (1ll << 31)) return false;   // job indices are 32-bit

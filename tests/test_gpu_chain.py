@@ -2,7 +2,8 @@
 fp64 oracle.
 
 The cases cover: one tile, a single token, lengths one below / above a tile,
-ragged lengths, head pairs of one or several groups; chains split across CTAs
+ragged lengths, head pairs of one or several groups, headdim 128 (a chain
+per head); chains split across CTAs
 (a hand-off at every block, and hand-offs in the middle of long chains);
 blocks that run whole, blocks split into 64-, 32- and 16-token sub-blocks by
 their decay, and 16-token sub-blocks whose decay is still too strong
@@ -48,6 +49,13 @@ CHAIN_SHAPES = [
     (1, 1000, 6, 64, 3, 256),
     (1, 2000, 2, 64, 1, 256),     # a hand-off at every block
     (2, 4100, 6, 64, 1, 256),
+    # headdim 128: a chain is one head, its two 64-row halves in one MMA
+    (1, 128, 1, 128, 1, 128),     # one tile, one head
+    (2, 300, 3, 128, 3, 128),     # ragged; three groups of one head (odd heads per group)
+    (1, 1000, 5, 128, 1, 128),
+    (1, 2000, 1, 128, 1, 128),    # one chain over many CTAs: a hand-off at every block
+    (2, 300, 4, 128, 2, 256),     # dstate 256
+    (1, 2000, 2, 128, 1, 256),
 ]
 
 
@@ -57,12 +65,12 @@ def test_chain_path_matches_oracle(shape, chunk_len):
     check_against_oracle(shape, "bf16", chunk_len, "chain", seed=sum(shape) + chunk_len + 1)
 
 
-@pytest.mark.parametrize("n", [128, 256])
+@pytest.mark.parametrize("n,p", [(128, 64), (256, 64), (128, 128)])
 @pytest.mark.parametrize("dt_shift,A_scale", [(3.0, 4.0), (1.0, 2.0), (-2.0, 0.25), (0.0, 1.0)])
-def test_chain_path_strong_and_weak_decay(dt_shift, A_scale, n):
+def test_chain_path_strong_and_weak_decay(dt_shift, A_scale, n, p):
     """Uniformly strong decay (most 16-token sub-blocks extreme), moderate
     (blocks split into sub-blocks), weak (whole blocks)."""
-    inp = make_inputs(2, 1100, 8, 64, 2, n, io_dtype="bf16", init="normal", seed=43)
+    inp = make_inputs(2, 1100, 8, p, 2, n, io_dtype="bf16", init="normal", seed=43)
     inp["dt"] = (inp["dt"] + dt_shift).astype(np.float32)
     inp["A"] = (inp["A"] * A_scale).astype(np.float32)
     t = to_device(inp, "bf16")

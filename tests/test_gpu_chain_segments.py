@@ -110,3 +110,14 @@ def test_decay_sorted_pairs_map_heads_back(g):
     for mode in (0, 2):
         with warmup_mode(mode):
             check(inp)
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+def test_headdim_128_segments_match_oracle(mode):
+    """Headdim 128 (a chain per head, its two 64-row halves in one MMA): chains
+    across many CTAs with hand-offs or warm-ups."""
+    inp = make_inputs(1, 3000, 3, 128, 1, 128, io_dtype="bf16", init="normal", seed=91)
+    inp["dt"] = (inp["dt"] + 1.5).astype(np.float32)
+    inp["A"] = (inp["A"] * 3.0).astype(np.float32)
+    with warmup_mode(mode):
+        check(inp)

@@ -37,7 +37,7 @@ def debug_lib():
         pkg.use_library(old)
 
 
-# (path, b, L, h, g, n, chunk, warm-up mode, dt shift, A scale, seq cuts)
+# (path, b, L, h, g, n, chunk, warm-up mode, dt shift, A scale, seq cuts[, headdim (64)])
 CASES = [
     ("chain", 1, 1, 2, 1, 128, 256, 1, 0.0, 1.0, ()),          # a single token
     ("chain", 2, 127, 4, 2, 128, 128, 1, 0.0, 1.0, ()),        # one below a tile
@@ -48,6 +48,8 @@ CASES = [
     ("chain", 1, 1000, 6, 3, 256, 256, 1, 0.0, 1.0, ()),       # dstate 256
     ("chain", 1, 2000, 2, 1, 256, 256, 2, 1.0, 2.0, ()),       # dstate 256, warm-ups, splits
     ("chain", 1, 2600, 2, 1, 128, 256, 1, 0.0, 1.0, (300, 301, 1024)),  # packed sequences
+    ("chain", 2, 700, 3, 3, 128, 256, 2, 1.0, 2.0, (), 128),   # headdim 128, warm-ups, splits
+    ("chain", 1, 2000, 1, 1, 256, 256, 0, 0.0, 1.0, (), 128),  # headdim 128, dstate 256, hand-offs
     ("tc", 2, 300, 4, 2, 128, 256, 1, 0.0, 1.0, ()),
     ("tc", 1, 600, 8, 1, 256, 256, 1, 0.0, 1.0, ()),
     ("tc", 2, 700, 4, 2, 128, 128, 1, 1.0, 3.0, (1, 200, 513)),
@@ -57,8 +59,9 @@ CASES = [
 @pytest.mark.parametrize("case", CASES)
 def test_debug_build_checks_pass_and_results_match(debug_lib, case):
     pkg = debug_lib
-    path, b, L, h, g, n, Q, mode, dt_shift, A_scale, cuts = case
-    inp = make_inputs(b, L, h, 64, g, n, io_dtype="bf16", init="normal", seed=b + L + h + n)
+    path, b, L, h, g, n, Q, mode, dt_shift, A_scale, cuts = case[:11]
+    p = case[11] if len(case) > 11 else 64
+    inp = make_inputs(b, L, h, p, g, n, io_dtype="bf16", init="normal", seed=b + L + h + n)
     inp["dt"] = (inp["dt"] + dt_shift).astype(np.float32)
     inp["A"] = (inp["A"] * A_scale).astype(np.float32)
     ids = None

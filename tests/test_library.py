@@ -151,6 +151,9 @@ def test_path_selection(lib):
     assert pkg.ssd_select_path(1, 256, 4, 16, 1, 16, "f32", 64) == "simt"
     assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "f32", 256) == "simt"
     assert pkg.ssd_select_path(4, 4096, 80, 32, 1, 128, "bf16", 256) == "simt"
+    assert pkg.ssd_select_path(2, 4096, 40, 128, 1, 128, "bf16", 256) == "chain"  # headdim 128: a chain per head
+    assert pkg.ssd_select_path(1, 4096, 5, 128, 5, 256, "bf16", 256) == "chain"  # odd heads per group are fine
+    assert pkg.ssd_select_path(2, 4096, 40, 128, 1, 128, "f32", 256) == "simt"
     assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 64) == "simt"
 
 
