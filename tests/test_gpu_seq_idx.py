@@ -63,6 +63,7 @@ def run_case(inp, ids, io, chunk_len, path):
 PATH_CASES = [
     ("chain", "bf16", 256, 2, 700, 4, 64, 2, 128),
     ("chain", "bf16", 128, 1, 1100, 6, 64, 1, 128),
+    ("chain", "bf16", 256, 2, 900, 3, 128, 3, 128),     # headdim 128: a chain per head
     ("tc", "bf16", 256, 2, 700, 4, 64, 2, 128),
     ("tc", "bf16", 256, 1, 600, 8, 64, 1, 256),
     ("simt", "f32", 64, 2, 300, 3, 16, 1, 16),
