@@ -188,6 +188,31 @@ SSD_API ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype,
                         const void* B, const void* C, const float* D, const float* init_state,
                         int chunk_len, int ngroups, void* y, float* final_state, void* stream);
 
+/*
+ * ssd_check_inputs -- the input guard: counts the non-finite elements (NaN,
+ * +Inf, -Inf) of each input of an ssd_fwd call with these dims. The burn-mamba
+ * port runs a sanity check on every input before its kernels (`mamba2/ssd/
+ * serial.rs`, Mamba2::ssd_serial: x, dt, A, B, C, D and the initial state);
+ * a non-finite input spreads through the state to every later token of its
+ * chain, so a caller may refuse the forward instead.
+ *   dims, io_dtype, x, dt, dt_bias, A, B, C, D, init_state: as for ssd_fwd
+ *                 (device pointers, contiguous; x, B, C in io_dtype, the rest
+ *                 fp32; D and init_state may be NULL). Each pointer needs only
+ *                 its element's alignment. The inputs are only read.
+ *   counts        host int64[8], written on success: the counts for x, dt,
+ *                 dt_bias, A, B, C, D, init_state in that order (0 for a NULL
+ *                 D or init_state).
+ * One kernel over the eight tensors on `stream` (HBM bound: one read of each);
+ * the call synchronizes `stream` to return the counts. Errors:
+ * SSD_ERR_INVALID_ARG (NULL dims, counts or required input; dims < 1;
+ * nheads % ngroups != 0; unknown dtype), SSD_ERR_UNSUPPORTED (a pointer not
+ * aligned to its element), SSD_ERR_CUDA.
+ */
+SSD_API ssd_status ssd_check_inputs(const ssd_dims* dims, ssd_dtype io_dtype,
+                        const void* x, const float* dt, const float* dt_bias, const float* A,
+                        const void* B, const void* C, const float* D, const float* init_state,
+                        int64_t* counts, void* stream);
+
 /* Synchronizes `stream`, then returns and clears the current device's status
  * word: SSD_OK, SSD_ERR_DEVICE_TIMEOUT, SSD_ERR_DEBUG_CHECK (debug build only,
  * see ssd_debug_build), or SSD_ERR_CUDA if the sync failed. */

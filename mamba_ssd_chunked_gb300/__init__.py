@@ -19,7 +19,7 @@ import os
 from typing import Optional, Tuple
 
 __all__ = [
-    "SsdError", "library", "ssd_fwd", "ssd_fwd_host", "ssd_device_status", "ssd_fwd_workspace_bytes",
+    "SsdError", "library", "ssd_fwd", "ssd_fwd_host", "ssd_check_inputs", "ssd_device_status", "ssd_fwd_workspace_bytes",
     "ssd_select_path", "ssd_kernel_launches", "ssd_kernel_timing", "ssd_kernel_timing_read", "ssd_release", "ssd_step", "ssd_conv1d_silu", "ssd_conv1d_step",
     "ssd_gated_rmsnorm", "Dims", "ConvDims", "DtLimit", "PATHS", "STATUS",
 ]
@@ -86,6 +86,8 @@ def library() -> ctypes.CDLL:
     lib.ssd_select_path.restype = i
     lib.ssd_select_path.argtypes = [pdims, i, i]
     lib.ssd_device_status.restype = i
+    lib.ssd_check_inputs.restype = i
+    lib.ssd_check_inputs.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, ctypes.POINTER(ctypes.c_int64), vp]
     lib.ssd_device_status.argtypes = [vp]
     lib.ssd_status_string.restype = ctypes.c_char_p
     lib.ssd_status_string.argtypes = [i]
@@ -177,10 +179,33 @@ def _check_all(x, dt, dt_bias, A, B, C, D, init_state, device_type):
     _check(init_state, "init_state", (b, h, p, n), f32, device_type, optional=True)
 
 
+INPUT_NAMES = ("x", "dt", "dt_bias", "A", "B", "C", "D", "init_state")
+
+
+def ssd_check_inputs(x, dt, dt_bias, A, B, C, D=None, init_state=None, stream=None) -> dict:
+    """Count the non-finite elements (NaN, +-Inf) of each forward input on the
+    GPU through ssd_check_inputs; returns {name: count} over INPUT_NAMES (0 for
+    an absent D / init_state). Synchronizes `stream` (default: torch's current
+    stream)."""
+    torch = _torch()
+    _check_all(x, dt, dt_bias, A, B, C, D, init_state, "cuda")
+    lib = library()
+    dims = _dims(x, B)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    counts = (ctypes.c_int64 * len(INPUT_NAMES))()
+    rc = lib.ssd_check_inputs(ctypes.byref(dims), _io_code(x), _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B),
+                              _ptr(C), _ptr(D), _ptr(init_state), counts, stream)
+    if rc != 0:
+        raise SsdError(rc, "ssd_check_inputs")
+    return {name: int(c) for name, c in zip(INPUT_NAMES, counts)}
+
+
 def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: int = 256,
             ngroups: Optional[int] = None, y=None, final_state=None, return_final_state: bool = True,
             path: str = "auto", workspace=None, stream=None,
-            dt_limit: Optional[Tuple[float, float]] = None, seq_idx=None) -> Tuple[object, Optional[object]]:
+            dt_limit: Optional[Tuple[float, float]] = None, seq_idx=None,
+            check_inputs: bool = False) -> Tuple[object, Optional[object]]:
     """Run the SSD forward on the GPU through ssd_fwd / ssd_fwd_ws (ssd_fwd_ex
     when a dt_limit = (lo, hi) clamp of softplus(dt + dt_bias) or packed
     sequences seq_idx [b, L] int32 are given: the state restarts from zero
@@ -191,12 +216,18 @@ def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, init_state=None, chunk_len: int = 2
     the call goes through ssd_fwd_ws (a caller workspace must be zero-filled
     before its first use); otherwise through ssd_fwd with the library-owned
     workspace. Asynchronous on `stream` (default: torch's
-    current stream).
+    current stream). With check_inputs, the inputs first go through
+    ssd_check_inputs (which synchronizes `stream`), and a non-finite element
+    in any of them raises ValueError before the forward is launched.
     """
     torch = _torch()
     _check_all(x, dt, dt_bias, A, B, C, D, init_state, "cuda")
     lib = library()
     dims = _dims(x, B)
+    if check_inputs:
+        bad = {k: v for k, v in ssd_check_inputs(x, dt, dt_bias, A, B, C, D, init_state, stream=stream).items() if v}
+        if bad:
+            raise ValueError(f"ssd_fwd: non-finite input elements {bad}")
     if ngroups is None:
         ngroups = dims.ngroups
     if y is None:

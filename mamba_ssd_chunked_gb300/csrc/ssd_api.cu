@@ -460,6 +460,22 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
     return ssd_device_status(stream);
 }
 
+ssd_status ssd_check_inputs(const ssd_dims* dims, ssd_dtype io_dtype, const void* x, const float* dt,
+                            const float* dt_bias, const float* A, const void* B, const void* C, const float* D,
+                            const float* init_state, int64_t* counts, void* stream) {
+    if (!dims || !counts) return SSD_ERR_INVALID_ARG;
+    const ssd_status st = check_dims(dims, io_dtype, 1, static_cast<int>(dims->ngroups));
+    if (st != SSD_OK) return st;
+    if (!x || !dt || !dt_bias || !A || !B || !C) return SSD_ERR_INVALID_ARG;
+    const uintptr_t io_size = io_dtype == SSD_BF16 ? 2 : 4;
+    for (const void* p : {x, B, C})
+        if (reinterpret_cast<uintptr_t>(p) % io_size != 0) return SSD_ERR_UNSUPPORTED;
+    for (const float* p : {dt, dt_bias, A, D, init_state})
+        if (p && reinterpret_cast<uintptr_t>(p) % 4 != 0) return SSD_ERR_UNSUPPORTED;
+    const CheckArgs a{*dims, io_dtype, x, dt, dt_bias, A, B, C, D, init_state, static_cast<cudaStream_t>(stream)};
+    return check_inputs(a, counts);
+}
+
 ssd_status ssd_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSD_ERR_CUDA;
     int dev = 0;

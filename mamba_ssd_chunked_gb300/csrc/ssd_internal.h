@@ -87,6 +87,25 @@ struct StepArgs {
 bool step_supported(const ssd_dims& d);
 ssd_status step_forward(const StepArgs& a);
 
+// The inputs of one forward for the input guard (ssd_check_inputs), already
+// validated: x, B, C element-aligned in io, the fp32 ones 4-byte aligned.
+struct CheckArgs {
+    ssd_dims d;
+    ssd_dtype io;
+    const void* x;
+    const float* dt;
+    const float* dt_bias;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;     // nullable
+    const float* init;  // nullable
+    cudaStream_t stream;
+};
+// Non-finite element counts of x, dt, dt_bias, A, B, C, D, init into counts[8]
+// (host); synchronizes a.stream.
+ssd_status check_inputs(const CheckArgs& a, int64_t* counts);
+
 // Launch bookkeeping (every kernel launch of the library goes through it).
 void note_launches(uint64_t n);
 

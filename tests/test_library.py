@@ -30,7 +30,7 @@ def test_header_declares_the_documented_entry_points():
     for n in ("ssd_fwd", "ssd_fwd_ws", "ssd_fwd_host", "ssd_fwd_workspace_bytes", "ssd_device_status",
               "ssd_status_string", "ssd_kernel_launches", "ssd_release", "ssd_select_path", "ssd_step",
               "ssd_conv1d_silu", "ssd_conv1d_step", "ssd_gated_rmsnorm", "ssd_fwd_ex", "ssd_step_ex",
-              "ssd_debug_build", "ssd_debug_failed_line"):
+              "ssd_debug_build", "ssd_debug_failed_line", "ssd_check_inputs"):
         assert n in names
 
 
@@ -157,6 +157,17 @@ def test_path_selection(lib):
     assert pkg.ssd_select_path(4, 4096, 80, 64, 1, 128, "bf16", 64) == "simt"
 
 
+def visible_sm_count() -> int:
+    """SM count of the current CUDA device, 0 where none is visible."""
+    try:
+        import torch
+    except ImportError:
+        return 0
+    if not torch.cuda.is_available():
+        return 0
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
 def test_workspace_sizes(lib):
     # tensor-core path: a work counter, two ready flags per (batch, head) and
     # two fp32 state slots per (batch, head)
@@ -169,12 +180,15 @@ def test_workspace_sizes(lib):
     need = pkg.ssd_fwd_workspace_bytes(1, 256, 4, 16, 1, 16, "f32", 64, "simt")
     assert need >= 4 * 1 * 4 * 4 * 16 * 16
     assert pkg.ssd_fwd_workspace_bytes(1, 256, 4, 16, 1, 16, "f32", 64, "tc") == 0
-    # chain path: a counter and flag per CTA, one hand-off state per CTA; without a
-    # device to ask for its SM count it sizes for 1024 CTAs of two heads
+    # chain path: a counter and flag per CTA, one hand-off state per CTA (two
+    # heads), one CTA per SM; without a device to ask for its SM count it sizes
+    # for 1024 CTAs
+    ncta = min(visible_sm_count() or 1024, b * (h // 2) * 16)
     need = pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, n, "bf16", 256, "chain")
-    assert need >= 1024 * 2 * p * n * 4
+    assert need >= ncta * 2 * p * n * 4
     need256 = pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, 256, "bf16", 256, "chain")
-    assert need256 >= 1024 * 2 * p * 256 * 4  # the hand-off states are twice as wide
+    assert need256 >= ncta * 2 * p * 256 * 4  # the hand-off states are twice as wide
+    assert need256 - need >= ncta * 2 * p * 128 * 4
     assert pkg.ssd_fwd_workspace_bytes(b, 4096, h, p, 1, 192, "bf16", 256, "chain") == 0
 
 
@@ -231,3 +245,21 @@ def test_misaligned_seq_idx_is_unsupported(lib):
     d = pkg.Dims(1, 8, 2, 64, 1, 128)
     assert lib.ssd_fwd_ex(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 256, 1, FAKE, None,
                           None, FAKE + 2, 0, None, 0, None) == 2
+
+
+def test_input_guard_rejects_bad_arguments_on_host(lib):
+    d = pkg.Dims(1, 8, 2, 64, 1, 128)
+    counts = (ctypes.c_int64 * 8)()
+    f = lib.ssd_check_inputs
+    assert f(None, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, counts, None) == 1    # no dims
+    assert f(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None) == 1  # no counts
+    assert f(ctypes.byref(d), 1, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, counts, None) == 1  # no x
+    assert f(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, counts, None) == 1  # no C
+    assert f(ctypes.byref(d), 7, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, counts, None) == 1  # dtype
+    bad = pkg.Dims(1, 8, 3, 64, 2, 128)                                                           # 3 % 2
+    assert f(ctypes.byref(bad), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, counts, None) == 1
+    # element alignment only: bf16 x may sit at 2 bytes, fp32 x or dt may not
+    assert f(ctypes.byref(d), 1, FAKE + 1, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, counts, None) == 2
+    assert f(ctypes.byref(d), 0, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, counts, None) == 2
+    assert f(ctypes.byref(d), 1, FAKE, FAKE + 2, FAKE, FAKE, FAKE, FAKE, None, None, counts, None) == 2
+    assert f(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, None, counts, None) == 2
