@@ -176,12 +176,15 @@ SSD_API ssd_path ssd_select_path(const ssd_dims* dims, ssd_dtype io_dtype, int c
  * as ssd_fwd; pinned host memory makes the copies asynchronous). Copies the
  * inputs to library-owned device buffers, runs the forward, copies y (and
  * final_state when non-NULL) back, and synchronizes `stream` before
- * returning, so the outputs are ready on return. The batch rows are
- * independent problems: up to four slices of them run on library-owned
- * streams, each with its own workspace, so that one slice's upload overlaps
- * another's forward and a third's download; they start after the work already
- * queued on `stream`, which waits for all of them before the call returns.
- * Device-side timeouts are reported in the return value.
+ * returning, so the outputs are ready on return. The sequence is cut into up
+ * to eight token slices of at least 512 tokens (cuts on multiples of 256),
+ * each covering every batch row; a slice's final state is the next slice's
+ * initial state, which is exact for any cut (results match one ssd_fwd call up
+ * to rounding). Library-owned streams upload, compute and download the slices
+ * in order, so that one slice's upload overlaps another's forward and a third's
+ * download; they start after the work already queued on `stream`, which waits
+ * for all of them before the call returns. Device-side timeouts are reported
+ * in the return value.
  */
 SSD_API ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype,
                         const void* x, const float* dt, const float* dt_bias, const float* A,

@@ -20,20 +20,23 @@ __device__ unsigned g_status_word[2];
 
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s per device-side wait
 constexpr int kMaxDevices = 64;
-constexpr int kHostSlices = 4;  // ssd_fwd_host: batch slices in flight on their own streams
+constexpr int kHostSlices = 8;            // ssd_fwd_host: token slices in the upload / forward / download pipeline
+constexpr int64_t kHostSliceMinTokens = 512;  // ssd_fwd_host: no slice shorter (unless the sequence is)
+constexpr int64_t kHostCutAlign = 256;        // ssd_fwd_host: cuts on multiples of this many tokens
 
 struct DeviceState {
     unsigned* status = nullptr;     // device address of g_status_word
     void* ws = nullptr;             // library-owned workspace
     size_t ws_bytes = 0;
     // staging for ssd_fwd_host: device copies of the inputs and outputs, one
-    // stream and one workspace per batch slice, events that order them
+    // workspace (the slices' forwards run one after another), three streams
+    // (uploads, forwards, downloads) and the events that order them
     void* dev_io = nullptr;
     size_t dev_io_bytes = 0;
-    cudaStream_t slice_stream[kHostSlices] = {};
-    cudaEvent_t slice_event[kHostSlices + 1] = {};
+    cudaStream_t host_stream[3] = {};
+    cudaEvent_t host_event[2 * kHostSlices + 2] = {};
     void* slice_ws = nullptr;
-    size_t slice_ws_bytes = 0;  // per slice
+    size_t slice_ws_bytes = 0;
 };
 
 std::mutex g_mu;
@@ -330,33 +333,43 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
     if (!x || !dt || !dt_bias || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
     const ssd_dims& d = *dims;
     const size_t eb = elem_bytes(io_dtype);
-    // bytes per batch row of each batched tensor (batch is the outermost dimension of all of them)
-    const size_t row_x = eb * d.seqlen * d.nheads * d.headdim;
-    const size_t row_dt = 4 * d.seqlen * d.nheads;
-    const size_t row_bc = eb * d.seqlen * d.ngroups * d.dstate;
+    const size_t nb = static_cast<size_t>(d.batch), L = static_cast<size_t>(d.seqlen);
+    // bytes per token of one batch row of each batched tensor, and one batch row's state
+    const size_t tok_x = eb * d.nheads * d.headdim;
+    const size_t tok_dt = 4 * d.nheads;
+    const size_t tok_bc = eb * d.ngroups * d.dstate;
     const size_t row_state = 4 * d.nheads * d.headdim * d.dstate;
     const size_t sz_h = 4 * d.nheads;
-    // device layout: x, y, dt, B, C, dt_bias, A, D, init, final
-    const size_t sizes[10] = {row_x * d.batch, row_x * d.batch, row_dt * d.batch, row_bc * d.batch, row_bc * d.batch,
-                              sz_h, sz_h, sz_h, row_state * d.batch, row_state * d.batch};
+    // device layout: x, y, dt, B, C (each holding slice after slice, a slice as
+    // [batch, its tokens, ...]), dt_bias, A, D, the initial state, and two states
+    // that pass from one slice's forward to the next
+    const size_t sizes[10] = {tok_x * L * nb, tok_x * L * nb, tok_dt * L * nb, tok_bc * L * nb, tok_bc * L * nb,
+                              sz_h, sz_h, sz_h, row_state * nb, 2 * row_state * nb};
     size_t offs[10], total = 0;
     for (int i = 0; i < 10; ++i) {
         offs[i] = total;
         total += align_up(sizes[i], kWorkspaceAlign);
     }
-    // The batch rows are independent problems: slice them so that the upload of
-    // one slice, the forward of another and the download of a third overlap.
-    const int nsl = static_cast<int>(std::min<int64_t>(d.batch, kHostSlices));
-    auto slice_rows = [&](int i, int64_t* b0, int64_t* nb) {
-        *b0 = d.batch * i / nsl;
-        *nb = d.batch * (i + 1) / nsl - *b0;
-    };
+    // The sequence is cut into token slices of all batch rows; each slice's
+    // final state is the next one's initial state, which is exact for any cut
+    // (the state carries everything before it). The upload of one slice, the
+    // forward of another and the download of a third overlap, while every
+    // forward still covers the whole batch. Each of the three steps has a stream
+    // of its own and takes the slices in order. Cuts fall on whole multiples of
+    // kHostCutAlign tokens (whole chunks and blocks of the tensor-core paths).
+    const int nsl = static_cast<int>(
+        std::max<int64_t>(1, std::min<int64_t>(kHostSlices, d.seqlen / kHostSliceMinTokens)));
+    int64_t cut[kHostSlices + 1];
+    cut[0] = 0;
+    cut[nsl] = d.seqlen;
+    for (int i = 1; i < nsl; ++i) {
+        const int64_t c = d.seqlen * i / nsl;  // at least kHostSliceMinTokens past the previous cut
+        cut[i] = c / kHostCutAlign * kHostCutAlign;
+    }
     size_t ws_need = 0;
     for (int i = 0; i < nsl; ++i) {
-        int64_t b0, nb;
-        slice_rows(i, &b0, &nb);
         ssd_dims ds = d;
-        ds.batch = nb;
+        ds.seqlen = cut[i + 1] - cut[i];
         const ssd_path p = resolve_path(ds, io_dtype, chunk_len, SSD_PATH_AUTO);
         if (!path_supported(ds, io_dtype, chunk_len, p)) return SSD_ERR_UNSUPPORTED;
         ws_need = std::max(ws_need, align_up(workspace_for(ds, chunk_len, p), kWorkspaceAlign));
@@ -364,10 +377,12 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
     int dev = 0;
     st = current_device(&dev);
     if (st != SSD_OK) return st;
+    int max_pitch = 0;
+    if (cudaDeviceGetAttribute(&max_pitch, cudaDevAttrMaxPitch, dev) != cudaSuccess) return SSD_ERR_CUDA;
     char* base = nullptr;
     char* wsb = nullptr;
-    cudaStream_t ss[kHostSlices];
-    cudaEvent_t ev[kHostSlices + 1];
+    cudaStream_t up = nullptr, comp = nullptr, down = nullptr;
+    cudaEvent_t ev[2 * kHostSlices + 2];
     {
         std::lock_guard<std::mutex> lock(g_mu);
         DeviceState& s = g_dev[dev];
@@ -384,79 +399,100 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
                 if (s.slice_ws) cudaFree(s.slice_ws);
                 s.slice_ws = nullptr;
                 s.slice_ws_bytes = 0;
-                if (cudaMalloc(&s.slice_ws, ws_need * kHostSlices) != cudaSuccess) return SSD_ERR_CUDA;
+                if (cudaMalloc(&s.slice_ws, ws_need) != cudaSuccess) return SSD_ERR_CUDA;
                 // the tensor-core path's state slots must start zero-filled (see ssd_fwd_ws)
-                if (cudaMemset(s.slice_ws, 0, ws_need * kHostSlices) != cudaSuccess) return SSD_ERR_CUDA;
+                if (cudaMemset(s.slice_ws, 0, ws_need) != cudaSuccess) return SSD_ERR_CUDA;
                 s.slice_ws_bytes = ws_need;
             }
         }
-        for (int i = 0; i < kHostSlices; ++i)
-            if (!s.slice_stream[i] && cudaStreamCreateWithFlags(&s.slice_stream[i], cudaStreamNonBlocking) != cudaSuccess)
-                return SSD_ERR_CUDA;
-        for (int i = 0; i <= kHostSlices; ++i)
-            if (!s.slice_event[i] && cudaEventCreateWithFlags(&s.slice_event[i], cudaEventDisableTiming) != cudaSuccess)
-                return SSD_ERR_CUDA;
+        for (cudaStream_t& hs : s.host_stream)
+            if (!hs && cudaStreamCreateWithFlags(&hs, cudaStreamNonBlocking) != cudaSuccess) return SSD_ERR_CUDA;
+        for (cudaEvent_t& he : s.host_event)
+            if (!he && cudaEventCreateWithFlags(&he, cudaEventDisableTiming) != cudaSuccess) return SSD_ERR_CUDA;
         base = static_cast<char*>(s.dev_io);
         wsb = static_cast<char*>(s.slice_ws);
-        for (int i = 0; i < kHostSlices; ++i) ss[i] = s.slice_stream[i];
-        for (int i = 0; i <= kHostSlices; ++i) ev[i] = s.slice_event[i];
+        up = s.host_stream[0];
+        comp = s.host_stream[1];
+        down = s.host_stream[2];
+        for (int i = 0; i < 2 * kHostSlices + 2; ++i) ev[i] = s.host_event[i];
         ws_need = s.slice_ws_bytes;
     }
     cudaStream_t user = static_cast<cudaStream_t>(stream);
     auto cp = [](void* dst, const void* src, size_t n, cudaMemcpyKind k, cudaStream_t st_) {
         return n == 0 || cudaMemcpyAsync(dst, src, n, k, st_) == cudaSuccess;
     };
+    // a slice of every batch row in one 2-D copy: nb rows of `width` bytes,
+    // `spitch` apart in the source and `dpitch` apart in the destination (row by
+    // row where a pitch is beyond what a 2-D copy takes)
+    auto cp2 = [&](void* dst, size_t dpitch, const void* src, size_t spitch, size_t width, cudaMemcpyKind k,
+                   cudaStream_t st_) {
+        if (width == 0) return true;
+        if (dpitch <= static_cast<size_t>(max_pitch) && spitch <= static_cast<size_t>(max_pitch))
+            return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, nb, k, st_) == cudaSuccess;
+        for (size_t r = 0; r < nb; ++r)
+            if (cudaMemcpyAsync(static_cast<char*>(dst) + r * dpitch, static_cast<const char*>(src) + r * spitch, width,
+                                k, st_) != cudaSuccess)
+                return false;
+        return true;
+    };
     // on a failure after work was queued, nothing may still use the staging buffers on return
     auto fail = [&](ssd_status e) {
-        for (int i = 0; i < kHostSlices; ++i) cudaStreamSynchronize(ss[i]);
-        cudaStreamSynchronize(user);
+        for (cudaStream_t t : {up, comp, down, user}) cudaStreamSynchronize(t);
         return e;
     };
-    // the per-head parameters go first on the caller's stream; every slice waits for them
+    // events: uploaded[i], computed[i], the per-head parameters, all downloads done
+    cudaEvent_t* uploaded = ev;
+    cudaEvent_t* computed = ev + kHostSlices;
+    cudaEvent_t params = ev[2 * kHostSlices], done = ev[2 * kHostSlices + 1];
+    // the per-head parameters go first on the caller's stream; the pipeline waits for them
+    // (and so for everything the caller queued before)
     if (!cp(base + offs[5], dt_bias, sz_h, cudaMemcpyHostToDevice, user) ||
         !cp(base + offs[6], A, sz_h, cudaMemcpyHostToDevice, user) ||
         (D && !cp(base + offs[7], D, sz_h, cudaMemcpyHostToDevice, user)))
         return fail(SSD_ERR_CUDA);
-    if (cudaEventRecord(ev[kHostSlices], user) != cudaSuccess) return fail(SSD_ERR_CUDA);
+    if (cudaEventRecord(params, user) != cudaSuccess || cudaStreamWaitEvent(up, params, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(comp, params, 0) != cudaSuccess || cudaStreamWaitEvent(down, params, 0) != cudaSuccess)
+        return fail(SSD_ERR_CUDA);
     const char* hx = static_cast<const char*>(x);
     const char* hdt = reinterpret_cast<const char*>(dt);
     const char* hB = static_cast<const char*>(B);
     const char* hC = static_cast<const char*>(C);
-    const char* hinit = reinterpret_cast<const char*>(init_state);
     char* hy = static_cast<char*>(y);
-    char* hfs = reinterpret_cast<char*>(final_state);
+    char* dinit = base + offs[8];
+    float* pass[2] = {reinterpret_cast<float*>(base + offs[9]), reinterpret_cast<float*>(base + offs[9] + row_state * nb)};
+    if (init_state && !cp(dinit, init_state, row_state * nb, cudaMemcpyHostToDevice, up)) return fail(SSD_ERR_CUDA);
     for (int i = 0; i < nsl; ++i) {
-        int64_t b0, nb;
-        slice_rows(i, &b0, &nb);
-        cudaStream_t si = ss[i];
-        if (cudaStreamWaitEvent(si, ev[kHostSlices], 0) != cudaSuccess) return fail(SSD_ERR_CUDA);
-        char* dx = base + offs[0] + b0 * row_x;
-        char* dy = base + offs[1] + b0 * row_x;
-        char* ddt = base + offs[2] + b0 * row_dt;
-        char* dB = base + offs[3] + b0 * row_bc;
-        char* dC = base + offs[4] + b0 * row_bc;
-        char* dinit = base + offs[8] + b0 * row_state;
-        char* dfs = base + offs[9] + b0 * row_state;
-        if (!cp(dx, hx + b0 * row_x, nb * row_x, cudaMemcpyHostToDevice, si) ||
-            !cp(ddt, hdt + b0 * row_dt, nb * row_dt, cudaMemcpyHostToDevice, si) ||
-            !cp(dB, hB + b0 * row_bc, nb * row_bc, cudaMemcpyHostToDevice, si) ||
-            !cp(dC, hC + b0 * row_bc, nb * row_bc, cudaMemcpyHostToDevice, si) ||
-            (hinit && !cp(dinit, hinit + b0 * row_state, nb * row_state, cudaMemcpyHostToDevice, si)))
+        const size_t l0 = static_cast<size_t>(cut[i]), ls = static_cast<size_t>(cut[i + 1] - cut[i]);
+        // slice i of each batched tensor sits after slices 0 .. i-1, which hold l0 tokens of every row
+        char* dx = base + offs[0] + tok_x * nb * l0;
+        char* dy = base + offs[1] + tok_x * nb * l0;
+        char* ddt = base + offs[2] + tok_dt * nb * l0;
+        char* dB = base + offs[3] + tok_bc * nb * l0;
+        char* dC = base + offs[4] + tok_bc * nb * l0;
+        if (!cp2(dx, tok_x * ls, hx + tok_x * l0, tok_x * L, tok_x * ls, cudaMemcpyHostToDevice, up) ||
+            !cp2(ddt, tok_dt * ls, hdt + tok_dt * l0, tok_dt * L, tok_dt * ls, cudaMemcpyHostToDevice, up) ||
+            !cp2(dB, tok_bc * ls, hB + tok_bc * l0, tok_bc * L, tok_bc * ls, cudaMemcpyHostToDevice, up) ||
+            !cp2(dC, tok_bc * ls, hC + tok_bc * l0, tok_bc * L, tok_bc * ls, cudaMemcpyHostToDevice, up) ||
+            cudaEventRecord(uploaded[i], up) != cudaSuccess || cudaStreamWaitEvent(comp, uploaded[i], 0) != cudaSuccess)
             return fail(SSD_ERR_CUDA);
         ssd_dims ds = d;
-        ds.batch = nb;
+        ds.seqlen = static_cast<int64_t>(ls);
+        const float* init = i > 0 ? pass[(i - 1) & 1] : (init_state ? reinterpret_cast<const float*>(dinit) : nullptr);
+        float* fin = (i + 1 < nsl || final_state) ? pass[i & 1] : nullptr;
         st = run(&ds, io_dtype, dx, reinterpret_cast<const float*>(ddt),
                  reinterpret_cast<const float*>(base + offs[5]), reinterpret_cast<const float*>(base + offs[6]), dB,
-                 dC, D ? reinterpret_cast<const float*>(base + offs[7]) : nullptr,
-                 hinit ? reinterpret_cast<const float*>(dinit) : nullptr, chunk_len, ngroups, dy,
-                 hfs ? reinterpret_cast<float*>(dfs) : nullptr, SSD_PATH_AUTO, wsb + i * ws_need, ws_need, false, si);
+                 dC, D ? reinterpret_cast<const float*>(base + offs[7]) : nullptr, init, chunk_len, ngroups, dy, fin,
+                 SSD_PATH_AUTO, wsb, ws_need, false, comp);
         if (st != SSD_OK) return fail(st);
-        if (!cp(hy + b0 * row_x, dy, nb * row_x, cudaMemcpyDeviceToHost, si) ||
-            (hfs && !cp(hfs + b0 * row_state, dfs, nb * row_state, cudaMemcpyDeviceToHost, si)))
+        if (cudaEventRecord(computed[i], comp) != cudaSuccess || cudaStreamWaitEvent(down, computed[i], 0) != cudaSuccess)
             return fail(SSD_ERR_CUDA);
-        if (cudaEventRecord(ev[i], si) != cudaSuccess || cudaStreamWaitEvent(user, ev[i], 0) != cudaSuccess)
+        if (!cp2(hy + tok_x * l0, tok_x * L, dy, tok_x * ls, tok_x * ls, cudaMemcpyDeviceToHost, down))
             return fail(SSD_ERR_CUDA);
     }
+    if (final_state && !cp(final_state, pass[(nsl - 1) & 1], row_state * nb, cudaMemcpyDeviceToHost, down))
+        return fail(SSD_ERR_CUDA);
+    if (cudaEventRecord(done, down) != cudaSuccess || cudaStreamWaitEvent(user, done, 0) != cudaSuccess)
+        return fail(SSD_ERR_CUDA);
     return ssd_device_status(stream);
 }
 
@@ -555,16 +591,16 @@ void ssd_release(void) {
     const bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
     for (int d = 0; d < kMaxDevices; ++d) {
         DeviceState& s = g_dev[d];
-        if (!s.ws && !s.dev_io && !s.slice_ws && !s.slice_stream[0]) continue;
+        if (!s.ws && !s.dev_io && !s.slice_ws && !s.host_stream[0]) continue;
         if (cudaSetDevice(d) != cudaSuccess) continue;
         cudaDeviceSynchronize();
         if (s.ws) cudaFree(s.ws);
         if (s.dev_io) cudaFree(s.dev_io);
         if (s.slice_ws) cudaFree(s.slice_ws);
-        for (int i = 0; i < kHostSlices; ++i)
-            if (s.slice_stream[i]) cudaStreamDestroy(s.slice_stream[i]);
-        for (int i = 0; i <= kHostSlices; ++i)
-            if (s.slice_event[i]) cudaEventDestroy(s.slice_event[i]);
+        for (cudaStream_t& hs : s.host_stream)
+            if (hs) cudaStreamDestroy(hs);
+        for (cudaEvent_t& he : s.host_event)
+            if (he) cudaEventDestroy(he);
         s = DeviceState{};
     }
     if (have_prev) cudaSetDevice(prev);

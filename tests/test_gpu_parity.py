@@ -158,14 +158,20 @@ def test_caller_workspace_and_explicit_stream():
     assert rel_err(y.float().cpu().numpy(), y_ref) < 2e-2 and rel_err(fs.cpu().numpy(), f_ref) < 2e-2
 
 
-# (shape b, L, h, p, g, n; io; init; with D; final state): one to five batch rows, so
-# that the host entry point's batch slices (up to 4, on their own streams) come
-# out even, uneven (5 rows) and single
+# (shape b, L, h, p, g, n; io; init; with D; final state): the host entry point cuts
+# the sequence into token slices of at least 512 tokens (cuts on multiples of 256)
+# and passes the state from slice to slice: one slice (L < 1024), two with a ragged
+# second one, four with a ragged last one, eight; with and without an initial and a
+# final state, on the chain and the SIMT paths
 HOST_CASES = [
     ((2, 300, 4, 64, 2, 128), "bf16", "normal", True, True),
     ((5, 200, 4, 64, 1, 128), "bf16", "normal", True, True),
     ((1, 129, 2, 64, 1, 128), "bf16", "zero", False, False),
     ((3, 150, 4, 16, 2, 16), "f32", "normal", True, True),
+    ((2, 1100, 4, 64, 2, 128), "bf16", "normal", True, True),
+    ((1, 2100, 2, 64, 1, 128), "bf16", "zero", True, True),
+    ((2, 4096, 2, 64, 1, 128), "bf16", "normal", True, False),
+    ((1, 1100, 4, 16, 2, 16), "f32", "normal", False, True),
 ]
 
 
