@@ -184,7 +184,9 @@ SSD_API ssd_path ssd_select_path(const ssd_dims* dims, ssd_dtype io_dtype, int c
  * in order, so that one slice's upload overlaps another's forward and a third's
  * download; they start after the work already queued on `stream`, which waits
  * for all of them before the call returns. Device-side timeouts are reported
- * in the return value.
+ * in the return value. The staging buffers and streams belong to the device:
+ * ssd_fwd_host calls on one device must not overlap (issue them from one host
+ * thread at a time).
  */
 SSD_API ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype,
                         const void* x, const float* dt, const float* dt_bias, const float* A,
