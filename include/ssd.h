@@ -176,11 +176,12 @@ SSD_API ssd_path ssd_select_path(const ssd_dims* dims, ssd_dtype io_dtype, int c
  * as ssd_fwd; pinned host memory makes the copies asynchronous). Copies the
  * inputs to library-owned device buffers, runs the forward, copies y (and
  * final_state when non-NULL) back, and synchronizes `stream` before
- * returning, so the outputs are ready on return. The sequence is cut into up
- * to eight token slices of at least 512 tokens (cuts on multiples of 256),
- * each covering every batch row; a slice's final state is the next slice's
- * initial state, which is exact for any cut (results match one ssd_fwd call up
- * to rounding). Library-owned streams upload, compute and download the slices
+ * returning, so the outputs are ready on return. The sequence is cut into
+ * token slices, each covering every batch row: one per 96 MiB of copies, at
+ * least 4 and at most 16, none shorter than 512 tokens, cuts on multiples of
+ * 256 (the environment variable SSD_HOST_SLICES, 1 to 16, replaces the count
+ * from the copies). A slice's final state is the next slice's initial state,
+ * which is exact for any cut (results match one ssd_fwd call up to rounding). Library-owned streams upload, compute and download the slices
  * in order, so that one slice's upload overlaps another's forward and a third's
  * download; they start after the work already queued on `stream`, which waits
  * for all of them before the call returns. Device-side timeouts are reported

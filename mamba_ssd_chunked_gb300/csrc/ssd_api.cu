@@ -1,5 +1,6 @@
 // The C ABI of libssd (include/ssd.h): argument checks, path selection,
 // library-owned workspaces and staging buffers, the device status word.
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -20,7 +21,9 @@ __device__ unsigned g_status_word[2];
 
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s per device-side wait
 constexpr int kMaxDevices = 64;
-constexpr int kHostSlices = 8;            // ssd_fwd_host: token slices in the upload / forward / download pipeline
+constexpr int kHostSlices = 16;           // ssd_fwd_host: token slices in the upload / forward / download pipeline, at most
+constexpr int kHostMinSlices = 4;         // ssd_fwd_host: at least, where the sequence allows
+constexpr int64_t kHostSliceBytes = 96ll << 20;  // ssd_fwd_host: copy bytes per slice above kHostMinSlices slices
 constexpr int64_t kHostSliceMinTokens = 512;  // ssd_fwd_host: no slice shorter (unless the sequence is)
 constexpr int64_t kHostCutAlign = 256;        // ssd_fwd_host: cuts on multiples of this many tokens
 
@@ -52,6 +55,19 @@ unsigned long long wait_limit_ns() {
         if (x > 0) return x;
     }
     return kDefaultWaitNs;
+}
+
+// ssd_fwd_host's slice count before the caps of the sequence length: the
+// environment variable SSD_HOST_SLICES (read at every call, 1 .. kHostSlices)
+// overrides the rule from the copy bytes; tests use it to force many slices on
+// small inputs.
+int64_t host_slices_wanted(int64_t copy_bytes) {
+    const char* e = std::getenv("SSD_HOST_SLICES");
+    if (e && *e) {
+        const long v = std::strtol(e, nullptr, 10);
+        if (v >= 1 && v <= kHostSlices) return v;
+    }
+    return std::max<int64_t>(kHostMinSlices, (copy_bytes + kHostSliceBytes - 1) / kHostSliceBytes);
 }
 
 // Chain path warm-up mode (FwdArgs::chain_warmup). The environment variable
@@ -357,8 +373,13 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
     // forward still covers the whole batch. Each of the three steps has a stream
     // of its own and takes the slices in order. Cuts fall on whole multiples of
     // kHostCutAlign tokens (whole chunks and blocks of the tensor-core paths).
-    const int nsl = static_cast<int>(
-        std::max<int64_t>(1, std::min<int64_t>(kHostSlices, d.seqlen / kHostSliceMinTokens)));
+    // Slices: one per kHostSliceBytes of copies, at least kHostMinSlices (fewer slices
+    // leave the link idle in one direction for longer at both ends, more pay each
+    // forward's fixed cost more often), none shorter than kHostSliceMinTokens.
+    const int64_t copy_bytes = static_cast<int64_t>(2 * tok_x + tok_dt + 2 * tok_bc) * d.seqlen * d.batch;
+    const int nsl = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>({static_cast<int64_t>(kHostSlices), d.seqlen / kHostSliceMinTokens,
+                              host_slices_wanted(copy_bytes)})));
     int64_t cut[kHostSlices + 1];
     cut[0] = 0;
     cut[nsl] = d.seqlen;

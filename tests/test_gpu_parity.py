@@ -196,6 +196,29 @@ def test_host_buffer_entry_point(shape, io, init, with_D, final):
         assert fs is None
 
 
+@pytest.mark.parametrize("slices,shape", [(16, (1, 8192, 2, 64, 1, 128)), (5, (2, 2600, 4, 64, 2, 128)),
+                                          (3, (1, 1700, 4, 16, 2, 16))])
+def test_host_entry_point_forced_slices(slices, shape, monkeypatch):
+    # SSD_HOST_SLICES overrides the slice count the copy bytes give (small inputs
+    # would get the minimum): the most slices the pipeline takes, an odd count
+    # with a ragged last slice, and the SIMT path
+    import mamba_ssd_chunked_gb300 as pkg
+    b, L, h_, p, g, n = shape
+    io = "bf16" if p == 64 else "f32"
+    inp = make_inputs(b, L, h_, p, g, n, io_dtype=io, init="normal", seed=41 + slices)
+    h = {k: torch.from_numpy(v) for k, v in inp.items()}
+    if io == "bf16":
+        for k in ("x", "B", "C"):
+            h[k] = h[k].to(torch.bfloat16)
+    h = {k: v.contiguous().pin_memory() for k, v in h.items()}
+    monkeypatch.setenv("SSD_HOST_SLICES", str(slices))
+    y, fs = pkg.ssd_fwd_host(h["x"], h["dt"], h["dt_bias"], h["A"], h["B"], h["C"], h["D"], h["init_state"],
+                             chunk_len=256 if io == "bf16" else 64)
+    y_ref, f_ref = oracle_full(inp)
+    assert rel_err(y.float().numpy(), y_ref) <= TOL[io]
+    assert rel_err(fs.numpy(), f_ref) <= TOL[io]
+
+
 @pytest.mark.parametrize("path", ["chain", "tc", "simt"])
 def test_kernel_timing_records_one_pair_per_forward(path):
     import mamba_ssd_chunked_gb300 as pkg
