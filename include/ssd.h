@@ -194,6 +194,10 @@ SSD_API ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype,
                         const void* B, const void* C, const float* D, const float* init_state,
                         int chunk_len, int ngroups, void* y, float* final_state, void* stream);
 
+/* The number of token slices ssd_fwd_host cuts a call with these dims into
+ * (after SSD_HOST_SLICES, if set); 0 for invalid dims. Host only. */
+SSD_API int ssd_host_slices(const ssd_dims* dims, ssd_dtype io_dtype);
+
 /*
  * ssd_check_inputs -- the input guard: counts the non-finite elements (NaN,
  * +Inf, -Inf) of each input of an ssd_fwd call with these dims. The burn-mamba

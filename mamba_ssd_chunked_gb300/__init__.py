@@ -20,7 +20,7 @@ from typing import Optional, Tuple
 
 __all__ = [
     "SsdError", "library", "ssd_fwd", "ssd_fwd_host", "ssd_check_inputs", "ssd_device_status", "ssd_fwd_workspace_bytes",
-    "ssd_select_path", "ssd_kernel_launches", "ssd_kernel_timing", "ssd_kernel_timing_read", "ssd_release", "ssd_step", "ssd_conv1d_silu", "ssd_conv1d_step",
+    "ssd_select_path", "ssd_host_slices", "ssd_kernel_launches", "ssd_kernel_timing", "ssd_kernel_timing_read", "ssd_release", "ssd_step", "ssd_conv1d_silu", "ssd_conv1d_step",
     "ssd_gated_rmsnorm", "Dims", "ConvDims", "DtLimit", "PATHS", "STATUS",
 ]
 
@@ -85,6 +85,8 @@ def library() -> ctypes.CDLL:
     lib.ssd_fwd_workspace_bytes.argtypes = [pdims, i, i, i]
     lib.ssd_select_path.restype = i
     lib.ssd_select_path.argtypes = [pdims, i, i]
+    lib.ssd_host_slices.restype = i
+    lib.ssd_host_slices.argtypes = [pdims, i]
     lib.ssd_device_status.restype = i
     lib.ssd_check_inputs.restype = i
     lib.ssd_check_inputs.argtypes = [pdims, i, vp, fp, fp, fp, vp, vp, fp, fp, ctypes.POINTER(ctypes.c_int64), vp]
@@ -468,6 +470,12 @@ def ssd_select_path(batch, seqlen, nheads, headdim, ngroups, dstate, io="bf16", 
     d = Dims(batch, seqlen, nheads, headdim, ngroups, dstate)
     code = int(library().ssd_select_path(ctypes.byref(d), DTYPES[io], int(chunk_len)))
     return {v: k for k, v in PATHS.items()}[code]
+
+
+def ssd_host_slices(batch, seqlen, nheads, headdim, ngroups, dstate, io="bf16") -> int:
+    """Token slices ssd_fwd_host cuts a call of these dims into (0 for invalid dims)."""
+    d = Dims(batch, seqlen, nheads, headdim, ngroups, dstate)
+    return int(library().ssd_host_slices(ctypes.byref(d), DTYPES[io]))
 
 
 def ssd_kernel_launches() -> int:

@@ -216,6 +216,19 @@ ssd_status run(const ssd_dims* dims, ssd_dtype io, const void* x, const float* d
 
 size_t elem_bytes(ssd_dtype io) { return io == SSD_F32 ? 4 : 2; }
 
+// Token slices of ssd_fwd_host for valid dims: one per kHostSliceBytes of
+// copies, at least kHostMinSlices (fewer slices leave the link idle in one
+// direction for longer at both ends, more pay each forward's fixed cost more
+// often), at most kHostSlices, none shorter than kHostSliceMinTokens.
+int host_slice_count(const ssd_dims& d, ssd_dtype io) {
+    const int64_t eb = static_cast<int64_t>(elem_bytes(io));
+    const int64_t per_token = 2 * eb * d.nheads * d.headdim + 4 * d.nheads + 2 * eb * d.ngroups * d.dstate;
+    const int64_t copy_bytes = per_token * d.seqlen * d.batch;
+    return static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>({static_cast<int64_t>(kHostSlices), d.seqlen / kHostSliceMinTokens,
+                              host_slices_wanted(copy_bytes)})));
+}
+
 // A dt limit is 0 <= dt_min <= dt_max (dt_max may be +inf); NULL means none.
 bool dt_limit_ok(const ssd_dt_limit* lim, float* lo, float* hi) {
     *lo = 0.f;
@@ -335,6 +348,11 @@ size_t ssd_fwd_workspace_bytes(const ssd_dims* dims, ssd_dtype io_dtype, int chu
     return workspace_for(*dims, chunk_len, p);
 }
 
+int ssd_host_slices(const ssd_dims* dims, ssd_dtype io_dtype) {
+    if (!dims || check_dims(dims, io_dtype, 1, static_cast<int>(dims->ngroups)) != SSD_OK) return 0;
+    return host_slice_count(*dims, io_dtype);
+}
+
 ssd_path ssd_select_path(const ssd_dims* dims, ssd_dtype io_dtype, int chunk_len) {
     if (!dims) return SSD_PATH_SIMT;
     return resolve_path(*dims, io_dtype, chunk_len, SSD_PATH_AUTO);
@@ -373,13 +391,7 @@ ssd_status ssd_fwd_host(const ssd_dims* dims, ssd_dtype io_dtype, const void* x,
     // forward still covers the whole batch. Each of the three steps has a stream
     // of its own and takes the slices in order. Cuts fall on whole multiples of
     // kHostCutAlign tokens (whole chunks and blocks of the tensor-core paths).
-    // Slices: one per kHostSliceBytes of copies, at least kHostMinSlices (fewer slices
-    // leave the link idle in one direction for longer at both ends, more pay each
-    // forward's fixed cost more often), none shorter than kHostSliceMinTokens.
-    const int64_t copy_bytes = static_cast<int64_t>(2 * tok_x + tok_dt + 2 * tok_bc) * d.seqlen * d.batch;
-    const int nsl = static_cast<int>(std::max<int64_t>(
-        1, std::min<int64_t>({static_cast<int64_t>(kHostSlices), d.seqlen / kHostSliceMinTokens,
-                              host_slices_wanted(copy_bytes)})));
+    const int nsl = host_slice_count(d, io_dtype);
     int64_t cut[kHostSlices + 1];
     cut[0] = 0;
     cut[nsl] = d.seqlen;

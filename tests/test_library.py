@@ -30,7 +30,7 @@ def test_header_declares_the_documented_entry_points():
     for n in ("ssd_fwd", "ssd_fwd_ws", "ssd_fwd_host", "ssd_fwd_workspace_bytes", "ssd_device_status",
               "ssd_status_string", "ssd_kernel_launches", "ssd_release", "ssd_select_path", "ssd_step",
               "ssd_conv1d_silu", "ssd_conv1d_step", "ssd_gated_rmsnorm", "ssd_fwd_ex", "ssd_step_ex",
-              "ssd_debug_build", "ssd_debug_failed_line", "ssd_check_inputs"):
+              "ssd_debug_build", "ssd_debug_failed_line", "ssd_check_inputs", "ssd_host_slices"):
         assert n in names
 
 
@@ -263,3 +263,24 @@ def test_input_guard_rejects_bad_arguments_on_host(lib):
     assert f(ctypes.byref(d), 0, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, counts, None) == 2
     assert f(ctypes.byref(d), 1, FAKE, FAKE + 2, FAKE, FAKE, FAKE, FAKE, None, None, counts, None) == 2
     assert f(ctypes.byref(d), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, None, counts, None) == 2
+
+
+def test_host_entry_point_slice_rule(lib, monkeypatch):
+    # one token slice per 96 MiB of copies (x and y in the io dtype, dt, B and C),
+    # at least 4 and at most 16, none shorter than 512 tokens
+    monkeypatch.delenv("SSD_HOST_SLICES", raising=False)
+    f = pkg.ssd_host_slices
+    assert f(4, 4096, 80, 64, 1, 128) == 4          # the 2.7B layer: 349 MB of copies
+    assert f(1, 131072, 64, 64, 1, 256) == 16       # long context: 2.3 GB, capped
+    assert f(2, 16000, 128, 64, 8, 128) == 12       # 1.2 GB
+    assert f(8, 2048, 24, 64, 1, 128) == 4          # 111 MB: the minimum
+    assert f(2, 1536, 4, 64, 2, 128) == 3           # 512-token floor
+    assert f(2, 1023, 4, 64, 2, 128) == 1
+    assert f(1, 1, 2, 64, 1, 128) == 1
+    assert f(0, 4096, 80, 64, 1, 128) == 0          # invalid dims
+    assert f(1, 4096, 6, 64, 4, 128) == 0
+    monkeypatch.setenv("SSD_HOST_SLICES", "16")
+    assert f(1, 8192, 2, 64, 1, 128) == 16
+    assert f(2, 2600, 4, 64, 2, 128) == 5           # still no slice below 512 tokens
+    monkeypatch.setenv("SSD_HOST_SLICES", "17")     # out of range: the rule from the copies
+    assert f(4, 4096, 80, 64, 1, 128) == 4
